@@ -1,0 +1,213 @@
+"""FP64 CPU oracle for paged MQA/GQA decode attention (test infrastructure).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The CUDA library never calls it, and it
+imports nothing from the CUDA library's package.
+
+The arithmetic lives in ``paged_attn_oracle.c`` (plain C, double precision,
+loops that state the definition of the operator). This module compiles it
+with gcc on first use and marshals numpy arrays into it. Inputs are the raw
+16-bit storage patterns of bf16/fp16 tensors (numpy ``uint16``), so the
+conversion to double is the oracle's own exact decode.
+
+Parity pins (all in ``tests/test_oracle_*.py``): brute-force dense attention
+in arbitrary precision on tiny inputs, closed forms (one token, constant V,
+constant logits, two tokens), invariance under block-table permutation and
+block size, GQA reductions (MHA, MQA, duplicated heads), split-K merge equal
+to the unsplit result, exact RNE rounding against numpy/torch conversions,
+and a mutation test that plants plausible mistakes in a copy of the C source
+and checks that the pins catch each one.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+BF16 = 0
+FP16 = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "paged_attn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+_lock = threading.Lock()
+_lib = None
+
+# -ffp-contract=off: no fused multiply-add contraction, so the double
+# arithmetic is the same on x86_64 and aarch64 hosts.
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+
+
+def compile_oracle(src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the oracle's C source into a shared library at ``out``."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", *CFLAGS, "-o", tmp, src, "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _needs_build() -> bool:
+    if not os.path.exists(_LIB_PATH):
+        return True
+    return os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+
+
+def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    P = ctypes.c_void_p
+    i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+    lib.oracle_paged_decode.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, i32,
+                                        f64, P, i32]
+    lib.oracle_paged_decode.restype = i32
+    lib.oracle_paged_decode_rows.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64,
+                                             i32, f64, P, i64, P, i32]
+    lib.oracle_paged_decode_rows.restype = i32
+    lib.oracle_split_partials.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, i32,
+                                          f64, i32, i32, P, P]
+    lib.oracle_split_partials.restype = i32
+    lib.oracle_lse_merge.argtypes = [P, P, i64, i32, i32, P]
+    lib.oracle_lse_merge.restype = i32
+    lib.oracle_round_array.argtypes = [P, i64, i32, P, P]
+    lib.oracle_round_array.restype = None
+    lib.oracle_decode_array.argtypes = [P, i64, i32, P]
+    lib.oracle_decode_array.restype = None
+    return lib
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load (building if needed) the oracle library. ``path`` loads another
+    build of it (used by the mutation test)."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            if _needs_build():
+                compile_oracle()
+            _lib = _bind(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _as_bits(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError(f"expected raw 16-bit patterns (uint16), got {a.dtype}")
+    return a
+
+
+def _as_i32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+_ERRORS = {-1: "invalid argument", -2: "index or length out of range", -3: "out of memory"}
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise ValueError(f"oracle {what}: {_ERRORS.get(status, status)}")
+
+
+def default_threads() -> int:
+    return os.cpu_count() or 1
+
+
+def paged_decode(q, k_cache, v_cache, block_table, context_lens, dtype: int, scale: float,
+                 threads: int | None = None, lib=None) -> np.ndarray:
+    """out[B, Hq, D] (float64) of softmax(scale * q . K^T) . V over each
+    sequence's paged K/V.
+
+    q: uint16 [B, Hq, D]; k_cache/v_cache: uint16 [num_blocks, bs, Hkv, D];
+    block_table: int32 [B, max_blocks]; context_lens: int32 [B].
+    """
+    lib = lib or load()
+    q, k, v = _as_bits(q), _as_bits(k_cache), _as_bits(v_cache)
+    bt, cl = _as_i32(block_table), _as_i32(context_lens)
+    B, Hq, D = q.shape
+    nb, bs, Hkv, Dk = k.shape
+    assert Dk == D and v.shape == k.shape and bt.shape[0] == B and cl.shape == (B,)
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    st = lib.oracle_paged_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(bt), _ptr(cl), B, Hq, Hkv, D,
+                                 bs, bt.shape[1], nb, dtype, float(scale), _ptr(out),
+                                 threads or default_threads())
+    _check(st, "paged_decode")
+    return out
+
+
+def paged_decode_rows(q, k_cache, v_cache, block_table, context_lens, dtype: int, scale: float,
+                      rows, threads: int | None = None, lib=None) -> np.ndarray:
+    """Like :func:`paged_decode` for the (b, hq) pairs in ``rows`` only;
+    returns float64 [len(rows), D]."""
+    lib = lib or load()
+    q, k, v = _as_bits(q), _as_bits(k_cache), _as_bits(v_cache)
+    bt, cl = _as_i32(block_table), _as_i32(context_lens)
+    rows = _as_i32(rows).reshape(-1, 2)
+    B, Hq, D = q.shape
+    nb, bs, Hkv, _ = k.shape
+    out = np.zeros((rows.shape[0], D), dtype=np.float64)
+    st = lib.oracle_paged_decode_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(bt), _ptr(cl), B, Hq, Hkv,
+                                      D, bs, bt.shape[1], nb, dtype, float(scale), _ptr(rows),
+                                      rows.shape[0], _ptr(out), threads or default_threads())
+    _check(st, "paged_decode_rows")
+    return out
+
+
+def split_partials(q, k_cache, v_cache, block_table, context_lens, dtype: int, scale: float,
+                   chunk_pages: int, num_splits: int, lib=None):
+    """(lse[B, Hq, S], o[B, Hq, S, D]) of split-K partials; split s covers
+    pages [s*chunk_pages, (s+1)*chunk_pages) of each sequence."""
+    lib = lib or load()
+    q, k, v = _as_bits(q), _as_bits(k_cache), _as_bits(v_cache)
+    bt, cl = _as_i32(block_table), _as_i32(context_lens)
+    B, Hq, D = q.shape
+    nb, bs, Hkv, _ = k.shape
+    lse = np.zeros((B, Hq, num_splits), dtype=np.float64)
+    o = np.zeros((B, Hq, num_splits, D), dtype=np.float64)
+    st = lib.oracle_split_partials(_ptr(q), _ptr(k), _ptr(v), _ptr(bt), _ptr(cl), B, Hq, Hkv, D,
+                                   bs, bt.shape[1], nb, dtype, float(scale), chunk_pages,
+                                   num_splits, _ptr(lse), _ptr(o))
+    _check(st, "split_partials")
+    return lse, o
+
+
+def lse_merge(lse, o, lib=None) -> np.ndarray:
+    """Merge partials: lse[..., S], o[..., S, D] -> out[..., D] (float64)."""
+    lib = lib or load()
+    lse = np.ascontiguousarray(lse, dtype=np.float64)
+    o = np.ascontiguousarray(o, dtype=np.float64)
+    S, D = o.shape[-2], o.shape[-1]
+    lead = o.shape[:-2]
+    assert lse.shape == lead + (S,)
+    n = int(np.prod(lead)) if lead else 1
+    out = np.zeros(lead + (D,), dtype=np.float64)
+    _check(lib.oracle_lse_merge(_ptr(lse), _ptr(o), n, S, D, _ptr(out)), "lse_merge")
+    return out
+
+
+def round_to(x, dtype: int, lib=None):
+    """Round float64 values to bf16/fp16 with ties to even, directly from
+    double. Returns (bits uint16, rounded float64)."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    bits = np.zeros(x.shape, dtype=np.uint16)
+    rounded = np.zeros(x.shape, dtype=np.float64)
+    lib.oracle_round_array(_ptr(x), x.size, dtype, _ptr(bits), _ptr(rounded))
+    return bits, rounded
+
+
+def decode(bits, dtype: int, lib=None) -> np.ndarray:
+    """Exact float64 values of raw bf16/fp16 patterns."""
+    lib = lib or load()
+    bits = _as_bits(bits)
+    out = np.zeros(bits.shape, dtype=np.float64)
+    lib.oracle_decode_array(_ptr(bits), bits.size, dtype, _ptr(out))
+    return out

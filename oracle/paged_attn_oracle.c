@@ -1,0 +1,414 @@
+/*
+ * FP64 CPU oracle for paged MQA/GQA decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the plain, slow, obviously correct
+ * statement of what the GPU path computes. Only the test suite, the smoke
+ * check and the CPU-baseline leg of the benchmark may load it. It shares no
+ * code, header, table or helper with the CUDA library, and the library never
+ * calls it.
+ *
+ * What it follows (Loom Kernels landing page, "Supported now", the
+ * "Paged MQA/GQA decode" entry: GQA packing + local split-K/LSE; and the
+ * benchmark page, "Current qualified results": the D128 long-context
+ * split-K/LSE path). The pages name the operator but print no formula, so the
+ * operator is the textbook one its name denotes:
+ *
+ *   for every sequence b and query head hq, with G = Hq / Hkv,
+ *   kv head h = floor(hq / G), context length L = context_lens[b]:
+ *     k_t = k_cache[block_table[b, floor(t / bs)], t mod bs, h, :]   (t < L)
+ *     v_t = v_cache[block_table[b, floor(t / bs)], t mod bs, h, :]
+ *     s_t = scale * sum_d q[b, hq, d] * k_t[d]
+ *     out[b, hq, :] = sum_t softmax(s)_t * v_t
+ *
+ * Every input element is converted exactly to double; every sum is a plain
+ * left-to-right double sum in token order; softmax subtracts the row maximum
+ * before exponentiating. There is no blocking, no online softmax and no
+ * re-association: the loops below are the definition written out.
+ *
+ * Readings where the pages are silent:
+ *   - no mask other than t < L (plain decode over the whole context);
+ *   - contiguous GQA groups: query head hq reads kv head floor(hq / G);
+ *   - block-table entries at page index >= ceil(L / bs) are never read;
+ *   - L == 0 yields a zero output row (the GPU path does the same);
+ *   - split-K: a sequence's pages are cut into contiguous, page-aligned
+ *     chunks of `chunk_pages` pages; a chunk with no tokens has lse = -inf and
+ *     o = 0; chunks are merged by log-sum-exp weighting.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_BF16 0
+#define ORACLE_FP16 1
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL (-1)
+#define ORACLE_ERANGE (-2)
+#define ORACLE_ENOMEM (-3)
+
+/* ---------------------------------------------------------------------------
+ * Exact conversions between 16-bit storage formats and double.
+ * bfloat16: 1 sign, 8 exponent (bias 127), 7 fraction bits (the top half of
+ * an IEEE binary32). binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits.
+ * ------------------------------------------------------------------------- */
+
+double oracle_bf16_to_f64(uint16_t bits) {
+  int sign = (bits >> 15) & 1;
+  int exp = (bits >> 7) & 0xff;
+  int frac = bits & 0x7f;
+  double mag;
+  if (exp == 0xff) {
+    mag = frac ? NAN : INFINITY;
+  } else if (exp == 0) {
+    mag = ldexp((double)frac, -126 - 7); /* subnormal: frac * 2^-133 */
+  } else {
+    mag = ldexp((double)(128 + frac), exp - 127 - 7);
+  }
+  return sign ? -mag : mag;
+}
+
+double oracle_fp16_to_f64(uint16_t bits) {
+  int sign = (bits >> 15) & 1;
+  int exp = (bits >> 10) & 0x1f;
+  int frac = bits & 0x3ff;
+  double mag;
+  if (exp == 0x1f) {
+    mag = frac ? NAN : INFINITY;
+  } else if (exp == 0) {
+    mag = ldexp((double)frac, -14 - 10); /* subnormal: frac * 2^-24 */
+  } else {
+    mag = ldexp((double)(1024 + frac), exp - 15 - 10);
+  }
+  return sign ? -mag : mag;
+}
+
+double oracle_to_f64(uint16_t bits, int dtype) {
+  return dtype == ORACLE_BF16 ? oracle_bf16_to_f64(bits) : oracle_fp16_to_f64(bits);
+}
+
+/* Round a double to the nearest value with `mant_bits` fraction bits and
+ * minimum normal exponent `emin`, ties to even, directly from double (no
+ * intermediate float, so no double rounding). Returns the rounded double;
+ * values beyond the largest finite number of the format become infinity. */
+static double round_to_format(double x, int mant_bits, int emin, double max_finite) {
+  if (x == 0.0 || isnan(x) || isinf(x)) return x;
+  int e;
+  frexp(x, &e);            /* |x| = f * 2^e, f in [0.5, 1) */
+  int exp_unbiased = e - 1; /* |x| in [2^(e-1), 2^e) */
+  if (exp_unbiased < emin) exp_unbiased = emin; /* subnormal spacing */
+  double quantum = ldexp(1.0, exp_unbiased - mant_bits);
+  double scaled = x / quantum; /* exact: division by a power of two */
+  /* ties to even on the integer grid */
+  double fl = floor(scaled);
+  double diff = scaled - fl;
+  double r;
+  if (diff > 0.5) {
+    r = fl + 1.0;
+  } else if (diff < 0.5) {
+    r = fl;
+  } else {
+    r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+  }
+  double y = r * quantum;
+  if (fabs(y) > max_finite) return x > 0 ? INFINITY : -INFINITY;
+  return copysign(y, x); /* a value that rounds to zero keeps its sign */
+}
+
+/* bfloat16 largest finite: (2 - 2^-7) * 2^127; binary16: 65504. */
+double oracle_round_bf16(double x) {
+  return round_to_format(x, 7, -126, ldexp(255.0, 120));
+}
+
+double oracle_round_fp16(double x) { return round_to_format(x, 10, -14, 65504.0); }
+
+/* Encode an already-rounded double as a 16-bit pattern. */
+static uint16_t encode_bf16(double y) {
+  float f = (float)y; /* exact: y is representable in binary32 */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if (isnan(y)) return 0x7fc0;
+  return (uint16_t)(u >> 16);
+}
+
+static uint16_t encode_fp16(double y) {
+  if (isnan(y)) return 0x7e00;
+  uint16_t sign = signbit(y) ? 0x8000 : 0;
+  double a = fabs(y);
+  if (isinf(a)) return sign | 0x7c00;
+  if (a == 0.0) return sign;
+  int e;
+  frexp(a, &e);
+  int exp_unbiased = e - 1;
+  if (exp_unbiased < -14) { /* subnormal: a = frac * 2^-24 */
+    return sign | (uint16_t)ldexp(a, 24);
+  }
+  uint16_t frac = (uint16_t)(ldexp(a, 10 - exp_unbiased) - 1024.0);
+  return sign | (uint16_t)((exp_unbiased + 15) << 10) | frac;
+}
+
+void oracle_round_array(const double* x, int64_t n, int dtype, uint16_t* bits_out,
+                        double* rounded_out) {
+  for (int64_t i = 0; i < n; ++i) {
+    double y = dtype == ORACLE_BF16 ? oracle_round_bf16(x[i]) : oracle_round_fp16(x[i]);
+    if (rounded_out) rounded_out[i] = y;
+    if (bits_out) bits_out[i] = dtype == ORACLE_BF16 ? encode_bf16(y) : encode_fp16(y);
+  }
+}
+
+void oracle_decode_array(const uint16_t* bits, int64_t n, int dtype, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_to_f64(bits[i], dtype);
+}
+
+/* ---------------------------------------------------------------------------
+ * Problem description shared by the entry points below.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  const uint16_t* q;       /* [B, Hq, D] */
+  const uint16_t* k_cache; /* [num_blocks, bs, Hkv, D] */
+  const uint16_t* v_cache; /* [num_blocks, bs, Hkv, D] */
+  const int32_t* block_table; /* [B, max_blocks] */
+  const int32_t* context_lens; /* [B] */
+  int B, Hq, Hkv, D, bs, max_blocks;
+  int64_t num_blocks;
+  int dtype;
+  double scale;
+} problem;
+
+static int check_problem(const problem* p) {
+  if (!p->q || !p->k_cache || !p->v_cache || !p->block_table || !p->context_lens)
+    return ORACLE_EINVAL;
+  if (p->B < 0 || p->Hq <= 0 || p->Hkv <= 0 || p->D <= 0 || p->bs <= 0 || p->max_blocks < 0)
+    return ORACLE_EINVAL;
+  if (p->Hq % p->Hkv != 0) return ORACLE_EINVAL;
+  if (p->dtype != ORACLE_BF16 && p->dtype != ORACLE_FP16) return ORACLE_EINVAL;
+  for (int b = 0; b < p->B; ++b) {
+    int L = p->context_lens[b];
+    if (L < 0 || (int64_t)L > (int64_t)p->max_blocks * p->bs) return ORACLE_ERANGE;
+    int pages = (L + p->bs - 1) / p->bs;
+    for (int i = 0; i < pages; ++i) {
+      int32_t blk = p->block_table[(int64_t)b * p->max_blocks + i];
+      if (blk < 0 || (int64_t)blk >= p->num_blocks) return ORACLE_ERANGE;
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* Address of element (token t of sequence b, kv head h, dim 0) in a cache. */
+static const uint16_t* cache_row(const problem* p, const uint16_t* cache, int b, int t, int h) {
+  int32_t blk = p->block_table[(int64_t)b * p->max_blocks + t / p->bs];
+  int off = t % p->bs;
+  return cache + (((int64_t)blk * p->bs + off) * p->Hkv + h) * p->D;
+}
+
+/* Scaled logit s_t = scale * q[b,hq,:] . k_t */
+static double logit(const problem* p, int b, int hq, int h, int t) {
+  const uint16_t* qrow = p->q + ((int64_t)b * p->Hq + hq) * p->D;
+  const uint16_t* krow = cache_row(p, p->k_cache, b, t, h);
+  double dot = 0.0;
+  for (int d = 0; d < p->D; ++d) dot += oracle_to_f64(qrow[d], p->dtype) * oracle_to_f64(krow[d], p->dtype);
+  return p->scale * dot;
+}
+
+/* softmax(s) . V over tokens [t0, t1) of one (b, hq) row.
+ * Writes the normalised output to o[0..D), and returns via *m_out / *l_out
+ * the row maximum and the sum of exp(s - max). Empty ranges give m = -inf,
+ * l = 0 and o = 0. `s` is caller scratch of length >= t1 - t0. */
+static void attend_range(const problem* p, int b, int hq, int t0, int t1, double* s, double* o,
+                         double* m_out, double* l_out) {
+  int G = p->Hq / p->Hkv;
+  int h = hq / G;
+  for (int d = 0; d < p->D; ++d) o[d] = 0.0;
+  if (t1 <= t0) {
+    *m_out = -INFINITY;
+    *l_out = 0.0;
+    return;
+  }
+  double m = -INFINITY;
+  for (int t = t0; t < t1; ++t) {
+    s[t - t0] = logit(p, b, hq, h, t);
+    if (s[t - t0] > m) m = s[t - t0];
+  }
+  double l = 0.0;
+  for (int t = t0; t < t1; ++t) {
+    double w = exp(s[t - t0] - m);
+    l += w;
+    const uint16_t* vrow = cache_row(p, p->v_cache, b, t, h);
+    for (int d = 0; d < p->D; ++d) o[d] += w * oracle_to_f64(vrow[d], p->dtype);
+  }
+  for (int d = 0; d < p->D; ++d) o[d] /= l;
+  *m_out = m;
+  *l_out = l;
+}
+
+/* ---------------------------------------------------------------------------
+ * Row-parallel driver: rows are (b, hq) pairs, handed out in contiguous
+ * slices to plain pthreads. Each row is computed independently.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  const problem* p;
+  const int32_t* rows; /* pairs (b, hq); NULL = all rows in order */
+  int64_t row_begin, row_end;
+  double* out;         /* [n_rows, D] */
+  int status;
+} row_job;
+
+static void* run_rows(void* arg) {
+  row_job* j = (row_job*)arg;
+  const problem* p = j->p;
+  int max_len = p->max_blocks * p->bs;
+  double* s = (double*)malloc(sizeof(double) * (max_len > 0 ? max_len : 1));
+  if (!s) {
+    j->status = ORACLE_ENOMEM;
+    return NULL;
+  }
+  for (int64_t r = j->row_begin; r < j->row_end; ++r) {
+    int b, hq;
+    if (j->rows) {
+      b = j->rows[2 * r];
+      hq = j->rows[2 * r + 1];
+    } else {
+      b = (int)(r / p->Hq);
+      hq = (int)(r % p->Hq);
+    }
+    double m, l;
+    attend_range(p, b, hq, 0, p->context_lens[b], s, j->out + r * p->D, &m, &l);
+  }
+  free(s);
+  j->status = ORACLE_OK;
+  return NULL;
+}
+
+static int run_parallel(const problem* p, const int32_t* rows, int64_t n_rows, double* out,
+                        int num_threads) {
+  if (num_threads < 1) num_threads = 1;
+  if (num_threads > 256) num_threads = 256;
+  if ((int64_t)num_threads > n_rows) num_threads = n_rows > 0 ? (int)n_rows : 1;
+  pthread_t tids[256];
+  row_job jobs[256];
+  int64_t per = (n_rows + num_threads - 1) / num_threads;
+  int started = 0;
+  for (int i = 0; i < num_threads; ++i) {
+    jobs[i].p = p;
+    jobs[i].rows = rows;
+    jobs[i].row_begin = i * per < n_rows ? i * per : n_rows;
+    jobs[i].row_end = (i + 1) * per < n_rows ? (i + 1) * per : n_rows;
+    jobs[i].out = out;
+    jobs[i].status = ORACLE_OK;
+  }
+  if (num_threads == 1) {
+    run_rows(&jobs[0]);
+    return jobs[0].status;
+  }
+  for (int i = 0; i < num_threads; ++i) {
+    if (pthread_create(&tids[i], NULL, run_rows, &jobs[i]) != 0) break;
+    ++started;
+  }
+  for (int i = 0; i < started; ++i) pthread_join(tids[i], NULL);
+  if (started != num_threads) {
+    /* fall back to finishing the remaining slices on this thread */
+    for (int i = started; i < num_threads; ++i) run_rows(&jobs[i]);
+  }
+  for (int i = 0; i < num_threads; ++i)
+    if (jobs[i].status != ORACLE_OK) return jobs[i].status;
+  return ORACLE_OK;
+}
+
+/* Full output: out[B, Hq, D] in double. */
+int oracle_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                        const int32_t* block_table, const int32_t* context_lens, int B, int Hq,
+                        int Hkv, int D, int block_size, int max_blocks, int64_t num_blocks,
+                        int dtype, double scale, double* out, int num_threads) {
+  problem p = {q, k_cache, v_cache, block_table, context_lens, B, Hq, Hkv, D,
+               block_size, max_blocks, num_blocks, dtype, scale};
+  int st = check_problem(&p);
+  if (st != ORACLE_OK) return st;
+  if (!out) return ORACLE_EINVAL;
+  return run_parallel(&p, NULL, (int64_t)B * Hq, out, num_threads);
+}
+
+/* Selected rows only: rows = n_rows pairs (b, hq); out_rows[n_rows, D]. */
+int oracle_paged_decode_rows(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                             const int32_t* block_table, const int32_t* context_lens, int B,
+                             int Hq, int Hkv, int D, int block_size, int max_blocks,
+                             int64_t num_blocks, int dtype, double scale, const int32_t* rows,
+                             int64_t n_rows, double* out_rows, int num_threads) {
+  problem p = {q, k_cache, v_cache, block_table, context_lens, B, Hq, Hkv, D,
+               block_size, max_blocks, num_blocks, dtype, scale};
+  int st = check_problem(&p);
+  if (st != ORACLE_OK) return st;
+  if (!rows || !out_rows || n_rows < 0) return ORACLE_EINVAL;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[2 * r] < 0 || rows[2 * r] >= B || rows[2 * r + 1] < 0 || rows[2 * r + 1] >= Hq)
+      return ORACLE_EINVAL;
+  return run_parallel(&p, rows, n_rows, out_rows, num_threads);
+}
+
+/* Split-K partials. Split s of sequence b covers pages
+ * [s * chunk_pages, (s + 1) * chunk_pages) clipped to the sequence's
+ * ceil(L / bs) pages, i.e. tokens [s * chunk_pages * bs, ...) clipped to L.
+ * For every (b, hq, s < num_splits):
+ *   lse[b, hq, s] = log sum_{t in split} exp(s_t)   (-inf if the split is empty)
+ *   o[b, hq, s, :] = softmax over the split's tokens, applied to V (0 if empty)
+ */
+int oracle_split_partials(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                          const int32_t* block_table, const int32_t* context_lens, int B, int Hq,
+                          int Hkv, int D, int block_size, int max_blocks, int64_t num_blocks,
+                          int dtype, double scale, int chunk_pages, int num_splits,
+                          double* lse, double* o) {
+  problem p = {q, k_cache, v_cache, block_table, context_lens, B, Hq, Hkv, D,
+               block_size, max_blocks, num_blocks, dtype, scale};
+  int st = check_problem(&p);
+  if (st != ORACLE_OK) return st;
+  if (chunk_pages < 1 || num_splits < 1 || !lse || !o) return ORACLE_EINVAL;
+  int max_len = max_blocks * block_size;
+  double* s = (double*)malloc(sizeof(double) * (max_len > 0 ? max_len : 1));
+  if (!s) return ORACLE_ENOMEM;
+  for (int b = 0; b < B; ++b) {
+    int L = context_lens[b];
+    for (int hq = 0; hq < Hq; ++hq) {
+      for (int sp = 0; sp < num_splits; ++sp) {
+        int64_t t0 = (int64_t)sp * chunk_pages * block_size;
+        int64_t t1 = t0 + (int64_t)chunk_pages * block_size;
+        if (t0 > L) t0 = L;
+        if (t1 > L) t1 = L;
+        int64_t idx = ((int64_t)b * Hq + hq) * num_splits + sp;
+        double m, l;
+        attend_range(&p, b, hq, (int)t0, (int)t1, s, o + idx * D, &m, &l);
+        lse[idx] = (l > 0.0) ? m + log(l) : -INFINITY;
+      }
+    }
+  }
+  free(s);
+  return ORACLE_OK;
+}
+
+/* Log-sum-exp merge of split partials, per row r < n_rows:
+ *   M = max_s lse[r, s]
+ *   out[r, :] = sum_s exp(lse[r, s] - M) * o[r, s, :] / sum_s exp(lse[r, s] - M)
+ * Splits with lse = -inf carry weight 0; a row whose splits are all empty
+ * yields zeros. */
+int oracle_lse_merge(const double* lse, const double* o, int64_t n_rows, int num_splits, int D,
+                     double* out) {
+  if (!lse || !o || !out || n_rows < 0 || num_splits < 1 || D < 1) return ORACLE_EINVAL;
+  for (int64_t r = 0; r < n_rows; ++r) {
+    double M = -INFINITY;
+    for (int sp = 0; sp < num_splits; ++sp)
+      if (lse[r * num_splits + sp] > M) M = lse[r * num_splits + sp];
+    double* orow = out + r * D;
+    for (int d = 0; d < D; ++d) orow[d] = 0.0;
+    if (M == -INFINITY) continue;
+    double wsum = 0.0;
+    for (int sp = 0; sp < num_splits; ++sp) {
+      double l = lse[r * num_splits + sp];
+      if (l == -INFINITY) continue;
+      double w = exp(l - M);
+      wsum += w;
+      const double* os = o + (r * num_splits + sp) * D;
+      for (int d = 0; d < D; ++d) orow[d] += w * os[d];
+    }
+    for (int d = 0; d < D; ++d) orow[d] /= wsum;
+  }
+  return ORACLE_OK;
+}

@@ -1,0 +1,323 @@
+"""Pins for the FP64 oracle: checks against things other than the oracle
+itself (arbitrary-precision brute force on a dense layout, closed forms,
+invariances, library routines). Each pin takes the loaded oracle library so
+that the mutation test can run the same pins against broken builds of it.
+
+A pin raises AssertionError when it fails.
+"""
+from __future__ import annotations
+
+import math
+
+import mpmath
+import numpy as np
+import torch
+
+import oracle
+
+BF16, FP16 = oracle.BF16, oracle.FP16
+TORCH_DT = {BF16: torch.bfloat16, FP16: torch.float16}
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# a tiny problem built from a DENSE layout, then scattered into pages
+# ---------------------------------------------------------------------------
+
+class Dense:
+    """Dense per-sequence K/V plus a paged copy of them.
+
+    The dense tensors are the ground truth; the paged cache is produced by
+    scattering them through a random block table (the writer's view), with
+    every slot nobody owns filled with NaN, so reading outside the contract
+    (past L, or an unused table entry) poisons the result.
+    """
+
+    def __init__(self, seed, B, Hq, Hkv, D, bs, lens, dtype=BF16, spare_blocks=5,
+                 q=None, k=None, v=None):
+        g = torch.Generator().manual_seed(seed)
+        rng = np.random.default_rng(seed)
+        dt = TORCH_DT[dtype]
+        Lmax = max(lens) if lens else 1
+        self.B, self.Hq, self.Hkv, self.D, self.bs = B, Hq, Hkv, D, bs
+        self.lens = np.asarray(lens, dtype=np.int32)
+        self.dtype = dtype
+        self.q = q if q is not None else torch.randn(B, Hq, D, generator=g).to(dt)
+        self.k = k if k is not None else torch.randn(B, Lmax, Hkv, D, generator=g).to(dt)
+        self.v = v if v is not None else torch.randn(B, Lmax, Hkv, D, generator=g).to(dt)
+        pages = [(int(L) + bs - 1) // bs for L in lens]
+        self.max_blocks = max(1, max(pages) if pages else 1) + 1
+        nb = sum(pages) + spare_blocks
+        perm = rng.permutation(nb)
+        nan = torch.tensor(float("nan")).to(dt)
+        kc = torch.full((nb, bs, Hkv, D), nan.item(), dtype=dt)
+        vc = torch.full((nb, bs, Hkv, D), nan.item(), dtype=dt)
+        table = np.zeros((B, self.max_blocks), dtype=np.int32)
+        spare = perm[sum(pages):]
+        pos = 0
+        for b in range(B):
+            for p in range(pages[b]):
+                blk = int(perm[pos])
+                pos += 1
+                table[b, p] = blk
+                t0, t1 = p * bs, min(int(lens[b]), (p + 1) * bs)
+                kc[blk, : t1 - t0] = self.k[b, t0:t1]
+                vc[blk, : t1 - t0] = self.v[b, t0:t1]
+            # unused entries point at NaN-filled spare blocks
+            for p in range(pages[b], self.max_blocks):
+                table[b, p] = int(spare[(b + p) % len(spare)]) if len(spare) else 0
+        self.k_cache, self.v_cache, self.table = kc, vc, table
+        self.num_blocks = nb
+        self.scale = 1.0 / math.sqrt(D)
+
+    def args(self):
+        return (_bits(self.q), _bits(self.k_cache), _bits(self.v_cache), self.table,
+                self.lens)
+
+    def run(self, lib, scale=None):
+        return oracle.paged_decode(*self.args(), self.dtype, self.scale if scale is None else scale,
+                                   threads=2, lib=lib)
+
+
+def brute_force(dense: Dense, scale: float, dps: int = 40) -> np.ndarray:
+    """Softmax attention on the dense tensors in mpmath at ``dps`` digits.
+    The exponentials are normalised by their plain sum (no max shift), and
+    each query head hq reads the dense KV head hq // (Hq / Hkv)."""
+    mpmath.mp.dps = dps
+    G = dense.Hq // dense.Hkv
+    q = dense.q.double().numpy()
+    k = dense.k.double().numpy()
+    v = dense.v.double().numpy()
+    out = np.zeros((dense.B, dense.Hq, dense.D))
+    for b in range(dense.B):
+        L = int(dense.lens[b])
+        for hq in range(dense.Hq):
+            if L == 0:
+                continue
+            h = hq // G
+            logits = [mpmath.mpf(scale) * mpmath.fsum(mpmath.mpf(float(x)) * mpmath.mpf(float(y))
+                                                      for x, y in zip(q[b, hq], k[b, t, h]))
+                      for t in range(L)]
+            w = [mpmath.exp(s) for s in logits]
+            Z = mpmath.fsum(w)
+            for d in range(dense.D):
+                out[b, hq, d] = float(mpmath.fsum(w[t] * mpmath.mpf(float(v[b, t, h, d]))
+                                                  for t in range(L)) / Z)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# pins
+# ---------------------------------------------------------------------------
+
+def pin_brute_force(lib):
+    """Oracle == arbitrary-precision dense attention on tiny ragged inputs
+    (GQA, MQA and MHA geometries, both dtypes, both block sizes)."""
+    cases = [
+        (1, 2, 8, 2, 8, 4, [1, 5], BF16),
+        (2, 3, 4, 2, 8, 4, [9, 16, 3], BF16),
+        (3, 2, 6, 1, 4, 8, [17, 8], FP16),
+        (4, 2, 2, 2, 8, 16, [33, 2], BF16),
+    ]
+    for seed, B, Hq, Hkv, D, bs, lens, dt in cases:
+        dn = Dense(seed, B, Hq, Hkv, D, bs, lens, dtype=dt)
+        got = dn.run(lib)
+        ref = brute_force(dn, dn.scale)
+        err = np.max(np.abs(got - ref))
+        assert np.isfinite(got).all(), "oracle read a slot outside the contract"
+        assert err < 1e-12, f"brute force mismatch {err} (case seed {seed})"
+
+
+def pin_closed_forms(lib):
+    """Closed forms: one token returns v_0 exactly; constant V returns V;
+    zero query returns the mean of V (numpy.mean); two tokens follow the
+    logistic form v0 + sigmoid(s1 - s0) (v1 - v0); one logit 4096 above the
+    rest returns that token's v exactly."""
+    # one token
+    dn = Dense(11, 2, 4, 2, 8, 4, [1, 1])
+    got = dn.run(lib)
+    G = 2
+    for b in range(2):
+        for hq in range(4):
+            np.testing.assert_array_equal(got[b, hq], dn.v[b, 0, hq // G].double().numpy())
+    # constant V across tokens
+    dn = Dense(12, 1, 4, 2, 8, 4, [13])
+    dn.v[:] = dn.v[:, :1]
+    dn = Dense(12, 1, 4, 2, 8, 4, [13], q=dn.q, k=dn.k, v=dn.v)
+    got = dn.run(lib)
+    for hq in range(4):
+        ref = dn.v[0, 0, hq // 2].double().numpy()
+        assert np.max(np.abs(got[0, hq] - ref)) < 1e-13, "constant V"
+    # zero query: uniform weights, mean of V over the context
+    dn = Dense(13, 2, 4, 2, 8, 4, [7, 10])
+    dn.q.zero_()
+    got = dn.run(lib)
+    for b in range(2):
+        L = int(dn.lens[b])
+        for hq in range(4):
+            ref = np.mean(dn.v[b, :L, hq // 2].double().numpy(), axis=0)
+            assert np.max(np.abs(got[b, hq] - ref)) < 1e-13, "zero query != mean(V)"
+    # two tokens, exact integer logits: q = (2, 1, 0, ...), k0 = (1, 0, ..), k1 = (0, 3, ..)
+    # scale 0.5 -> s0 = 1, s1 = 1.5
+    D = 8
+    q = torch.zeros(1, 1, D)
+    q[0, 0, :2] = torch.tensor([2.0, 1.0])
+    k = torch.zeros(1, 2, 1, D)
+    k[0, 0, 0, 0] = 1.0
+    k[0, 1, 0, 1] = 3.0
+    v = torch.randn(1, 2, 1, D, generator=torch.Generator().manual_seed(5))
+    dn = Dense(14, 1, 1, 1, D, 4, [2], q=q.bfloat16(), k=k.bfloat16(), v=v.bfloat16())
+    got = dn.run(lib, scale=0.5)
+    sig = 1.0 / (1.0 + math.exp(-(1.5 - 1.0)))
+    v0 = dn.v[0, 0, 0].double().numpy()
+    v1 = dn.v[0, 1, 0].double().numpy()
+    ref = v0 + sig * (v1 - v0)
+    assert np.max(np.abs(got[0, 0] - ref)) < 1e-14, "two-token logistic form"
+    # one dominant logit
+    q = torch.zeros(1, 2, D)
+    q[0, :, 0] = 64.0
+    k = torch.zeros(1, 9, 1, D)
+    k[0, 6, 0, 0] = 64.0
+    v = torch.randn(1, 9, 1, D, generator=torch.Generator().manual_seed(6))
+    dn = Dense(15, 1, 2, 1, D, 4, [9], q=q.bfloat16(), k=k.bfloat16(), v=v.bfloat16())
+    got = dn.run(lib, scale=1.0)
+    for hq in range(2):
+        np.testing.assert_array_equal(got[0, hq], dn.v[0, 6, 0].double().numpy())
+
+
+def pin_block_table_invariance(lib):
+    """Relabelling physical blocks (cache rows permuted, table remapped) and
+    re-paging the same logical K/V with another block size leave the FP64
+    result bit-identical."""
+    dn = Dense(21, 3, 8, 2, 16, 4, [13, 4, 9])
+    base = dn.run(lib)
+    rng = np.random.default_rng(3)
+    perm = rng.permutation(dn.num_blocks)
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(len(perm))
+    kc = dn.k_cache.clone()
+    vc = dn.v_cache.clone()
+    kc[torch.from_numpy(perm)] = dn.k_cache
+    vc[torch.from_numpy(perm)] = dn.v_cache
+    table = perm[dn.table].astype(np.int32)
+    got = oracle.paged_decode(_bits(dn.q), _bits(kc), _bits(vc), table, dn.lens, BF16, dn.scale,
+                              threads=2, lib=lib)
+    np.testing.assert_array_equal(got, base)
+    for bs in (1, 2, 8, 16):
+        dn2 = Dense(21, 3, 8, 2, 16, bs, [13, 4, 9], q=dn.q, k=dn.k, v=dn.v)
+        np.testing.assert_array_equal(dn2.run(lib), base)
+
+
+def pin_gqa_reductions(lib):
+    """GQA equals MHA over K/V heads repeated G times (torch.repeat_interleave);
+    MHA equals independent single-head problems; duplicated query heads in a
+    group give identical rows."""
+    B, Hq, Hkv, D, bs, lens = 2, 8, 2, 8, 4, [11, 6]
+    dn = Dense(31, B, Hq, Hkv, D, bs, lens)
+    gqa = dn.run(lib)
+    G = Hq // Hkv
+    mha = Dense(31, B, Hq, Hq, D, bs, lens, q=dn.q, k=dn.k.repeat_interleave(G, dim=2),
+                v=dn.v.repeat_interleave(G, dim=2))
+    np.testing.assert_array_equal(mha.run(lib), gqa)
+    for hq in range(Hq):
+        one = Dense(31, B, 1, 1, D, bs, lens, q=dn.q[:, hq:hq + 1].contiguous(),
+                    k=mha.k[:, :, hq:hq + 1].contiguous(), v=mha.v[:, :, hq:hq + 1].contiguous())
+        np.testing.assert_array_equal(one.run(lib)[:, 0], gqa[:, hq])
+    q = dn.q.clone()
+    q[:, 1] = q[:, 0]
+    dup = Dense(31, B, Hq, Hkv, D, bs, lens, q=q, k=dn.k, v=dn.v).run(lib)
+    np.testing.assert_array_equal(dup[:, 0], dup[:, 1])
+
+
+def pin_split_merge(lib):
+    """Split-K: the LSE merge of the per-split partials equals the unsplit
+    result for every split count 1..64; one split is the identity; each
+    split's lse equals log(sum exp(s_t)) computed in mpmath."""
+    lens = [37, 64, 1, 20]
+    dn = Dense(41, 4, 4, 2, 8, 1, lens)  # block size 1: every token its own page
+    full = dn.run(lib)
+    q, k, v, bt, cl = dn.args()
+    for S in range(1, 65):
+        chunk = max(1, -(-max(lens) // S))
+        lse, o = oracle.split_partials(q, k, v, bt, cl, BF16, dn.scale, chunk, S, lib=lib)
+        merged = oracle.lse_merge(lse, o, lib=lib)
+        assert np.max(np.abs(merged - full)) < 1e-13, f"split-merge S={S}"
+        if S == 1:
+            np.testing.assert_array_equal(o[:, :, 0], full)
+    # lse of a split against mpmath
+    lse, o = oracle.split_partials(q, k, v, bt, cl, BF16, dn.scale, 10, 7, lib=lib)
+    mpmath.mp.dps = 40
+    qd, kd = dn.q.double().numpy(), dn.k.double().numpy()
+    for b, hq, s in [(0, 1, 2), (1, 3, 6), (3, 0, 1), (2, 2, 0), (2, 2, 1)]:
+        t0, t1 = s * 10, min(lens[b], (s + 1) * 10)
+        if t1 <= t0:
+            assert lse[b, hq, s] == -np.inf and not o[b, hq, s].any()
+            continue
+        ref = mpmath.log(mpmath.fsum(
+            mpmath.exp(mpmath.mpf(dn.scale) * mpmath.fsum(
+                mpmath.mpf(float(a)) * mpmath.mpf(float(c)) for a, c in zip(qd[b, hq], kd[b, t, hq // 2])))
+            for t in range(t0, t1)))
+        assert abs(lse[b, hq, s] - float(ref)) < 1e-12, "split lse"
+
+
+def pin_merge_special_cases(lib):
+    """Merge: all-empty rows give zeros; a single non-empty split returns its
+    o exactly; two splits with equal lse give the plain average; weights
+    follow exp(lse) (a split 1000 below the max contributes nothing)."""
+    rng = np.random.default_rng(7)
+    o = rng.standard_normal((4, 3, 5))
+    lse = np.full((4, 3), -np.inf)
+    lse[1, 2] = 3.0
+    lse[2, 0] = lse[2, 1] = -1.5
+    lse[3, 0], lse[3, 1] = 2.0, -998.0
+    out = oracle.lse_merge(lse, o, lib=lib)
+    assert not out[0].any()
+    np.testing.assert_array_equal(out[1], o[1, 2])
+    assert np.max(np.abs(out[2] - 0.5 * (o[2, 0] + o[2, 1]))) < 1e-15
+    np.testing.assert_array_equal(out[3], o[3, 0])
+    # general weights against mpmath: sum_s e^lse_s o_s / sum_s e^lse_s
+    lse = rng.standard_normal((2, 6)) * 30
+    o = rng.standard_normal((2, 6, 5))
+    out = oracle.lse_merge(lse, o, lib=lib)
+    mpmath.mp.dps = 40
+    for r in range(2):
+        w = [mpmath.exp(mpmath.mpf(float(x))) for x in lse[r]]
+        Z = mpmath.fsum(w)
+        for d in range(5):
+            ref = float(mpmath.fsum(w[s] * mpmath.mpf(float(o[r, s, d])) for s in range(6)) / Z)
+            assert abs(out[r, d] - ref) < 1e-13, "merge weights"
+
+
+def pin_dtype_conversions(lib):
+    """Exact decode of all 65536 bf16 and fp16 patterns equals torch's
+    upcast; rounding from double equals numpy's float64 -> float16 and
+    torch's float32 -> bfloat16 conversions (both round to nearest even),
+    and bf16 rounding of a double just above a tie rounds up (no double
+    rounding through float32)."""
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    for dt, tdt in ((BF16, torch.bfloat16), (FP16, torch.float16)):
+        got = oracle.decode(allbits, dt, lib=lib)
+        ref = torch.from_numpy(allbits.view(np.int16)).view(tdt).double().numpy()
+        nan = np.isnan(ref)
+        assert np.array_equal(np.isnan(got), nan)
+        np.testing.assert_array_equal(got[~nan], ref[~nan])
+    rng = np.random.default_rng(9)
+    x = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-9, 5, 20000),
+                        [0.0, -0.0, 65504.0, 65520.0, 70000.0, 6e-8, 3e-8, 2.9e-8]])
+    bits16, r16 = oracle.round_to(x, FP16, lib=lib)
+    np.testing.assert_array_equal(bits16, x.astype(np.float16).view(np.uint16))
+    xf = x.astype(np.float32).astype(np.float64)  # values exactly representable in binary32
+    bitsb, rb = oracle.round_to(xf, BF16, lib=lib)
+    ref = torch.from_numpy(xf.astype(np.float32)).bfloat16().view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(bitsb, ref)
+    # ties and the double-rounding trap
+    _, r = oracle.round_to(np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, 1 + 2.0 ** -8 + 2.0 ** -30]),
+                           BF16, lib=lib)
+    np.testing.assert_array_equal(r, [1.0, 1 + 2.0 ** -6, 1 + 2.0 ** -7])
+
+
+ALL_PINS = [pin_brute_force, pin_closed_forms, pin_block_table_invariance, pin_gqa_reductions,
+            pin_split_merge, pin_merge_special_cases, pin_dtype_conversions]
