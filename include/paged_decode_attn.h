@@ -1,0 +1,188 @@
+/*
+ * paged_decode_attn.h - C ABI of the GB300 (sm_103a) paged MQA/GQA
+ * decode-attention library.
+ *
+ * The operation (Loom Kernels landing page, "Supported now": "Paged MQA/GQA
+ * decode", GQA packing + local split-K/LSE; benchmark page, "Current
+ * qualified results": the D128 long-context split-K/LSE path). For every
+ * sequence b < batch and query head hq < Hq, with G = Hq / Hkv, kv head
+ * h = hq / G and L = context_lens[b]:
+ *
+ *   k_t = k_cache[block_table[b, t / block_size], t % block_size, h, :]   t < L
+ *   v_t = v_cache[block_table[b, t / block_size], t % block_size, h, :]
+ *   out[b, hq, :] = sum_t softmax_t(scale * q[b, hq, :] . k_t) * v_t
+ *
+ * The G query heads of one kv head are processed together against a single
+ * read of that head's K/V pages (GQA packing). Long contexts are cut along
+ * the sequence into page-aligned splits (split-K); each split yields a
+ * normalised partial output and its log-sum-exp, and the splits are merged
+ * by log-sum-exp weighting. Accumulation is in fp32.
+ *
+ * Conventions (Loom Kernels landing page, "Architecture": one versioned,
+ * panic-contained framework boundary; borrowed streams and memory; explicit
+ * layouts, aliasing rules and capabilities):
+ *   - every function returns a pda_status (or a value documented below) and
+ *     never throws, aborts or exits; on failure the reason is kept in a
+ *     thread-local string returned by paged_decode_attn_last_error();
+ *   - all tensors are caller-owned DEVICE memory, borrowed for the duration
+ *     of the launch; the handle owns only its split-K workspace;
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream); run calls are asynchronous on it and never synchronise,
+ *     allocate or read device memory from the host;
+ *   - layouts are dense and row-major exactly as written below; element
+ *     counts are int64-safe;
+ *   - only `out` is written; it must not overlap q, k_cache, v_cache,
+ *     block_table or context_lens (PDA_EALIAS). Repeated entries inside
+ *     block_table (shared prefix pages) are legal;
+ *   - one handle must not be used by two streams at the same time: the
+ *     split-K workspace is per handle.
+ *
+ * Preconditions the host cannot check (device-resident values), and what
+ * happens when they are broken:
+ *   - 0 <= context_lens[b] <= max_blocks * block_size: larger values are
+ *     clamped to max_blocks * block_size, negative values act as 0;
+ *   - 0 <= block_table[b, p] < num_blocks for p < ceil(L / block_size):
+ *     out-of-range ids read zeros (the tensor-memory-access unit bounds-checks
+ *     every page fetch); entries at p >= ceil(L / block_size) are never read;
+ *   - a row with L == 0 is written as zeros.
+ *   paged_decode_attn_validate() reports broken preconditions without
+ *   faulting.
+ */
+#ifndef PAGED_DECODE_ATTN_H
+#define PAGED_DECODE_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PDA_ABI_VERSION 1
+
+typedef enum {
+  PDA_OK = 0,
+  PDA_EINVAL = -1,       /* bad argument (null pointer, shape, size limit) */
+  PDA_EUNSUPPORTED = -2, /* valid but not built: head_dim, group size, block size */
+  PDA_ENOMEM = -3,       /* workspace allocation failed in create */
+  PDA_ECUDA = -4,        /* a CUDA runtime/driver call failed (message says which) */
+  PDA_EALIAS = -5,       /* out overlaps an input */
+  PDA_EDEVICE = -6       /* the device reported an error word (see check_device_error) */
+} pda_status;
+
+typedef enum {
+  PDA_BF16 = 0,
+  PDA_FP16 = 1,
+  PDA_F32 = 2 /* output only: fp32 out for accuracy checks */
+} pda_dtype;
+
+/* Fixed at create time. */
+typedef struct {
+  int num_q_heads;        /* Hq; a multiple of num_kv_heads */
+  int num_kv_heads;       /* Hkv; G = Hq / Hkv must be 1, 2, 4 or 8 */
+  int head_dim;           /* D; 128 */
+  int block_size;         /* tokens per page; 16 or 32 */
+  int dtype;              /* pda_dtype of q, k_cache, v_cache: PDA_BF16 or PDA_FP16 */
+  int max_batch;          /* largest batch a run may pass (1 .. 65535) */
+  int max_blocks_per_seq; /* largest max_blocks a run may pass */
+  int max_splits;         /* largest split count (1 .. 64); sizes the workspace */
+  int device;             /* CUDA device ordinal the handle and its launches use */
+} pda_config;
+
+typedef struct pda_handle_s* pda_handle;
+
+/* PDA_ABI_VERSION of the loaded library. */
+int paged_decode_attn_abi_version(void);
+
+/* Thread-local description of the last failure on this thread ("" if none).
+ * The pointer stays valid until the next call on the same thread. */
+const char* paged_decode_attn_last_error(void);
+
+/* Validate `cfg`, select cfg->device, and allocate the handle plus its
+ * device workspace: max_batch * Hq * max_splits * (head_dim + 1) floats of
+ * split partials, and a small error-word area, zeroed.
+ * Returns PDA_OK and stores the handle in *out_handle, or an error (and
+ * *out_handle = NULL). Configuration errors are reported before any CUDA call. */
+int paged_decode_attn_create(const pda_config* cfg, pda_handle* out_handle);
+
+/* Release the handle and its workspace. NULL is a no-op. The caller must
+ * make sure no launch using the handle is still running. */
+void paged_decode_attn_destroy(pda_handle handle);
+
+/* Paged decode attention for one decode step.
+ *   q            [batch, Hq, D]                          cfg->dtype
+ *   k_cache      [num_blocks, block_size, Hkv, D]        cfg->dtype
+ *   v_cache      [num_blocks, block_size, Hkv, D]        cfg->dtype
+ *   block_table  [batch, max_blocks]                     int32
+ *   context_lens [batch]                                 int32
+ *   out          [batch, Hq, D]                          cfg->dtype
+ * batch <= cfg->max_batch (0 is a no-op), max_blocks <= cfg->max_blocks_per_seq,
+ * num_blocks * block_size < 2^31; q, caches and out 16-byte aligned.
+ * scale multiplies q . k (typically 1/sqrt(D)); it must be finite.
+ * The split count comes from the built-in heuristic (paged_decode_attn_plan). */
+int paged_decode_attn_run(pda_handle handle, const void* q, const void* k_cache,
+                          const void* v_cache, const int32_t* block_table,
+                          const int32_t* context_lens, int batch, int max_blocks,
+                          int64_t num_blocks, float scale, void* out, void* stream);
+
+/* As paged_decode_attn_run, plus:
+ *   num_splits            0 = heuristic; otherwise the split count to use
+ *                         (1 .. cfg->max_splits, clipped to the page count
+ *                         implied by max_context_len_hint)
+ *   max_context_len_hint  0 = max_blocks * block_size; otherwise the length
+ *                         the planner sizes splits for. A longer sequence is
+ *                         still exact: its last split takes the remaining
+ *                         pages (less balanced, never wrong).
+ *   out_dtype             PDA_F32 writes fp32 `out`; -1 or cfg->dtype writes
+ *                         the input dtype (round to nearest even). */
+int paged_decode_attn_run_ex(pda_handle handle, const void* q, const void* k_cache,
+                             const void* v_cache, const int32_t* block_table,
+                             const int32_t* context_lens, int batch, int max_blocks,
+                             int64_t num_blocks, float scale, void* out, void* stream,
+                             int num_splits, int max_context_len_hint, int out_dtype);
+
+/* The split plan the heuristic picks (host only, no CUDA call): for a
+ * problem of `batch` sequences, `max_blocks` table columns and an optional
+ * length hint (0 = max_blocks * block_size), on a GPU with `num_sms` SMs.
+ * *num_splits receives S (1 .. cfg->max_splits) and *chunk_pages the pages
+ * each split covers; sequence b then uses min(S, ceil(ceil(L_b / block_size)
+ * / chunk_pages)) splits. */
+int paged_decode_attn_plan(const pda_config* cfg, int num_sms, int batch, int max_blocks,
+                           int max_context_len_hint, int* num_splits, int* chunk_pages);
+
+/* Log-sum-exp merge of split partials (the split-K merge step on its own,
+ * e.g. for partials computed elsewhere):
+ *   partial_o   [rows, num_splits, head_dim] fp32, each split's normalised output
+ *   partial_lse [rows, num_splits] fp32, natural-log sum of exp(scaled logits)
+ *               of each split; -inf marks an empty split (weight 0)
+ *   out         [rows, head_dim] in out_dtype (PDA_BF16, PDA_FP16 or PDA_F32)
+ *   out[r] = sum_s exp(lse[r,s] - M) o[r,s] / sum_s exp(lse[r,s] - M),
+ *   M = max_s lse[r,s]; a row of all-empty splits is written as zeros.
+ * head_dim must be a multiple of 4 (<= 512), num_splits 1 .. 64; device pointers,
+ * asynchronous on `stream`. No handle needed. */
+int paged_decode_attn_merge(const float* partial_o, const float* partial_lse, int rows,
+                            int num_splits, int head_dim, void* out, int out_dtype,
+                            int device, void* stream);
+
+/* Opt-in precondition check on device-resident inputs (asynchronous on
+ * `stream`): flags context_lens[b] outside [0, max_blocks * block_size] and
+ * block_table entries outside [0, num_blocks) among the pages a sequence
+ * reads. It records the first problem found in the handle's device error
+ * word; it never traps. Read it with paged_decode_attn_check_device_error. */
+int paged_decode_attn_validate(pda_handle handle, const int32_t* block_table,
+                               const int32_t* context_lens, int batch, int max_blocks,
+                               int64_t num_blocks, void* stream);
+
+/* Synchronise `stream`, read and clear the handle's device error word.
+ * *code receives 0 (no error) or a nonzero code:
+ *   1 = context length out of range, 2 = block id out of range (validator);
+ *   3 = a pipeline wait inside a kernel gave up after its time limit.
+ * *detail receives the sequence index (codes 1, 2) or the split index (3).
+ * Returns PDA_OK, or PDA_ECUDA if the synchronisation or the copy failed. */
+int paged_decode_attn_check_device_error(pda_handle handle, int* code, int* detail,
+                                         void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_DECODE_ATTN_H */

@@ -1,0 +1,238 @@
+"""ctypes binding of the C ABI in include/paged_decode_attn.h.
+
+Argument marshalling only: torch tensors are checked for dtype, shape,
+device and contiguity and passed as raw device pointers together with the
+current CUDA stream. Every step of the computation runs in the CUDA library;
+there is no fallback. If the library is missing the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+PDA_OK, PDA_EINVAL, PDA_EUNSUPPORTED, PDA_ENOMEM, PDA_ECUDA, PDA_EALIAS, PDA_EDEVICE = (
+    0, -1, -2, -3, -4, -5, -6)
+PDA_BF16, PDA_FP16, PDA_F32 = 0, 1, 2
+ABI_VERSION = 1
+
+_STATUS_NAMES = {0: "PDA_OK", -1: "PDA_EINVAL", -2: "PDA_EUNSUPPORTED", -3: "PDA_ENOMEM",
+                 -4: "PDA_ECUDA", -5: "PDA_EALIAS", -6: "PDA_EDEVICE"}
+_DT = {torch.bfloat16: PDA_BF16, torch.float16: PDA_FP16, torch.float32: PDA_F32}
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpaged_decode_attn.so")
+
+# Every function the header declares (tests check the library exports them).
+EXPORTS = [
+    "paged_decode_attn_abi_version",
+    "paged_decode_attn_last_error",
+    "paged_decode_attn_create",
+    "paged_decode_attn_destroy",
+    "paged_decode_attn_run",
+    "paged_decode_attn_run_ex",
+    "paged_decode_attn_plan",
+    "paged_decode_attn_merge",
+    "paged_decode_attn_validate",
+    "paged_decode_attn_check_device_error",
+]
+
+
+class PDAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("block_size", ctypes.c_int),
+                ("dtype", ctypes.c_int), ("max_batch", ctypes.c_int),
+                ("max_blocks_per_seq", ctypes.c_int), ("max_splits", ctypes.c_int),
+                ("device", ctypes.c_int)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load the CUDA library (built by ``paged_gqa_decode_attention_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"CUDA library {p} is missing: run paged_gqa_decode_attention_gb300.build.build()")
+        lib = ctypes.CDLL(p)
+        P, I, I64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        lib.paged_decode_attn_abi_version.argtypes = []
+        lib.paged_decode_attn_abi_version.restype = I
+        lib.paged_decode_attn_last_error.argtypes = []
+        lib.paged_decode_attn_last_error.restype = ctypes.c_char_p
+        lib.paged_decode_attn_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(P)]
+        lib.paged_decode_attn_create.restype = I
+        lib.paged_decode_attn_destroy.argtypes = [P]
+        lib.paged_decode_attn_destroy.restype = None
+        lib.paged_decode_attn_run.argtypes = [P, P, P, P, P, P, I, I, I64, F, P, P]
+        lib.paged_decode_attn_run.restype = I
+        lib.paged_decode_attn_run_ex.argtypes = [P, P, P, P, P, P, I, I, I64, F, P, P, I, I, I]
+        lib.paged_decode_attn_run_ex.restype = I
+        lib.paged_decode_attn_plan.argtypes = [ctypes.POINTER(Config), I, I, I, I,
+                                               ctypes.POINTER(I), ctypes.POINTER(I)]
+        lib.paged_decode_attn_plan.restype = I
+        lib.paged_decode_attn_merge.argtypes = [P, P, I, I, I, P, I, I, P]
+        lib.paged_decode_attn_merge.restype = I
+        lib.paged_decode_attn_validate.argtypes = [P, P, P, I, I, I64, P]
+        lib.paged_decode_attn_validate.restype = I
+        lib.paged_decode_attn_check_device_error.argtypes = [P, ctypes.POINTER(I),
+                                                             ctypes.POINTER(I), P]
+        lib.paged_decode_attn_check_device_error.restype = I
+        if lib.paged_decode_attn_abi_version() != ABI_VERSION:
+            raise RuntimeError("ABI version mismatch between binding and library")
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(lib, status: int):
+    if status != PDA_OK:
+        raise PDAError(status, lib.paged_decode_attn_last_error().decode())
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev_ptr(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def make_config(num_q_heads: int, num_kv_heads: int, head_dim: int = 128, block_size: int = 16,
+                dtype=torch.bfloat16, max_batch: int = 256, max_blocks_per_seq: int = 4096,
+                max_splits: int = 64, device: int = 0) -> Config:
+    return Config(num_q_heads, num_kv_heads, head_dim, block_size, _DT[dtype], max_batch,
+                  max_blocks_per_seq, max_splits, device)
+
+
+def plan(config: Config, num_sms: int, batch: int, max_blocks: int,
+         max_context_len_hint: int = 0) -> tuple[int, int]:
+    """(num_splits, chunk_pages) the split heuristic picks (host only)."""
+    lib = load_library()
+    s, c = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib, lib.paged_decode_attn_plan(ctypes.byref(config), num_sms, batch, max_blocks,
+                                           max_context_len_hint, ctypes.byref(s),
+                                           ctypes.byref(c)))
+    return s.value, c.value
+
+
+class PagedDecodeAttention:
+    """One library handle: fixed geometry, owns the split-K workspace."""
+
+    def __init__(self, num_q_heads: int, num_kv_heads: int, head_dim: int = 128,
+                 block_size: int = 16, dtype=torch.bfloat16, max_batch: int = 256,
+                 max_blocks_per_seq: int = 4096, max_splits: int = 64, device=None):
+        self.lib = load_library()
+        if device is None:
+            device = torch.cuda.current_device()
+        if isinstance(device, torch.device):
+            device = device.index if device.index is not None else torch.cuda.current_device()
+        self.device = int(device)
+        self.dtype = dtype
+        self.config = make_config(num_q_heads, num_kv_heads, head_dim, block_size, dtype,
+                                  max_batch, max_blocks_per_seq, max_splits, self.device)
+        h = ctypes.c_void_p(None)
+        _check(self.lib, self.lib.paged_decode_attn_create(ctypes.byref(self.config),
+                                                           ctypes.byref(h)))
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            self.lib.paged_decode_attn_destroy(self.handle)
+            self.handle = ctypes.c_void_p(None)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def run(self, q, k_cache, v_cache, block_table, context_lens, scale: float | None = None,
+            out=None, num_splits: int = 0, max_context_len_hint: int = 0, out_dtype=None,
+            stream=None):
+        """out[B, Hq, D] = paged decode attention; asynchronous on ``stream``
+        (default: torch's current stream)."""
+        c = self.config
+        B = q.shape[0]
+        if scale is None:
+            scale = 1.0 / math.sqrt(c.head_dim)
+        if out_dtype is None:
+            out_dtype = self.dtype
+        if out is None:
+            out = torch.empty((B, c.num_q_heads, c.head_dim), dtype=out_dtype, device=q.device)
+        args = (self.handle,
+                _dev_ptr(q, "q", self.dtype), _dev_ptr(k_cache, "k_cache", self.dtype),
+                _dev_ptr(v_cache, "v_cache", self.dtype),
+                _dev_ptr(block_table, "block_table", torch.int32),
+                _dev_ptr(context_lens, "context_lens", torch.int32),
+                B, block_table.shape[1], k_cache.shape[0], float(scale),
+                _dev_ptr(out, "out", out_dtype), _stream_ptr(stream),
+                int(num_splits), int(max_context_len_hint), _DT[out_dtype])
+        _check(self.lib, self.lib.paged_decode_attn_run_ex(*args))
+        return out
+
+    def run_raw(self, q_ptr: int, k_ptr: int, v_ptr: int, table_ptr: int, lens_ptr: int,
+                batch: int, max_blocks: int, num_blocks: int, scale: float, out_ptr: int,
+                stream: int = 0) -> int:
+        """paged_decode_attn_run on raw device pointers; returns the status."""
+        return self.lib.paged_decode_attn_run(self.handle, q_ptr, k_ptr, v_ptr, table_ptr,
+                                              lens_ptr, batch, max_blocks, num_blocks,
+                                              float(scale), out_ptr, stream)
+
+    def validate(self, block_table, context_lens, num_blocks: int, stream=None):
+        B = context_lens.shape[0]
+        _check(self.lib, self.lib.paged_decode_attn_validate(
+            self.handle, _dev_ptr(block_table, "block_table", torch.int32),
+            _dev_ptr(context_lens, "context_lens", torch.int32), B, block_table.shape[1],
+            int(num_blocks), _stream_ptr(stream)))
+
+    def check_device_error(self, stream=None) -> tuple[int, int]:
+        code, detail = ctypes.c_int(0), ctypes.c_int(0)
+        _check(self.lib, self.lib.paged_decode_attn_check_device_error(
+            self.handle, ctypes.byref(code), ctypes.byref(detail), _stream_ptr(stream)))
+        return code.value, detail.value
+
+
+def merge(partial_o: torch.Tensor, partial_lse: torch.Tensor, out_dtype=torch.float32,
+          out=None, stream=None) -> torch.Tensor:
+    """LSE merge: partial_o [rows, S, D] fp32, partial_lse [rows, S] fp32
+    (natural log, -inf = empty split) -> out [rows, D]."""
+    lib = load_library()
+    rows, S, D = partial_o.shape
+    if out is None:
+        out = torch.empty((rows, D), dtype=out_dtype, device=partial_o.device)
+    dev = partial_o.device.index if partial_o.device.index is not None else 0
+    _check(lib, lib.paged_decode_attn_merge(
+        _dev_ptr(partial_o, "partial_o", torch.float32),
+        _dev_ptr(partial_lse, "partial_lse", torch.float32), rows, S, D,
+        _dev_ptr(out, "out", out_dtype), _DT[out_dtype], dev, _stream_ptr(stream)))
+    return out

@@ -1,0 +1,426 @@
+// C ABI of the paged decode-attention library: argument checks, the split
+// planner, the per-handle workspace and TMA descriptor cache, and the two
+// launches (partial, merge). Nothing here throws across the ABI.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "paged_decode_attn.h"
+#include "pda_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+int cuda_fail(const char* what, cudaError_t e) {
+  return fail(PDA_ECUDA, std::string(what) + ": " + cudaGetErrorName(e) + " (" +
+                             cudaGetErrorString(e) + ")");
+}
+
+// Planner cost constants, in token-equivalents of one CTA's streaming time:
+// the fixed cost of a CTA (launch, barrier set-up, q load, the final merge of
+// its warps) and of the separate merge launch.
+constexpr int kOverheadTokens = 64;
+constexpr int kMergeTokens = 96;
+
+int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+// Shape checks shared by create and plan; returns PDA_OK or an error.
+int check_config(const pda_config* c) {
+  if (!c) return fail(PDA_EINVAL, "config is NULL");
+  if (c->num_q_heads <= 0 || c->num_kv_heads <= 0)
+    return fail(PDA_EINVAL, "num_q_heads and num_kv_heads must be positive");
+  if (c->num_q_heads % c->num_kv_heads != 0)
+    return fail(PDA_EINVAL, "num_q_heads must be a multiple of num_kv_heads");
+  if (c->num_kv_heads > 65535) return fail(PDA_EINVAL, "num_kv_heads > 65535");
+  const int G = c->num_q_heads / c->num_kv_heads;
+  if (c->head_dim <= 0 || c->block_size <= 0)
+    return fail(PDA_EINVAL, "head_dim and block_size must be positive");
+  if (c->dtype != PDA_BF16 && c->dtype != PDA_FP16)
+    return fail(PDA_EINVAL, "dtype must be PDA_BF16 or PDA_FP16");
+  if (c->max_batch < 1 || c->max_batch > 65535)
+    return fail(PDA_EINVAL, "max_batch must be in [1, 65535]");
+  if (c->max_blocks_per_seq < 1) return fail(PDA_EINVAL, "max_blocks_per_seq must be >= 1");
+  if ((int64_t)c->max_blocks_per_seq * c->block_size > INT_MAX)
+    return fail(PDA_EINVAL, "max_blocks_per_seq * block_size overflows int32");
+  if (c->max_splits < 1 || c->max_splits > pda::kMaxSplits)
+    return fail(PDA_EINVAL, "max_splits must be in [1, 64]");
+  if (c->device < 0) return fail(PDA_EINVAL, "device must be >= 0");
+  if (c->head_dim != pda::kHeadDim) return fail(PDA_EUNSUPPORTED, "head_dim must be 128");
+  if (!pda::partial_supported(G, c->block_size, c->dtype))
+    return fail(PDA_EUNSUPPORTED,
+                "unsupported geometry: group size must be 1, 2, 4 or 8 and block_size 16 or 32");
+  return PDA_OK;
+}
+
+void plan_splits(const pda_config& c, int num_sms, int ctas_per_sm, int batch, int max_blocks,
+                 int hint, int forced, int* S_out, int* chunk_out) {
+  const int bs = c.block_size;
+  int64_t max_len = (int64_t)max_blocks * bs;
+  if (hint > 0 && hint < max_len) max_len = hint;
+  const int max_pages = max_len > 0 ? ceil_div(max_len, bs) : 1;
+  const int cap = c.max_splits < max_pages ? c.max_splits : max_pages;
+  int S = 1;
+  if (forced > 0) {
+    S = forced < cap ? forced : cap;
+  } else {
+    const int64_t base = (int64_t)(batch > 0 ? batch : 1) * c.num_kv_heads;
+    const int64_t slots = (int64_t)(num_sms > 0 ? num_sms : 1) * (ctas_per_sm > 0 ? ctas_per_sm : 1);
+    double best = INFINITY;
+    for (int s = 1; s <= cap; ++s) {
+      const int chunk = ceil_div(max_pages, s);
+      const int s_eff = ceil_div(max_pages, chunk);
+      if (s_eff != s) continue;  // identical to a smaller split count
+      const int64_t waves = (base * s_eff + slots - 1) / slots;
+      const double cost = (double)waves * ((double)chunk * bs + kOverheadTokens) +
+                          (s_eff > 1 ? kMergeTokens : 0);
+      if (cost < best * (1.0 - 1e-9)) {
+        best = cost;
+        S = s_eff;
+      }
+    }
+  }
+  const int chunk = ceil_div(max_pages, S);
+  *S_out = ceil_div(max_pages, chunk);
+  *chunk_out = chunk;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A [num_blocks * block_size, Hkv * 128] view of a cache, loaded as boxes of
+// 64 dims x block_size rows with 128-byte swizzle.
+int encode_cache_map(CUtensorMap* m, const void* base, int Hkv, int bs, int64_t num_blocks) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return fail(PDA_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {(cuuint64_t)Hkv * pda::kHeadDim, (cuuint64_t)num_blocks * bs};
+  cuuint64_t strides[1] = {(cuuint64_t)Hkv * pda::kHeadDim * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)bs};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(PDA_ECUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
+  return PDA_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return na && nb && a0 < b0 + nb && b0 < a0 + na;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Makes `dev` current for the scope and restores the caller's device.
+struct DeviceGuard {
+  int prev = -1;
+  cudaError_t err = cudaSuccess;
+  explicit DeviceGuard(int dev) {
+    err = cudaGetDevice(&prev);
+    if (err == cudaSuccess && prev != dev) err = cudaSetDevice(dev);
+    else if (err == cudaSuccess) prev = -1;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+struct pda_handle_s {
+  pda_config cfg;
+  int group = 1;
+  int num_sms = 1;
+  int ctas_per_sm = 1;
+  void* ws = nullptr;
+  float* ws_o = nullptr;
+  float* ws_lse = nullptr;
+  int* err = nullptr;
+  // TMA descriptors for the last (k_cache, v_cache, num_blocks) seen
+  const void* tm_k = nullptr;
+  const void* tm_v = nullptr;
+  int64_t tm_nb = -1;
+  alignas(64) CUtensorMap tmap_k;
+  alignas(64) CUtensorMap tmap_v;
+};
+
+extern "C" {
+
+int paged_decode_attn_abi_version(void) { return PDA_ABI_VERSION; }
+
+const char* paged_decode_attn_last_error(void) { return g_last_error.c_str(); }
+
+int paged_decode_attn_create(const pda_config* cfg, pda_handle* out_handle) {
+  if (!out_handle) return fail(PDA_EINVAL, "out_handle is NULL");
+  *out_handle = nullptr;
+  int st = check_config(cfg);
+  if (st != PDA_OK) return st;
+  DeviceGuard guard(cfg->device);
+  if (guard.err != cudaSuccess) return cuda_fail("cudaSetDevice", guard.err);
+  pda_handle h = new (std::nothrow) pda_handle_s();
+  if (!h) return fail(PDA_ENOMEM, "host allocation of the handle failed");
+  h->cfg = *cfg;
+  h->group = cfg->num_q_heads / cfg->num_kv_heads;
+  cudaError_t e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, cfg->device);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail("cudaDeviceGetAttribute", e);
+  }
+  e = pda::partial_prepare(h->group, cfg->block_size, cfg->dtype);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail("cudaFuncSetAttribute", e);
+  }
+  h->ctas_per_sm = pda::partial_ctas_per_sm(h->group, cfg->block_size, cfg->dtype);
+  const size_t rows = (size_t)cfg->max_batch * cfg->num_q_heads * cfg->max_splits;
+  const size_t o_bytes = rows * cfg->head_dim * sizeof(float);
+  const size_t lse_bytes = ((rows * sizeof(float)) + 255) & ~size_t(255);
+  const size_t err_bytes = 256;
+  e = cudaMalloc(&h->ws, o_bytes + lse_bytes + err_bytes);
+  if (e != cudaSuccess) {
+    delete h;
+    cudaGetLastError();
+    return fail(PDA_ENOMEM, std::string("workspace cudaMalloc failed: ") + cudaGetErrorString(e));
+  }
+  h->ws_o = static_cast<float*>(h->ws);
+  h->ws_lse = reinterpret_cast<float*>(static_cast<char*>(h->ws) + o_bytes);
+  h->err = reinterpret_cast<int*>(static_cast<char*>(h->ws) + o_bytes + lse_bytes);
+  e = cudaMemset(h->err, 0, err_bytes);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(h->ws);
+    delete h;
+    return cuda_fail("cudaMemset", e);
+  }
+  *out_handle = h;
+  return PDA_OK;
+}
+
+void paged_decode_attn_destroy(pda_handle h) {
+  if (!h) return;
+  if (h->ws) {
+    DeviceGuard guard(h->cfg.device);
+    cudaFree(h->ws);
+  }
+  delete h;
+}
+
+int paged_decode_attn_plan(const pda_config* cfg, int num_sms, int batch, int max_blocks,
+                           int max_context_len_hint, int* num_splits, int* chunk_pages) {
+  int st = check_config(cfg);
+  if (st != PDA_OK) return st;
+  if (!num_splits || !chunk_pages) return fail(PDA_EINVAL, "output pointer is NULL");
+  if (num_sms < 1) return fail(PDA_EINVAL, "num_sms must be >= 1");
+  if (batch < 0 || batch > cfg->max_batch) return fail(PDA_EINVAL, "batch out of range");
+  if (max_blocks < 1 || max_blocks > cfg->max_blocks_per_seq)
+    return fail(PDA_EINVAL, "max_blocks out of range");
+  if (max_context_len_hint < 0) return fail(PDA_EINVAL, "max_context_len_hint < 0");
+  const int G = cfg->num_q_heads / cfg->num_kv_heads;
+  plan_splits(*cfg, num_sms, pda::partial_ctas_per_sm_hint(G), batch, max_blocks,
+              max_context_len_hint, 0, num_splits, chunk_pages);
+  return PDA_OK;
+}
+
+int paged_decode_attn_run_ex(pda_handle h, const void* q, const void* k_cache,
+                             const void* v_cache, const int32_t* block_table,
+                             const int32_t* context_lens, int batch, int max_blocks,
+                             int64_t num_blocks, float scale, void* out, void* stream,
+                             int num_splits, int max_context_len_hint, int out_dtype) {
+  if (!h) return fail(PDA_EINVAL, "handle is NULL");
+  const pda_config& c = h->cfg;
+  if (batch < 0 || batch > c.max_batch) return fail(PDA_EINVAL, "batch out of [0, max_batch]");
+  if (batch == 0) return PDA_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out)
+    return fail(PDA_EINVAL, "a tensor pointer is NULL");
+  if (max_blocks < 1 || max_blocks > c.max_blocks_per_seq)
+    return fail(PDA_EINVAL, "max_blocks out of [1, max_blocks_per_seq]");
+  if (num_blocks < 1 || num_blocks * c.block_size > (int64_t)INT_MAX)
+    return fail(PDA_EINVAL, "num_blocks * block_size must be in [1, 2^31)");
+  if (!std::isfinite(scale)) return fail(PDA_EINVAL, "scale is not finite");
+  if (num_splits < 0 || num_splits > c.max_splits)
+    return fail(PDA_EINVAL, "num_splits out of [0, max_splits]");
+  if (max_context_len_hint < 0) return fail(PDA_EINVAL, "max_context_len_hint < 0");
+  if (out_dtype == -1) out_dtype = c.dtype;
+  if (out_dtype != c.dtype && out_dtype != PDA_F32)
+    return fail(PDA_EINVAL, "out_dtype must be -1, the input dtype or PDA_F32");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return fail(PDA_EINVAL, "q, k_cache, v_cache and out must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_table) | reinterpret_cast<uintptr_t>(context_lens)) & 3u)
+    return fail(PDA_EINVAL, "block_table and context_lens must be 4-byte aligned");
+
+  const size_t esz = 2;
+  const size_t out_esz = out_dtype == PDA_F32 ? 4 : 2;
+  const size_t n_q = (size_t)batch * c.num_q_heads * c.head_dim;
+  const size_t cache_bytes = (size_t)num_blocks * c.block_size * c.num_kv_heads * c.head_dim * esz;
+  const size_t out_bytes = n_q * out_esz;
+  if (overlaps(out, out_bytes, q, n_q * esz) || overlaps(out, out_bytes, k_cache, cache_bytes) ||
+      overlaps(out, out_bytes, v_cache, cache_bytes) ||
+      overlaps(out, out_bytes, block_table, (size_t)batch * max_blocks * 4) ||
+      overlaps(out, out_bytes, context_lens, (size_t)batch * 4))
+    return fail(PDA_EALIAS, "out overlaps an input");
+
+  DeviceGuard guard(c.device);
+  if (guard.err != cudaSuccess) return cuda_fail("cudaSetDevice", guard.err);
+
+  if (h->tm_k != k_cache || h->tm_v != v_cache || h->tm_nb != num_blocks) {
+    int st = encode_cache_map(&h->tmap_k, k_cache, c.num_kv_heads, c.block_size, num_blocks);
+    if (st == PDA_OK)
+      st = encode_cache_map(&h->tmap_v, v_cache, c.num_kv_heads, c.block_size, num_blocks);
+    if (st != PDA_OK) {
+      h->tm_k = h->tm_v = nullptr;
+      h->tm_nb = -1;
+      return st;
+    }
+    h->tm_k = k_cache;
+    h->tm_v = v_cache;
+    h->tm_nb = num_blocks;
+  }
+
+  int S = 1, chunk = 1;
+  plan_splits(c, h->num_sms, h->ctas_per_sm, batch, max_blocks, max_context_len_hint, num_splits,
+              &S, &chunk);
+
+  pda::PartialParams p;
+  p.q = q;
+  p.block_table = block_table;
+  p.context_lens = context_lens;
+  p.out = out;
+  p.ws_o = h->ws_o;
+  p.ws_lse = h->ws_lse;
+  p.err = h->err;
+  p.Hq = c.num_q_heads;
+  p.Hkv = c.num_kv_heads;
+  p.max_blocks = max_blocks;
+  p.chunk_pages = chunk;
+  p.num_splits = S;
+  p.qscale = scale * pda::kLog2e;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = pda::launch_partial(h->group, c.block_size, c.dtype, out_dtype == PDA_F32,
+                                      &h->tmap_k, &h->tmap_v, p, batch, s);
+  if (e != cudaSuccess) return cuda_fail("partial kernel launch", e);
+  if (S > 1) {
+    pda::MergeParams m;
+    m.o = h->ws_o;
+    m.lse = h->ws_lse;
+    m.context_lens = context_lens;
+    m.out = out;
+    m.rows = batch * c.num_q_heads;
+    m.num_splits = S;
+    m.head_dim = c.head_dim;
+    m.Hq = c.num_q_heads;
+    m.block_size = c.block_size;
+    m.max_blocks = max_blocks;
+    m.chunk_pages = chunk;
+    e = pda::launch_merge(m, out_dtype, s);
+    if (e != cudaSuccess) return cuda_fail("merge kernel launch", e);
+  }
+  return PDA_OK;
+}
+
+int paged_decode_attn_run(pda_handle h, const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_table, const int32_t* context_lens, int batch,
+                          int max_blocks, int64_t num_blocks, float scale, void* out,
+                          void* stream) {
+  return paged_decode_attn_run_ex(h, q, k_cache, v_cache, block_table, context_lens, batch,
+                                  max_blocks, num_blocks, scale, out, stream, 0, 0, -1);
+}
+
+int paged_decode_attn_merge(const float* partial_o, const float* partial_lse, int rows,
+                            int num_splits, int head_dim, void* out, int out_dtype, int device,
+                            void* stream) {
+  if (rows < 0) return fail(PDA_EINVAL, "rows < 0");
+  if (num_splits < 1 || num_splits > pda::kMaxSplits)
+    return fail(PDA_EINVAL, "num_splits must be in [1, 64]");
+  if (head_dim < 4 || head_dim > 512 || head_dim % 4 != 0)
+    return fail(PDA_EINVAL, "head_dim must be a multiple of 4 in [4, 512]");
+  if (out_dtype != PDA_BF16 && out_dtype != PDA_FP16 && out_dtype != PDA_F32)
+    return fail(PDA_EINVAL, "out_dtype must be PDA_BF16, PDA_FP16 or PDA_F32");
+  if (device < 0) return fail(PDA_EINVAL, "device < 0");
+  if (rows == 0) return PDA_OK;
+  if (!partial_o || !partial_lse || !out) return fail(PDA_EINVAL, "a pointer is NULL");
+  if (!aligned16(partial_o) || !aligned16(out) || (reinterpret_cast<uintptr_t>(partial_lse) & 3u))
+    return fail(PDA_EINVAL, "partial_o and out must be 16-byte aligned, partial_lse 4-byte");
+  const size_t out_bytes = (size_t)rows * head_dim * (out_dtype == PDA_F32 ? 4 : 2);
+  if (overlaps(out, out_bytes, partial_o, (size_t)rows * num_splits * head_dim * 4) ||
+      overlaps(out, out_bytes, partial_lse, (size_t)rows * num_splits * 4))
+    return fail(PDA_EALIAS, "out overlaps an input");
+  DeviceGuard guard(device);
+  if (guard.err != cudaSuccess) return cuda_fail("cudaSetDevice", guard.err);
+  pda::MergeParams m;
+  m.o = partial_o;
+  m.lse = partial_lse;
+  m.context_lens = nullptr;
+  m.out = out;
+  m.rows = rows;
+  m.num_splits = num_splits;
+  m.head_dim = head_dim;
+  m.Hq = 1;
+  m.block_size = 1;
+  m.max_blocks = 1;
+  m.chunk_pages = 1;
+  cudaError_t e = pda::launch_merge(m, out_dtype, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("merge kernel launch", e);
+  return PDA_OK;
+}
+
+int paged_decode_attn_validate(pda_handle h, const int32_t* block_table,
+                               const int32_t* context_lens, int batch, int max_blocks,
+                               int64_t num_blocks, void* stream) {
+  if (!h) return fail(PDA_EINVAL, "handle is NULL");
+  if (batch < 0 || batch > h->cfg.max_batch) return fail(PDA_EINVAL, "batch out of range");
+  if (batch == 0) return PDA_OK;
+  if (!block_table || !context_lens) return fail(PDA_EINVAL, "a pointer is NULL");
+  if (max_blocks < 1 || max_blocks > h->cfg.max_blocks_per_seq)
+    return fail(PDA_EINVAL, "max_blocks out of range");
+  if (num_blocks < 1) return fail(PDA_EINVAL, "num_blocks < 1");
+  DeviceGuard guard(h->cfg.device);
+  if (guard.err != cudaSuccess) return cuda_fail("cudaSetDevice", guard.err);
+  cudaError_t e = pda::launch_validate(block_table, context_lens, batch, max_blocks,
+                                       h->cfg.block_size, num_blocks, h->err,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("validate kernel launch", e);
+  return PDA_OK;
+}
+
+int paged_decode_attn_check_device_error(pda_handle h, int* code, int* detail, void* stream) {
+  if (!h || !code || !detail) return fail(PDA_EINVAL, "a pointer is NULL");
+  DeviceGuard guard(h->cfg.device);
+  if (guard.err != cudaSuccess) return cuda_fail("cudaSetDevice", guard.err);
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
+  int host[2] = {0, 0};
+  e = cudaMemcpy(host, h->err, sizeof host, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof host);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail("reading the device error word", e);
+  *code = host[0];
+  *detail = host[1];
+  return PDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,480 @@
+// Split-K partial kernel for paged MQA/GQA decode attention (sm_103a).
+//
+// Loom Kernels landing page, "Supported now" ("Paged MQA/GQA decode": GQA
+// packing + local split-K/LSE) and benchmark page, "Current qualified
+// results" (the D128 long-context split-K/LSE path) name the method; this is
+// a GB300 design of it.
+//
+// One CTA handles one (split s, kv head h, sequence b). It streams the
+// split's K/V pages for head h from HBM into shared memory with TMA tiled
+// loads (one 64-dim x block_size box per half-row, 128-byte swizzle), through
+// a kStages-deep ring of stages guarded by mbarriers:
+//   warp kNW (producer): reads block-table entries (32 at a time, shared by
+//     shuffles) and issues the TMA loads for the next stage once the
+//     consumers have released it;
+//   warps 0..kNW-1 (consumers): each owns kTPW tokens of every stage and runs
+//     its own online softmax over them for all G query heads of the group:
+//       QK: LPT lanes per token, each holding a slice of the G pre-scaled
+//           query rows in registers, dot products reduced by xor-shuffles;
+//       softmax: chunk max by shuffles, rescale of the running state;
+//       PV: each lane owns 4 of the 128 output dims for all G heads.
+// At the end the consumer warps' (max, sum, acc) states are merged through
+// shared memory; a sequence handled by a single split writes `out` directly,
+// otherwise the split writes its normalised partial and natural-log LSE to
+// the workspace for the merge kernel.
+//
+// Logits are kept in base-2 units (q is pre-multiplied by scale * log2 e) so
+// the exponentials are exp2f; the LSE is converted back to natural log.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
+#include "pda_internal.h"
+#include "ptx.cuh"
+
+namespace pda {
+namespace partial {
+
+constexpr int kNW = 4;                    // consumer warps
+constexpr int kTPW = 16;                  // tokens per consumer warp per stage
+constexpr int kChunk = kNW * kTPW;        // tokens per stage
+constexpr int kStages = 3;                // pipeline depth
+constexpr int kRowBytes = 128;            // one 64-element half of a 128-dim row
+constexpr int kHalfBytes = kChunk * kRowBytes;
+constexpr int kStageBytes = 4 * kHalfBytes;  // K lo, K hi, V lo, V hi
+constexpr int kThreads = (kNW + 1) * 32;
+constexpr int kPBufBytes = kNW * kTPW * 8 * 4;  // probabilities, room for G <= 8
+constexpr int kBarBytes = 2 * kStages * 8;
+constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + kPBufBytes + kBarBytes;
+constexpr unsigned kFull = 0xffffffffu;
+
+static_assert(kHeadDim == 128, "the partial kernel is written for head_dim 128");
+
+template <bool FP16>
+__device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
+  if constexpr (FP16) {
+    __half2 h2;
+    memcpy(&h2, &w, 4);
+    const float2 f = __half22float2(h2);
+    lo = f.x;
+    hi = f.y;
+  } else {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xffff0000u);
+  }
+}
+
+template <bool FP16>
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  unpack2<FP16>(u.x, f[0], f[1]);
+  unpack2<FP16>(u.y, f[2], f[3]);
+  unpack2<FP16>(u.z, f[4], f[5]);
+  unpack2<FP16>(u.w, f[6], f[7]);
+}
+
+template <typename TOut>
+__device__ __forceinline__ TOut to_out(float x) {
+  if constexpr (std::is_same_v<TOut, float>) {
+    return x;
+  } else if constexpr (std::is_same_v<TOut, __half>) {
+    return __float2half_rn(x);
+  } else {
+    return __float2bfloat16_rn(x);
+  }
+}
+
+__device__ __forceinline__ void record_error(int* err, int code, int detail) {
+  if (atomicCAS(err, 0, code) == 0) err[1] = detail;
+}
+
+template <int G, int BS, bool FP16, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(G))
+    paged_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                         const __grid_constant__ CUtensorMap tmap_v, const PartialParams p) {
+  constexpr int LPT = (G >= 4) ? 8 : 4;  // lanes per token in QK (q slice <= 128 regs)
+  constexpr int TPP = 32 / LPT;          // tokens per QK pass
+  constexpr int PASSES = kTPW / TPP;
+  constexpr int CPS = 8 / LPT;           // 16-byte chunks per lane per half-row
+  constexpr int PPS = kChunk / BS;       // pages per stage
+  static_assert(kChunk % BS == 0 && PPS <= 32, "stage must hold whole pages");
+  using TOut = std::conditional_t<OUT_F32, float, std::conditional_t<FP16, __half, __nv_bfloat16>>;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;  // 128B-swizzle atoms need 1 KiB
+  uint8_t* base = smem_raw + (base_u32 - raw_u32);
+  float* pbuf = reinterpret_cast<float*>(base + kStages * kStageBytes);
+  const uint32_t bar0 = base_u32 + kStages * kStageBytes + kPBufBytes;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+
+  const int split = blockIdx.x;
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int hq0 = h * G;
+  TOut* out = static_cast<TOut*>(p.out);
+
+  // Context length, clamped to what the block table can address.
+  int L = __ldg(p.context_lens + b);
+  const int maxL = p.max_blocks * BS;
+  L = L < 0 ? 0 : (L > maxL ? maxL : L);
+  const int n_pages = (L + BS - 1) / BS;
+  int n_splits_b = (n_pages + p.chunk_pages - 1) / p.chunk_pages;
+  if (n_splits_b > p.num_splits) n_splits_b = p.num_splits;  // last split takes the rest
+
+  if (n_splits_b == 0) {  // empty context: zero output rows
+    if (split == 0) {
+      for (int i = threadIdx.x; i < G * kHeadDim; i += kThreads)
+        out[((int64_t)b * p.Hq + hq0) * kHeadDim + i] = to_out<TOut>(0.f);
+    }
+    return;
+  }
+  if (split >= n_splits_b) return;
+
+  const int p0 = split * p.chunk_pages;
+  const int p1 = (split == n_splits_b - 1) ? n_pages : min(p0 + p.chunk_pages, n_pages);
+  const int t0 = p0 * BS;
+  const int t1 = min(p1 * BS, L);
+  const int n_chunks = (p1 - p0 + PPS - 1) / PPS;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), kNW);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  bool failed = false;
+  float m_run[G], l_run[G], acc[G][4];
+  const int dh = lane >> 4;          // PV: which 64-dim half
+  const int vch = (lane & 15) >> 1;  // PV: 16-byte chunk within the half
+  const int vsub = lane & 1;         // PV: which 8 bytes of the chunk
+
+  if (warp == kNW) {
+    // ------------------------------ producer ------------------------------
+    if (lane == 0) {
+      prefetch_tensormap(&tmap_k);
+      prefetch_tensormap(&tmap_v);
+    }
+    const int32_t* table = p.block_table + (int64_t)b * p.max_blocks;
+    int win_base = p0;
+    int win_blk = (p0 + lane < p1) ? __ldg(table + p0 + lane) : 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      const int slot = c % kStages;
+      if (c >= kStages) {
+        const bool ok = mbar_wait(empty_bar(slot), ((c / kStages) - 1) & 1);
+        if (!__all_sync(kFull, ok)) {
+          failed = true;
+          break;
+        }
+      }
+      const int pg0 = p0 + c * PPS;
+      const int npg = min(PPS, p1 - pg0);
+      if (pg0 + PPS > win_base + 32) {
+        win_base = pg0;
+        win_blk = (pg0 + lane < p1) ? __ldg(table + pg0 + lane) : 0;
+      }
+      int blk[PPS];
+#pragma unroll
+      for (int i = 0; i < PPS; ++i) blk[i] = __shfl_sync(kFull, win_blk, (pg0 + i - win_base) & 31);
+      if (lane == 0) {
+        const uint32_t fb = full_bar(slot);
+        mbar_arrive_expect_tx(fb, (uint32_t)npg * BS * 4 * kRowBytes);
+        const uint32_t st = base_u32 + slot * kStageBytes;
+#pragma unroll
+        for (int i = 0; i < PPS; ++i) {
+          if (i < npg) {
+            const int y = blk[i] * BS;
+            const uint32_t ro = (uint32_t)(i * BS * kRowBytes);
+            tma_load_2d(st + 0 * kHalfBytes + ro, &tmap_k, h * kHeadDim, y, fb);
+            tma_load_2d(st + 1 * kHalfBytes + ro, &tmap_k, h * kHeadDim + 64, y, fb);
+            tma_load_2d(st + 2 * kHalfBytes + ro, &tmap_v, h * kHeadDim, y, fb);
+            tma_load_2d(st + 3 * kHalfBytes + ro, &tmap_v, h * kHeadDim + 64, y, fb);
+          }
+        }
+      }
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------ consumers -----------------------------
+    const int j = lane / LPT;  // token within a QK pass
+    const int s = lane % LPT;  // segment: chunks [s*CPS, (s+1)*CPS) of each half-row
+
+    float qf[G][2][CPS][8];
+    {
+      const uint8_t* qb = static_cast<const uint8_t*>(p.q) +
+                          (((int64_t)b * p.Hq + hq0) * kHeadDim) * 2;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int i = 0; i < CPS; ++i) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4*>(
+                qb + (g * kHeadDim + hh * 64 + (s * CPS + i) * 8) * 2));
+            float t[8];
+            unpack8<FP16>(u, t);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qf[g][hh][i][e] = t[e] * p.qscale;
+          }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m_run[g] = -INFINITY;
+      l_run[g] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[g][e] = 0.f;
+    }
+    float* pw = pbuf + warp * kTPW * G;
+
+    for (int c = 0; c < n_chunks; ++c) {
+      const int slot = c % kStages;
+      const bool ok = mbar_wait(full_bar(slot), (c / kStages) & 1);
+      if (!__all_sync(kFull, ok)) {
+        failed = true;
+        break;
+      }
+      const int n_valid = min(kChunk, t1 - (t0 + c * kChunk));
+      const int n_w = min(kTPW, max(0, n_valid - warp * kTPW));
+      if (n_w > 0) {
+        const uint8_t* kst = base + slot * kStageBytes;
+        const uint8_t* vst = kst + 2 * kHalfBytes;
+        float sc[PASSES][G];
+#pragma unroll
+        for (int pass = 0; pass < PASSES; ++pass) {
+          const int tl = pass * TPP + j;
+          const int row = warp * kTPW + tl;
+          float a[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) a[g] = 0.f;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int i = 0; i < CPS; ++i) {
+              const int phys = (s * CPS + i) ^ (row & 7);
+              const uint4 u = *reinterpret_cast<const uint4*>(kst + hh * kHalfBytes +
+                                                              row * kRowBytes + phys * 16);
+              float kf[8];
+              unpack8<FP16>(u, kf);
+#pragma unroll
+              for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) a[g] = fmaf(qf[g][hh][i][e], kf[e], a[g]);
+            }
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+#pragma unroll
+            for (int off = 1; off < LPT; off <<= 1) a[g] += __shfl_xor_sync(kFull, a[g], off);
+            sc[pass][g] = (tl < n_w) ? a[g] : -INFINITY;
+          }
+        }
+        // online softmax over this warp's tokens of the stage
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float mx = sc[0][g];
+#pragma unroll
+          for (int pass = 1; pass < PASSES; ++pass) mx = fmaxf(mx, sc[pass][g]);
+#pragma unroll
+          for (int off = LPT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+          const float mn = fmaxf(m_run[g], mx);  // finite: n_w > 0
+          const float alpha = exp2f(m_run[g] - mn);
+          m_run[g] = mn;
+          float ls = 0.f;
+#pragma unroll
+          for (int pass = 0; pass < PASSES; ++pass) {
+            sc[pass][g] = exp2f(sc[pass][g] - mn);
+            ls += sc[pass][g];
+          }
+          l_run[g] = l_run[g] * alpha + ls;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[g][e] *= alpha;
+        }
+        if (s == 0) {
+#pragma unroll
+          for (int pass = 0; pass < PASSES; ++pass)
+#pragma unroll
+            for (int g = 0; g < G; ++g) pw[(pass * TPP + j) * G + g] = sc[pass][g];
+        }
+        __syncwarp();
+#pragma unroll 4
+        for (int t = 0; t < n_w; ++t) {
+          const int row = warp * kTPW + t;
+          const uint2 u = *reinterpret_cast<const uint2*>(vst + dh * kHalfBytes + row * kRowBytes +
+                                                          ((vch ^ (row & 7)) * 16) + vsub * 8);
+          float vf[4];
+          unpack2<FP16>(u.x, vf[0], vf[1]);
+          unpack2<FP16>(u.y, vf[2], vf[3]);
+          float pp[G];
+          if constexpr (G % 4 == 0) {
+#pragma unroll
+            for (int g4 = 0; g4 < G / 4; ++g4) {
+              const float4 v4 = *reinterpret_cast<const float4*>(pw + t * G + 4 * g4);
+              pp[4 * g4 + 0] = v4.x;
+              pp[4 * g4 + 1] = v4.y;
+              pp[4 * g4 + 2] = v4.z;
+              pp[4 * g4 + 3] = v4.w;
+            }
+          } else {
+#pragma unroll
+            for (int g = 0; g < G; ++g) pp[g] = pw[t * G + g];
+          }
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[g][e] = fmaf(pp[g], vf[e], acc[g][e]);
+        }
+        __syncwarp();
+      }
+      if (lane == 0) mbar_arrive(empty_bar(slot));
+    }
+    // the warp's softmax sum: each token's p is held by its LPT lanes; add
+    // over the token lanes only
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int off = LPT; off < 32; off <<= 1) l_run[g] += __shfl_xor_sync(kFull, l_run[g], off);
+  }
+
+  if (failed && lane == 0) record_error(p.err, kErrWaitTimeout, split);
+  if (warp == kNW) return;
+
+  // ---------------- merge the consumer warps' states ----------------------
+  // Scratch aliases the stage ring: every stage has been consumed (all full
+  // barriers observed) before the first named barrier.
+  named_bar_sync(1, kNW * 32);
+  float* mw = reinterpret_cast<float*>(base);  // [kNW][G]
+  float* lw = mw + kNW * G;                    // [kNW][G]
+  float* aw = lw + kNW * G;                    // [kNW][G][128]
+  if (lane == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      mw[warp * G + g] = m_run[g];
+      lw[warp * G + g] = l_run[g];
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float4 v4 = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+    *reinterpret_cast<float4*>(aw + (warp * G + g) * kHeadDim + dh * 64 + vch * 8 + vsub * 4) = v4;
+  }
+  named_bar_sync(1, kNW * 32);
+  const int d = threadIdx.x;  // 0 .. 127
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kNW; ++w) M = fmaxf(M, mw[w * G + g]);
+    float Ls = 0.f, o = 0.f;
+#pragma unroll
+    for (int w = 0; w < kNW; ++w) {
+      const float mwv = mw[w * G + g];
+      const float f = (mwv == -INFINITY) ? 0.f : exp2f(mwv - M);
+      Ls += f * lw[w * G + g];
+      o += f * aw[(w * G + g) * kHeadDim + d];
+    }
+    o = o / Ls;
+    const int64_t row = (int64_t)b * p.Hq + hq0 + g;
+    if (n_splits_b == 1) {
+      out[row * kHeadDim + d] = to_out<TOut>(o);
+    } else {
+      const int64_t r = row * p.num_splits + split;
+      p.ws_o[r * kHeadDim + d] = o;
+      if (d == 0) p.ws_lse[r] = (M + log2f(Ls)) * kLn2;
+    }
+  }
+}
+
+template <int G, int BS, bool FP16, bool OUT_F32>
+cudaError_t launch_one(const CUtensorMap* tk, const CUtensorMap* tv, const PartialParams& p,
+                       int batch, cudaStream_t stream) {
+  dim3 grid(p.num_splits, p.Hkv, batch);
+  paged_partial_kernel<G, BS, FP16, OUT_F32><<<grid, kThreads, kSmemBytes, stream>>>(*tk, *tv, p);
+  return cudaGetLastError();
+}
+
+template <int G, int BS, bool FP16, bool OUT_F32>
+cudaError_t prepare_one() {
+  return cudaFuncSetAttribute(paged_partial_kernel<G, BS, FP16, OUT_F32>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+}
+
+template <int G, int BS, bool FP16>
+int occupancy_one() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_partial_kernel<G, BS, FP16, false>,
+                                                    kThreads, kSmemBytes) != cudaSuccess)
+    return 1;
+  return n > 0 ? n : 1;
+}
+
+// Dispatch over (G, block size, out dtype) for one input dtype.
+template <bool FP16>
+struct Dispatch {
+  template <int G, int BS>
+  static cudaError_t launch_g(bool f32, const CUtensorMap* tk, const CUtensorMap* tv,
+                              const PartialParams& p, int batch, cudaStream_t s) {
+    return f32 ? launch_one<G, BS, FP16, true>(tk, tv, p, batch, s)
+               : launch_one<G, BS, FP16, false>(tk, tv, p, batch, s);
+  }
+  template <int BS>
+  static cudaError_t launch_bs(int G, bool f32, const CUtensorMap* tk, const CUtensorMap* tv,
+                               const PartialParams& p, int batch, cudaStream_t s) {
+    switch (G) {
+      case 1: return launch_g<1, BS>(f32, tk, tv, p, batch, s);
+      case 2: return launch_g<2, BS>(f32, tk, tv, p, batch, s);
+      case 4: return launch_g<4, BS>(f32, tk, tv, p, batch, s);
+      case 8: return launch_g<8, BS>(f32, tk, tv, p, batch, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  static cudaError_t launch(int G, int BS, bool f32, const CUtensorMap* tk, const CUtensorMap* tv,
+                            const PartialParams& p, int batch, cudaStream_t s) {
+    if (BS == 16) return launch_bs<16>(G, f32, tk, tv, p, batch, s);
+    if (BS == 32) return launch_bs<32>(G, f32, tk, tv, p, batch, s);
+    return cudaErrorInvalidValue;
+  }
+  template <int G, int BS>
+  static cudaError_t prepare_g() {
+    cudaError_t e = prepare_one<G, BS, FP16, false>();
+    if (e != cudaSuccess) return e;
+    return prepare_one<G, BS, FP16, true>();
+  }
+  template <int BS>
+  static cudaError_t prepare_bs(int G) {
+    switch (G) {
+      case 1: return prepare_g<1, BS>();
+      case 2: return prepare_g<2, BS>();
+      case 4: return prepare_g<4, BS>();
+      case 8: return prepare_g<8, BS>();
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  static cudaError_t prepare(int G, int BS) {
+    if (BS == 16) return prepare_bs<16>(G);
+    if (BS == 32) return prepare_bs<32>(G);
+    return cudaErrorInvalidValue;
+  }
+  template <int BS>
+  static int occupancy_bs(int G) {
+    switch (G) {
+      case 1: return occupancy_one<1, BS, FP16>();
+      case 2: return occupancy_one<2, BS, FP16>();
+      case 4: return occupancy_one<4, BS, FP16>();
+      case 8: return occupancy_one<8, BS, FP16>();
+      default: return 1;
+    }
+  }
+  static int occupancy(int G, int BS) {
+    return BS == 16 ? occupancy_bs<16>(G) : occupancy_bs<32>(G);
+  }
+};
+
+}  // namespace partial
+}  // namespace pda

@@ -1,0 +1,75 @@
+// Private launch boundary between the C ABI (api.cpp) and the CUDA kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace pda {
+
+constexpr int kHeadDim = 128;
+constexpr int kMaxSplits = 64;
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+// Device error word layout: err[0] = code (0 = none), err[1] = detail.
+enum DeviceError : int {
+  kErrNone = 0,
+  kErrContextLen = 1,
+  kErrBlockId = 2,
+  kErrWaitTimeout = 3,
+};
+
+struct PartialParams {
+  const void* q;               // [B, Hq, D]
+  const int32_t* block_table;  // [B, max_blocks]
+  const int32_t* context_lens; // [B]
+  void* out;                   // [B, Hq, D]
+  float* ws_o;                 // [B, Hq, num_splits, D]
+  float* ws_lse;               // [B, Hq, num_splits]
+  int* err;                    // device error word
+  int Hq;
+  int Hkv;
+  int max_blocks;
+  int chunk_pages;  // pages per split
+  int num_splits;   // S (grid.x); row stride of the workspace
+  float qscale;     // scale * log2(e): logits are kept in base-2 units
+};
+
+struct MergeParams {
+  const float* o;               // [rows, num_splits, head_dim]
+  const float* lse;             // [rows, num_splits], natural log
+  const int32_t* context_lens;  // decode path: per-sequence split counts; null = all splits
+  void* out;                    // [rows, head_dim]
+  int rows;
+  int num_splits;
+  int head_dim;
+  int Hq;           // decode path: rows = b * Hq + hq
+  int block_size;   // decode path
+  int max_blocks;   // decode path
+  int chunk_pages;  // decode path
+};
+
+// Kernel geometry facts the host planner needs.
+int partial_threads();
+size_t partial_smem_bytes(int group);
+bool partial_supported(int group, int block_size, int dtype);
+cudaError_t partial_prepare(int group, int block_size, int dtype);  // set smem attributes
+int partial_ctas_per_sm(int group, int block_size, int dtype);
+// CTAs per SM the kernel is built for (its launch bounds); the planner's
+// figure when no GPU is queried.
+constexpr int partial_ctas_per_sm_hint(int group) { return group >= 8 ? 1 : 2; }
+
+cudaError_t launch_partial(int group, int block_size, int dtype, bool out_f32,
+                           const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                           const PartialParams& p, int batch, cudaStream_t stream);
+
+// out_dtype: 0 bf16, 1 fp16, 2 f32
+cudaError_t launch_merge(const MergeParams& p, int out_dtype, cudaStream_t stream);
+
+cudaError_t launch_validate(const int32_t* block_table, const int32_t* context_lens, int batch,
+                            int max_blocks, int block_size, int64_t num_blocks, int* err,
+                            cudaStream_t stream);
+
+}  // namespace pda

@@ -1,0 +1,130 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+symbol the header declares, rejects bad arguments with the documented codes
+before touching CUDA, and the split planner's host logic."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_gqa_decode_attention_gb300 as pda
+from paged_gqa_decode_attention_gb300 import build as pda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pda_build.build()
+    return pda.load_library()
+
+
+def header_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"^\s*(?:[\w\*]+\s+)+\**(paged_decode_attn_\w+)\s*\(", text,
+                                    re.M))
+    return names
+
+
+def test_exports_every_header_function(lib):
+    declared = header_functions()
+    assert declared, "no declarations parsed"
+    assert declared == set(pda.EXPORTS), declared ^ set(pda.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_abi_version(lib):
+    assert lib.paged_decode_attn_abi_version() == pda.ABI_VERSION == 1
+
+
+def test_library_needs_no_driver_to_load(lib):
+    out = os.popen(f"ldd {pda_build.LIB_PATH}").read()
+    assert "libcuda.so" not in out and "libcudart" not in out
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("num_q_heads", 0, pda.PDA_EINVAL),
+    ("num_q_heads", 30, pda.PDA_EINVAL),        # not a multiple of Hkv = 8
+    ("num_q_heads", 8 * 3, pda.PDA_EUNSUPPORTED),  # group size 3
+    ("head_dim", 64, pda.PDA_EUNSUPPORTED),
+    ("head_dim", 0, pda.PDA_EINVAL),
+    ("block_size", 8, pda.PDA_EUNSUPPORTED),
+    ("dtype", 7, pda.PDA_EINVAL),
+    ("max_batch", 0, pda.PDA_EINVAL),
+    ("max_batch", 70000, pda.PDA_EINVAL),
+    ("max_splits", 65, pda.PDA_EINVAL),
+    ("max_blocks_per_seq", 0, pda.PDA_EINVAL),
+    ("device", -1, pda.PDA_EINVAL),
+])
+def test_create_rejects_bad_config_before_cuda(lib, field, value, status):
+    cfg = pda.make_config(32, 8, 128, 16)
+    setattr(cfg, field, value)
+    h = ctypes.c_void_p(123)
+    assert lib.paged_decode_attn_create(ctypes.byref(cfg), ctypes.byref(h)) == status
+    assert h.value is None
+    assert lib.paged_decode_attn_last_error()
+
+
+def test_null_arguments(lib):
+    h = ctypes.c_void_p()
+    assert lib.paged_decode_attn_create(None, ctypes.byref(h)) == pda.PDA_EINVAL
+    cfg = pda.make_config(32, 8)
+    assert lib.paged_decode_attn_create(ctypes.byref(cfg), None) == pda.PDA_EINVAL
+    assert lib.paged_decode_attn_run(None, 0, 0, 0, 0, 0, 1, 1, 1, 1.0, 0, 0) == pda.PDA_EINVAL
+    lib.paged_decode_attn_destroy(None)  # NULL-safe
+    assert lib.paged_decode_attn_validate(None, 0, 0, 1, 1, 1, 0) == pda.PDA_EINVAL
+    code = ctypes.c_int()
+    assert lib.paged_decode_attn_check_device_error(None, ctypes.byref(code), ctypes.byref(code),
+                                                    0) == pda.PDA_EINVAL
+
+
+def test_merge_rejects_bad_arguments_before_cuda(lib):
+    assert lib.paged_decode_attn_merge(0, 0, 1, 0, 128, 0, 0, 0, 0) == pda.PDA_EINVAL  # S = 0
+    assert lib.paged_decode_attn_merge(0, 0, 1, 65, 128, 0, 0, 0, 0) == pda.PDA_EINVAL
+    assert lib.paged_decode_attn_merge(0, 0, 1, 4, 130, 0, 0, 0, 0) == pda.PDA_EINVAL
+    assert lib.paged_decode_attn_merge(0, 0, 1, 4, 128, 0, 9, 0, 0) == pda.PDA_EINVAL
+    assert lib.paged_decode_attn_merge(0, 0, 0, 4, 128, 0, 0, 0, 0) == pda.PDA_OK  # no rows
+    assert lib.paged_decode_attn_merge(0, 0, 2, 4, 128, 0, 0, 0, 0) == pda.PDA_EINVAL  # NULL
+
+
+# --------------------------- split planner --------------------------------
+
+def plan(B, max_blocks, hint=0, Hq=32, Hkv=8, bs=16, sms=152, max_splits=64):
+    cfg = pda.make_config(Hq, Hkv, 128, bs, max_batch=max(1, B), max_blocks_per_seq=max_blocks,
+                          max_splits=max_splits)
+    return pda.plan(cfg, sms, B, max_blocks, hint)
+
+
+@pytest.mark.parametrize("B,pages", [(1, 2), (1, 512), (4, 2048), (32, 4), (8, 64), (128, 128),
+                                     (1, 1), (3, 1000), (64, 4096)])
+def test_plan_covers_every_page(lib, B, pages):
+    S, chunk = plan(B, pages)
+    assert 1 <= S <= 64 and chunk >= 1
+    assert S * chunk >= pages > (S - 1) * chunk  # S splits of chunk pages cover all, none empty
+
+
+def test_plan_no_split_when_grid_is_full(lib):
+    assert plan(128, 128, Hq=64, bs=32)[0] == 1       # 1024 CTAs already
+    assert plan(32, 4)[0] == 1                         # short contexts
+    assert plan(1, 2)[0] == 1                          # tiny
+
+
+def test_plan_splits_long_contexts_to_fill_the_gpu(lib):
+    S1, _ = plan(1, 512)    # B=1, L=8192: 8 CTAs without splitting
+    S4, _ = plan(4, 2048)   # B=4, L=32768
+    assert S1 * 8 >= 152 and S4 * 32 >= 152
+    assert plan(1, 2048)[0] >= plan(4, 2048)[0]
+
+
+def test_plan_respects_hint_and_caps(lib):
+    assert plan(1, 2048, hint=64)[0] <= 4
+    assert plan(1, 4096, max_splits=8)[0] <= 8
+    cfg = pda.make_config(32, 8)
+    with pytest.raises(pda.PDAError):
+        pda.plan(cfg, 0, 1, 16)           # no SMs
+    with pytest.raises(pda.PDAError):
+        pda.plan(cfg, 152, 1, 10 ** 6)    # max_blocks beyond the config

@@ -1,0 +1,209 @@
+"""GPU parity: the CUDA path against the FP64 oracle, element by element, on
+seeded inputs of every workload family, the split-count sweep, edge cases,
+and sampled rows of the full-size long-context workload. Calls go through
+the C ABI (ctypes binding)."""
+import hashlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_gqa_decode_attention_gb300 import (PDA_EALIAS, PDA_EINVAL, PagedDecodeAttention,
+                                              PDAError, merge, workloads)
+from parity import assert_close, make_attn, oracle_ref, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+DEV = torch.device("cuda", torch.cuda.current_device())
+
+
+def check(wl_host, **kw):
+    wl = wl_host.to(DEV)
+    attn = make_attn(wl)
+    out = run_gpu(attn, wl, **kw)
+    attn.close()
+    return assert_close(out, oracle_ref(wl_host), wl.name)
+
+
+def test_tiny():
+    check(workloads.tiny(seed=0))
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("bs", [16, 32])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_short_batch(seed, bs, dtype):
+    check(workloads.short_batch(seed=seed, block_size=bs, dtype=dtype))
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_mid_ragged_peaky(seed):
+    check(workloads.mid_ragged(seed=seed))
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 4, 5, 8, 16, 32, 64])
+def test_long_split_sweep(splits):
+    """Every split count gives the same result (ragged 3000-token tail)."""
+    wl = workloads.long_context(seed=1, batch=2, context=3000, num_blocks=1024)
+    check(wl, num_splits=splits)
+
+
+@pytest.mark.parametrize("batch,context", [(1, 8192), (4, 8192)])
+def test_long_context_heuristic(batch, context):
+    check(workloads.long_context(seed=2, batch=batch, context=context, num_blocks=4096))
+
+
+@pytest.mark.parametrize("batch", [16, 128])
+def test_serving_mix(batch):
+    check(workloads.serving_mix(seed=0, batch=batch))
+
+
+def test_fp32_output_mode():
+    """The kernel's own accuracy: fp32 out within 2e-3 of FP64 (peaky rows)."""
+    err = check(workloads.mid_ragged(seed=0), out_dtype=torch.float32)
+    assert err < 1e-4, err  # fp32 accumulation is far inside the bar
+
+
+@pytest.mark.parametrize("G,Hkv", [(1, 8), (2, 4), (4, 2), (8, 1), (8, 8), (4, 8)])
+@pytest.mark.parametrize("bs", [16, 32])
+def test_edge_lengths_and_groups(G, Hkv, bs):
+    lens = [1, bs - 1, bs, bs + 1, 2 * bs, 63, 64, 65, 0, 257, 1000]
+    wl = workloads.custom(seed=G * 10 + Hkv, B=len(lens), Hq=G * Hkv, Hkv=Hkv, D=128,
+                          block_size=bs, lens=lens, num_blocks=200)
+    for splits in (0, 3, 64):
+        check(wl, num_splits=splits)
+
+
+def test_context_hint_below_actual_is_still_exact():
+    wl = workloads.custom(seed=5, B=3, Hq=32, Hkv=8, D=128, block_size=16, lens=[900, 40, 2000])
+    check(wl, max_context_len_hint=64)
+
+
+def test_full_size_long_context_sampled_rows():
+    """The bench workload itself (B=4, L=32768, 40 GiB pool, heuristic splits):
+    sampled rows against the oracle run on the pages those rows read."""
+    wl = workloads.long_context(seed=0, batch=4, context=32768, device=DEV)
+    attn = make_attn(wl)
+    out = run_gpu(attn, wl)
+    attn.close()
+    rng = np.random.default_rng(0)
+    for b in (0, 3):
+        q, k, v, bt, cl = workloads.compact_for_rows(wl, [b])
+        hqs = rng.choice(32, size=6, replace=False)
+        rows = np.array([[0, int(h)] for h in hqs], dtype=np.int32)
+        ref = oracle.paged_decode_rows(q, k, v, bt, cl, oracle.BF16, wl.scale, rows)
+        assert_close(out[b, torch.from_numpy(hqs).to(DEV)], ref, f"b={b}")
+    del wl
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16, torch.float16])
+def test_merge_entry_point(out_dtype):
+    rng = np.random.default_rng(3)
+    rows, S, D = 37, 13, 128
+    o = rng.standard_normal((rows, S, D))
+    lse = rng.standard_normal((rows, S)) * 5
+    lse[rng.random((rows, S)) < 0.3] = -np.inf
+    lse[5, :] = -np.inf  # a row of empty splits
+    o32 = torch.from_numpy(o.astype(np.float32))
+    l32 = torch.from_numpy(lse.astype(np.float32))
+    ref = oracle.lse_merge(l32.double().numpy(), o32.double().numpy())
+    out = merge(o32.to(DEV), l32.to(DEV), out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert_close(out, ref, "merge")
+    assert not out[5].any()
+
+
+def _digest(t):
+    return hashlib.sha256(t.detach().contiguous().view(torch.uint8).cpu().numpy().tobytes()).hexdigest()
+
+
+def test_inputs_unchanged_only_out_written():
+    wl = workloads.mid_ragged(seed=1).to(DEV)
+    before = [_digest(t) for t in (wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.context_lens)]
+    attn = make_attn(wl)
+    n = wl.batch * wl.num_q_heads * wl.head_dim
+    buf = torch.full((n + 4096,), 7.0, dtype=torch.bfloat16, device=DEV)
+    out = buf[:n].view(wl.batch, wl.num_q_heads, wl.head_dim)
+    attn.run(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.context_lens, wl.scale, out=out)
+    torch.cuda.synchronize()
+    after = [_digest(t) for t in (wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.context_lens)]
+    assert before == after
+    assert bool((buf[n:] == 7.0).all())  # nothing written past out
+    attn.close()
+
+
+def test_handle_reuse_across_workloads():
+    a = workloads.custom(seed=7, B=4, Hq=32, Hkv=8, D=128, block_size=16, lens=[100, 2000, 5, 64])
+    b = workloads.custom(seed=8, B=2, Hq=32, Hkv=8, D=128, block_size=16, lens=[3000, 17],
+                         num_blocks=300)
+    attn = PagedDecodeAttention(32, 8, 128, 16, torch.bfloat16, max_batch=8,
+                                max_blocks_per_seq=256, max_splits=64)
+    for wl_host in (a, b, a):
+        wl = wl_host.to(DEV)
+        assert_close(run_gpu(attn, wl), oracle_ref(wl_host), wl.name)
+    attn.close()
+
+
+def test_cuda_graph_capture_replay():
+    wl = workloads.long_context(seed=3, batch=2, context=2500, num_blocks=512).to(DEV)
+    attn = make_attn(wl)
+    eager = run_gpu(attn, wl).clone()
+    out = torch.empty_like(eager)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        attn.run(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.context_lens, wl.scale, out=out)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    attn.close()
+
+
+def test_validator_flags_without_faulting():
+    wl = workloads.custom(seed=9, B=3, Hq=32, Hkv=8, D=128, block_size=16, lens=[40, 17, 90]).to(DEV)
+    attn = make_attn(wl)
+    attn.validate(wl.block_table, wl.context_lens, wl.num_blocks)
+    assert attn.check_device_error() == (0, 0)
+    lens = wl.context_lens.clone()
+    lens[1] = wl.max_blocks * 16 + 1
+    attn.validate(wl.block_table, lens, wl.num_blocks)
+    assert attn.check_device_error() == (1, 1)
+    table = wl.block_table.clone()
+    table[2, 3] = wl.num_blocks + 5
+    attn.validate(table, wl.context_lens, wl.num_blocks)
+    assert attn.check_device_error() == (2, 2)
+    # the kernel itself stays memory-safe on the bad table: the bad page reads zeros
+    out = attn.run(wl.q, wl.k_cache, wl.v_cache, table, wl.context_lens, wl.scale)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+    assert attn.check_device_error() == (0, 0)
+    attn.close()
+
+
+def test_abi_errors_on_gpu():
+    wl = workloads.tiny(seed=0).to(DEV)
+    attn = make_attn(wl)
+    with pytest.raises(PDAError) as e:
+        attn.run(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.context_lens, wl.scale,
+                 out=wl.q)
+    assert e.value.status == PDA_EALIAS
+    lib = attn.lib
+    bad = wl.q.data_ptr() + 2  # misaligned
+    st = attn.run_raw(bad, wl.k_cache.data_ptr(), wl.v_cache.data_ptr(), wl.block_table.data_ptr(),
+                      wl.context_lens.data_ptr(), 1, wl.max_blocks, wl.num_blocks, wl.scale,
+                      torch.empty_like(wl.q).data_ptr())
+    assert st == PDA_EINVAL and b"aligned" in lib.paged_decode_attn_last_error()
+    st = attn.run_raw(wl.q.data_ptr(), wl.k_cache.data_ptr(), wl.v_cache.data_ptr(),
+                      wl.block_table.data_ptr(), wl.context_lens.data_ptr(), 2, wl.max_blocks,
+                      wl.num_blocks, wl.scale, torch.empty_like(wl.q).data_ptr())
+    assert st == PDA_EINVAL  # batch > max_batch
+    # batch 0 is a no-op
+    assert attn.run_raw(0, 0, 0, 0, 0, 0, 1, 1, 1.0, 0) == 0
+    attn.close()
