@@ -1,0 +1,425 @@
+#!/usr/bin/env python
+"""Benchmark of the paged GQA decode-attention hot path on GB300.
+
+One step = one decode-attention call (the whole hot path: split plan, the
+split-K partial kernel with its log-sum-exp merge) over one batch of seeded
+synthetic inputs already resident in HBM. Default workload: the long-context
+split-K case B=4, Hq 32, Hkv 8, D 128, block 16, context 32768, random
+block tables over a 40 GiB K+V pool (512 MiB of KV read per step, 4x the L2,
+so consecutive steps do not hit in L2).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+Prints one JSON line (rank 0). Under torchrun each rank runs its own batch
+(seed + rank) with no data-path collective (weak scaling); the timed region
+is bracketed by a barrier and a device synchronize on both sides and the
+time is the max over ranks. ``--impl reference`` times the FP64 CPU oracle on
+the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "decode tokens/s and KV-read HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes (read + write) per launch of the partial kernel from one ncu
+# capture of this workload (profiles/); None when not measured for the
+# current kernel.
+NCU_TRAFFIC_BYTES = {
+    # profiles/paged_partial_kernel_long_b4_l32768.md: 537.02 MB read + 4.18 MB
+    # written per launch (captured on the same step over a 1 GiB pool)
+    "long_b4_l32768": 541_207_808,
+}
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+def make_workload(name: str, seed: int, device):
+    from paged_gqa_decode_attention_gb300 import workloads as W
+    if name == "long_b4_l32768":
+        return W.long_context(seed=seed, batch=4, context=32768, device=device)
+    if name == "long_b4_l32768_pool1g":  # same step over a 1 GiB pool (for ncu captures)
+        return W.long_context(seed=seed, batch=4, context=32768, num_blocks=16384, device=device)
+    if name == "long_b1_l32768":
+        return W.long_context(seed=seed, batch=1, context=32768, device=device)
+    if name == "long_b4_l8192":
+        return W.long_context(seed=seed, batch=4, context=8192, device=device)
+    if name == "long_b1_l8192":
+        return W.long_context(seed=seed, batch=1, context=8192, device=device)
+    if name == "serving_b128":
+        return W.serving_mix(seed=seed, batch=128, device=device)
+    if name == "mid_ragged_b8":
+        return W.mid_ragged(seed=seed, device=device)
+    if name == "short_b32":
+        return W.short_batch(seed=seed, device=device)
+    raise SystemExit(f"unknown workload {name}")
+
+
+WORKLOAD_DESC = {
+    "long_b4_l32768": "long-context split-K: B=4, Hq 32, Hkv 8, D 128, block 16, context 32768, "
+                      "bf16 N(0,1), random block tables over a 40 GiB K+V pool",
+}
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (weak scaling, no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def shard_seed(base_seed: int, rank: int) -> int:
+    """Each rank decodes its own batch of sequences."""
+    return base_seed + 1000 * rank
+
+
+def reduce_max(x: float, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (identity without a process group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region (NVML through ctypes; read-only)
+# ---------------------------------------------------------------------------
+
+_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+class ClockSampler:
+    """Polls SM clock and clock-event reasons every ``period`` seconds in a
+    thread while the timed region runs."""
+
+    def __init__(self, uuid: str | None, period: float = 0.002):
+        self.period = period
+        self.samples = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._nvml = None
+        self._dev = None
+        try:
+            nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if nvml.nvmlInit_v2() != 0:
+                return
+            dev = ctypes.c_void_p()
+            ok = -1
+            if uuid:
+                ok = nvml.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(dev))
+            if ok != 0:
+                ok = nvml.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(dev))
+            if ok != 0:
+                return
+            mx = ctypes.c_uint()
+            if nvml.nvmlDeviceGetMaxClockInfo(dev, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._nvml, self._dev = nvml, dev
+        except OSError:
+            pass
+
+    def _reasons(self) -> int:
+        r = ctypes.c_ulonglong()
+        fn = getattr(self._nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self._nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        return r.value if fn(self._dev, ctypes.byref(r)) == 0 else 0
+
+    def _run(self):
+        mhz = ctypes.c_uint()
+        while not self._stop.is_set():
+            if self._nvml.nvmlDeviceGetClockInfo(self._dev, 1, ctypes.byref(mhz)) == 0:
+                self.samples.append((mhz.value, self._reasons()))
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self._nvml is not None:
+            self._thr = threading.Thread(target=self._run, daemon=True)
+            self._thr.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._nvml is not None:
+            self._thr.join()
+
+    def summary(self) -> dict:
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "note": "NVML unavailable"}
+        mhz = [m for m, _ in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        reasons = sorted({name for b, name in _REASONS.items() if bits & b})
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+def measured_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the FP64 oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_sample(wl, target_s: float = 10.0):
+    """Time the FP64 oracle on whole sequences of ``wl`` (all query heads of
+    every sequence, passes repeated until about ``target_s`` of wall time).
+    Returns (tokens_per_s, sample_description, threads, seconds)."""
+    import oracle
+    from paged_gqa_decode_attention_gb300 import workloads as W
+    threads = os.cpu_count() or 1
+    dt = oracle.BF16 if wl.q.dtype == torch.bfloat16 else oracle.FP16
+    q, k, v, bt, cl = W.compact_for_rows(wl, list(range(wl.batch)))
+    rows = np.array([[b, h] for b in range(q.shape[0]) for h in range(q.shape[1])],
+                    dtype=np.int32)
+    passes, elapsed = 0, 0.0
+    while elapsed < target_s and passes < 1000:
+        t0 = time.perf_counter()
+        oracle.paged_decode_rows(q, k, v, bt, cl, dt, wl.scale, rows, threads=threads)
+        elapsed += time.perf_counter() - t0
+        passes += 1
+    seqs = passes * q.shape[0]
+    desc = (f"{passes} pass(es) over all {q.shape[0]} sequences x {q.shape[1]} query heads "
+            f"({int(cl.sum())} tokens per pass) of the same workload; oracle over {threads} "
+            f"threads")
+    return seqs / elapsed, desc, threads, elapsed
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    if dev.type == "cpu" and args.workload.startswith("long_"):
+        # without a GPU, draw the same shapes over a pool just large enough
+        from paged_gqa_decode_attention_gb300 import workloads as W
+        B = 4 if "_b4_" in args.workload else 1
+        L = int(args.workload.split("_l")[-1])
+        wl = W.long_context(seed=args.seed, batch=B, context=L,
+                            num_blocks=B * (L // 16) + 64)
+    else:
+        wl = make_workload(args.workload, args.seed, dev)
+    import oracle
+    from paged_gqa_decode_attention_gb300 import workloads as W
+    threads = os.cpu_count() or 1
+    dt = oracle.BF16 if wl.q.dtype == torch.bfloat16 else oracle.FP16
+    q, k, v, bt, cl = W.compact_for_rows(wl, [0])
+    rows = np.array([[0, h] for h in range(q.shape[1])], dtype=np.int32)
+    for _ in range(args.warmup):
+        oracle.paged_decode_rows(q, k, v, bt, cl, dt, wl.scale, rows, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.paged_decode_rows(q, k, v, bt, cl, dt, wl.scale, rows, threads=threads)
+    el = time.perf_counter() - t0
+    value = args.steps / el  # one sequence (all query heads) per step
+    sample = (f"per step: sequence 0 (all {q.shape[1]} query heads, {int(cl[0])} tokens) of "
+              f"the {args.workload} workload")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "desc": WORKLOAD_DESC.get(args.workload, "")},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    import torch.distributed as dist
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+
+    from paged_gqa_decode_attention_gb300 import PagedDecodeAttention
+    from paged_gqa_decode_attention_gb300 import build as pda_build
+    pda_build.build()
+
+    wl = make_workload(args.workload, shard_seed(args.seed, rank), dev)
+    B, Hq, D = wl.batch, wl.num_q_heads, wl.head_dim
+    attn = PagedDecodeAttention(Hq, wl.num_kv_heads, D, wl.block_size, wl.q.dtype,
+                                max_batch=B, max_blocks_per_seq=wl.max_blocks, max_splits=64,
+                                device=dev)
+    out = torch.empty((B, Hq, D), dtype=wl.q.dtype, device=dev)
+    kv_bytes = wl.kv_bytes()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = kv_bytes < 4 * l2
+    flush_buf = torch.empty(2 * max(l2, 1 << 27), dtype=torch.uint8, device=dev) if flush else None
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        attn.run(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.context_lens, wl.scale, out=out)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: K steps, inputs resident in HBM ----
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    region0, region1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with sampler:
+        region0.record(stream)
+        for i in range(args.steps):
+            if flush:
+                flush_buf.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        region1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    region_ms = region0.elapsed_time(region1)
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    step_ms_sum = sum(kernel_ms)
+    # with L2 flushing between steps the flush is not part of a step
+    timed_ms = step_ms_sum if flush else region_ms
+    timed_ms_max = reduce_max(timed_ms, dev)
+    value = (B * world * args.steps) / (timed_ms_max / 1e3)
+    avg_launch_ms = statistics.mean(kernel_ms)
+
+    # ---- end to end: host buffers, copies inside the timed region ----
+    q_h = wl.q.cpu().pin_memory()
+    bt_h = wl.block_table.cpu().pin_memory()
+    cl_h = wl.context_lens.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_d, bt_d, cl_d = torch.empty_like(wl.q), torch.empty_like(wl.block_table), \
+        torch.empty_like(wl.context_lens)
+    h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + cl_h.numel() * 4
+    d2h = out_h.numel() * out_h.element_size()
+    e2e_steps = args.steps
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        q_d.copy_(q_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        cl_d.copy_(cl_h, non_blocking=True)
+        attn.run(q_d, wl.k_cache, wl.v_cache, bt_d, cl_d, wl.scale, out=out)
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+    e2e_s = reduce_max(time.perf_counter() - t0, dev)
+    e2e_value = B * world * e2e_steps / e2e_s
+
+    peak, peak_kind = measured_peaks()
+    achieved = kv_bytes / (avg_launch_ms / 1e3) / 1e9
+    traffic = NCU_TRAFFIC_BYTES.get(args.workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": timed_ms_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "desc": WORKLOAD_DESC.get(args.workload, ""),
+                   "batch_per_gpu": B, "global_batch": B * world,
+                   "kv_bytes_per_step": kv_bytes,
+                   "l2": "inputs larger than L2 (KV per step >= 4x L2)" if not flush
+                   else "L2 flushed between steps (256 MiB write, outside the step events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "kv_gbs": achieved,
+        "kv_frac_of_peak": achieved / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} (hbm_gbs)",
+                     "kernel": "paged_partial_kernel (+ merge when split)",
+                     "per_launch_ms": avg_launch_ms},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * launches_per_step(attn, wl),
+        "clocks": sampler.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, desc, cores, secs = oracle_sample(wl)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": desc, "seconds": secs}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    attn.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def launches_per_step(attn, wl) -> int:
+    """Kernels one call launches: the partial kernel, plus the merge kernel
+    when the plan splits the sequences."""
+    from paged_gqa_decode_attention_gb300 import plan
+    sms = torch.cuda.get_device_properties(wl.q.device).multi_processor_count
+    S, _ = plan(attn.config, sms, wl.batch, wl.max_blocks, 0)
+    return 1 + (1 if S > 1 else 0)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="long_b4_l32768")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

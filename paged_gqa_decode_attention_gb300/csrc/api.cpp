@@ -196,7 +196,11 @@ int paged_decode_attn_create(const pda_config* cfg, pda_handle* out_handle) {
     delete h;
     return cuda_fail("cudaFuncSetAttribute", e);
   }
-  h->ctas_per_sm = pda::partial_ctas_per_sm(h->group, cfg->block_size, cfg->dtype);
+  // Plan with the residency the kernel is built for, so paged_decode_attn_plan
+  // (no GPU) and run agree; fall back to the measured figure if it is lower.
+  const int occ = pda::partial_ctas_per_sm(h->group, cfg->block_size, cfg->dtype);
+  const int hint = pda::partial_ctas_per_sm_hint(h->group);
+  h->ctas_per_sm = occ < hint ? occ : hint;
   const size_t rows = (size_t)cfg->max_batch * cfg->num_q_heads * cfg->max_splits;
   const size_t o_bytes = rows * cfg->head_dim * sizeof(float);
   const size_t lse_bytes = ((rows * sizeof(float)) + 255) & ~size_t(255);
