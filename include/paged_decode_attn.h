@@ -181,6 +181,46 @@ int paged_decode_attn_validate(pda_handle handle, const int32_t* block_table,
 int paged_decode_attn_check_device_error(pda_handle handle, int* code, int* detail,
                                          void* stream);
 
+/* Decode attention for callers that cannot allocate device memory.
+ * (No counterpart in the paper: this entry point exists for integration.)
+ *
+ * Who needs it: code that runs where cudaMalloc is off limits, for example
+ * inside a host callback or another library's allocator-free region, or a
+ * runtime that owns every byte of device memory through its own pool and
+ * forbids allocations behind its back. paged_decode_attn_create allocates
+ * the split-K workspace, so such callers cannot use a handle.
+ *
+ * This call takes the geometry directly (no handle) and allocates nothing:
+ * the split-K partials live in one fixed scratch array of 8 MiB of fp32
+ * partial outputs plus 256 KiB of fp32 log-sum-exps, built into the library
+ * and held on every GPU that loads it until the process exits. The split
+ * count the heuristic picks is lowered until the partials fit
+ * (batch * Hq * S * head_dim <= 2^21 and batch * Hq * S <= 2^16); a
+ * sequence with a single split needs no scratch at all. An explicit
+ * num_splits > 0 whose partials do not fit is rejected with PDA_EINVAL.
+ *
+ * Set-up: the first call on a device looks up the scratch array's device
+ * address and sets the kernels' shared-memory limits for that device; make
+ * that first call before any stream capture. Later calls only launch.
+ *
+ * Sharing: every call on a device uses the same scratch and it keeps the
+ * last call's contents. Calls that can overlap on the GPU (different
+ * streams, or different host threads) race on it and give wrong results;
+ * serialise them. Device-side pipeline timeouts are not reported by this
+ * entry point (it has no error word the caller can read).
+ *
+ * Arguments are those of paged_decode_attn_run_ex, with the geometry of
+ * pda_config (num_q_heads, num_kv_heads, head_dim, block_size, dtype) in
+ * place of the handle, out in the input dtype, and `device` the CUDA
+ * ordinal the pointers belong to. Same layouts, alignment, aliasing rules,
+ * return codes and asynchrony. */
+int paged_decode_attn_run_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_table, const int32_t* context_lens,
+                                  int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int block_size, int dtype, int max_blocks, int64_t num_blocks,
+                                  float scale, void* out, int num_splits, int device,
+                                  void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -38,6 +38,7 @@ EXPORTS = [
     "paged_decode_attn_merge",
     "paged_decode_attn_validate",
     "paged_decode_attn_check_device_error",
+    "paged_decode_attn_run_noalloc",
 ]
 
 
@@ -93,6 +94,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.paged_decode_attn_check_device_error.argtypes = [P, ctypes.POINTER(I),
                                                              ctypes.POINTER(I), P]
         lib.paged_decode_attn_check_device_error.restype = I
+        lib.paged_decode_attn_run_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I64, F,
+                                                      P, I, I, P]
+        lib.paged_decode_attn_run_noalloc.restype = I
         if lib.paged_decode_attn_abi_version() != ABI_VERSION:
             raise RuntimeError("ABI version mismatch between binding and library")
         if path is None:

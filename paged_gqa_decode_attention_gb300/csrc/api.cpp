@@ -152,6 +152,8 @@ struct DeviceGuard {
 
 }  // namespace
 
+int pda::set_last_error(int code, const char* msg) { return fail(code, msg); }
+
 struct pda_handle_s {
   pda_config cfg;
   int group = 1;

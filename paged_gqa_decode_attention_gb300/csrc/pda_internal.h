@@ -72,4 +72,8 @@ cudaError_t launch_validate(const int32_t* block_table, const int32_t* context_l
                             int max_blocks, int block_size, int64_t num_blocks, int* err,
                             cudaStream_t stream);
 
+// Records `msg` as this thread's last error (paged_decode_attn_last_error)
+// and returns `code`.
+int set_last_error(int code, const char* msg);
+
 }  // namespace pda
