@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <climits>
+#include <cstdlib>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -157,6 +158,7 @@ int pda::set_last_error(int code, const char* msg) { return fail(code, msg); }
 struct pda_handle_s {
   pda_config cfg;
   int group = 1;
+  int kernel = 0;  // pda::PartialKernel
   int num_sms = 1;
   int ctas_per_sm = 1;
   void* ws = nullptr;
@@ -193,15 +195,25 @@ int paged_decode_attn_create(const pda_config* cfg, pda_handle* out_handle) {
     delete h;
     return cuda_fail("cudaDeviceGetAttribute", e);
   }
-  e = pda::partial_prepare(h->group, cfg->block_size, cfg->dtype);
+  // The partial kernel: PDA_PARTIAL_KERNEL=tensor_core (groups of 4 or 8
+  // query heads) or cuda_core overrides the default; read here, once per
+  // handle (A/B measurements and tests).
+  h->kernel = pda::default_partial_kernel(h->group);
+  if (const char* env = std::getenv("PDA_PARTIAL_KERNEL")) {
+    if (std::strcmp(env, "cuda_core") == 0) h->kernel = pda::kPartialCudaCore;
+    else if (std::strcmp(env, "tensor_core") == 0 &&
+             pda::partial_kernel_supported(pda::kPartialTensorCore, h->group))
+      h->kernel = pda::kPartialTensorCore;
+  }
+  e = pda::partial_prepare(h->kernel, h->group, cfg->block_size, cfg->dtype);
   if (e != cudaSuccess) {
     delete h;
     return cuda_fail("cudaFuncSetAttribute", e);
   }
   // Plan with the residency the kernel is built for, so paged_decode_attn_plan
   // (no GPU) and run agree; fall back to the measured figure if it is lower.
-  const int occ = pda::partial_ctas_per_sm(h->group, cfg->block_size, cfg->dtype);
-  const int hint = pda::partial_ctas_per_sm_hint(h->group);
+  const int occ = pda::partial_ctas_per_sm(h->kernel, h->group, cfg->block_size, cfg->dtype);
+  const int hint = pda::partial_ctas_per_sm_hint(h->kernel, h->group);
   h->ctas_per_sm = occ < hint ? occ : hint;
   const size_t rows = (size_t)cfg->max_batch * cfg->num_q_heads * cfg->max_splits;
   const size_t o_bytes = rows * cfg->head_dim * sizeof(float);
@@ -247,7 +259,8 @@ int paged_decode_attn_plan(const pda_config* cfg, int num_sms, int batch, int ma
     return fail(PDA_EINVAL, "max_blocks out of range");
   if (max_context_len_hint < 0) return fail(PDA_EINVAL, "max_context_len_hint < 0");
   const int G = cfg->num_q_heads / cfg->num_kv_heads;
-  plan_splits(*cfg, num_sms, pda::partial_ctas_per_sm_hint(G), batch, max_blocks,
+  plan_splits(*cfg, num_sms,
+              pda::partial_ctas_per_sm_hint(pda::default_partial_kernel(G), G), batch, max_blocks,
               max_context_len_hint, 0, num_splits, chunk_pages);
   return PDA_OK;
 }
@@ -326,7 +339,8 @@ int paged_decode_attn_run_ex(pda_handle h, const void* q, const void* k_cache,
   p.num_splits = S;
   p.qscale = scale * pda::kLog2e;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = pda::launch_partial(h->group, c.block_size, c.dtype, out_dtype == PDA_F32,
+  cudaError_t e = pda::launch_partial(h->kernel, h->group, c.block_size, c.dtype,
+                                      out_dtype == PDA_F32,
                                       &h->tmap_k, &h->tmap_v, p, batch, s);
   if (e != cudaSuccess) return cuda_fail("partial kernel launch", e);
   if (S > 1) {

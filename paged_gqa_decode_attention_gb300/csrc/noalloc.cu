@@ -100,7 +100,7 @@ int setup_device(int dev, int group, int bs, int dtype, void** scratch, int* num
   }
   const auto key = std::make_tuple(dev, group, bs, dtype);
   if (!g_prepared.count(key)) {
-    cudaError_t e = pda::partial_prepare(group, bs, dtype);
+    cudaError_t e = pda::partial_prepare(pda::default_partial_kernel(group), group, bs, dtype);
     if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", e);
     g_prepared.insert(key);
   }
@@ -216,7 +216,8 @@ extern "C" int paged_decode_attn_run_noalloc(const void* q, const void* k_cache,
   p.chunk_pages = chunk;
   p.num_splits = S;
   p.qscale = scale * pda::kLog2e;
-  e = pda::launch_partial(group, block_size, dtype, false, &tk, &tv, p, batch, s);
+  e = pda::launch_partial(pda::default_partial_kernel(group), group, block_size, dtype, false,
+                          &tk, &tv, p, batch, s);
   if (e != cudaSuccess) return cuda_fail("partial kernel launch", e);
   if (S > 1) {
     pda::MergeParams m;

@@ -91,7 +91,7 @@ __device__ __forceinline__ void record_error(int* err, int code, int detail) {
 }
 
 template <int G, int BS, bool FP16, bool OUT_F32>
-__global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(G))
+__global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCudaCore, G))
     paged_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v, const PartialParams p) {
   constexpr int LPT = (G >= 4) ? 8 : 4;  // lanes per token in QK (q slice <= 128 regs)

@@ -1,5 +1,5 @@
-// Host-side entry points of the partial kernel: geometry facts for the
-// planner and dtype dispatch.
+// Host-side entry points of the partial kernels: support checks, shared-memory
+// attributes, occupancy, and dispatch over (kernel, input dtype).
 #include "partial_kernel.cuh"
 
 namespace pda {
@@ -8,14 +8,18 @@ cudaError_t launch_partial_bf16(int, int, bool, const CUtensorMap*, const CUtens
                                const PartialParams&, int, cudaStream_t);
 cudaError_t launch_partial_fp16(int, int, bool, const CUtensorMap*, const CUtensorMap*,
                                const PartialParams&, int, cudaStream_t);
+cudaError_t launch_partial_tc_bf16(int, int, bool, const CUtensorMap*, const CUtensorMap*,
+                                  const PartialParams&, int, cudaStream_t);
+cudaError_t launch_partial_tc_fp16(int, int, bool, const CUtensorMap*, const CUtensorMap*,
+                                  const PartialParams&, int, cudaStream_t);
 cudaError_t prepare_partial_bf16(int, int);
 cudaError_t prepare_partial_fp16(int, int);
+cudaError_t prepare_partial_tc_bf16(int, int);
+cudaError_t prepare_partial_tc_fp16(int, int);
 int occupancy_partial_bf16(int, int);
 int occupancy_partial_fp16(int, int);
-
-int partial_threads() { return partial::kThreads; }
-
-size_t partial_smem_bytes(int) { return partial::kSmemBytes; }
+int occupancy_partial_tc_bf16(int, int);
+int occupancy_partial_tc_fp16(int, int);
 
 bool partial_supported(int group, int block_size, int dtype) {
   const bool g_ok = group == 1 || group == 2 || group == 4 || group == 8;
@@ -23,22 +27,35 @@ bool partial_supported(int group, int block_size, int dtype) {
   return g_ok && bs_ok && (dtype == 0 || dtype == 1);
 }
 
-cudaError_t partial_prepare(int group, int block_size, int dtype) {
+bool partial_kernel_supported(int kernel, int group) {
+  if (kernel == kPartialTensorCore) return group == 4 || group == 8;
+  return kernel == kPartialCudaCore;
+}
+
+cudaError_t partial_prepare(int kernel, int group, int block_size, int dtype) {
+  if (kernel == kPartialTensorCore)
+    return dtype == 1 ? prepare_partial_tc_fp16(group, block_size)
+                      : prepare_partial_tc_bf16(group, block_size);
   return dtype == 1 ? prepare_partial_fp16(group, block_size)
                     : prepare_partial_bf16(group, block_size);
 }
 
-int partial_ctas_per_sm(int group, int block_size, int dtype) {
+int partial_ctas_per_sm(int kernel, int group, int block_size, int dtype) {
+  if (kernel == kPartialTensorCore)
+    return dtype == 1 ? occupancy_partial_tc_fp16(group, block_size)
+                      : occupancy_partial_tc_bf16(group, block_size);
   return dtype == 1 ? occupancy_partial_fp16(group, block_size)
                     : occupancy_partial_bf16(group, block_size);
 }
 
-cudaError_t launch_partial(int group, int block_size, int dtype, bool out_f32,
-                           const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
-                           const PartialParams& p, int batch, cudaStream_t stream) {
-  return dtype == 1
-             ? launch_partial_fp16(group, block_size, out_f32, tmap_k, tmap_v, p, batch, stream)
-             : launch_partial_bf16(group, block_size, out_f32, tmap_k, tmap_v, p, batch, stream);
+cudaError_t launch_partial(int kernel, int group, int block_size, int dtype, bool out_f32,
+                           const CUtensorMap* tk, const CUtensorMap* tv, const PartialParams& p,
+                           int batch, cudaStream_t stream) {
+  if (kernel == kPartialTensorCore)
+    return dtype == 1 ? launch_partial_tc_fp16(group, block_size, out_f32, tk, tv, p, batch, stream)
+                      : launch_partial_tc_bf16(group, block_size, out_f32, tk, tv, p, batch, stream);
+  return dtype == 1 ? launch_partial_fp16(group, block_size, out_f32, tk, tv, p, batch, stream)
+                    : launch_partial_bf16(group, block_size, out_f32, tk, tv, p, batch, stream);
 }
 
 }  // namespace pda

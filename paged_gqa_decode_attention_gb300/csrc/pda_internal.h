@@ -51,17 +51,28 @@ struct MergeParams {
   int chunk_pages;  // decode path
 };
 
-// Kernel geometry facts the host planner needs.
-int partial_threads();
-size_t partial_smem_bytes(int group);
-bool partial_supported(int group, int block_size, int dtype);
-cudaError_t partial_prepare(int group, int block_size, int dtype);  // set smem attributes
-int partial_ctas_per_sm(int group, int block_size, int dtype);
-// CTAs per SM the kernel is built for (its launch bounds); the planner's
-// figure when no GPU is queried.
-constexpr int partial_ctas_per_sm_hint(int group) { return group >= 8 ? 1 : 2; }
+// The two implementations of the split-K partial kernel.
+enum PartialKernel : int {
+  kPartialCudaCore = 0,    // QK/PV on the FMA pipe (partial_kernel.cuh), G in {1, 2, 4, 8}
+  kPartialTensorCore = 1,  // QK/PV with tcgen05 MMAs into TMEM (partial_tc_kernel.cuh), G in {4, 8}
+};
 
-cudaError_t launch_partial(int group, int block_size, int dtype, bool out_f32,
+// The kernel a geometry uses unless overridden (PDA_PARTIAL_KERNEL): the
+// CUDA-core kernel, the faster one on the measured workloads so far.
+constexpr int default_partial_kernel(int group) { return group > 0 ? kPartialCudaCore : 0; }
+
+// CTAs per SM each kernel is built for (its launch bounds and shared memory);
+// the planner's figure when no GPU is queried.
+constexpr int partial_ctas_per_sm_hint(int kernel, int group) {
+  return kernel == kPartialTensorCore ? 1 : (group >= 8 ? 1 : 2);
+}
+
+bool partial_supported(int group, int block_size, int dtype);
+bool partial_kernel_supported(int kernel, int group);
+cudaError_t partial_prepare(int kernel, int group, int block_size, int dtype);
+int partial_ctas_per_sm(int kernel, int group, int block_size, int dtype);
+
+cudaError_t launch_partial(int kernel, int group, int block_size, int dtype, bool out_f32,
                            const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
                            const PartialParams& p, int batch, cudaStream_t stream);
 

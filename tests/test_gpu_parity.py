@@ -207,3 +207,30 @@ def test_abi_errors_on_gpu():
     # batch 0 is a no-op
     assert attn.run_raw(0, 0, 0, 0, 0, 0, 1, 1, 1.0, 0) == 0
     attn.close()
+
+
+KERNELS = ["cuda_core", "tensor_core"]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("G,Hkv", [(4, 8), (8, 8), (4, 2), (8, 1)])
+@pytest.mark.parametrize("bs", [16, 32])
+def test_both_partial_kernels_exact(kernel, G, Hkv, bs, monkeypatch):
+    """Both implementations of the partial kernel (CUDA cores; tcgen05 tensor
+    cores) are exact on ragged lengths, block sizes 16/32, with and without
+    splitting."""
+    monkeypatch.setenv("PDA_PARTIAL_KERNEL", kernel)
+    wl = workloads.custom(seed=21 + G + bs, B=5, Hq=G * Hkv, Hkv=Hkv, D=128, block_size=bs,
+                          lens=[3000, 1, 129, 700, 128], num_blocks=400)
+    for splits in (0, 1, 5, 64):
+        check(wl, num_splits=splits)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_both_partial_kernels_peaky_and_fp16(kernel, monkeypatch):
+    monkeypatch.setenv("PDA_PARTIAL_KERNEL", kernel)
+    check(workloads.mid_ragged(seed=4))
+    check(workloads.short_batch(seed=4, block_size=32, dtype="fp16"))
+    check(workloads.serving_mix(seed=1, batch=24))
+    err = check(workloads.mid_ragged(seed=5), out_dtype=torch.float32)
+    assert err < 1e-4, err
