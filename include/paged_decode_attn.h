@@ -99,7 +99,9 @@ const char* paged_decode_attn_last_error(void);
 
 /* Validate `cfg`, select cfg->device, and allocate the handle plus its
  * device workspace: max_batch * Hq * max_splits * (head_dim + 1) floats of
- * split partials, and a small error-word area, zeroed.
+ * split partials, max_batch * Hkv ints of split tickets (the last split of a
+ * sequence's kv head to finish merges the splits; tickets return to zero by
+ * the end of every call) and a small error-word area, all zeroed.
  * Returns PDA_OK and stores the handle in *out_handle, or an error (and
  * *out_handle = NULL). Configuration errors are reported before any CUDA call. */
 int paged_decode_attn_create(const pda_config* cfg, pda_handle* out_handle);
@@ -192,12 +194,13 @@ int paged_decode_attn_check_device_error(pda_handle handle, int* code, int* deta
  *
  * This call takes the geometry directly (no handle) and allocates nothing:
  * the split-K partials live in one fixed scratch array of 8 MiB of fp32
- * partial outputs plus 256 KiB of fp32 log-sum-exps, built into the library
- * and held on every GPU that loads it until the process exits. The split
- * count the heuristic picks is lowered until the partials fit
- * (batch * Hq * S * head_dim <= 2^21 and batch * Hq * S <= 2^16); a
- * sequence with a single split needs no scratch at all. An explicit
- * num_splits > 0 whose partials do not fit is rejected with PDA_EINVAL.
+ * partial outputs, 256 KiB of fp32 log-sum-exps and 256 KiB of split
+ * tickets, built into the library and held on every GPU that loads it until
+ * the process exits. The split count the heuristic picks is lowered until
+ * the partials fit (batch * Hq * S * head_dim <= 2^21, batch * Hq * S <= 2^16,
+ * and no splitting at all if batch * Hkv > 2^16); a sequence with a single
+ * split needs no scratch. An explicit num_splits > 1 that does not fit is
+ * rejected with PDA_EINVAL. Each call clears the tickets it uses.
  *
  * Set-up: the first call on a device looks up the scratch array's device
  * address and sets the kernels' shared-memory limits for that device; make

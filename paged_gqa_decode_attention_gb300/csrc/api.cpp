@@ -1,6 +1,7 @@
 // C ABI of the paged decode-attention library: argument checks, the split
-// planner, the per-handle workspace and TMA descriptor cache, and the two
-// launches (partial, merge). Nothing here throws across the ABI.
+// planner, the per-handle workspace and TMA descriptor cache, and the launch
+// of the partial kernel (which also merges the splits). Nothing here throws
+// across the ABI.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -165,6 +166,8 @@ struct pda_handle_s {
   float* ws_o = nullptr;
   float* ws_lse = nullptr;
   int* err = nullptr;
+  int* counters = nullptr;  // [max_batch, Hkv] split tickets
+  size_t counter_bytes = 0;
   // TMA descriptors for the last (k_cache, v_cache, num_blocks) seen
   const void* tm_k = nullptr;
   const void* tm_v = nullptr;
@@ -219,7 +222,8 @@ int paged_decode_attn_create(const pda_config* cfg, pda_handle* out_handle) {
   const size_t o_bytes = rows * cfg->head_dim * sizeof(float);
   const size_t lse_bytes = ((rows * sizeof(float)) + 255) & ~size_t(255);
   const size_t err_bytes = 256;
-  e = cudaMalloc(&h->ws, o_bytes + lse_bytes + err_bytes);
+  h->counter_bytes = (size_t)cfg->max_batch * cfg->num_kv_heads * sizeof(int);
+  e = cudaMalloc(&h->ws, o_bytes + lse_bytes + err_bytes + h->counter_bytes);
   if (e != cudaSuccess) {
     delete h;
     cudaGetLastError();
@@ -228,7 +232,8 @@ int paged_decode_attn_create(const pda_config* cfg, pda_handle* out_handle) {
   h->ws_o = static_cast<float*>(h->ws);
   h->ws_lse = reinterpret_cast<float*>(static_cast<char*>(h->ws) + o_bytes);
   h->err = reinterpret_cast<int*>(static_cast<char*>(h->ws) + o_bytes + lse_bytes);
-  e = cudaMemset(h->err, 0, err_bytes);
+  h->counters = reinterpret_cast<int*>(static_cast<char*>(h->ws) + o_bytes + lse_bytes + err_bytes);
+  e = cudaMemset(h->err, 0, err_bytes + h->counter_bytes);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     cudaFree(h->ws);
@@ -332,6 +337,7 @@ int paged_decode_attn_run_ex(pda_handle h, const void* q, const void* k_cache,
   p.ws_o = h->ws_o;
   p.ws_lse = h->ws_lse;
   p.err = h->err;
+  p.counters = h->counters;
   p.Hq = c.num_q_heads;
   p.Hkv = c.num_kv_heads;
   p.max_blocks = max_blocks;
@@ -343,22 +349,6 @@ int paged_decode_attn_run_ex(pda_handle h, const void* q, const void* k_cache,
                                       out_dtype == PDA_F32,
                                       &h->tmap_k, &h->tmap_v, p, batch, s);
   if (e != cudaSuccess) return cuda_fail("partial kernel launch", e);
-  if (S > 1) {
-    pda::MergeParams m;
-    m.o = h->ws_o;
-    m.lse = h->ws_lse;
-    m.context_lens = context_lens;
-    m.out = out;
-    m.rows = batch * c.num_q_heads;
-    m.num_splits = S;
-    m.head_dim = c.head_dim;
-    m.Hq = c.num_q_heads;
-    m.block_size = c.block_size;
-    m.max_blocks = max_blocks;
-    m.chunk_pages = chunk;
-    e = pda::launch_merge(m, out_dtype, s);
-    if (e != cudaSuccess) return cuda_fail("merge kernel launch", e);
-  }
   return PDA_OK;
 }
 
@@ -436,6 +426,9 @@ int paged_decode_attn_check_device_error(pda_handle h, int* code, int* detail, v
   int host[2] = {0, 0};
   e = cudaMemcpy(host, h->err, sizeof host, cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof host);
+  // a kernel that gave up may have left split tickets behind
+  if (e == cudaSuccess && host[0] == pda::kErrWaitTimeout)
+    e = cudaMemset(h->counters, 0, h->counter_bytes);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail("reading the device error word", e);
   *code = host[0];

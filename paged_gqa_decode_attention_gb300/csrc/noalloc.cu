@@ -1,9 +1,9 @@
 // paged_decode_attn_run_noalloc: the decode-attention call for callers that
 // must not allocate device memory (see the header for who they are).
 //
-// It launches the same split-K partial and merge kernels as
-// paged_decode_attn_run_ex, but their scratch (split partials, split LSEs and
-// the kernels' error word) is a fixed array compiled into this library
+// It launches the same split-K partial kernel as paged_decode_attn_run_ex,
+// but its scratch (split partials, split LSEs, split tickets and the error
+// word) is a fixed array compiled into this library
 // instead of a handle's cudaMalloc'd workspace. Nothing here allocates:
 // no cudaMalloc/cudaFree, no allocating library routine.
 #include <cuda.h>
@@ -24,11 +24,13 @@
 namespace {
 
 // Scratch capacity: 2^21 floats (8 MiB) of split partial outputs, 2^16 floats
-// (256 KiB) of split LSEs, and 64 ints for the kernels' error word.
+// (256 KiB) of split LSEs, 64 ints for the kernels' error word and 2^16 ints
+// (256 KiB) of split tickets, one per (sequence, kv head).
 constexpr size_t kPartialFloats = size_t(1) << 21;
 constexpr size_t kLseFloats = size_t(1) << 16;
 constexpr size_t kErrInts = 64;
-constexpr size_t kScratchBytes = (kPartialFloats + kLseFloats) * 4 + kErrInts * 4;
+constexpr size_t kCounterInts = size_t(1) << 16;
+constexpr size_t kScratchBytes = (kPartialFloats + kLseFloats) * 4 + (kErrInts + kCounterInts) * 4;
 
 // One copy per GPU that loads the library, alive until the process exits.
 // In host code this name is only a stand-in for the symbol; the device
@@ -151,6 +153,7 @@ extern "C" int paged_decode_attn_run_noalloc(const void* q, const void* k_cache,
   const size_t rows = (size_t)batch * num_q_heads;
   size_t fit = kPartialFloats / (rows * head_dim);
   if (kLseFloats / rows < fit) fit = kLseFloats / rows;
+  if ((size_t)batch * num_kv_heads > kCounterInts) fit = 1;  // no room for split tickets
   if (num_splits > 1 && (size_t)num_splits > fit) {
     char buf[256];
     snprintf(buf, sizeof buf,
@@ -198,9 +201,13 @@ extern "C" int paged_decode_attn_run_noalloc(const void* q, const void* k_cache,
   float* ws_lse = ws_o + kPartialFloats;
   int* err = reinterpret_cast<int*>(ws_lse + kLseFloats);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the error word must start at zero; the partials are fully written before use
+  int* counters = err + kErrInts;
+  // the error word and the split tickets must start at zero; the partials are
+  // fully written before use
   e = cudaMemsetAsync(err, 0, 2 * sizeof(int), s);
-  if (e != cudaSuccess) return cuda_fail("cudaMemsetAsync(error word)", e);
+  if (e == cudaSuccess && S > 1)
+    e = cudaMemsetAsync(counters, 0, (size_t)batch * num_kv_heads * sizeof(int), s);
+  if (e != cudaSuccess) return cuda_fail("cudaMemsetAsync(scratch)", e);
 
   pda::PartialParams p;
   p.q = q;
@@ -210,6 +217,7 @@ extern "C" int paged_decode_attn_run_noalloc(const void* q, const void* k_cache,
   p.ws_o = ws_o;
   p.ws_lse = ws_lse;
   p.err = err;
+  p.counters = counters;
   p.Hq = num_q_heads;
   p.Hkv = num_kv_heads;
   p.max_blocks = max_blocks;
@@ -219,21 +227,5 @@ extern "C" int paged_decode_attn_run_noalloc(const void* q, const void* k_cache,
   e = pda::launch_partial(pda::default_partial_kernel(group), group, block_size, dtype, false,
                           &tk, &tv, p, batch, s);
   if (e != cudaSuccess) return cuda_fail("partial kernel launch", e);
-  if (S > 1) {
-    pda::MergeParams m;
-    m.o = ws_o;
-    m.lse = ws_lse;
-    m.context_lens = context_lens;
-    m.out = out;
-    m.rows = (int)rows;
-    m.num_splits = S;
-    m.head_dim = head_dim;
-    m.Hq = num_q_heads;
-    m.block_size = block_size;
-    m.max_blocks = max_blocks;
-    m.chunk_pages = chunk;
-    e = pda::launch_merge(m, dtype, s);
-    if (e != cudaSuccess) return cuda_fail("merge kernel launch", e);
-  }
   return PDA_OK;
 }

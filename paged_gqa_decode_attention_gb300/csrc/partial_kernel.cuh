@@ -21,7 +21,7 @@
 // At the end the consumer warps' (max, sum, acc) states are merged through
 // shared memory; a sequence handled by a single split writes `out` directly,
 // otherwise the split writes its normalised partial and natural-log LSE to
-// the workspace for the merge kernel.
+// the workspace and the last split to finish merges them (split_merge.cuh).
 //
 // Logits are kept in base-2 units (q is pre-multiplied by scale * log2 e) so
 // the exponentials are exp2f; the LSE is converted back to natural log.
@@ -34,6 +34,7 @@
 
 #include "pda_internal.h"
 #include "ptx.cuh"
+#include "split_merge.cuh"
 
 namespace pda {
 namespace partial {
@@ -389,6 +390,9 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
       if (d == 0) p.ws_lse[r] = (M + log2f(Ls)) * kLn2;
     }
   }
+  // the last split of this (sequence, kv head) merges all of them into `out`
+  if (n_splits_b > 1)
+    finish_split<G, TOut>(p, b, h, n_splits_b, d, reinterpret_cast<float*>(base + 2 * kStageBytes), 1);
 }
 
 template <int G, int BS, bool FP16, bool OUT_F32>

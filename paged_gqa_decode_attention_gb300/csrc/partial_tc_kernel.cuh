@@ -47,6 +47,7 @@
 
 #include "pda_internal.h"
 #include "ptx.cuh"
+#include "split_merge.cuh"
 
 namespace pda {
 namespace tc {
@@ -434,6 +435,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (d == 0) p.ws_lse[r] = (m_run[g] + log2f(Ls)) * kLn2;
       }
     }
+    // the last split of this (sequence, kv head) merges all of them into `out`
+    // (the P operands are free: every PV has completed)
+    if (n_splits_b > 1)
+      finish_split<G, TOut>(p, b, h, n_splits_b, d, reinterpret_cast<float*>(base + kOffP), 1);
   }
 
   if (failed && lane == 0 && atomicCAS(p.err, 0, kErrWaitTimeout) == 0) p.err[1] = split;

@@ -29,6 +29,7 @@ struct PartialParams {
   float* ws_o;                 // [B, Hq, num_splits, D]
   float* ws_lse;               // [B, Hq, num_splits]
   int* err;                    // device error word
+  int* counters;               // [B, Hkv] split tickets for the fused merge; zero between calls
   int Hq;
   int Hkv;
   int max_blocks;
@@ -58,8 +59,12 @@ enum PartialKernel : int {
 };
 
 // The kernel a geometry uses unless overridden (PDA_PARTIAL_KERNEL): the
-// CUDA-core kernel, the faster one on the measured workloads so far.
-constexpr int default_partial_kernel(int group) { return group > 0 ? kPartialCudaCore : 0; }
+// faster one as measured on GB300. At G = 8 the CUDA-core kernel is bound by
+// its FMA work (2.1x slower than the tensor-core kernel on the 128-sequence
+// serving mix); at G <= 4 it is the faster one.
+constexpr int default_partial_kernel(int group) {
+  return group == 8 ? kPartialTensorCore : kPartialCudaCore;
+}
 
 // CTAs per SM each kernel is built for (its launch bounds and shared memory);
 // the planner's figure when no GPU is queried.

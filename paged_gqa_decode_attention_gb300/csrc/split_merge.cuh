@@ -1,0 +1,93 @@
+// Fused log-sum-exp merge, run by the last CTA of a (sequence, kv head) to
+// finish its splits (Loom Kernels landing page, "Supported now": the LSE part
+// of "Paged MQA/GQA decode - GQA packing + local split-K/LSE").
+//
+// Every split CTA writes its normalised partial o_s and natural-log lse_s,
+// makes them visible device-wide (__threadfence) and takes a ticket from an
+// atomic counter. The CTA that draws the last ticket merges:
+//   M = max_s lse_s,  w_s = exp(lse_s - M) / sum_s' exp(lse_s' - M),
+//   out = sum_s w_s o_s,
+// then resets the counter to zero for the next call. No CTA waits for
+// another: there is no spin, only the ticket.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
+#include "pda_internal.h"
+#include "ptx.cuh"
+
+namespace pda {
+
+template <typename TOut>
+__device__ __forceinline__ TOut merge_to_out(float x) {
+  if constexpr (std::is_same_v<TOut, float>) {
+    return x;
+  } else if constexpr (std::is_same_v<TOut, __half>) {
+    return __float2half_rn(x);
+  } else {
+    return __float2bfloat16_rn(x);
+  }
+}
+
+// Called by 128 threads (tid 0..127, thread tid owns output dim tid) after
+// each has written its part of this split's partial. `sw` is shared scratch
+// of at least G * 64 + 1 floats, `bar_id` a named barrier over exactly these
+// 128 threads.
+template <int G, typename TOut>
+__device__ __forceinline__ void finish_split(const PartialParams& p, int b, int h, int n_splits_b,
+                                             int tid, float* sw, int bar_id) {
+  static_assert(kHeadDim == 128, "one thread per output dim");
+  __threadfence();
+  named_bar_sync(bar_id, 128);
+  int* flag = reinterpret_cast<int*>(sw + G * 64);
+  if (tid == 0) {
+    const int prev = atomicAdd(p.counters + (int64_t)b * p.Hkv + h, 1);
+    *flag = (prev == n_splits_b - 1);
+  }
+  named_bar_sync(bar_id, 128);
+  if (!*flag) return;
+  __threadfence();
+  const int hq0 = h * G;
+  const int64_t row0 = (int64_t)b * p.Hq + hq0;
+  for (int i = tid; i < G * n_splits_b; i += 128) {
+    const int g = i / n_splits_b, s = i - g * n_splits_b;
+    sw[g * 64 + s] = __ldcg(p.ws_lse + (row0 + g) * p.num_splits + s);
+  }
+  named_bar_sync(bar_id, 128);
+  if (tid < G) {
+    float* w = sw + tid * 64;
+    float M = -INFINITY;
+    for (int s = 0; s < n_splits_b; ++s) M = fmaxf(M, w[s]);
+    float sum = 0.f;
+    for (int s = 0; s < n_splits_b; ++s) {
+      const float e = (w[s] == -INFINITY) ? 0.f : exp2f((w[s] - M) * kLog2e);
+      w[s] = e;
+      sum += e;
+    }
+    const float inv = 1.f / sum;
+    for (int s = 0; s < n_splits_b; ++s) w[s] *= inv;
+  }
+  named_bar_sync(bar_id, 128);
+  TOut* out = static_cast<TOut*>(p.out);
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float* o = p.ws_o + ((row0 + g) * p.num_splits) * kHeadDim + tid;
+    const float* w = sw + g * 64;
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    int s = 0;
+    for (; s + 4 <= n_splits_b; s += 4) {
+      acc0 = fmaf(w[s + 0], __ldcg(o + (s + 0) * kHeadDim), acc0);
+      acc1 = fmaf(w[s + 1], __ldcg(o + (s + 1) * kHeadDim), acc1);
+      acc2 = fmaf(w[s + 2], __ldcg(o + (s + 2) * kHeadDim), acc2);
+      acc3 = fmaf(w[s + 3], __ldcg(o + (s + 3) * kHeadDim), acc3);
+    }
+    for (; s < n_splits_b; ++s) acc0 = fmaf(w[s], __ldcg(o + s * kHeadDim), acc0);
+    out[(row0 + g) * kHeadDim + tid] = merge_to_out<TOut>((acc0 + acc1) + (acc2 + acc3));
+  }
+  if (tid == 0) p.counters[(int64_t)b * p.Hkv + h] = 0;  // ready for the next call
+}
+
+}  // namespace pda
