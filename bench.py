@@ -303,15 +303,21 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        attn.run(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.context_lens, wl.scale, out=out)
+        attn.run(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.context_lens, wl.scale, out=out,
+                 num_splits=args.splits)
 
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize(dev)
 
     # ---- timed region: K steps, inputs resident in HBM ----
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # graph timing (default when no L2 flush is needed): the K calls are
+    # captured as CUDA graphs of n_inner calls and replayed back to back, so
+    # host-side launch cost cannot leave the GPU idle between steps; one call
+    # is one kernel launch, so K / region time is the per-launch duration.
+    # eager timing (with L2 flushes): one call per step, CUDA events around
+    # each call on the launching stream.
+    use_graph = (args.timing == "graph") or (args.timing == "auto" and not flush)
     region0, region1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     uuid = None
     try:
@@ -319,28 +325,59 @@ def run_ours(args):
     except Exception:
         pass
     sampler = ClockSampler(uuid)
-    barrier()
-    torch.cuda.synchronize(dev)
-    with sampler:
-        region0.record(stream)
-        for i in range(args.steps):
-            if flush:
-                flush_buf.zero_()
-                flush_read.max()
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        region1.record(stream)
+    if use_graph:
+        n_inner = max(d for d in range(1, min(args.steps, 100) + 1) if args.steps % d == 0)
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for _ in range(n_inner):
+                step()
         torch.cuda.synchronize(dev)
-    barrier()
-    region_ms = region0.elapsed_time(region1)
-    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    step_ms_sum = sum(kernel_ms)
-    # with L2 flushing between steps the flush is not part of a step
-    timed_ms = step_ms_sum if flush else region_ms
+        graph.replay()  # warm replay
+        torch.cuda.synchronize(dev)
+        barrier()
+        torch.cuda.synchronize(dev)
+        with sampler:
+            cpu0 = time.perf_counter()
+            region0.record(stream)
+            for _ in range(args.steps // n_inner):
+                graph.replay()
+            region1.record(stream)
+            cpu_submit = time.perf_counter() - cpu0
+            torch.cuda.synchronize(dev)
+        barrier()
+        timed_ms = region0.elapsed_time(region1)
+        avg_launch_ms = timed_ms / args.steps
+        timing_desc = f"CUDA graph of {n_inner} calls replayed {args.steps // n_inner}x"
+    else:
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize(dev)
+        with sampler:
+            cpu0 = time.perf_counter()
+            region0.record(stream)
+            for i in range(args.steps):
+                if flush:
+                    flush_buf.zero_()
+                    flush_read.max()
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+            region1.record(stream)
+            cpu_submit = time.perf_counter() - cpu0
+            torch.cuda.synchronize(dev)
+        barrier()
+        kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        # with L2 flushing between steps the flush is not part of a step
+        timed_ms = sum(kernel_ms) if flush else region0.elapsed_time(region1)
+        avg_launch_ms = statistics.mean(kernel_ms)
+        timing_desc = "eager calls, CUDA events around each call"
+    print(f"[bench] timed {timed_ms:.3f} ms for {args.steps} steps; host submit "
+          f"{1e3 * cpu_submit:.3f} ms; {timing_desc}", file=sys.stderr)
     timed_ms_max = reduce_max(timed_ms, dev)
     value = (B * world * args.steps) / (timed_ms_max / 1e3)
-    avg_launch_ms = statistics.mean(kernel_ms)
 
     # ---- end to end: host buffers, copies inside the timed region ----
     q_h = wl.q.cpu().pin_memory()
@@ -359,7 +396,7 @@ def run_ours(args):
         q_d.copy_(q_h, non_blocking=True)
         bt_d.copy_(bt_h, non_blocking=True)
         cl_d.copy_(cl_h, non_blocking=True)
-        attn.run(q_d, wl.k_cache, wl.v_cache, bt_d, cl_d, wl.scale, out=out)
+        attn.run(q_d, wl.k_cache, wl.v_cache, bt_d, cl_d, wl.scale, out=out, num_splits=args.splits)
         out_h.copy_(out, non_blocking=True)
         stream.synchronize()
     e2e_s = reduce_max(time.perf_counter() - t0, dev)
@@ -378,7 +415,8 @@ def run_ours(args):
                    "kv_bytes_per_step": kv_bytes,
                    "l2": "inputs larger than L2 (KV per step >= 2x L2, no flush)" if not flush
                    else "L2 flushed between steps (write + read of 2x L2, outside the step events)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "timing": timing_desc},
         "kv_gbs": achieved,
         "kv_frac_of_peak": achieved / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -418,6 +456,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="long_b4_l32768")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--timing", choices=["auto", "graph", "eager"], default="auto")
+    ap.add_argument("--splits", type=int, default=0, help="split count (0 = the planner's)")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)

@@ -131,6 +131,23 @@ int encode_cache_map(CUtensorMap* m, const void* base, int Hkv, int bs, int64_t 
   return PDA_OK;
 }
 
+// A [B * Hq, 128] view of q, loaded as boxes of 64 dims x G rows (the G
+// query heads of one kv head) with 128-byte swizzle.
+int encode_q_map(CUtensorMap* m, const void* q, int64_t rows, int group) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return fail(PDA_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {(cuuint64_t)pda::kHeadDim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)pda::kHeadDim * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)group};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(q), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(PDA_ECUDA, "cuTensorMapEncodeTiled (q) failed with CUresult " + std::to_string(r));
+  return PDA_OK;
+}
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
   return na && nb && a0 < b0 + nb && b0 < a0 + na;
@@ -328,6 +345,15 @@ int paged_decode_attn_run_ex(pda_handle h, const void* q, const void* k_cache,
   int S = 1, chunk = 1;
   plan_splits(c, h->num_sms, h->ctas_per_sm, batch, max_blocks, max_context_len_hint, num_splits,
               &S, &chunk);
+  const int64_t units = (int64_t)S * c.num_kv_heads * batch;
+  if (units > INT_MAX) return fail(PDA_EINVAL, "splits * num_kv_heads * batch exceeds 2^31");
+  alignas(64) CUtensorMap tmap_q;
+  if (h->kernel == pda::kPartialTensorCore) {
+    int st = encode_q_map(&tmap_q, q, (int64_t)batch * c.num_q_heads, h->group);
+    if (st != PDA_OK) return st;
+  } else {
+    std::memset(&tmap_q, 0, sizeof tmap_q);
+  }
 
   pda::PartialParams p;
   p.q = q;
@@ -344,10 +370,12 @@ int paged_decode_attn_run_ex(pda_handle h, const void* q, const void* k_cache,
   p.chunk_pages = chunk;
   p.num_splits = S;
   p.qscale = scale * pda::kLog2e;
+  p.num_units = (int)units;
+  p.max_ctas = h->num_sms * h->ctas_per_sm;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = pda::launch_partial(h->kernel, h->group, c.block_size, c.dtype,
-                                      out_dtype == PDA_F32,
-                                      &h->tmap_k, &h->tmap_v, p, batch, s);
+                                      out_dtype == PDA_F32, &h->tmap_k, &h->tmap_v, &tmap_q, p,
+                                      batch, s);
   if (e != cudaSuccess) return cuda_fail("partial kernel launch", e);
   return PDA_OK;
 }

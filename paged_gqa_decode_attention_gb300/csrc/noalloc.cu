@@ -14,6 +14,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 #include <set>
 #include <tuple>
@@ -84,6 +85,19 @@ bool encode(CUtensorMap* m, const void* base, int Hkv, int bs, int64_t num_block
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [B * Hq, 128] view of q, boxes of 64 dims x G rows (tensor-core kernel).
+bool encode_q(CUtensorMap* m, const void* q, int64_t rows, int group) {
+  auto fn = encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)pda::kHeadDim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)pda::kHeadDim * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)group};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(q), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Once per device (with `dev` current): the scratch array's device address,
@@ -192,9 +206,15 @@ extern "C" int paged_decode_attn_run_noalloc(const void* q, const void* k_cache,
     if (st != PDA_OK) return st;
   }
 
-  alignas(64) CUtensorMap tk, tv;
+  const int kernel = pda::default_partial_kernel(group);
+  const int64_t units = (int64_t)S * num_kv_heads * batch;
+  if (units > INT_MAX) return fail(PDA_EINVAL, "splits * num_kv_heads * batch exceeds 2^31");
+  alignas(64) CUtensorMap tk, tv, tq;
+  std::memset(&tq, 0, sizeof tq);
   if (!encode(&tk, k_cache, num_kv_heads, block_size, num_blocks) ||
-      !encode(&tv, v_cache, num_kv_heads, block_size, num_blocks))
+      !encode(&tv, v_cache, num_kv_heads, block_size, num_blocks) ||
+      (kernel == pda::kPartialTensorCore &&
+       !encode_q(&tq, q, (int64_t)batch * num_q_heads, group)))
     return fail(PDA_ECUDA, "cuTensorMapEncodeTiled failed");
 
   float* ws_o = static_cast<float*>(scratch);
@@ -224,8 +244,9 @@ extern "C" int paged_decode_attn_run_noalloc(const void* q, const void* k_cache,
   p.chunk_pages = chunk;
   p.num_splits = S;
   p.qscale = scale * pda::kLog2e;
-  e = pda::launch_partial(pda::default_partial_kernel(group), group, block_size, dtype, false,
-                          &tk, &tv, p, batch, s);
+  p.num_units = (int)units;
+  p.max_ctas = num_sms * pda::partial_ctas_per_sm_hint(kernel, group);
+  e = pda::launch_partial(kernel, group, block_size, dtype, false, &tk, &tv, &tq, p, batch, s);
   if (e != cudaSuccess) return cuda_fail("partial kernel launch", e);
   return PDA_OK;
 }

@@ -165,8 +165,10 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
       prefetch_tensormap(&tmap_v);
     }
     const int32_t* table = p.block_table + (int64_t)b * p.max_blocks;
+    // block-table entries in windows of 32 pages, the next window prefetched
     int win_base = p0;
     int win_blk = (p0 + lane < p1) ? __ldg(table + p0 + lane) : 0;
+    int nxt_blk = (p0 + 32 + lane < p1) ? __ldg(table + p0 + 32 + lane) : 0;
     for (int c = 0; c < n_chunks; ++c) {
       const int slot = c % kStages;
       if (c >= kStages) {
@@ -178,9 +180,10 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
       }
       const int pg0 = p0 + c * PPS;
       const int npg = min(PPS, p1 - pg0);
-      if (pg0 + PPS > win_base + 32) {
-        win_base = pg0;
-        win_blk = (pg0 + lane < p1) ? __ldg(table + pg0 + lane) : 0;
+      if (pg0 + PPS > win_base + 32) {  // pg0 == win_base + 32: PPS divides 32
+        win_base += 32;
+        win_blk = nxt_blk;
+        nxt_blk = (win_base + 32 + lane < p1) ? __ldg(table + win_base + 32 + lane) : 0;
       }
       int blk[PPS];
 #pragma unroll

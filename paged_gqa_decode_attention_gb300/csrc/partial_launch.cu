@@ -9,9 +9,9 @@ cudaError_t launch_partial_bf16(int, int, bool, const CUtensorMap*, const CUtens
 cudaError_t launch_partial_fp16(int, int, bool, const CUtensorMap*, const CUtensorMap*,
                                const PartialParams&, int, cudaStream_t);
 cudaError_t launch_partial_tc_bf16(int, int, bool, const CUtensorMap*, const CUtensorMap*,
-                                  const PartialParams&, int, cudaStream_t);
+                                  const CUtensorMap*, const PartialParams&, cudaStream_t);
 cudaError_t launch_partial_tc_fp16(int, int, bool, const CUtensorMap*, const CUtensorMap*,
-                                  const PartialParams&, int, cudaStream_t);
+                                  const CUtensorMap*, const PartialParams&, cudaStream_t);
 cudaError_t prepare_partial_bf16(int, int);
 cudaError_t prepare_partial_fp16(int, int);
 cudaError_t prepare_partial_tc_bf16(int, int);
@@ -49,11 +49,11 @@ int partial_ctas_per_sm(int kernel, int group, int block_size, int dtype) {
 }
 
 cudaError_t launch_partial(int kernel, int group, int block_size, int dtype, bool out_f32,
-                           const CUtensorMap* tk, const CUtensorMap* tv, const PartialParams& p,
-                           int batch, cudaStream_t stream) {
+                           const CUtensorMap* tk, const CUtensorMap* tv, const CUtensorMap* tq,
+                           const PartialParams& p, int batch, cudaStream_t stream) {
   if (kernel == kPartialTensorCore)
-    return dtype == 1 ? launch_partial_tc_fp16(group, block_size, out_f32, tk, tv, p, batch, stream)
-                      : launch_partial_tc_bf16(group, block_size, out_f32, tk, tv, p, batch, stream);
+    return dtype == 1 ? launch_partial_tc_fp16(group, block_size, out_f32, tk, tv, tq, p, stream)
+                      : launch_partial_tc_bf16(group, block_size, out_f32, tk, tv, tq, p, stream);
   return dtype == 1 ? launch_partial_fp16(group, block_size, out_f32, tk, tv, p, batch, stream)
                     : launch_partial_bf16(group, block_size, out_f32, tk, tv, p, batch, stream);
 }

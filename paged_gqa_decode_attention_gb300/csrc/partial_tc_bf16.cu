@@ -4,9 +4,9 @@
 namespace pda {
 
 cudaError_t launch_partial_tc_bf16(int G, int BS, bool f32, const CUtensorMap* tk,
-                                  const CUtensorMap* tv, const PartialParams& p, int batch,
-                                  cudaStream_t s) {
-  return tc::Dispatch<false>::launch(G, BS, f32, tk, tv, p, batch, s);
+                                  const CUtensorMap* tv, const CUtensorMap* tq,
+                                  const PartialParams& p, cudaStream_t s) {
+  return tc::Dispatch<false>::launch(G, BS, f32, tk, tv, tq, p, s);
 }
 
 cudaError_t prepare_partial_tc_bf16(int G, int BS) { return tc::Dispatch<false>::prepare(G, BS); }

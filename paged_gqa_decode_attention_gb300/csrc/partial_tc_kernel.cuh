@@ -1,12 +1,14 @@
 // Split-K partial kernel on the 5th-generation tensor cores (tcgen05, TMEM
 // accumulators) for GQA groups of G = 4 or 8 query heads per kv head.
 //
-// Same method and work decomposition as the CUDA-core kernel
-// (partial_kernel.cuh): one CTA per (split, kv head, sequence), split-K with
-// a normalised partial and its log-sum-exp per split (Loom Kernels landing
-// page, "Supported now": Paged MQA/GQA decode, GQA packing + local
-// split-K/LSE). What changes is where the two contractions of a 128-token
-// chunk run. With the G query rows packed as the N side of the MMA:
+// Same method and work units as the CUDA-core kernel (partial_kernel.cuh):
+// a unit is one (split, kv head, sequence), split-K with a normalised partial
+// and its log-sum-exp per split (Loom Kernels landing page, "Supported now":
+// Paged MQA/GQA decode, GQA packing + local split-K/LSE). Here the kernel is
+// persistent: one CTA per SM walks the units u = blockIdx.x + k * gridDim.x,
+// and every role streams across unit boundaries, so the TMA rings stay full
+// from the first unit to the last. The two contractions of a 128-token chunk
+// run on the tensor cores, with the G query rows packed as the N side:
 //
 //   S^T [128 tokens x 16]  = K_chunk [128 x 128 dims] . Q^T [128 dims x 16]
 //   O^T [128 dims   x 16]  = V_chunk^T [128 dims x 128 tokens] . P^T [128 x 16]
@@ -29,6 +31,8 @@
 //   warps 4 and 5: producers, TMA page loads of K and of V into two separate
 //     3-slot rings (a slot is 128 tokens, 32 KiB): a K slot is released as
 //     soon as its QK^T completes, a V slot after its PV, so K loads run ahead.
+//     The K producer also loads each unit's G query rows (a TMA box) into one
+//     of two Q operand buffers.
 //   warp 6: allocates 64 TMEM columns (S0, S1, O0, O1, 16 each), issues the
 //     MMAs and commits their completion to mbarriers.
 // S, O and P are double-buffered by chunk parity so the chunks overlap: the
@@ -69,12 +73,12 @@ constexpr unsigned kFull = 0xffffffffu;
 
 constexpr int kOffK = 0;
 constexpr int kOffV = kStages * kSlotBytes;
-constexpr int kOffQ = 2 * kStages * kSlotBytes;
-constexpr int kOffP = kOffQ + kOpBytes;         // [2 buffers][hi, lo] operands
+constexpr int kOffQ = 2 * kStages * kSlotBytes;  // [2 buffers] Q operands
+constexpr int kOffP = kOffQ + 2 * kOpBytes;      // [2 buffers][hi, lo] operands
 constexpr int kOffRed = kOffP + 4 * kOpBytes;    // 2 x [4 warps][8] floats (chunk maxima)
 constexpr int kOffLred = kOffRed + 2 * 4 * 8 * 4;  // [4 warps][8] floats (final sums)
 constexpr int kOffBar = kOffLred + 4 * 8 * 4;
-constexpr int kNumBars = 4 * kStages + 10;
+constexpr int kNumBars = 4 * kStages + 14;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr size_t kSmemBytes = 1024 + kOffTmem + 16;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -110,10 +114,75 @@ __device__ __forceinline__ uint32_t op_offset(int n, int k) {
          (col & 7) * 2;
 }
 
+// One work unit: (split, kv head, sequence) and its page / token / chunk range.
+struct Unit {
+  int b, h, split, n_splits_b;
+  int p0, p1, t0, t1, n_chunks;
+  bool zero_fill;  // an empty context whose output rows this unit writes as zeros
+};
+
+template <int BS>
+__device__ __forceinline__ Unit load_unit(const PartialParams& p, int u) {
+  constexpr int PPS = kT / BS;
+  Unit U;
+  U.split = u % p.num_splits;
+  const int rest = u / p.num_splits;
+  U.h = rest % p.Hkv;
+  U.b = rest / p.Hkv;
+  int L = __ldg(p.context_lens + U.b);
+  const int maxL = p.max_blocks * BS;
+  L = L < 0 ? 0 : (L > maxL ? maxL : L);
+  const int n_pages = (L + BS - 1) / BS;
+  int nsb = (n_pages + p.chunk_pages - 1) / p.chunk_pages;
+  if (nsb > p.num_splits) nsb = p.num_splits;  // the last split takes the rest
+  U.n_splits_b = nsb;
+  U.zero_fill = (nsb == 0 && U.split == 0);
+  if (U.split >= nsb) {
+    U.p0 = U.p1 = U.t0 = U.t1 = U.n_chunks = 0;
+    return U;
+  }
+  U.p0 = U.split * p.chunk_pages;
+  U.p1 = (U.split == nsb - 1) ? n_pages : min(U.p0 + p.chunk_pages, n_pages);
+  U.t0 = U.p0 * BS;
+  U.t1 = min(U.p1 * BS, L);
+  U.n_chunks = (U.p1 - U.p0 + PPS - 1) / PPS;
+  return U;
+}
+
+// Walks this CTA's units with work, chunk by chunk: c counts chunks over the
+// whole walk (ring slots and buffer parities follow it), j counts units.
+template <int BS>
+struct Cursor {
+  int u, i, c, j;
+  Unit U;
+  __device__ __forceinline__ void seek(const PartialParams& p) {
+    for (; u < p.num_units; u += gridDim.x) {
+      U = load_unit<BS>(p, u);
+      if (U.n_chunks > 0) return;
+    }
+  }
+  __device__ __forceinline__ void start(const PartialParams& p) {
+    u = blockIdx.x;
+    i = c = j = 0;
+    seek(p);
+  }
+  __device__ __forceinline__ bool valid(const PartialParams& p) const { return u < p.num_units; }
+  __device__ __forceinline__ void advance(const PartialParams& p) {
+    ++c;
+    if (++i == U.n_chunks) {
+      i = 0;
+      ++j;
+      u += gridDim.x;
+      seek(p);
+    }
+  }
+};
+
 template <int G, int BS, bool FP16, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_partial_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                            const __grid_constant__ CUtensorMap tmap_v, const PartialParams p) {
+                            const __grid_constant__ CUtensorMap tmap_v,
+                            const __grid_constant__ CUtensorMap tmap_q, const PartialParams p) {
   static_assert(G == 4 || G == 8, "tensor-core path packs 4 or 8 query heads");
   constexpr int PPS = kT / BS;  // pages per stage
   static_assert(kT % BS == 0 && PPS <= 32, "stage must hold whole pages");
@@ -134,36 +203,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto p_full = [&](int b) { return bar0 + 8u * (4 * kStages + 4 + b); };
   auto o_full = [&](int b) { return bar0 + 8u * (4 * kStages + 6 + b); };
   auto o_free = [&](int b) { return bar0 + 8u * (4 * kStages + 8 + b); };
+  auto q_full = [&](int b) { return bar0 + 8u * (4 * kStages + 10 + b); };
+  auto q_empty = [&](int b) { return bar0 + 8u * (4 * kStages + 12 + b); };
 
-  const int split = blockIdx.x;
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int hq0 = h * G;
-  TOut* out = static_cast<TOut*>(p.out);
-
-  int L = __ldg(p.context_lens + b);
-  const int maxL = p.max_blocks * BS;
-  L = L < 0 ? 0 : (L > maxL ? maxL : L);
-  const int n_pages = (L + BS - 1) / BS;
-  int n_splits_b = (n_pages + p.chunk_pages - 1) / p.chunk_pages;
-  if (n_splits_b > p.num_splits) n_splits_b = p.num_splits;
-
-  if (n_splits_b == 0) {  // empty context: zero output rows
-    if (split == 0) {
-      for (int i = threadIdx.x; i < G * kHeadDim; i += kThreads)
-        out[((int64_t)b * p.Hq + hq0) * kHeadDim + i] = to_out<TOut>(0.f);
-    }
-    return;
-  }
-  if (split >= n_splits_b) return;
-
-  const int p0 = split * p.chunk_pages;
-  const int p1 = (split == n_splits_b - 1) ? n_pages : min(p0 + p.chunk_pages, n_pages);
-  const int t0 = p0 * BS;
-  const int t1 = min(p1 * BS, L);
-  const int n_chunks = (p1 - p0 + PPS - 1) / PPS;
 
   if (threadIdx.x == 0) {
     for (int r = 0; r < 2; ++r)
@@ -177,6 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(p_full(b2), 4);
       mbar_init(o_full(b2), 1);
       mbar_init(o_free(b2), 4);
+      mbar_init(q_full(b2), 1);
+      mbar_init(q_empty(b2), 1);
     }
     fence_mbar_init();
   }
@@ -185,19 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp < 4) {
-    // Q rows of the group as the B operand of QK^T (raw values; the scale is
-    // applied to S in fp32), rows G..15 zero; both P operands zeroed.
-    const int t = threadIdx.x;
-    const uint8_t* qb = static_cast<const uint8_t*>(p.q) + (((int64_t)b * p.Hq + hq0) * kHeadDim) * 2;
-    for (int i = t; i < 2 * kN * 8; i += 128) {
-      const int half = i >> 7, g = (i >> 3) & 15, c = i & 7;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (g < G) v = __ldg(reinterpret_cast<const uint4*>(qb + (g * kHeadDim + half * 64 + c * 8) * 2));
-      *reinterpret_cast<uint4*>(base + kOffQ + half * kOpHalf + (g >> 3) * 1024 + (g & 7) * 128 +
-                                ((c ^ (g & 7)) << 4)) = v;
-    }
-    for (int i = t; i < 4 * kOpBytes / 16; i += 128)
-      *reinterpret_cast<uint4*>(base + kOffP + i * 16) = make_uint4(0, 0, 0, 0);
+    // Q operands (rows G..15 stay zero; the TMA box fills rows 0..G-1) and
+    // both P operand pairs start zeroed.
+    for (int i = threadIdx.x; i < (2 * kOpBytes + 4 * kOpBytes) / 16; i += 128)
+      *reinterpret_cast<uint4*>(base + kOffQ + i * 16) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -213,11 +250,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------- producers: K ring (warp 4), V ring (warp 5) -------------------
     const int r = warp - kWarpProducerK;
     const CUtensorMap* map = r == 0 ? &tmap_k : &tmap_v;
-    if (lane == 0) prefetch_tensormap(map);
-    const int32_t* table = p.block_table + (int64_t)b * p.max_blocks;
-    int win_base = p0;
-    int win_blk = (p0 + lane < p1) ? __ldg(table + p0 + lane) : 0;
-    for (int c = 0; c < n_chunks; ++c) {
+    if (lane == 0) {
+      prefetch_tensormap(map);
+      if (r == 0) prefetch_tensormap(&tmap_q);
+    }
+    Cursor<BS> cur;
+    cur.start(p);
+    // block-table entries in windows of 32 pages, the next window prefetched
+    int win_base = 0, win_blk = 0, nxt_blk = 0;
+    while (cur.valid(p) && !failed) {
+      const Unit& U = cur.U;
+      const int32_t* table = p.block_table + (int64_t)U.b * p.max_blocks;
+      if (cur.i == 0) {
+        win_base = U.p0;
+        win_blk = (U.p0 + lane < U.p1) ? __ldg(table + U.p0 + lane) : 0;
+        nxt_blk = (U.p0 + 32 + lane < U.p1) ? __ldg(table + U.p0 + 32 + lane) : 0;
+        if (r == 0) {
+          // this unit's G query rows -> Q operand buffer j & 1
+          const int qb = cur.j & 1;
+          bool ok = true;
+          if (cur.j >= 2) ok = mbar_wait(q_empty(qb), ((cur.j - 2) >> 1) & 1);
+          if (!__all_sync(kFull, ok)) {
+            failed = true;
+            break;
+          }
+          if (lane == 0) {
+            const uint32_t fb = q_full(qb);
+            mbar_arrive_expect_tx(fb, (uint32_t)G * 2 * kRowBytes);
+            const uint32_t qdst = base_u32 + kOffQ + qb * kOpBytes;
+            const int row = U.b * p.Hq + U.h * G;
+            tma_load_2d(qdst, &tmap_q, 0, row, fb);
+            tma_load_2d(qdst + kOpHalf, &tmap_q, 64, row, fb);
+          }
+          __syncwarp();
+        }
+      }
+      const int c = cur.c;
       const int slot = c % kStages;
       if (c >= kStages) {
         const bool ok = mbar_wait(empty_bar(r, slot), ((c / kStages) - 1) & 1);
@@ -226,11 +294,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
-      const int pg0 = p0 + c * PPS;
-      const int npg = min(PPS, p1 - pg0);
-      if (pg0 + PPS > win_base + 32) {
-        win_base = pg0;
-        win_blk = (pg0 + lane < p1) ? __ldg(table + pg0 + lane) : 0;
+      const int pg0 = U.p0 + cur.i * PPS;
+      const int npg = min(PPS, U.p1 - pg0);
+      if (pg0 + PPS > win_base + 32) {  // pg0 == win_base + 32: PPS divides 32
+        win_base += 32;
+        win_blk = nxt_blk;
+        nxt_blk = (win_base + 32 + lane < U.p1) ? __ldg(table + win_base + 32 + lane) : 0;
       }
       int blk[PPS];
 #pragma unroll
@@ -244,73 +313,91 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (i < npg) {
             const int y = blk[i] * BS;
             const uint32_t ro = (uint32_t)(i * BS * kRowBytes);
-            tma_load_2d(st + ro, map, h * kHeadDim, y, fb);
-            tma_load_2d(st + kHalf + ro, map, h * kHeadDim + 64, y, fb);
+            tma_load_2d(st + ro, map, U.h * kHeadDim, y, fb);
+            tma_load_2d(st + kHalf + ro, map, U.h * kHeadDim + 64, y, fb);
           }
         }
       }
       __syncwarp();
+      cur.advance(p);
     }
   } else if (warp == kWarpMma) {
     // ------------------------------ MMA issue -----------------------------
     constexpr uint32_t idesc_qk = idesc_f16(128, kN, !FP16, false, false);
     constexpr uint32_t idesc_pv = idesc_f16(128, kN, !FP16, true, false);
-    const uint32_t q_u32 = base_u32 + kOffQ;
-    // S(c) = K(c) . Q^T into S[c & 1]; needs the stage and the softmax's read of S(c-2)
-    auto issue_qk = [&](int c) {
-      const int slot = c % kStages;
+    // S(c) = K(c) . Q^T into S[c & 1]; needs the K slot, the unit's Q and the
+    // softmax's read of S(c-2)
+    auto issue_qk = [&](const Cursor<BS>& cur) {
+      const int c = cur.c, slot = c % kStages, qb = cur.j & 1;
       bool ok = !failed && mbar_wait(full_bar(0, slot), (c / kStages) & 1);
       if (ok && c >= 2) ok = mbar_wait(s_free(c & 1), ((c - 2) >> 1) & 1);
+      if (ok && cur.i == 0) ok = mbar_wait(q_full(qb), (cur.j >> 1) & 1);
       if (!__all_sync(kFull, ok)) failed = true;
       if (failed) return;
       tc_fence_after();
       if (lane == 0) {
         const uint32_t kb = base_u32 + kOffK + slot * kSlotBytes;
+        const uint32_t qa = base_u32 + kOffQ + qb * kOpBytes;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint64_t a = sdesc_sw128(kb + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
-          const uint64_t bq = sdesc_sw128(q_u32 + (k >> 2) * kOpHalf + (k & 3) * 32, 16, 1024);
+          const uint64_t bq = sdesc_sw128(qa + (k >> 2) * kOpHalf + (k & 3) * 32, 16, 1024);
           mma_f16_ss(tS(c & 1), a, bq, idesc_qk, k > 0 ? 1u : 0u);
         }
         mma_commit(s_full(c & 1));
-        mma_commit(empty_bar(0, slot));  // K slot free once QK^T has read it
+        mma_commit(empty_bar(0, slot));                          // K slot read
+        if (cur.i == cur.U.n_chunks - 1) mma_commit(q_empty(qb));  // unit's Q read
       }
       __syncwarp();
     };
-    if (n_chunks > 0) issue_qk(0);
-    for (int c = 0; c < n_chunks; ++c) {
-      if (c + 1 < n_chunks) issue_qk(c + 1);
-      // O(c) = V(c)^T . P(c)^T into O[c & 1]; needs P(c) and the fold of O(c-2)
-      const int vslot = c % kStages;
-      bool ok = !failed && mbar_wait(full_bar(1, vslot), (c / kStages) & 1);
+    // O(c) = V(c)^T . P(c)^T into O[c & 1]; needs the V slot, P(c) and the
+    // fold of O(c-2)
+    auto issue_pv = [&](const Cursor<BS>& cur) {
+      const int c = cur.c, slot = c % kStages;
+      bool ok = !failed && mbar_wait(full_bar(1, slot), (c / kStages) & 1);
       if (ok) ok = mbar_wait(p_full(c & 1), (c >> 1) & 1);
       if (ok && c >= 2) ok = mbar_wait(o_free(c & 1), ((c - 2) >> 1) & 1);
       if (!__all_sync(kFull, ok)) failed = true;
-      if (!failed) {
-        tc_fence_after();
-        if (lane == 0) {
-          const int slot = vslot;
-          const uint32_t vb = base_u32 + kOffV + slot * kSlotBytes;
-          const uint32_t phi = base_u32 + kOffP + (c & 1) * 2 * kOpBytes;
-          const uint32_t plo = phi + kOpBytes;
+      if (failed) return;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t vb = base_u32 + kOffV + slot * kSlotBytes;
+        const uint32_t phi = base_u32 + kOffP + (c & 1) * 2 * kOpBytes;
+        const uint32_t plo = phi + kOpBytes;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            // V^T as an MN-major A operand: 64-dim halves kHalf apart (LBO),
-            // 8-token row groups 1 KiB apart (SBO); 16 tokens per step
-            const uint64_t a = sdesc_sw128(vb + k * 2048, kHalf, 1024);
-            const uint32_t po = (k >> 2) * kOpHalf + (k & 3) * 32;
-            mma_f16_ss(tO(c & 1), a, sdesc_sw128(phi + po, 16, 1024), idesc_pv, k > 0 ? 1u : 0u);
-            mma_f16_ss(tO(c & 1), a, sdesc_sw128(plo + po, 16, 1024), idesc_pv, 1u);
-          }
-          mma_commit(o_full(c & 1));
-          mma_commit(empty_bar(1, slot));
+        for (int k = 0; k < 8; ++k) {
+          // V^T as an MN-major A operand: 64-dim halves kHalf apart (LBO),
+          // 8-token row groups 1 KiB apart (SBO); 16 tokens per step
+          const uint64_t a = sdesc_sw128(vb + k * 2048, kHalf, 1024);
+          const uint32_t po = (k >> 2) * kOpHalf + (k & 3) * 32;
+          mma_f16_ss(tO(c & 1), a, sdesc_sw128(phi + po, 16, 1024), idesc_pv, k > 0 ? 1u : 0u);
+          mma_f16_ss(tO(c & 1), a, sdesc_sw128(plo + po, 16, 1024), idesc_pv, 1u);
         }
-        __syncwarp();
+        mma_commit(o_full(c & 1));
+        mma_commit(empty_bar(1, slot));  // V slot read
       }
+      __syncwarp();
+    };
+    Cursor<BS> qk, pv;
+    qk.start(p);
+    pv = qk;
+    if (qk.valid(p)) {
+      issue_qk(qk);
+      qk.advance(p);
     }
-    // Drain the last stages' completion arrivals so that no MMA commit lands
-    // on this CTA's shared memory after it exits.
-    for (int c = n_chunks > kStages ? n_chunks - kStages : 0; c < n_chunks && !failed; ++c) {
+    int last_c = -1;
+    while (pv.valid(p) && !failed) {
+      if (qk.valid(p)) {
+        issue_qk(qk);
+        qk.advance(p);
+      }
+      issue_pv(pv);
+      last_c = pv.c;
+      pv.advance(p);
+    }
+    // Drain the last slots' completion arrivals so that no MMA commit lands on
+    // this CTA's shared memory after it exits.
+    for (int c = last_c - kStages + 1 > 0 ? last_c - kStages + 1 : 0; c <= last_c && !failed; ++c) {
       bool ok = mbar_wait(empty_bar(0, c % kStages), (c / kStages) & 1);
       if (ok) ok = mbar_wait(empty_bar(1, c % kStages), (c / kStages) & 1);
       if (!__all_sync(kFull, ok)) failed = true;
@@ -319,16 +406,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------- softmax and epilogue ------------------------
     const int t = threadIdx.x;  // token row of S; output dim of O
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float m_run[G], l_th[G], acc[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      m_run[g] = -INFINITY;
-      l_th[g] = 0.f;
-      acc[g] = 0.f;
-    }
+    TOut* out = static_cast<TOut*>(p.out);
     float* red = reinterpret_cast<float*>(base + kOffRed);
-    float alpha_prev[G];
-    // acc = acc * alpha(c) + O(c), for the chunk before the current one
+    float* lred = reinterpret_cast<float*>(base + kOffLred);
+    float m_run[G], l_th[G], acc[G], alpha_prev[G];
+    // acc = acc * alpha(c) + O(c)
     auto fold = [&](int c) {
       bool ok = !failed && mbar_wait(o_full(c & 1), (c >> 1) & 1);
       if (!__all_sync(kFull, ok)) failed = true;
@@ -346,102 +428,122 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int g = 0; g < G; ++g) acc[g] = acc[g] * alpha_prev[g] + o[g];
     };
-    for (int c = 0; c < n_chunks; ++c) {
-      const int slot = c % kStages;
-      const int n_valid = min(kT, t1 - (t0 + c * kT));
-      bool ok = !failed && mbar_wait(s_full(c & 1), (c >> 1) & 1);
-      if (!__all_sync(kFull, ok)) failed = true;
-      tc_fence_after();
-      float s[G];
-      if constexpr (G == 4) {
-        tmem_ld_x4(tS(c & 1) + lane_base, s);
-      } else {
-        tmem_ld_x8(tS(c & 1) + lane_base, s);
+    int c = 0;
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+      const Unit U = load_unit<BS>(p, u);
+      const int hq0 = U.h * G;
+      if (U.zero_fill) {
+        for (int i = t; i < G * kHeadDim; i += 128)
+          out[((int64_t)U.b * p.Hq + hq0) * kHeadDim + i] = to_out<TOut>(0.f);
       }
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free(c & 1));
-#pragma unroll
-      for (int g = 0; g < G; ++g) s[g] = (t < n_valid) ? s[g] * p.qscale : -INFINITY;
-      float* rb = red + (c & 1) * 32;
+      if (U.n_chunks == 0) continue;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float mx = s[g];
+        m_run[g] = -INFINITY;
+        l_th[g] = 0.f;
+        acc[g] = 0.f;
+      }
+      for (int i = 0; i < U.n_chunks; ++i, ++c) {
+        const int slot = c % kStages;
+        const int n_valid = min(kT, U.t1 - (U.t0 + i * kT));
+        bool ok = !failed && mbar_wait(s_full(c & 1), (c >> 1) & 1);
+        if (!__all_sync(kFull, ok)) failed = true;
+        tc_fence_after();
+        float s[G];
+        if constexpr (G == 4) {
+          tmem_ld_x4(tS(c & 1) + lane_base, s);
+        } else {
+          tmem_ld_x8(tS(c & 1) + lane_base, s);
+        }
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free(c & 1));
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
-        if (lane == 0) rb[warp * 8 + g] = mx;
+        for (int g = 0; g < G; ++g) s[g] = (t < n_valid) ? s[g] * p.qscale : -INFINITY;
+        float* rb = red + (c & 1) * 32;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float mx = s[g];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+          if (lane == 0) rb[warp * 8 + g] = mx;
+        }
+        named_bar_sync(1, 128);
+        float alpha[G];
+        uint8_t* pb = base + kOffP + (c & 1) * 2 * kOpBytes;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float mx = fmaxf(fmaxf(rb[g], rb[8 + g]), fmaxf(rb[16 + g], rb[24 + g]));
+          const float mn = fmaxf(m_run[g], mx);  // finite: every chunk holds a valid token
+          alpha[g] = exp2f(m_run[g] - mn);
+          m_run[g] = mn;
+          const float pr = exp2f(s[g] - mn);
+          l_th[g] = l_th[g] * alpha[g] + pr;
+          const typename H::T hi = H::from(pr);
+          const typename H::T lo = H::from(pr - H::to(hi));
+          const uint32_t off = op_offset(g, t);
+          *reinterpret_cast<typename H::T*>(pb + off) = hi;
+          *reinterpret_cast<typename H::T*>(pb + kOpBytes + off) = lo;
+        }
+        if (n_valid < kT) {
+          // keep stale or out-of-context V rows out of the MMA; the V tile of
+          // this chunk must have landed first (its last page may be partial)
+          ok = !failed && mbar_wait(full_bar(1, slot), (c / kStages) & 1);
+          if (!__all_sync(kFull, ok)) failed = true;
+        }
+        if (t >= n_valid) {
+          uint8_t* vrow = base + kOffV + slot * kSlotBytes + t * kRowBytes;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<uint4*>(vrow + hh * kHalf + q * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(c & 1));
+        if (i > 0) fold(c - 1);
+#pragma unroll
+        for (int g = 0; g < G; ++g) alpha_prev[g] = alpha[g];
+      }
+      fold(c - 1);
+      // softmax denominators: sum the per-token partial sums over 128 threads
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float v = l_th[g];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+        if (lane == 0) lred[warp * 8 + g] = v;
       }
       named_bar_sync(1, 128);
-      float alpha[G];
-      uint8_t* pb = base + kOffP + (c & 1) * 2 * kOpBytes;
+      const int d = t;
+      float Ls[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) Ls[g] = lred[g] + lred[8 + g] + lred[16 + g] + lred[24 + g];
+      named_bar_sync(1, 128);  // lred is rewritten by the next unit
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float mx = fmaxf(fmaxf(rb[g], rb[8 + g]), fmaxf(rb[16 + g], rb[24 + g]));
-        const float mn = fmaxf(m_run[g], mx);  // finite: every chunk holds a valid token
-        alpha[g] = exp2f(m_run[g] - mn);
-        m_run[g] = mn;
-        const float pr = exp2f(s[g] - mn);
-        l_th[g] = l_th[g] * alpha[g] + pr;
-        const typename H::T hi = H::from(pr);
-        const typename H::T lo = H::from(pr - H::to(hi));
-        const uint32_t off = op_offset(g, t);
-        *reinterpret_cast<typename H::T*>(pb + off) = hi;
-        *reinterpret_cast<typename H::T*>(pb + kOpBytes + off) = lo;
+        const float o = acc[g] / Ls[g];
+        const int64_t row = (int64_t)U.b * p.Hq + hq0 + g;
+        if (U.n_splits_b == 1) {
+          out[row * kHeadDim + d] = to_out<TOut>(o);
+        } else {
+          const int64_t r = row * p.num_splits + U.split;
+          p.ws_o[r * kHeadDim + d] = o;
+          if (d == 0) p.ws_lse[r] = (m_run[g] + log2f(Ls[g])) * kLn2;
+        }
       }
-      if (n_valid < kT) {
-        // keep stale or out-of-context V rows out of the MMA; the V tile of
-        // this chunk must have landed first (its last page may be partial)
-        ok = !failed && mbar_wait(full_bar(1, slot), (c / kStages) & 1);
-        if (!__all_sync(kFull, ok)) failed = true;
-      }
-      if (t >= n_valid) {
-        uint8_t* vrow = base + kOffV + slot * kSlotBytes + t * kRowBytes;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            *reinterpret_cast<uint4*>(vrow + hh * kHalf + i * 16) = make_uint4(0, 0, 0, 0);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full(c & 1));
-      if (c > 0) fold(c - 1);
-#pragma unroll
-      for (int g = 0; g < G; ++g) alpha_prev[g] = alpha[g];
+      // the last split of this (sequence, kv head) merges all of them into
+      // `out` (the P operands are free: every PV of this unit has completed
+      // and the next unit's first PV waits for P written after this)
+      if (U.n_splits_b > 1)
+        finish_split<G, TOut>(p, U.b, U.h, U.n_splits_b, d, reinterpret_cast<float*>(base + kOffP),
+                              1);
     }
-    if (n_chunks > 0) fold(n_chunks - 1);
-    // softmax denominators: sum the per-token partial sums over 128 threads
-    float* lred = reinterpret_cast<float*>(base + kOffLred);
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float v = l_th[g];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
-      if (lane == 0) lred[warp * 8 + g] = v;
-    }
-    named_bar_sync(1, 128);
-    const int d = t;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float Ls = lred[g] + lred[8 + g] + lred[16 + g] + lred[24 + g];
-      const float o = acc[g] / Ls;
-      const int64_t row = (int64_t)b * p.Hq + hq0 + g;
-      if (n_splits_b == 1) {
-        out[row * kHeadDim + d] = to_out<TOut>(o);
-      } else {
-        const int64_t r = row * p.num_splits + split;
-        p.ws_o[r * kHeadDim + d] = o;
-        if (d == 0) p.ws_lse[r] = (m_run[g] + log2f(Ls)) * kLn2;
-      }
-    }
-    // the last split of this (sequence, kv head) merges all of them into `out`
-    // (the P operands are free: every PV has completed)
-    if (n_splits_b > 1)
-      finish_split<G, TOut>(p, b, h, n_splits_b, d, reinterpret_cast<float*>(base + kOffP), 1);
   }
 
-  if (failed && lane == 0 && atomicCAS(p.err, 0, kErrWaitTimeout) == 0) p.err[1] = split;
+  if (failed && lane == 0 && atomicCAS(p.err, 0, kErrWaitTimeout) == 0) p.err[1] = blockIdx.x;
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpMma) {
@@ -451,11 +553,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int G, int BS, bool FP16, bool OUT_F32>
-cudaError_t launch_one(const CUtensorMap* tk, const CUtensorMap* tv, const PartialParams& p,
-                       int batch, cudaStream_t stream) {
-  dim3 grid(p.num_splits, p.Hkv, batch);
-  paged_partial_tc_kernel<G, BS, FP16, OUT_F32><<<grid, kThreads, kSmemBytes, stream>>>(*tk, *tv,
-                                                                                      p);
+cudaError_t launch_one(const CUtensorMap* tk, const CUtensorMap* tv, const CUtensorMap* tq,
+                       const PartialParams& p, cudaStream_t stream) {
+  const int ctas = p.num_units < p.max_ctas ? p.num_units : p.max_ctas;
+  if (ctas <= 0) return cudaSuccess;
+  paged_partial_tc_kernel<G, BS, FP16, OUT_F32><<<ctas, kThreads, kSmemBytes, stream>>>(
+      *tk, *tv, *tq, p);
   return cudaGetLastError();
 }
 
@@ -478,16 +581,16 @@ template <bool FP16>
 struct Dispatch {
   template <int G, int BS>
   static cudaError_t launch_g(bool f32, const CUtensorMap* tk, const CUtensorMap* tv,
-                              const PartialParams& p, int batch, cudaStream_t s) {
-    return f32 ? launch_one<G, BS, FP16, true>(tk, tv, p, batch, s)
-               : launch_one<G, BS, FP16, false>(tk, tv, p, batch, s);
+                              const CUtensorMap* tq, const PartialParams& p, cudaStream_t s) {
+    return f32 ? launch_one<G, BS, FP16, true>(tk, tv, tq, p, s)
+               : launch_one<G, BS, FP16, false>(tk, tv, tq, p, s);
   }
   static cudaError_t launch(int G, int BS, bool f32, const CUtensorMap* tk, const CUtensorMap* tv,
-                            const PartialParams& p, int batch, cudaStream_t s) {
-    if (G == 4 && BS == 16) return launch_g<4, 16>(f32, tk, tv, p, batch, s);
-    if (G == 4 && BS == 32) return launch_g<4, 32>(f32, tk, tv, p, batch, s);
-    if (G == 8 && BS == 16) return launch_g<8, 16>(f32, tk, tv, p, batch, s);
-    if (G == 8 && BS == 32) return launch_g<8, 32>(f32, tk, tv, p, batch, s);
+                            const CUtensorMap* tq, const PartialParams& p, cudaStream_t s) {
+    if (G == 4 && BS == 16) return launch_g<4, 16>(f32, tk, tv, tq, p, s);
+    if (G == 4 && BS == 32) return launch_g<4, 32>(f32, tk, tv, tq, p, s);
+    if (G == 8 && BS == 16) return launch_g<8, 16>(f32, tk, tv, tq, p, s);
+    if (G == 8 && BS == 32) return launch_g<8, 32>(f32, tk, tv, tq, p, s);
     return cudaErrorInvalidValue;
   }
   template <int G, int BS>

@@ -36,6 +36,8 @@ struct PartialParams {
   int chunk_pages;  // pages per split
   int num_splits;   // S (grid.x); row stride of the workspace
   float qscale;     // scale * log2(e): logits are kept in base-2 units
+  int num_units;    // S * Hkv * B work units (persistent tensor-core kernel)
+  int max_ctas;     // resident CTAs the persistent kernel launches at most
 };
 
 struct MergeParams {
@@ -77,9 +79,12 @@ bool partial_kernel_supported(int kernel, int group);
 cudaError_t partial_prepare(int kernel, int group, int block_size, int dtype);
 int partial_ctas_per_sm(int kernel, int group, int block_size, int dtype);
 
+// tmap_q (a [B * Hq, 128] view of q, boxes of 64 dims x G rows) is read by
+// the tensor-core kernel only.
 cudaError_t launch_partial(int kernel, int group, int block_size, int dtype, bool out_f32,
                            const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
-                           const PartialParams& p, int batch, cudaStream_t stream);
+                           const CUtensorMap* tmap_q, const PartialParams& p, int batch,
+                           cudaStream_t stream);
 
 // out_dtype: 0 bf16, 1 fp16, 2 f32
 cudaError_t launch_merge(const MergeParams& p, int out_dtype, cudaStream_t stream);
