@@ -44,9 +44,9 @@ FALLBACK_HBM_GBS = 6800.0
 # capture of this workload (profiles/); None when not measured for the
 # current kernel.
 NCU_TRAFFIC_BYTES = {
-    # profiles/paged_partial_kernel_long_b4_l32768.md: 537.02 MB read + 4.18 MB
+    # profiles/paged_partial_kernel_long_b4_l32768.md: 537.07 MB read + 3.26 MB
     # written per launch (captured on the same step over a 1 GiB pool)
-    "long_b4_l32768": 541_207_808,
+    "long_b4_l32768": 540_324_864,
 }
 
 
@@ -66,6 +66,12 @@ def make_workload(name: str, seed: int, device):
         return W.long_context(seed=seed, batch=4, context=8192, device=device)
     if name == "long_b1_l8192":
         return W.long_context(seed=seed, batch=1, context=8192, device=device)
+    if name == "long_b4_l32768_bs32":  # same step with 32-token pages (40 GiB pool)
+        return W.custom(seed=seed, B=4, Hq=32, Hkv=8, D=128, block_size=32, lens=[32768] * 4,
+                        num_blocks=327680, device=device)
+    if name == "long_b32_l32768_mqa4":  # same bytes and G as long_b4_l32768, one kv head
+        return W.custom(seed=seed, B=32, Hq=4, Hkv=1, D=128, block_size=16, lens=[32768] * 32,
+                        num_blocks=4 * 65536, device=device)
     if name == "serving_b128":
         return W.serving_mix(seed=seed, batch=128, device=device)
     if name == "mid_ragged_b8":

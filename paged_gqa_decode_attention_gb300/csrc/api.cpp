@@ -33,9 +33,12 @@ int cuda_fail(const char* what, cudaError_t e) {
 }
 
 // Planner cost constants, in token-equivalents of one CTA's streaming time:
-// the fixed cost of a CTA (launch, barrier set-up, q load, the final merge of
-// its warps) and of the separate merge launch.
-constexpr int kOverheadTokens = 64;
+// the fixed cost of a CTA (launch, barrier set-up, q and first-page latency,
+// the final merge of its warps) and of merging split partials. Chosen from a
+// split-count sweep on GB300 (B=1 L=32768, B=4 L=8192, B=4 L=32768, the
+// 128-sequence serving mix): with these the planner picks the measured
+// fastest split count on all four.
+constexpr int kOverheadTokens = 256;
 constexpr int kMergeTokens = 96;
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }

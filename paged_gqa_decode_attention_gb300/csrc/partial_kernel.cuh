@@ -120,6 +120,12 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
   const int hq0 = h * G;
   TOut* out = static_cast<TOut*>(p.out);
 
+  // The producer's first block-table window depends only on the split index,
+  // so its load is issued before the context length arrives.
+  const int p0_spec = split * p.chunk_pages;
+  int spec_blk = 0;
+  if ((threadIdx.x >> 5) == kNW && p0_spec + (threadIdx.x & 31) < p.max_blocks)
+    spec_blk = __ldg(p.block_table + (int64_t)b * p.max_blocks + p0_spec + (threadIdx.x & 31));
   // Context length, clamped to what the block table can address.
   int L = __ldg(p.context_lens + b);
   const int maxL = p.max_blocks * BS;
@@ -167,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
     const int32_t* table = p.block_table + (int64_t)b * p.max_blocks;
     // block-table entries in windows of 32 pages, the next window prefetched
     int win_base = p0;
-    int win_blk = (p0 + lane < p1) ? __ldg(table + p0 + lane) : 0;
+    int win_blk = (p0 + lane < p1) ? spec_blk : 0;
     int nxt_blk = (p0 + 32 + lane < p1) ? __ldg(table + p0 + 32 + lane) : 0;
     for (int c = 0; c < n_chunks; ++c) {
       const int slot = c % kStages;

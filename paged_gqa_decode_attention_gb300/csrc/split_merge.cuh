@@ -32,14 +32,14 @@ __device__ __forceinline__ TOut merge_to_out(float x) {
   }
 }
 
-// Called by 128 threads (tid 0..127, thread tid owns output dim tid) after
-// each has written its part of this split's partial. `sw` is shared scratch
+// Called by 128 threads (tid 0..127) after each has written its part of this
+// split's partial. `sw` is shared scratch
 // of at least G * 64 + 1 floats, `bar_id` a named barrier over exactly these
 // 128 threads.
 template <int G, typename TOut>
 __device__ __forceinline__ void finish_split(const PartialParams& p, int b, int h, int n_splits_b,
                                              int tid, float* sw, int bar_id) {
-  static_assert(kHeadDim == 128, "one thread per output dim");
+  static_assert(kHeadDim == 128, "32 float4 columns per head");
   __threadfence();
   named_bar_sync(bar_id, 128);
   int* flag = reinterpret_cast<int*>(sw + G * 64);
@@ -71,21 +71,39 @@ __device__ __forceinline__ void finish_split(const PartialParams& p, int b, int 
     for (int s = 0; s < n_splits_b; ++s) w[s] *= inv;
   }
   named_bar_sync(bar_id, 128);
+  // thread -> (head g, 4 consecutive dims): G * 32 such pairs over 128 threads,
+  // float4 loads, 8 splits in flight per step
   TOut* out = static_cast<TOut*>(p.out);
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const float* o = p.ws_o + ((row0 + g) * p.num_splits) * kHeadDim + tid;
+  for (int pair = tid; pair < G * 32; pair += 128) {
+    const int g = pair >> 5, d4 = (pair & 31) * 4;
+    const float4* o = reinterpret_cast<const float4*>(p.ws_o + ((row0 + g) * p.num_splits) * kHeadDim + d4);
     const float* w = sw + g * 64;
-    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     int s = 0;
-    for (; s + 4 <= n_splits_b; s += 4) {
-      acc0 = fmaf(w[s + 0], __ldcg(o + (s + 0) * kHeadDim), acc0);
-      acc1 = fmaf(w[s + 1], __ldcg(o + (s + 1) * kHeadDim), acc1);
-      acc2 = fmaf(w[s + 2], __ldcg(o + (s + 2) * kHeadDim), acc2);
-      acc3 = fmaf(w[s + 3], __ldcg(o + (s + 3) * kHeadDim), acc3);
+    for (; s + 8 <= n_splits_b; s += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = __ldcg(o + (s + k) * (kHeadDim / 4));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        acc.x = fmaf(w[s + k], v[k].x, acc.x);
+        acc.y = fmaf(w[s + k], v[k].y, acc.y);
+        acc.z = fmaf(w[s + k], v[k].z, acc.z);
+        acc.w = fmaf(w[s + k], v[k].w, acc.w);
+      }
     }
-    for (; s < n_splits_b; ++s) acc0 = fmaf(w[s], __ldcg(o + s * kHeadDim), acc0);
-    out[(row0 + g) * kHeadDim + tid] = merge_to_out<TOut>((acc0 + acc1) + (acc2 + acc3));
+    for (; s < n_splits_b; ++s) {
+      const float4 v = __ldcg(o + s * (kHeadDim / 4));
+      acc.x = fmaf(w[s], v.x, acc.x);
+      acc.y = fmaf(w[s], v.y, acc.y);
+      acc.z = fmaf(w[s], v.z, acc.z);
+      acc.w = fmaf(w[s], v.w, acc.w);
+    }
+    TOut* dst = out + (row0 + g) * kHeadDim + d4;
+    dst[0] = merge_to_out<TOut>(acc.x);
+    dst[1] = merge_to_out<TOut>(acc.y);
+    dst[2] = merge_to_out<TOut>(acc.z);
+    dst[3] = merge_to_out<TOut>(acc.w);
   }
   if (tid == 0) p.counters[(int64_t)b * p.Hkv + h] = 0;  // ready for the next call
 }
