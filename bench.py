@@ -44,9 +44,9 @@ FALLBACK_HBM_GBS = 6800.0
 # capture of this workload (profiles/); None when not measured for the
 # current kernel.
 NCU_TRAFFIC_BYTES = {
-    # profiles/paged_partial_kernel_long_b4_l32768.md: 537.07 MB read + 3.26 MB
+    # profiles/paged_partial_tc_kernel_long_b4_l32768.md: 537.16 MB read + 3.61 MB
     # written per launch (captured on the same step over a 1 GiB pool)
-    "long_b4_l32768": 540_324_864,
+    "long_b4_l32768": 540_766_976,
 }
 
 
@@ -428,7 +428,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} (hbm_gbs)",
-                     "kernel": "paged_partial_kernel (split-K partials + fused LSE merge)",
+                     "kernel": "paged_partial_tc_kernel (tcgen05 split-K partials + fused LSE merge)",
                      "per_launch_ms": avg_launch_ms},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

@@ -242,7 +242,8 @@ int paged_decode_attn_create(const pda_config* cfg, pda_handle* out_handle) {
   const size_t o_bytes = rows * cfg->head_dim * sizeof(float);
   const size_t lse_bytes = ((rows * sizeof(float)) + 255) & ~size_t(255);
   const size_t err_bytes = 256;
-  h->counter_bytes = (size_t)cfg->max_batch * cfg->num_kv_heads * sizeof(int);
+  // split tickets [max_batch, Hkv], then the persistent kernel's 2 counters
+  h->counter_bytes = ((size_t)cfg->max_batch * cfg->num_kv_heads + 2) * sizeof(int);
   e = cudaMalloc(&h->ws, o_bytes + lse_bytes + err_bytes + h->counter_bytes);
   if (e != cudaSuccess) {
     delete h;
@@ -367,6 +368,7 @@ int paged_decode_attn_run_ex(pda_handle h, const void* q, const void* k_cache,
   p.ws_lse = h->ws_lse;
   p.err = h->err;
   p.counters = h->counters;
+  p.sched = h->counters + (size_t)c.max_batch * c.num_kv_heads;
   p.Hq = c.num_q_heads;
   p.Hkv = c.num_kv_heads;
   p.max_blocks = max_blocks;

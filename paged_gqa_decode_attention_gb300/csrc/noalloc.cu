@@ -25,13 +25,16 @@
 namespace {
 
 // Scratch capacity: 2^21 floats (8 MiB) of split partial outputs, 2^16 floats
-// (256 KiB) of split LSEs, 64 ints for the kernels' error word and 2^16 ints
-// (256 KiB) of split tickets, one per (sequence, kv head).
+// (256 KiB) of split LSEs, 64 ints for the kernels' error word, 2^16 ints
+// (256 KiB) of split tickets, one per (sequence, kv head), and the 2 work
+// counters of the persistent kernel.
 constexpr size_t kPartialFloats = size_t(1) << 21;
 constexpr size_t kLseFloats = size_t(1) << 16;
 constexpr size_t kErrInts = 64;
-constexpr size_t kCounterInts = size_t(1) << 16;
-constexpr size_t kScratchBytes = (kPartialFloats + kLseFloats) * 4 + (kErrInts + kCounterInts) * 4;
+constexpr size_t kCounterInts = size_t(1) << 16;  // split tickets
+constexpr size_t kSchedInts = 2;                  // persistent kernel's work counters
+constexpr size_t kScratchBytes =
+    (kPartialFloats + kLseFloats) * 4 + (kErrInts + kCounterInts + kSchedInts) * 4;
 
 // One copy per GPU that loads the library, alive until the process exits.
 // In host code this name is only a stand-in for the symbol; the device
@@ -224,7 +227,9 @@ extern "C" int paged_decode_attn_run_noalloc(const void* q, const void* k_cache,
   int* counters = err + kErrInts;
   // the error word and the split tickets must start at zero; the partials are
   // fully written before use
+  int* sched = counters + kCounterInts;
   e = cudaMemsetAsync(err, 0, 2 * sizeof(int), s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(sched, 0, kSchedInts * sizeof(int), s);
   if (e == cudaSuccess && S > 1)
     e = cudaMemsetAsync(counters, 0, (size_t)batch * num_kv_heads * sizeof(int), s);
   if (e != cudaSuccess) return cuda_fail("cudaMemsetAsync(scratch)", e);
@@ -238,6 +243,7 @@ extern "C" int paged_decode_attn_run_noalloc(const void* q, const void* k_cache,
   p.ws_lse = ws_lse;
   p.err = err;
   p.counters = counters;
+  p.sched = sched;
   p.Hq = num_q_heads;
   p.Hkv = num_kv_heads;
   p.max_blocks = max_blocks;

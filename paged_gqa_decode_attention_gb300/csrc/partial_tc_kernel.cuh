@@ -5,9 +5,10 @@
 // a unit is one (split, kv head, sequence), split-K with a normalised partial
 // and its log-sum-exp per split (Loom Kernels landing page, "Supported now":
 // Paged MQA/GQA decode, GQA packing + local split-K/LSE). Here the kernel is
-// persistent: one CTA per SM walks the units u = blockIdx.x + k * gridDim.x,
-// and every role streams across unit boundaries, so the TMA rings stay full
-// from the first unit to the last. The two contractions of a 128-token chunk
+// persistent: one CTA per SM takes units from a global work counter as it
+// goes (so faster SMs take more of them and ragged batches balance), and
+// every role streams across unit boundaries, so the TMA rings stay full from
+// the first unit to the last. The two contractions of a 128-token chunk
 // run on the tensor cores, with the G query rows packed as the N side:
 //
 //   S^T [128 tokens x 16]  = K_chunk [128 x 128 dims] . Q^T [128 dims x 16]
@@ -78,9 +79,13 @@ constexpr int kOffP = kOffQ + 2 * kOpBytes;      // [2 buffers][hi, lo] operands
 constexpr int kOffRed = kOffP + 4 * kOpBytes;    // 2 x [4 warps][8] floats (chunk maxima)
 constexpr int kOffLred = kOffRed + 2 * 4 * 8 * 4;  // [4 warps][8] floats (final sums)
 constexpr int kOffBar = kOffLred + 4 * 8 * 4;
-constexpr int kNumBars = 4 * kStages + 14;
+constexpr int kUnitRing = 4;               // slots of the shared unit queue
+constexpr int kUnitConsumers = 3;          // V producer, MMA warp, softmax warp 0
+constexpr int kNumBars = 4 * kStages + 14 + 2 * kUnitRing;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
-constexpr size_t kSmemBytes = 1024 + kOffTmem + 16;
+constexpr int kOffURing = kOffTmem + 16;          // [kUnitRing] unit indices
+constexpr int kOffUBcast = kOffURing + kUnitRing * 4;  // unit index, softmax warp 0 -> 1..3
+constexpr size_t kSmemBytes = 1024 + kOffUBcast + 16;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 template <bool FP16>
@@ -149,31 +154,31 @@ __device__ __forceinline__ Unit load_unit(const PartialParams& p, int u) {
   return U;
 }
 
-// Walks this CTA's units with work, chunk by chunk: c counts chunks over the
-// whole walk (ring slots and buffer parities follow it), j counts units.
-template <int BS>
+// Walks a sequence of units with work, chunk by chunk: c counts chunks over
+// the whole walk (ring slots and buffer parities follow it), j counts units.
+// `next()` of the source yields unit indices in order, -1 at the end; units
+// without chunks (empty splits, zero-filled rows) are skipped here.
+template <int BS, typename Source>
 struct Cursor {
   int u, i, c, j;
   Unit U;
-  __device__ __forceinline__ void seek(const PartialParams& p) {
-    for (; u < p.num_units; u += gridDim.x) {
+  __device__ __forceinline__ void seek(const PartialParams& p, Source& src) {
+    while ((u = src.next()) >= 0) {
       U = load_unit<BS>(p, u);
       if (U.n_chunks > 0) return;
     }
   }
-  __device__ __forceinline__ void start(const PartialParams& p) {
-    u = blockIdx.x;
+  __device__ __forceinline__ void start(const PartialParams& p, Source& src) {
     i = c = j = 0;
-    seek(p);
+    seek(p, src);
   }
-  __device__ __forceinline__ bool valid(const PartialParams& p) const { return u < p.num_units; }
-  __device__ __forceinline__ void advance(const PartialParams& p) {
+  __device__ __forceinline__ bool valid() const { return u >= 0; }
+  __device__ __forceinline__ void advance(const PartialParams& p, Source& src) {
     ++c;
     if (++i == U.n_chunks) {
       i = 0;
       ++j;
-      u += gridDim.x;
-      seek(p);
+      seek(p, src);
     }
   }
 };
@@ -206,10 +211,90 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto q_full = [&](int b) { return bar0 + 8u * (4 * kStages + 10 + b); };
   auto q_empty = [&](int b) { return bar0 + 8u * (4 * kStages + 12 + b); };
 
+  auto uring_full = [&](int s) { return bar0 + 8u * (4 * kStages + 14 + s); };
+  auto uring_empty = [&](int s) { return bar0 + 8u * (4 * kStages + 14 + kUnitRing + s); };
+  volatile int* uring = reinterpret_cast<volatile int*>(base + kOffURing);
+
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  bool failed = false;
+
+  // Work units are handed out dynamically: the K-producer warp takes unit
+  // indices from a global counter (p.sched[0]) and publishes every one that
+  // has output to write into the unit ring; the V producer, the MMA warp and
+  // softmax warp 0 read the ring in order. The CTA that runs out last resets
+  // the counters for the next call.
+  struct FetchSource {
+    const PartialParams* p;
+    volatile int* ring;
+    uint32_t full0, empty0;
+    int lane, k;
+    bool* failed;
+    __device__ __forceinline__ int next() {
+      while (true) {
+        int u = 0;
+        if (lane == 0) u = atomicAdd(p->sched, 1);
+        u = __shfl_sync(kFull, u, 0);
+        const int pub = u < p->num_units ? u : -1;
+        if (pub >= 0) {
+          const Unit U = load_unit<BS>(*p, pub);
+          if (U.n_chunks == 0 && !U.zero_fill) continue;  // nothing to do for this unit
+        }
+        const int slot = k % kUnitRing;
+        bool ok = true;
+        if (k >= kUnitRing) ok = mbar_wait(empty0 + 8u * slot, ((k / kUnitRing) - 1) & 1);
+        if (!__all_sync(kFull, ok)) {
+          *failed = true;
+          return -1;
+        }
+        if (lane == 0) {
+          ring[slot] = pub;
+          mbar_arrive(full0 + 8u * slot);
+        }
+        __syncwarp();
+        ++k;
+        if (pub < 0) {
+          if (lane == 0) {
+            __threadfence();  // this CTA's last fetch is ordered before its done count
+            if (atomicAdd(p->sched + 1, 1) == (int)gridDim.x - 1) {
+              p->sched[0] = 0;
+              p->sched[1] = 0;
+            }
+          }
+          return -1;
+        }
+        return pub;
+      }
+    }
+  };
+  struct RingSource {
+    volatile int* ring;
+    uint32_t full0, empty0;
+    int lane, k;
+    bool* failed;
+    __device__ __forceinline__ int next() {
+      const int slot = k % kUnitRing;
+      const bool ok = !*failed && mbar_wait(full0 + 8u * slot, (k / kUnitRing) & 1);
+      if (!__all_sync(kFull, ok)) {
+        *failed = true;
+        return -1;
+      }
+      const int u = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8u * slot);
+      ++k;
+      return u;
+    }
+  };
+  auto ring_source = [&]() {
+    return RingSource{uring, uring_full(0), uring_empty(0), lane, 0, &failed};
+  };
 
   if (threadIdx.x == 0) {
+    for (int s2 = 0; s2 < kUnitRing; ++s2) {
+      mbar_init(uring_full(s2), 1);
+      mbar_init(uring_empty(s2), kUnitConsumers);
+    }
     for (int r = 0; r < 2; ++r)
       for (int s = 0; s < kStages; ++s) {
         mbar_init(full_bar(r, s), 1);
@@ -244,8 +329,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tS = [&](int b2) { return tmem + (uint32_t)(b2 * kN); };
   auto tO = [&](int b2) { return tmem + (uint32_t)((2 + b2) * kN); };
 
-  bool failed = false;
-
   if (warp == kWarpProducerK || warp == kWarpProducerV) {
     // ------------------- producers: K ring (warp 4), V ring (warp 5) -------------------
     const int r = warp - kWarpProducerK;
@@ -254,22 +337,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(map);
       if (r == 0) prefetch_tensormap(&tmap_q);
     }
-    Cursor<BS> cur;
-    cur.start(p);
+    FetchSource fetch{&p, uring, uring_full(0), uring_empty(0), lane, 0, &failed};
+    RingSource ring = ring_source();
+    Cursor<BS, FetchSource> cur_k;
+    Cursor<BS, RingSource> cur_v;
+    if (r == 0) cur_k.start(p, fetch); else cur_v.start(p, ring);
     // block-table entries in windows of 32 pages, the next window prefetched
     int win_base = 0, win_blk = 0, nxt_blk = 0;
-    while (cur.valid(p) && !failed) {
-      const Unit& U = cur.U;
+    while (!failed && (r == 0 ? cur_k.valid() : cur_v.valid())) {
+      const int cu_i = r == 0 ? cur_k.i : cur_v.i;
+      const int cu_c = r == 0 ? cur_k.c : cur_v.c;
+      const int cu_j = r == 0 ? cur_k.j : cur_v.j;
+      const Unit& U = r == 0 ? cur_k.U : cur_v.U;
       const int32_t* table = p.block_table + (int64_t)U.b * p.max_blocks;
-      if (cur.i == 0) {
+      if (cu_i == 0) {
         win_base = U.p0;
         win_blk = (U.p0 + lane < U.p1) ? __ldg(table + U.p0 + lane) : 0;
         nxt_blk = (U.p0 + 32 + lane < U.p1) ? __ldg(table + U.p0 + 32 + lane) : 0;
         if (r == 0) {
           // this unit's G query rows -> Q operand buffer j & 1
-          const int qb = cur.j & 1;
+          const int qb = cu_j & 1;
           bool ok = true;
-          if (cur.j >= 2) ok = mbar_wait(q_empty(qb), ((cur.j - 2) >> 1) & 1);
+          if (cu_j >= 2) ok = mbar_wait(q_empty(qb), ((cu_j - 2) >> 1) & 1);
           if (!__all_sync(kFull, ok)) {
             failed = true;
             break;
@@ -285,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
       }
-      const int c = cur.c;
+      const int c = cu_c;
       const int slot = c % kStages;
       if (c >= kStages) {
         const bool ok = mbar_wait(empty_bar(r, slot), ((c / kStages) - 1) & 1);
@@ -294,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
-      const int pg0 = U.p0 + cur.i * PPS;
+      const int pg0 = U.p0 + cu_i * PPS;
       const int npg = min(PPS, U.p1 - pg0);
       if (pg0 + PPS > win_base + 32) {  // pg0 == win_base + 32: PPS divides 32
         win_base += 32;
@@ -319,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-      cur.advance(p);
+      if (r == 0) cur_k.advance(p, fetch); else cur_v.advance(p, ring);
     }
   } else if (warp == kWarpMma) {
     // ------------------------------ MMA issue -----------------------------
@@ -327,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc_pv = idesc_f16(128, kN, !FP16, true, false);
     // S(c) = K(c) . Q^T into S[c & 1]; needs the K slot, the unit's Q and the
     // softmax's read of S(c-2)
-    auto issue_qk = [&](const Cursor<BS>& cur) {
+    auto issue_qk = [&](const Cursor<BS, RingSource>& cur) {
       const int c = cur.c, slot = c % kStages, qb = cur.j & 1;
       bool ok = !failed && mbar_wait(full_bar(0, slot), (c / kStages) & 1);
       if (ok && c >= 2) ok = mbar_wait(s_free(c & 1), ((c - 2) >> 1) & 1);
@@ -352,8 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // O(c) = V(c)^T . P(c)^T into O[c & 1]; needs the V slot, P(c) and the
     // fold of O(c-2)
-    auto issue_pv = [&](const Cursor<BS>& cur) {
-      const int c = cur.c, slot = c % kStages;
+    auto issue_pv = [&](int c) {
+      const int slot = c % kStages;
       bool ok = !failed && mbar_wait(full_bar(1, slot), (c / kStages) & 1);
       if (ok) ok = mbar_wait(p_full(c & 1), (c >> 1) & 1);
       if (ok && c >= 2) ok = mbar_wait(o_free(c & 1), ((c - 2) >> 1) & 1);
@@ -378,22 +467,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
-    Cursor<BS> qk, pv;
-    qk.start(p);
-    pv = qk;
-    if (qk.valid(p)) {
+    RingSource ring = ring_source();
+    Cursor<BS, RingSource> qk;
+    qk.start(p, ring);
+    if (qk.valid()) {
       issue_qk(qk);
-      qk.advance(p);
+      qk.advance(p, ring);
     }
-    int last_c = -1;
-    while (pv.valid(p) && !failed) {
-      if (qk.valid(p)) {
+    // PV trails QK^T by one chunk: QK^T of chunk c+1 is issued before PV of c
+    int c_pv = 0, last_c = -1;
+    while (!failed) {
+      if (qk.valid()) {
         issue_qk(qk);
-        qk.advance(p);
+        qk.advance(p, ring);
       }
-      issue_pv(pv);
-      last_c = pv.c;
-      pv.advance(p);
+      if (c_pv >= qk.c) break;
+      issue_pv(c_pv);
+      last_c = c_pv++;
     }
     // Drain the last slots' completion arrivals so that no MMA commit lands on
     // this CTA's shared memory after it exits.
@@ -428,8 +518,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int g = 0; g < G; ++g) acc[g] = acc[g] * alpha_prev[g] + o[g];
     };
+    // Softmax warp 0 alone reads the unit ring and hands the index to warps
+    // 1-3, so the four always walk the same units through the same named
+    // barriers (a late timeout in one warp cannot split them).
+    RingSource ring = ring_source();
+    volatile int* ubc = reinterpret_cast<volatile int*>(base + kOffUBcast);
+    auto next_unit = [&]() {
+      int u = -1;
+      if (warp == 0) u = ring.next();
+      if (warp == 0 && lane == 0) *ubc = u;
+      named_bar_sync(1, 128);
+      u = *ubc;
+      named_bar_sync(1, 128);  // before warp 0 overwrites it
+      return u;
+    };
     int c = 0;
-    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    for (int u = next_unit(); u >= 0; u = next_unit()) {
       const Unit U = load_unit<BS>(p, u);
       const int hq0 = U.h * G;
       if (U.zero_fill) {

@@ -30,6 +30,8 @@ struct PartialParams {
   float* ws_lse;               // [B, Hq, num_splits]
   int* err;                    // device error word
   int* counters;               // [B, Hkv] split tickets for the fused merge; zero between calls
+  int* sched;                  // [2] work counter and done counter of the persistent kernel;
+                               // zero between calls
   int Hq;
   int Hkv;
   int max_blocks;
@@ -61,11 +63,12 @@ enum PartialKernel : int {
 };
 
 // The kernel a geometry uses unless overridden (PDA_PARTIAL_KERNEL): the
-// faster one as measured on GB300. At G = 8 the CUDA-core kernel is bound by
-// its FMA work (2.1x slower than the tensor-core kernel on the 128-sequence
-// serving mix); at G <= 4 it is the faster one.
+// faster one as measured on GB300. With G = 4 or 8 query heads per kv head
+// the packed tile is a real contraction and the tensor-core kernel wins (B=4,
+// L=32768 at G=4: 0.0974 vs 0.1000 ms; the 128-sequence serving mix at G=8:
+// 0.114 vs 0.255 ms); below that the CUDA-core kernel is used.
 constexpr int default_partial_kernel(int group) {
-  return group == 8 ? kPartialTensorCore : kPartialCudaCore;
+  return (group == 4 || group == 8) ? kPartialTensorCore : kPartialCudaCore;
 }
 
 // CTAs per SM each kernel is built for (its launch bounds and shared memory);
