@@ -41,6 +41,11 @@
 // softmax warps work on chunk c), then PV of chunk c once its P is written;
 // the softmax warps fold O of chunk c-1 into the running output after
 // writing P of chunk c.
+//   warps 7-10: epilogue. A finished unit's state (accumulators, max, sum)
+//     comes through a double-buffered shared-memory slot; this group
+//     normalises it, stores the output or the split partial, and runs the
+//     split ticket and merge, while the softmax warps go on with the next
+//     unit (the unit boundary does not stall the pipeline).
 // Every wait is bounded; a timed-out CTA records error code 3, stops issuing
 // work, still passes every barrier, and frees its TMEM.
 #pragma once
@@ -65,10 +70,11 @@ constexpr int kSlotBytes = 2 * kHalf;      // lo, hi halves of a K or V tile: 32
 constexpr int kN = 16;                     // MMA N: the group's query heads, padded
 constexpr int kOpHalf = 2048;              // 16 rows x 128 B of a K-major operand half
 constexpr int kOpBytes = 2 * kOpHalf;      // Q, P_hi or P_lo operand
-constexpr int kThreads = 224;
+constexpr int kThreads = 352;
 constexpr int kWarpProducerK = 4;
 constexpr int kWarpProducerV = 5;
 constexpr int kWarpMma = 6;
+constexpr int kWarpEpi0 = 7;               // warps 7-10: epilogue group
 constexpr uint32_t kTmemCols = 64;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -81,11 +87,16 @@ constexpr int kOffLred = kOffRed + 2 * 4 * 8 * 4;  // [4 warps][8] floats (final
 constexpr int kOffBar = kOffLred + 4 * 8 * 4;
 constexpr int kUnitRing = 4;               // slots of the shared unit queue
 constexpr int kUnitConsumers = 3;          // V producer, MMA warp, softmax warp 0
-constexpr int kNumBars = 4 * kStages + 14 + 2 * kUnitRing;
+constexpr int kNumBars = 4 * kStages + 14 + 2 * kUnitRing + 4;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kOffURing = kOffTmem + 16;          // [kUnitRing] unit indices
 constexpr int kOffUBcast = kOffURing + kUnitRing * 4;  // unit index, softmax warp 0 -> 1..3
-constexpr size_t kSmemBytes = 1024 + kOffUBcast + 16;
+constexpr int kOffEpiFlag = kOffUBcast + 4;            // epilogue group's shared wait outcome
+// A finished unit's state, softmax -> epilogue, double-buffered:
+// acc[8][128], max[8], sum[8], unit index (floats; the index as int).
+constexpr int kEpiFloats = 8 * 128 + 8 + 8 + 4;
+constexpr int kOffEpi = (kOffEpiFlag + 4 + 15) & ~15;
+constexpr size_t kSmemBytes = 1024 + kOffEpi + 2 * kEpiFloats * 4;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 template <bool FP16>
@@ -213,6 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   auto uring_full = [&](int s) { return bar0 + 8u * (4 * kStages + 14 + s); };
   auto uring_empty = [&](int s) { return bar0 + 8u * (4 * kStages + 14 + kUnitRing + s); };
+  auto ep_full = [&](int s) { return bar0 + 8u * (4 * kStages + 14 + 2 * kUnitRing + s); };
+  auto ep_empty = [&](int s) { return bar0 + 8u * (4 * kStages + 16 + 2 * kUnitRing + s); };
   volatile int* uring = reinterpret_cast<volatile int*>(base + kOffURing);
 
   const int warp = threadIdx.x >> 5;
@@ -294,6 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s2 = 0; s2 < kUnitRing; ++s2) {
       mbar_init(uring_full(s2), 1);
       mbar_init(uring_empty(s2), kUnitConsumers);
+    }
+    for (int s2 = 0; s2 < 2; ++s2) {
+      mbar_init(ep_full(s2), 4);
+      mbar_init(ep_empty(s2), 4);
     }
     for (int r = 0; r < 2; ++r)
       for (int s = 0; s < kStages; ++s) {
@@ -492,8 +509,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = mbar_wait(empty_bar(1, c % kStages), (c / kStages) & 1);
       if (!__all_sync(kFull, ok)) failed = true;
     }
-  } else {
-    // ------------------------- softmax and epilogue ------------------------
+  } else if (warp < 4) {
+    // ------------------------------ softmax -------------------------------
     const int t = threadIdx.x;  // token row of S; output dim of O
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     TOut* out = static_cast<TOut*>(p.out);
@@ -532,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(1, 128);  // before warp 0 overwrites it
       return u;
     };
-    int c = 0;
+    int c = 0, je = 0;  // je: units handed to the epilogue group
     for (int u = next_unit(); u >= 0; u = next_unit()) {
       const Unit U = load_unit<BS>(p, u);
       const int hq0 = U.h * G;
@@ -621,29 +638,83 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) lred[warp * 8 + g] = v;
       }
       named_bar_sync(1, 128);
-      const int d = t;
       float Ls[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) Ls[g] = lred[g] + lred[8 + g] + lred[16 + g] + lred[24 + g];
       named_bar_sync(1, 128);  // lred is rewritten by the next unit
+      // hand the unit's state to the epilogue group
+      {
+        const int es = je & 1;
+        bool ok2 = !failed;
+        if (ok2 && je >= 2) ok2 = mbar_wait(ep_empty(es), ((je - 2) >> 1) & 1);
+        if (!__all_sync(kFull, ok2)) failed = true;
+        float* st = reinterpret_cast<float*>(base + kOffEpi) + es * kEpiFloats;
+#pragma unroll
+        for (int g = 0; g < G; ++g) st[g * kHeadDim + t] = acc[g];
+        if (t == 0) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            st[8 * kHeadDim + g] = m_run[g];
+            st[8 * kHeadDim + 8 + g] = Ls[g];
+          }
+          reinterpret_cast<int*>(st)[8 * kHeadDim + 16] = u;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ep_full(es));
+        ++je;
+      }
+    }
+    // end of work: an empty state tells the epilogue group to stop
+    {
+      const int es = je & 1;
+      bool ok2 = !failed;
+      if (ok2 && je >= 2) ok2 = mbar_wait(ep_empty(es), ((je - 2) >> 1) & 1);
+      if (!__all_sync(kFull, ok2)) failed = true;
+      float* st = reinterpret_cast<float*>(base + kOffEpi) + es * kEpiFloats;
+      if (t == 0) reinterpret_cast<int*>(st)[8 * kHeadDim + 16] = -1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ep_full(es));
+    }
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int t = threadIdx.x - kWarpEpi0 * 32;  // output dim
+    volatile int* flag = reinterpret_cast<volatile int*>(base + kOffEpiFlag);
+    TOut* out = static_cast<TOut*>(p.out);
+    for (int je = 0;; ++je) {
+      const int es = je & 1;
+      const bool ok = !failed && mbar_wait(ep_full(es), (je >> 1) & 1);
+      // the four warps agree on the outcome before acting on it
+      if (t == 0) *flag = 0;
+      named_bar_sync(2, 128);
+      if (!ok && lane == 0) *flag = 1;
+      named_bar_sync(2, 128);
+      if (*flag) {
+        failed = true;
+        break;
+      }
+      float* st = reinterpret_cast<float*>(base + kOffEpi) + es * kEpiFloats;
+      const int u = reinterpret_cast<volatile int*>(st)[8 * kHeadDim + 16];
+      if (u < 0) break;
+      const Unit U = load_unit<BS>(p, u);
+      const int hq0 = U.h * G;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float o = acc[g] / Ls[g];
+        const float Ls = st[8 * kHeadDim + 8 + g];
+        const float o = st[g * kHeadDim + t] / Ls;
         const int64_t row = (int64_t)U.b * p.Hq + hq0 + g;
         if (U.n_splits_b == 1) {
-          out[row * kHeadDim + d] = to_out<TOut>(o);
+          out[row * kHeadDim + t] = to_out<TOut>(o);
         } else {
           const int64_t r = row * p.num_splits + U.split;
-          p.ws_o[r * kHeadDim + d] = o;
-          if (d == 0) p.ws_lse[r] = (m_run[g] + log2f(Ls[g])) * kLn2;
+          p.ws_o[r * kHeadDim + t] = o;
+          if (t == 0) p.ws_lse[r] = (st[8 * kHeadDim + g] + log2f(Ls)) * kLn2;
         }
       }
-      // the last split of this (sequence, kv head) merges all of them into
-      // `out` (the P operands are free: every PV of this unit has completed
-      // and the next unit's first PV waits for P written after this)
-      if (U.n_splits_b > 1)
-        finish_split<G, TOut>(p, U.b, U.h, U.n_splits_b, d, reinterpret_cast<float*>(base + kOffP),
-                              1);
+      named_bar_sync(2, 128);  // the state is read; the slot serves as merge scratch
+      // the last split of this (sequence, kv head) merges all of them into `out`
+      if (U.n_splits_b > 1) finish_split<G, TOut>(p, U.b, U.h, U.n_splits_b, t, st, 2);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ep_empty(es));
     }
   }
 
