@@ -77,6 +77,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_round_array.restype = None
     lib.oracle_decode_array.argtypes = [P, i64, i32, P]
     lib.oracle_decode_array.restype = None
+    lib.oracle_rope_kv_write.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                         i64, i32, P, P, P]
+    lib.oracle_rope_kv_write.restype = i32
     return lib
 
 
@@ -211,3 +214,30 @@ def decode(bits, dtype: int, lib=None) -> np.ndarray:
     out = np.zeros(bits.shape, dtype=np.float64)
     lib.oracle_decode_array(_ptr(bits), bits.size, dtype, _ptr(out))
     return out
+
+
+def rope_kv_write(q, k, v, positions, slot_mapping, cos_sin, rot_dim: int, neox: bool,
+                  dtype: int, k_cache, v_cache, q_out=None, lib=None):
+    """RoPE on q and k plus the paged cache write (test infrastructure).
+
+    q: uint16 [T, Hq, D]; k, v: uint16 [T, Hkv, D]; positions int32 [T];
+    slot_mapping int64 [T]; cos_sin float32 [max_position, rot_dim];
+    k_cache/v_cache uint16 [num_blocks, block_size, Hkv, D] (copied, not
+    modified); q_out: uint16 [T, Hq, D] starting contents (zeros when None;
+    tokens the call skips keep them). Returns (q_out, k_cache, v_cache)."""
+    lib = lib or load()
+    q, k, v = _as_bits(q), _as_bits(k), _as_bits(v)
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    cs = np.ascontiguousarray(cos_sin, dtype=np.float32)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    kc = np.array(k_cache, dtype=np.uint16, copy=True, order="C")
+    vc = np.array(v_cache, dtype=np.uint16, copy=True, order="C")
+    q_out = np.zeros_like(q) if q_out is None else np.array(q_out, dtype=np.uint16, copy=True)
+    num_slots = kc.shape[0] * kc.shape[1]
+    st = lib.oracle_rope_kv_write(_ptr(q), _ptr(k), _ptr(v), _ptr(pos), _ptr(slots), _ptr(cs), T,
+                                  Hq, Hkv, D, rot_dim, cs.shape[0], int(bool(neox)), num_slots,
+                                  dtype, _ptr(q_out), _ptr(kc), _ptr(vc))
+    _check(st, "rope_kv_write")
+    return q_out, kc, vc

@@ -412,3 +412,65 @@ int oracle_lse_merge(const double* lse, const double* o, int64_t n_rows, int num
   }
   return ORACLE_OK;
 }
+
+/* ---------------------------------------------------------------------------
+ * RoPE + paged-KV write (Loom Kernels landing page, "Supported now":
+ * "RoPE + paged-KV write - packed Q/K rotation + native cache write").
+ * The pages name the fused step but not its formula; the reading here is the
+ * rotary embedding as commonly defined: for token t at position pos_t, for
+ * each rotated pair j < rot_dim / 2 with angle table row cs = cos_sin[pos_t]
+ * (cos_j = cs[j], sin_j = cs[rot_dim / 2 + j]) and pair elements
+ *   (a, b) = (j, j + rot_dim / 2)   (rotate-halves, "neox")  or
+ *   (a, b) = (2j, 2j + 1)           (interleaved pairs),
+ *   y_a = x_a cos_j - x_b sin_j,   y_b = x_b cos_j + x_a sin_j;
+ * dims >= rot_dim pass through. q is rotated into q_out; the rotated k and
+ * the unchanged v go to cache row slot_mapping[t] (block-major layout: row
+ * index slot = block * block_size + offset). slot < 0 skips the cache write;
+ * a position outside [0, max_position) or a slot beyond the cache leaves the
+ * token's outputs untouched. Everything in double, rounded once (RNE) to the
+ * storage dtype.
+ * ------------------------------------------------------------------------- */
+static void rope_row(const uint16_t* x, uint16_t* y, const float* cs, int D, int rot_dim,
+                     int neox, int dtype) {
+  int half = rot_dim / 2;
+  for (int d = 0; d < D; ++d) y[d] = x[d];  /* pass-through dims */
+  for (int j = 0; j < half; ++j) {
+    int a = neox ? j : 2 * j;
+    int b = neox ? j + half : 2 * j + 1;
+    double c = (double)cs[j], s = (double)cs[half + j];
+    double xa = oracle_to_f64(x[a], dtype), xb = oracle_to_f64(x[b], dtype);
+    double ya = xa * c - xb * s;
+    double yb = xb * c + xa * s;
+    y[a] = dtype == ORACLE_BF16 ? encode_bf16(oracle_round_bf16(ya)) : encode_fp16(oracle_round_fp16(ya));
+    y[b] = dtype == ORACLE_BF16 ? encode_bf16(oracle_round_bf16(yb)) : encode_fp16(oracle_round_fp16(yb));
+  }
+}
+
+int oracle_rope_kv_write(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         const int32_t* positions, const int64_t* slot_mapping,
+                         const float* cos_sin, int T, int Hq, int Hkv, int D, int rot_dim,
+                         int max_position, int neox, int64_t num_slots, int dtype,
+                         uint16_t* q_out, uint16_t* k_cache, uint16_t* v_cache) {
+  if (!q || !k || !v || !positions || !slot_mapping || !cos_sin || !q_out || !k_cache || !v_cache)
+    return ORACLE_EINVAL;
+  if (T < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || rot_dim < 0 || rot_dim > D || rot_dim % 2)
+    return ORACLE_EINVAL;
+  for (int t = 0; t < T; ++t) {
+    int pos = positions[t];
+    if (pos < 0 || pos >= max_position) continue;
+    const float* cs = cos_sin + (int64_t)pos * rot_dim;
+    for (int h = 0; h < Hq; ++h) {
+      int64_t off = ((int64_t)t * Hq + h) * D;
+      rope_row(q + off, q_out + off, cs, D, rot_dim, neox, dtype);
+    }
+    int64_t slot = slot_mapping[t];
+    if (slot < 0 || slot >= num_slots) continue;
+    for (int h = 0; h < Hkv; ++h) {
+      int64_t src = ((int64_t)t * Hkv + h) * D;
+      int64_t dst = (slot * Hkv + h) * D;
+      rope_row(k + src, k_cache + dst, cs, D, rot_dim, neox, dtype);
+      for (int d = 0; d < D; ++d) v_cache[dst + d] = v[src + d];
+    }
+  }
+  return ORACLE_OK;
+}

@@ -319,5 +319,133 @@ def pin_dtype_conversions(lib):
     np.testing.assert_array_equal(r, [1.0, 1 + 2.0 ** -6, 1 + 2.0 ** -7])
 
 
+# ---------------------------------------------------------------------------
+# RoPE + paged-KV write
+# ---------------------------------------------------------------------------
+
+def _half_ulp(x: np.ndarray, dtype: int) -> np.ndarray:
+    """Half a unit in the last place of the storage format at |x| (bf16: 8
+    significant bits, fp16: 11 bits with subnormals below 2^-14)."""
+    mant, emin = (7, -126) if dtype == BF16 else (10, -14)
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** emin)))
+    return 2.0 ** (e - mant - 1)
+
+
+class RopeCase:
+    """Random q/k/v tokens, a random angle table (any angles: rotation is
+    what is pinned, not a frequency schedule), distinct cache slots with one
+    padding token (slot -1) and one token whose position is past the table."""
+
+    def __init__(self, seed, dtype, T=7, Hq=4, Hkv=2, D=32, P=9, blocks=5, bs=4):
+        g = torch.Generator().manual_seed(seed)
+        rng = np.random.default_rng(seed)
+        dt = TORCH_DT[dtype]
+        self.dtype, self.T, self.Hq, self.Hkv, self.D, self.P = dtype, T, Hq, Hkv, D, P
+        self.q = _bits(torch.randn(T, Hq, D, generator=g).to(dt))
+        self.k = _bits(torch.randn(T, Hkv, D, generator=g).to(dt))
+        self.v = _bits(torch.randn(T, Hkv, D, generator=g).to(dt))
+        self.theta = rng.uniform(-4 * np.pi, 4 * np.pi, size=(P, D // 2))
+        self.pos = rng.integers(0, P, size=T).astype(np.int32)
+        self.pos[-1] = P  # outside the table: the token is skipped
+        self.slots = rng.permutation(blocks * bs)[:T].astype(np.int64)
+        self.slots[1] = -1  # padding token: q rotated, no cache write
+        fill = _bits(torch.full((blocks, bs, Hkv, D), -7.0).to(dt))
+        self.kc0, self.vc0 = fill.copy(), fill.copy()
+        self.qo0 = _bits(torch.full((T, Hq, D), 5.0).to(dt))
+
+    def table(self, rot_dim):
+        th = self.theta[:, : rot_dim // 2]
+        return np.concatenate([np.cos(th), np.sin(th)], axis=1).astype(np.float32)
+
+    def run(self, lib, rot_dim, neox, table=None):
+        cs = self.table(rot_dim) if table is None else table
+        return oracle.rope_kv_write(self.q, self.k, self.v, self.pos, self.slots, cs, rot_dim,
+                                    neox, self.dtype, self.kc0, self.vc0, q_out=self.qo0,
+                                    lib=lib) + (cs,)
+
+
+def _complex_rotation(x_bits, cs_row, rot_dim, neox, dtype):
+    """Rotation of one head vector written as complex multiplication: pair
+    (a, b) is the number x_a + i x_b, turned by e^{i theta_j} (theta_j from
+    the table's cos/sin halves). Returns the exact rotated values (float64,
+    products of a 16-bit and a 32-bit float are exact in double)."""
+    x = oracle.decode(x_bits, dtype)
+    half = rot_dim // 2
+    a = np.arange(half) if neox else 2 * np.arange(half)
+    b = a + half if neox else a + 1
+    z = x[..., a] + 1j * x[..., b]
+    w = z * (cs_row[:half].astype(np.float64) + 1j * cs_row[half:].astype(np.float64))
+    y = x.copy()
+    y[..., a], y[..., b] = w.real, w.imag
+    return y
+
+
+def pin_rope_complex_form(lib):
+    """Every rotated element is the correctly rounded (within half an ulp)
+    value of the complex-multiplication form of the rotary embedding, for
+    rotate-halves and interleaved pairing, full and partial rotation, bf16
+    and fp16; pass-through dims, V and untouched cache rows are bit-exact;
+    a padding slot writes no cache row; an out-of-table position writes
+    nothing at all."""
+    for dtype in (BF16, FP16):
+        for neox in (True, False):
+            for rot_dim in (32, 16):
+                c = RopeCase(11 + dtype + 2 * neox, dtype)
+                q_out, kc, vc, cs = c.run(lib, rot_dim, neox)
+                written = np.zeros(kc.shape[0] * kc.shape[1], dtype=bool)
+                kcf, vcf = kc.reshape(-1, c.Hkv, c.D), vc.reshape(-1, c.Hkv, c.D)
+                for t in range(c.T):
+                    if c.pos[t] >= c.P:
+                        np.testing.assert_array_equal(q_out[t], c.qo0[t])
+                        continue
+                    row = cs[c.pos[t]]
+                    yq = _complex_rotation(c.q[t], row, rot_dim, neox, dtype)
+                    got = oracle.decode(q_out[t], dtype)
+                    assert np.all(np.abs(got - yq) <= _half_ulp(yq, dtype)), "q rotation"
+                    np.testing.assert_array_equal(q_out[t][:, rot_dim:], c.q[t][:, rot_dim:])
+                    if c.slots[t] < 0:
+                        continue
+                    sl = c.slots[t]
+                    written[sl] = True
+                    yk = _complex_rotation(c.k[t], row, rot_dim, neox, dtype)
+                    got = oracle.decode(kcf[sl], dtype)
+                    assert np.all(np.abs(got - yk) <= _half_ulp(yk, dtype)), "k rotation"
+                    np.testing.assert_array_equal(kcf[sl][:, rot_dim:], c.k[t][:, rot_dim:])
+                    np.testing.assert_array_equal(vcf[sl], c.v[t])
+                f0 = c.kc0.reshape(-1, c.Hkv, c.D)
+                np.testing.assert_array_equal(kcf[~written], f0[~written])
+                np.testing.assert_array_equal(vcf[~written], f0[~written])
+                assert written.sum() == c.T - 2
+
+
+def pin_rope_exact_turns(lib):
+    """Angles whose cos/sin are exactly 0 or +-1 give exact results: a zero
+    turn is the identity, a half turn negates, a quarter turn maps the pair
+    (x_a, x_b) to (-x_b, x_a) with a = j, b = j + rot_dim/2 (rotate-halves)
+    or a = 2j, b = 2j + 1 (interleaved)."""
+    c = RopeCase(5, BF16, T=3)
+    c.pos[:] = [0, 1, 2]
+    c.slots[:] = [0, 1, 2]
+    D, half = c.D, c.D // 2
+    table = np.zeros((c.P, D), dtype=np.float32)
+    table[0, :half] = 1.0                      # 0
+    table[1, :half] = -1.0                     # pi
+    table[2, half:] = 1.0                      # pi / 2
+    for neox in (True, False):
+        q_out, kc, _, _ = c.run(lib, D, neox, table=table)
+        x = oracle.decode(c.q, BF16)
+        y = oracle.decode(q_out, BF16)
+        np.testing.assert_array_equal(y[0], x[0])
+        np.testing.assert_array_equal(y[1], -x[1])
+        a = np.arange(half) if neox else 2 * np.arange(half)
+        b = a + half if neox else a + 1
+        np.testing.assert_array_equal(y[2][:, a], -x[2][:, b])
+        np.testing.assert_array_equal(y[2][:, b], x[2][:, a])
+        yk = oracle.decode(kc.reshape(-1, c.Hkv, D)[2], BF16)
+        xk = oracle.decode(c.k[2], BF16)
+        np.testing.assert_array_equal(yk[:, a], -xk[:, b])
+
+
 ALL_PINS = [pin_brute_force, pin_closed_forms, pin_block_table_invariance, pin_gqa_reductions,
-            pin_split_merge, pin_merge_special_cases, pin_dtype_conversions]
+            pin_split_merge, pin_merge_special_cases, pin_dtype_conversions,
+            pin_rope_complex_form, pin_rope_exact_turns]

@@ -41,6 +41,19 @@ MUTANTS = {
     "bf16_exponent_bias": ("exp - 127 - 7", "exp - 127 - 8"),
     "fp16_subnormal_scale": ("ldexp((double)frac, -14 - 10)", "ldexp((double)frac, -15 - 10)"),
     "rne_ties_away": ("r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;", "r = fl + 1.0;"),
+    "rope_second_sign": ("double yb = xb * c + xa * s;", "double yb = xb * c - xa * s;"),
+    "rope_first_sign": ("double ya = xa * c - xb * s;", "double ya = xa * c + xb * s;"),
+    "rope_neox_pairing": ("int b = neox ? j + half : 2 * j + 1;",
+                          "int b = neox ? rot_dim - 1 - j : 2 * j + 1;"),
+    "rope_interleaved_pairing": ("int a = neox ? j : 2 * j;", "int a = neox ? j : j;"),
+    "rope_sin_from_cos_half": ("s = (double)cs[half + j];", "s = (double)cs[j];"),
+    "rope_table_row_stride": ("cos_sin + (int64_t)pos * rot_dim;",
+                              "cos_sin + (int64_t)pos * (rot_dim / 2);"),
+    "rope_cache_head_stride": ("int64_t dst = (slot * Hkv + h) * D;",
+                               "int64_t dst = (slot + h * Hkv) * D;"),
+    "rope_v_copies_k": ("v_cache[dst + d] = v[src + d];", "v_cache[dst + d] = k[src + d];"),
+    "rope_writes_padding_slot": ("if (slot < 0 || slot >= num_slots) continue;",
+                                 "if (slot >= num_slots) continue; if (slot < 0) slot = 0;"),
 }
 
 RUNNER = textwrap.dedent("""
