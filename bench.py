@@ -86,6 +86,18 @@ WORKLOAD_DESC = {
                       "bf16 N(0,1), random block tables over a 40 GiB K+V pool",
 }
 
+# RoPE + paged-KV write workloads: the Qwen2.5-0.5B attention geometry
+# (14/2 heads, D 64, theta 1e6) at 1-512 new decode tokens, and a 32768-token
+# prefill at 32/8/128 that is large enough to measure HBM bandwidth.
+ROPE_WORKLOADS = {
+    "rope_qwen05b_t1": dict(tokens=1),
+    "rope_qwen05b_t32": dict(tokens=32),
+    "rope_qwen05b_t512": dict(tokens=512),
+    "rope_prefill_t32768": dict(tokens=32768, Hq=32, Hkv=8, D=128, theta=10000.0,
+                                mode="prefill"),
+}
+ROPE_METRIC = "RoPE + paged-KV write tokens/s and HBM GB/s (% of GB300 peak), 1 GPU"
+
 
 # ---------------------------------------------------------------------------
 # distributed helpers (weak scaling, no data-path collective)
@@ -453,6 +465,166 @@ def launches_per_step(attn, wl) -> int:
     return 1
 
 
+def rope_oracle_sample(wl, target_s: float = 5.0):
+    """Time the FP64 oracle on the first <= 4096 tokens of a RoPE workload,
+    repeated until about ``target_s``. Returns (tokens_per_s, description)."""
+    import oracle
+    n = min(wl.num_tokens, 4096)
+
+    def b(t):
+        return t[:n].contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+    args = (b(wl.q), b(wl.k), b(wl.v), wl.positions[:n].cpu().numpy(),
+            wl.slot_mapping[:n].cpu().numpy(), wl.cos_sin.cpu().numpy(), wl.rot_dim, wl.neox,
+            oracle.BF16 if wl.qkv.dtype == torch.bfloat16 else oracle.FP16,
+            wl.k_cache.cpu().view(torch.int16).numpy().view(np.uint16),
+            wl.v_cache.cpu().view(torch.int16).numpy().view(np.uint16))
+    passes, elapsed = 0, 0.0
+    while elapsed < target_s and passes < 10000:
+        t0 = time.perf_counter()
+        oracle.rope_kv_write(*args)
+        elapsed += time.perf_counter() - t0
+        passes += 1
+    return passes * n / elapsed, f"{passes} pass(es) over {n} tokens of the workload; 1 thread"
+
+
+def run_rope(args):
+    """One step = one RoPE + paged-KV write call over the workload's tokens."""
+    from paged_gqa_decode_attention_gb300 import build as pda_build
+    from paged_gqa_decode_attention_gb300 import rope_kv_write
+    from paged_gqa_decode_attention_gb300 import workloads as W
+    world, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    spec = ROPE_WORKLOADS[args.workload]
+    if args.impl == "reference":
+        wl = W.rope_batch(seed=args.seed, **spec)
+        v, desc = rope_oracle_sample(wl, target_s=max(1.0, 0.2 * args.steps))
+        line = {"impl": "reference", "metric": ROPE_METRIC, "value": v, "unit": "tokens/s",
+                "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * wl.num_tokens / v, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": args.workload, **spec},
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                 "sample": desc},
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pda_build.build()
+    wl = W.rope_batch(seed=args.seed, device=dev, **spec)
+    T = wl.num_tokens
+    q_out = torch.empty((T, wl.num_q_heads, wl.head_dim), dtype=wl.qkv.dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    moved = wl.moved_bytes()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    # small calls: L2 flushed between eager calls (cold), unless --timing graph
+    # asks for back-to-back graph replay (L2-warm, as right after the QKV
+    # projection that produces the inputs)
+    flush = moved < 2 * l2 and args.timing != "graph"
+    flush_buf = torch.empty(2 * max(l2, 1 << 27), dtype=torch.uint8, device=dev) if flush else None
+    flush_read = torch.empty(2 * max(l2, 1 << 27) // 4, dtype=torch.int32, device=dev) if flush else None
+
+    def step(qkv=None):
+        src = wl if qkv is None else qkv
+        rope_kv_write(src.q, src.k, src.v, wl.positions, wl.slot_mapping, wl.cos_sin,
+                      wl.k_cache, wl.v_cache, neox=wl.neox, q_out=q_out)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if flush:
+        with sampler:
+            for i in range(args.steps):
+                flush_buf.zero_()
+                flush_read.max()
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+            torch.cuda.synchronize(dev)
+        per_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+        timed_ms = sum(per_ms)
+        timing_desc = "eager calls, CUDA events around each call, L2 flushed between calls"
+    else:
+        n_inner = max(d for d in range(1, min(args.steps, 100) + 1) if args.steps % d == 0)
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for _ in range(n_inner):
+                step()
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        with sampler:
+            starts[0].record(stream)
+            for _ in range(args.steps // n_inner):
+                graph.replay()
+            ends[0].record(stream)
+            torch.cuda.synchronize(dev)
+        timed_ms = starts[0].elapsed_time(ends[0])
+        per_ms = [timed_ms / args.steps]
+        timing_desc = f"CUDA graph of {n_inner} calls replayed {args.steps // n_inner}x"
+    avg_ms = statistics.mean(per_ms)
+    value = T * args.steps / (timed_ms / 1e3)
+    # end to end: fused qkv projection output from pinned host memory, q_out back
+    qkv_h = wl.qkv.cpu().pin_memory()
+    pos_h = wl.positions.cpu().pin_memory()
+    slot_h = wl.slot_mapping.cpu().pin_memory()
+    out_h = torch.empty(q_out.shape, dtype=q_out.dtype).pin_memory()
+    qkv_d = torch.empty_like(wl.qkv)
+    e2e_wl = W.RopeWorkload(wl.name, qkv_d, wl.positions, wl.slot_mapping, wl.cos_sin,
+                            wl.k_cache, wl.v_cache, wl.num_q_heads, wl.num_kv_heads,
+                            wl.head_dim, wl.neox)
+    h2d = qkv_h.numel() * qkv_h.element_size() + pos_h.numel() * 4 + slot_h.numel() * 8
+    d2h = out_h.numel() * out_h.element_size()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        qkv_d.copy_(qkv_h, non_blocking=True)
+        wl.positions.copy_(pos_h, non_blocking=True)
+        wl.slot_mapping.copy_(slot_h, non_blocking=True)
+        step(e2e_wl)
+        out_h.copy_(q_out, non_blocking=True)
+        stream.synchronize()
+    e2e_value = T * args.steps / (time.perf_counter() - t0)
+    peak, peak_kind = measured_peaks()
+    achieved = moved / (avg_ms / 1e3) / 1e9
+    line = {
+        "metric": ROPE_METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": timed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, **spec, "bytes_per_step": moved,
+                   "l2": "L2 flushed between calls" if flush else
+                   ("inputs larger than L2 (>= 2x L2 per step, no flush)" if moved >= 2 * l2
+                    else "L2-warm: graph replay, no flush"),
+                   "timing": timing_desc},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_kind} (hbm_gbs)",
+                     "kernel": "rope_kv_write_kernel", "per_launch_ms": avg_ms},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(),
+    }
+    if not args.no_cpu_baseline:
+        v, desc = rope_oracle_sample(wl)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": desc}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -465,6 +637,8 @@ def main(argv=None):
     ap.add_argument("--timing", choices=["auto", "graph", "eager"], default="auto")
     ap.add_argument("--splits", type=int, default=0, help="split count (0 = the planner's)")
     args = ap.parse_args(argv)
+    if args.workload in ROPE_WORKLOADS:
+        return run_rope(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

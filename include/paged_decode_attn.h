@@ -178,10 +178,59 @@ int paged_decode_attn_validate(pda_handle handle, const int32_t* block_table,
  * *code receives 0 (no error) or a nonzero code:
  *   1 = context length out of range, 2 = block id out of range (validator);
  *   3 = a pipeline wait inside a kernel gave up after its time limit.
+ * (Codes 4 and 5 belong to paged_decode_attn_rope_kv_write's own error word.)
  * *detail receives the sequence index (codes 1, 2) or the split index (3).
  * Returns PDA_OK, or PDA_ECUDA if the synchronisation or the copy failed. */
 int paged_decode_attn_check_device_error(pda_handle handle, int* code, int* detail,
                                          void* stream);
+
+/* RoPE + paged-KV write (Loom Kernels landing page, "Supported now": "RoPE +
+ * paged-KV write", packed Q/K rotation + native cache write): rotates the
+ * new tokens' query and key heads and stores key and value heads into the
+ * paged cache read by paged_decode_attn_run, in one launch. No handle.
+ *
+ * For token t < num_tokens with p = positions[t] and table row
+ * cs = cos_sin_cache[p] (rot_dim floats: rot_dim/2 cosines, then rot_dim/2
+ * sines), every head vector x of q and k has its pairs j < rot_dim/2,
+ *   (a, b) = (j, j + rot_dim/2)   neox_style != 0 (rotate halves)
+ *   (a, b) = (2j, 2j + 1)         neox_style == 0 (interleaved pairs),
+ * rotated as y_a = x_a cos_j - x_b sin_j, y_b = x_b cos_j + x_a sin_j; dims
+ * >= rot_dim are copied. Outputs are exactly rounded (round to nearest even
+ * of the double-precision value), so the result is bit-identical to the FP64
+ * definition.
+ *   q        [num_tokens, num_q_heads, head_dim], token stride q_token_stride
+ *   k, v     [num_tokens, num_kv_heads, head_dim], token strides k/v_token_stride
+ *            (strides in elements; 0 = packed; e.g. views into a fused qkv
+ *            projection output)
+ *   positions     [num_tokens] int32
+ *   slot_mapping  [num_tokens] int64: cache row of the token
+ *                 (block * block_size + offset in block); < 0 = no cache write
+ *   cos_sin_cache [max_position, rot_dim] fp32 (may be NULL when rot_dim = 0)
+ *   q_out    [num_tokens, num_q_heads, head_dim], token stride q_out_token_stride;
+ *            q_out == q with equal strides rotates in place
+ *   k_cache, v_cache  [num_slots, num_kv_heads, head_dim] (the decode
+ *            layout [num_blocks, block_size, Hkv, D] with num_slots =
+ *            num_blocks * block_size); only the rows named by slot_mapping
+ *            are written
+ *   err      optional device int[2] (NULL = none): the first bad token sets
+ *            err[0] = 4 (position outside [0, max_position)) or 5 (slot >=
+ *            num_slots) and err[1] = its index; the caller zeroes it.
+ * A token with a bad position writes nothing; one with a bad slot writes
+ * q_out only. Two tokens with the same slot race (last writer undefined).
+ * dtype PDA_BF16 or PDA_FP16 for q, k, v, q_out and the caches; head_dim a
+ * multiple of 16 (<= 1024), rot_dim a multiple of 16 (<= head_dim); every
+ * pointer 16-byte aligned, token strides multiples of 8. Outputs must not
+ * overlap inputs or each other (PDA_EALIAS), except q_out == q. Asynchronous
+ * on `stream`; allocates nothing; graph-capturable. */
+int paged_decode_attn_rope_kv_write(const void* q, int64_t q_token_stride, const void* k,
+                                    int64_t k_token_stride, const void* v,
+                                    int64_t v_token_stride, const int32_t* positions,
+                                    const int64_t* slot_mapping, const float* cos_sin_cache,
+                                    int max_position, int rot_dim, int neox_style,
+                                    int num_tokens, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int dtype, void* q_out,
+                                    int64_t q_out_token_stride, void* k_cache, void* v_cache,
+                                    int64_t num_slots, int* err, int device, void* stream);
 
 /* Decode attention for callers that cannot allocate device memory.
  * (No counterpart in the paper: this entry point exists for integration.)

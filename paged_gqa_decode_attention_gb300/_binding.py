@@ -39,6 +39,7 @@ EXPORTS = [
     "paged_decode_attn_validate",
     "paged_decode_attn_check_device_error",
     "paged_decode_attn_run_noalloc",
+    "paged_decode_attn_rope_kv_write",
 ]
 
 
@@ -97,6 +98,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.paged_decode_attn_run_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I64, F,
                                                       P, I, I, P]
         lib.paged_decode_attn_run_noalloc.restype = I
+        lib.paged_decode_attn_rope_kv_write.argtypes = [P, I64, P, I64, P, I64, P, P, P, I, I, I,
+                                                        I, I, I, I, I, P, I64, P, P, I64, P, I,
+                                                        P]
+        lib.paged_decode_attn_rope_kv_write.restype = I
         if lib.paged_decode_attn_abi_version() != ABI_VERSION:
             raise RuntimeError("ABI version mismatch between binding and library")
         if path is None:
@@ -240,3 +245,65 @@ def merge(partial_o: torch.Tensor, partial_lse: torch.Tensor, out_dtype=torch.fl
         _dev_ptr(partial_lse, "partial_lse", torch.float32), rows, S, D,
         _dev_ptr(out, "out", out_dtype), _DT[out_dtype], dev, _stream_ptr(stream)))
     return out
+
+
+def _token_rows(t: torch.Tensor, name: str, dtype) -> tuple[int, int]:
+    """Pointer and token stride (elements) of a [T, H, D] tensor whose heads
+    are contiguous within a token (a packed tensor or a view into a fused
+    projection output)."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != 3:
+        raise ValueError(f"{name} must be [tokens, heads, head_dim]")
+    T, H, D = t.shape
+    if t.stride(2) != 1 or (H > 1 and t.stride(1) != D):
+        raise ValueError(f"{name}: heads must be contiguous within a token")
+    return t.data_ptr(), (t.stride(0) if T > 1 else H * D)
+
+
+def rope_kv_write(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, positions: torch.Tensor,
+                  slot_mapping: torch.Tensor, cos_sin_cache: torch.Tensor,
+                  k_cache: torch.Tensor, v_cache: torch.Tensor, neox: bool = True,
+                  q_out: torch.Tensor | None = None, err: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """RoPE on q and k plus the paged-cache write of k and v, one launch.
+
+    q [T, Hq, D], k/v [T, Hkv, D] (bf16/fp16; token-strided views allowed),
+    positions [T] int32, slot_mapping [T] int64 (< 0: no cache write),
+    cos_sin_cache [max_position, rot_dim] fp32 (cosines then sines),
+    k_cache/v_cache [num_blocks, block_size, Hkv, D]. Returns q_out (a new
+    tensor, or ``q_out``; pass ``q_out=q`` to rotate in place). ``err`` is an
+    optional int32 [2] device tensor receiving the first bad token."""
+    lib = load_library()
+    dt = q.dtype
+    qp, qs = _token_rows(q, "q", dt)
+    kp, ks = _token_rows(k, "k", dt)
+    vp, vs = _token_rows(v, "v", dt)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (T, Hkv, D) or v.shape != (T, Hkv, D):
+        raise ValueError("k and v must be [T, Hkv, D] with q's T and D")
+    if q_out is None:
+        q_out = torch.empty((T, Hq, D), dtype=dt, device=q.device)
+    qop, qos = _token_rows(q_out, "q_out", dt)
+    if q_out.shape != q.shape:
+        raise ValueError("q_out must have q's shape")
+    if k_cache.shape != v_cache.shape or k_cache.dim() != 4 or k_cache.shape[2:] != (Hkv, D):
+        raise ValueError("caches must be [num_blocks, block_size, Hkv, D]")
+    if cos_sin_cache.dim() != 2:
+        raise ValueError("cos_sin_cache must be [max_position, rot_dim]")
+    max_pos, rot_dim = cos_sin_cache.shape
+    if positions.shape != (T,) or slot_mapping.shape != (T,):
+        raise ValueError("positions and slot_mapping must be [T]")
+    dev = q.device.index if q.device.index is not None else 0
+    _check(lib, lib.paged_decode_attn_rope_kv_write(
+        qp, qs, kp, ks, vp, vs, _dev_ptr(positions, "positions", torch.int32),
+        _dev_ptr(slot_mapping, "slot_mapping", torch.int64),
+        _dev_ptr(cos_sin_cache, "cos_sin_cache", torch.float32), max_pos, rot_dim,
+        int(bool(neox)), T, Hq, Hkv, D, _DT[dt], qop, qos, _dev_ptr(k_cache, "k_cache", dt),
+        _dev_ptr(v_cache, "v_cache", dt), k_cache.shape[0] * k_cache.shape[1],
+        _dev_ptr(err, "err", torch.int32) if err is not None else None, dev,
+        _stream_ptr(stream)))
+    return q_out

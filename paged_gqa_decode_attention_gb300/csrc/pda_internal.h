@@ -19,6 +19,8 @@ enum DeviceError : int {
   kErrContextLen = 1,
   kErrBlockId = 2,
   kErrWaitTimeout = 3,
+  kErrPosition = 4,  // RoPE + KV write: position outside the cos/sin table
+  kErrSlot = 5,      // RoPE + KV write: slot beyond the cache
 };
 
 struct PartialParams {

@@ -326,3 +326,130 @@ def compact_for_rows(wl: Workload, seqs) -> tuple:
     v = bits(wl.v_cache.index_select(0, ids))
     q = bits(wl.q[seqs])
     return q, k, v, np.stack(tables).astype(np.int32), lens[seqs].astype(np.int32)
+
+
+# ---------------------------------------------------------------------------
+# RoPE + paged-KV write inputs
+# ---------------------------------------------------------------------------
+
+@dataclass
+class RopeWorkload:
+    """Inputs of one RoPE + paged-KV write call.
+
+    ``qkv`` is the fused projection output [T, (Hq + 2 Hkv) * D]; q, k and v
+    are token-strided views into it (the layout a fused QKV projection
+    produces). ``cos_sin`` [max_position, rot_dim] float32 holds cos(pos * f_j)
+    then sin(pos * f_j) with f_j = theta^(-2j / rot_dim): the usual rotary
+    frequency schedule, precomputed once per model like a weight, and an
+    input to both the kernel and the oracle."""
+    name: str
+    qkv: torch.Tensor
+    positions: torch.Tensor     # [T] int32
+    slot_mapping: torch.Tensor  # [T] int64
+    cos_sin: torch.Tensor       # [max_position, rot_dim] float32
+    k_cache: torch.Tensor       # [num_blocks, block_size, Hkv, D]
+    v_cache: torch.Tensor
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    neox: bool = True
+    meta: dict = field(default_factory=dict)
+
+    def _part(self, h0: int, h1: int) -> torch.Tensor:
+        D = self.head_dim
+        return self.qkv[:, h0 * D:h1 * D].view(-1, h1 - h0, D)
+
+    @property
+    def q(self) -> torch.Tensor:
+        return self._part(0, self.num_q_heads)
+
+    @property
+    def k(self) -> torch.Tensor:
+        return self._part(self.num_q_heads, self.num_q_heads + self.num_kv_heads)
+
+    @property
+    def v(self) -> torch.Tensor:
+        Hq, Hkv = self.num_q_heads, self.num_kv_heads
+        return self._part(Hq + Hkv, Hq + 2 * Hkv)
+
+    @property
+    def num_tokens(self) -> int:
+        return self.qkv.shape[0]
+
+    @property
+    def rot_dim(self) -> int:
+        return self.cos_sin.shape[1]
+
+    def moved_bytes(self) -> int:
+        """Bytes the operation must move: q, k, v read; q_out and the k/v
+        cache rows written (padding tokens write no cache rows); one table row
+        and the position and slot of every token."""
+        esz = self.qkv.element_size()
+        T, Hq, Hkv, D = self.num_tokens, self.num_q_heads, self.num_kv_heads, self.head_dim
+        written = int((self.slot_mapping >= 0).sum())
+        return (T * (Hq + 2 * Hkv) * D * esz + T * Hq * D * esz + written * 2 * Hkv * D * esz
+                + T * self.rot_dim * 4 + T * 12)
+
+    def to(self, device) -> "RopeWorkload":
+        return RopeWorkload(self.name, self.qkv.to(device), self.positions.to(device),
+                            self.slot_mapping.to(device), self.cos_sin.to(device),
+                            self.k_cache.to(device), self.v_cache.to(device), self.num_q_heads,
+                            self.num_kv_heads, self.head_dim, self.neox, dict(self.meta))
+
+
+def rope_cos_sin(max_position: int, rot_dim: int, theta: float) -> torch.Tensor:
+    """[max_position, rot_dim] float32: cosines then sines of pos * theta^(-2j/rot_dim),
+    evaluated in float64 and rounded once."""
+    j = np.arange(rot_dim // 2, dtype=np.float64)
+    freq = theta ** (-2.0 * j / rot_dim)
+    ang = np.arange(max_position, dtype=np.float64)[:, None] * freq[None, :]
+    return torch.from_numpy(np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32))
+
+
+def rope_batch(seed: int = 0, tokens: int = 512, Hq: int = 14, Hkv: int = 2, D: int = 64,
+               rot_dim: int | None = None, theta: float = 1.0e6, max_position: int = 32768,
+               block_size: int = 16, num_blocks: int | None = None, dtype: str = "bf16",
+               mode: str = "decode", neox: bool = True, pad_frac: float = 0.0,
+               device="cpu") -> RopeWorkload:
+    """Seeded RoPE + KV-write inputs. Defaults: the Qwen2.5-0.5B attention
+    geometry (14 query heads, 2 kv heads, D 64, full-width rotate-halves
+    rotary with theta 1e6, 32768 positions), bf16 N(0, 1) activations.
+
+    mode "decode": one new token per sequence, positions uniform in
+    [0, max_position), distinct random cache slots. mode "prefill": one
+    sequence of ``tokens`` tokens at positions 0 .. T-1 stored through a
+    random block table. ``pad_frac`` of the tokens get slot -1 (padding).
+    The cache pool starts filled with N(0, 1) values."""
+    rot_dim = D if rot_dim is None else rot_dim
+    dt = DTYPES[dtype]
+    rng = _rng(seed, 40)
+    T = tokens
+    if num_blocks is None:
+        num_blocks = max(64, 2 * ((T + block_size - 1) // block_size))
+    slots_total = num_blocks * block_size
+    if mode == "decode":
+        pos = rng.integers(0, max_position, size=T)
+        slots = rng.permutation(slots_total)[:T]
+    elif mode == "prefill":
+        if T > max_position:
+            raise ValueError("prefill longer than the position table")
+        pos = np.arange(T)
+        pages = rng.permutation(num_blocks)[: (T + block_size - 1) // block_size]
+        slots = pages[np.arange(T) // block_size] * block_size + np.arange(T) % block_size
+    else:
+        raise ValueError(mode)
+    if T > slots_total:
+        raise ValueError("cache pool smaller than the token count")
+    slots = slots.astype(np.int64)
+    if pad_frac > 0:
+        slots[rng.random(T) < pad_frac] = -1
+    qkv = _randn((T, (Hq + 2 * Hkv) * D), 1.0, dt, device, seed, 41)
+    kc = _randn((num_blocks * block_size, Hkv * D), 1.0, dt, device, seed, 42)
+    vc = _randn((num_blocks * block_size, Hkv * D), 1.0, dt, device, seed, 43)
+    return RopeWorkload(
+        f"rope_{mode}_t{T}_{Hq}x{Hkv}x{D}", qkv,
+        torch.as_tensor(pos.astype(np.int32)).to(device), torch.as_tensor(slots).to(device),
+        rope_cos_sin(max_position, rot_dim, theta).to(device),
+        kc.view(num_blocks, block_size, Hkv, D), vc.view(num_blocks, block_size, Hkv, D),
+        Hq, Hkv, D, neox, {"mode": mode, "theta": theta, "block_size": block_size,
+                           "dtype": dtype})

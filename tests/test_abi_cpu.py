@@ -128,3 +128,48 @@ def test_plan_respects_hint_and_caps(lib):
         pda.plan(cfg, 0, 1, 16)           # no SMs
     with pytest.raises(pda.PDAError):
         pda.plan(cfg, 152, 1, 10 ** 6)    # max_blocks beyond the config
+
+
+# --------------------------- RoPE + KV write -------------------------------
+
+def rope_call(lib, **kw):
+    a = dict(q=16, qs=0, k=32, ks=0, v=48, vs=0, pos=64, slots=80, cs=96, max_pos=10,
+             rot=64, neox=1, T=4, Hq=14, Hkv=2, D=64, dtype=0, qo=1 << 30, qos=0,
+             kc=1 << 31, vc=1 << 32, nslots=100, err=None, dev=0, stream=None)
+    a.update(kw)
+    return lib.paged_decode_attn_rope_kv_write(
+        a["q"], a["qs"], a["k"], a["ks"], a["v"], a["vs"], a["pos"], a["slots"], a["cs"],
+        a["max_pos"], a["rot"], a["neox"], a["T"], a["Hq"], a["Hkv"], a["D"], a["dtype"],
+        a["qo"], a["qos"], a["kc"], a["vc"], a["nslots"], a["err"], a["dev"], a["stream"])
+
+
+@pytest.mark.parametrize("kw", [dict(T=-1), dict(Hq=0), dict(D=72), dict(D=0), dict(rot=72),
+                                dict(rot=80), dict(dtype=2), dict(qs=100), dict(ks=8),
+                                dict(nslots=-1), dict(q=0), dict(cs=0), dict(q=18),
+                                dict(dev=-1)])
+def test_rope_kv_write_rejects_bad_arguments_before_cuda(lib, kw):
+    assert rope_call(lib, **kw) == pda.PDA_EINVAL
+    assert lib.paged_decode_attn_last_error()
+
+
+def test_rope_kv_write_aliasing_and_no_op(lib):
+    assert rope_call(lib, T=0, q=0, k=0) == pda.PDA_OK  # nothing to do
+    assert rope_call(lib, vc=1 << 31) == pda.PDA_EALIAS             # k_cache == v_cache
+    assert rope_call(lib, qo=16 + 64) == pda.PDA_EALIAS             # q_out inside q
+    assert rope_call(lib, kc=16) == pda.PDA_EALIAS                  # cache over q
+    assert rope_call(lib, qo=96) == pda.PDA_EALIAS                  # q_out over the table
+
+
+def test_rope_kv_write_fused_views_are_not_aliases(lib):
+    """q, k, v as views into one fused [T, (Hq + 2 Hkv) * D] buffer, rotated
+    in place: the row sets interleave without sharing a byte, so the call
+    passes the alias checks (and reaches CUDA, absent here)."""
+    row = (14 + 4) * 64
+    base = 1 << 20
+    st = rope_call(lib, q=base, qs=row, k=base + 14 * 64 * 2, ks=row, v=base + 16 * 64 * 2,
+                   vs=row, qo=base, qos=row)
+    assert st == pda.PDA_ECUDA, lib.paged_decode_attn_last_error()
+    # q_out as the k part of the same rows does overlap
+    st = rope_call(lib, q=base, qs=row, k=base + 14 * 64 * 2, ks=row, v=base + 16 * 64 * 2,
+                   vs=row, qo=base + 14 * 64 * 2, qos=row)
+    assert st == pda.PDA_EALIAS
