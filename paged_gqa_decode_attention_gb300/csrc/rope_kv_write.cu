@@ -22,7 +22,7 @@
 // algorithms using rounding to odd", 2008), which avoids double rounding.
 //
 // Memory-bound: token rows move through shared memory by bulk asynchronous
-// copies (no registers hold data in flight), so a 4-stage ring of ~24 KB
+// copies (no registers hold data in flight), so a ring of up to six ~16 KB
 // tiles per CTA keeps enough bytes in flight to stream at HBM speed, and a
 // dedicated mover warp lets the rotation of one tile overlap the copies of
 // the others.
@@ -68,6 +68,10 @@ struct RopeParams {
   int row_elems;    // (Hq + 2 Hkv) * D: one token's staged row
   int tile_tokens;  // tokens per tile (<= 32)
   int num_tiles;
+  uint32_t div_tok_mul, div_tok_shift;  // x / per_token == (x * mul) >> shift
+  uint32_t div_rot_mul, div_rot_shift;  // x / rot_items
+  int stages;       // ring stages (<= kRopeMaxStages)
+  int lag;          // a stage is refilled `lag` tiles after its stores were issued
   int fused;        // q, k, v are consecutive parts of one [T, row_elems] buffer
 };
 
@@ -107,12 +111,18 @@ __device__ __forceinline__ float round_to_odd_float(double d) {
 // RN_fmt(a1*b1 + c1*d1) in the high half, for storage-format values a, c and
 // fp32 b, d; equal to rounding the double-precision value (a*b and c*d are
 // exact in double, the sum is rounded once) to the format.
+// Fast path: r = fma(a, b, fl(c*d)) is within 2^-24 (|fl(c*d)| + |r|)(1 + 2^-23)
+// + 2^-149 of the exact value; m is twice that bound. If rounding r - m down
+// and r + m up gives the same storage values, the exact values, inside
+// [r - m, r + m], round to them too. Otherwise (about one output in 10^4)
+// both are recomputed in double and rounded through a round-to-odd float.
+// The bound is kept tight (per output) because a warp takes the slow path
+// whenever one of its lanes does.
 template <typename F>
 __device__ __forceinline__ uint32_t rounded_dot2_x2(float a0, float b0, float c0, float d0,
                                                     float a1, float b1, float c1, float d1) {
   const float p0 = __fmul_rn(c0, d0), p1 = __fmul_rn(c1, d1);
   const float r0 = __fmaf_rn(a0, b0, p0), r1 = __fmaf_rn(a1, b1, p1);
-  // |exact - r| <= 2^-24 (|p| + |r|) (1 + 2^-23) + 2^-149; m is twice that
   const float m0 = __fmaf_rn(fabsf(p0) + fabsf(r0), 0x1p-23f, 0x1p-147f);
   const float m1 = __fmaf_rn(fabsf(p1) + fabsf(r1), 0x1p-23f, 0x1p-147f);
   const uint32_t lo = F::pack2(__fsub_rd(r0, m0), __fsub_rd(r1, m1));
@@ -123,13 +133,18 @@ __device__ __forceinline__ uint32_t rounded_dot2_x2(float a0, float b0, float c0
   return F::pack2(round_to_odd_float(e0), round_to_odd_float(e1));
 }
 
+__device__ __forceinline__ int fast_div(int x, uint32_t mul, uint32_t shift) {
+  return (int)(((uint64_t)(uint32_t)x * mul) >> shift);
+}
+
 __device__ __forceinline__ void record_error(int* err, int code, int detail) {
   if (err != nullptr && atomicCAS(err, 0, code) == 0) err[1] = detail;
 }
 
-constexpr int kRopeStages = 4;
-constexpr int kRopeDataOff = 128;           // 2 x kRopeStages mbarriers first
-constexpr int kRopeStageTarget = 24 * 1024;  // bytes of token rows per stage
+constexpr int kRopeMaxStages = 6;
+constexpr int kRopeDataOff = 128;           // 2 x kRopeMaxStages mbarriers first
+constexpr int kRopeStageTarget = 16 * 1024;  // bytes of token rows per stage
+constexpr int kRopeRingBytes = 192 * 1024;   // at most, for the whole ring
 constexpr int kRopeMaxRowBytes = 48 * 1024;
 constexpr int kRopeMaxTileTokens = 32;       // one lane of warp 0 per token
 
@@ -178,7 +193,7 @@ __device__ __forceinline__ void rotate_item(uint16_t* row, const float* cs_row, 
 }
 
 // Persistent CTAs walk tiles of tile_tokens tokens (local tile i is tile
-// blockIdx.x + i * gridDim.x), through a ring of kRopeStages shared-memory
+// blockIdx.x + i * gridDim.x), through a ring of p.stages shared-memory
 // stages laid out [token][q heads | k heads | v heads][D].
 //   warp 8 (mover): bulk-loads each tile's rows into its stage (one copy
 //     when q, k, v are one contiguous fused buffer, else three per token);
@@ -188,13 +203,14 @@ __device__ __forceinline__ void rotate_item(uint16_t* row, const float* cs_row, 
 //     the tile it held have read it.
 //   warps 0-7 (rotators): wait for a stage, rotate its q and k pairs in
 //     place, release it. They never wait for stores, so up to
-//     kRopeStages - 1 tiles of loads stay in flight.
+//     stages - lag tiles of loads stay in flight ahead of the rotation.
 // No block-wide barrier inside the loop; every wait is bounded.
 template <typename F, bool kNeox>
-__global__ void __launch_bounds__(kRopeThreads) rope_kv_write_kernel(const RopeParams p) {
+__global__ void __launch_bounds__(kRopeThreads, 3) rope_kv_write_kernel(const RopeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* done = full + kRopeStages;
+  uint64_t* done = full + kRopeMaxStages;
+  const int K = p.stages, lag = p.lag;
   uint16_t* data = reinterpret_cast<uint16_t*>(smem + kRopeDataOff);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_local = (p.num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
@@ -203,8 +219,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kv_write_kernel(const RopeP
   const uint32_t q_bytes = (uint32_t)(p.Hq * p.D) * 2, kv_bytes = (uint32_t)(p.Hkv * p.D) * 2;
 
   if (tid == 0) {
-#pragma unroll
-    for (int s = 0; s < kRopeStages; ++s) {
+    for (int s = 0; s < K; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&done[s]), kRopeRotWarps);
     }
@@ -234,14 +249,16 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kv_write_kernel(const RopeP
         bulk_load(dst + q_bytes + kv_bytes, p.v + t * p.v_stride, kv_bytes, bar);
       }
     };
-    for (int s = 0; s < kRopeStages && s < n_local; ++s) issue_load(s, s);
+    for (int s = 0; s < K && s < n_local; ++s) issue_load(s, s);
     for (int i = 0; i < n_local; ++i) {
-      const int s = i % kRopeStages;
-      // refill the stage of tile i - 1 as soon as its stores have read it
-      if (i >= 1 && i - 1 + kRopeStages < n_local) {
-        bulk_wait_read<0>();
+      const int s = i % K;
+      // refill the stage of tile i - lag once its stores have read it (the
+      // stores of the lag - 1 tiles after it may still be reading)
+      if (i >= lag && i - lag + K < n_local) {
+        if (lag == 1) bulk_wait_read<0>();
+        else bulk_wait_read<1>();
         __syncwarp();
-        issue_load(i - 1 + kRopeStages, (i - 1) % kRopeStages);
+        issue_load(i - lag + K, (i - lag) % K);
       }
       const int t0 = first_token(i), nt = tile_len(t0);
       const int64_t t = t0 + lane;
@@ -251,7 +268,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kv_write_kernel(const RopeP
         pos = __ldg(p.positions + t);
         slot = __ldg(p.slots + t);
       }
-      const bool ok = mbar_wait(smem_u32(&done[s]), (uint32_t)(i / kRopeStages) & 1u);
+      const bool ok = mbar_wait_sleep(smem_u32(&done[s]), (uint32_t)(i / K) & 1u);
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) record_error(p.err, kErrWaitTimeout, t0);
         break;
@@ -280,22 +297,38 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kv_write_kernel(const RopeP
   const int rot_items = p.rot_dim >> 4, half = p.rot_dim >> 1;
   const int per_token = (p.Hq + p.Hkv) * rot_items;
   for (int i = 0; i < n_local; ++i) {
-    const int s = i % kRopeStages;
+    const int s = i % K;
     const int t0 = first_token(i), nt = tile_len(t0);
-    const bool ok = mbar_wait(smem_u32(&full[s]), (uint32_t)(i / kRopeStages) & 1u);
+    const bool ok = mbar_wait_sleep(smem_u32(&full[s]), (uint32_t)(i / K) & 1u);
     if (!__all_sync(0xffffffffu, ok)) {
       if (lane == 0) record_error(p.err, kErrWaitTimeout, t0);
       break;
     }
     uint16_t* st = data + s * stage_elems;
+    // item it = (token j, rem); j and rem advance without dividing, and the
+    // token's position and table row are looked up once per token
+    int j = fast_div(tid, p.div_tok_mul, p.div_tok_shift);
+    int rem = tid - j * per_token;
+    int cur_j = -1;
+    bool valid = false;
+    const float* cs_row = p.cos_sin;
     for (int it = tid; it < nt * per_token; it += kRopeRotThreads) {
-      const int j = it / per_token;
-      const int rem = it - j * per_token;
-      const int r = rem / rot_items;
-      const int pos = __ldg(p.positions + t0 + j);
-      if (pos < 0 || pos >= p.max_position) continue;
-      rotate_item<F, kNeox>(st + (int64_t)j * p.row_elems + r * p.D,
-                            p.cos_sin + (int64_t)pos * p.rot_dim, half, rem - r * rot_items);
+      if (j != cur_j) {
+        cur_j = j;
+        const int pos = __ldg(p.positions + t0 + j);
+        valid = pos >= 0 && pos < p.max_position;
+        cs_row = p.cos_sin + (int64_t)(valid ? pos : 0) * p.rot_dim;
+      }
+      if (valid) {
+        const int r = fast_div(rem, p.div_rot_mul, p.div_rot_shift);
+        rotate_item<F, kNeox>(st + (int64_t)j * p.row_elems + r * p.D, cs_row, half,
+                              rem - r * rot_items);
+      }
+      rem += kRopeRotThreads;
+      while (rem >= per_token) {
+        rem -= per_token;
+        ++j;
+      }
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -341,6 +374,17 @@ bool overlaps(Rows a, Rows b) {
 
 int fail(int code, const std::string& msg) { return set_last_error(code, msg.c_str()); }
 
+// Division by a fixed d >= 1 as one wide multiply and a shift, exact for
+// every x < 2^31 (Granlund and Montgomery, "Division by invariant integers
+// using multiplication", 1994): with l = ceil(log2 d), mul = ceil(2^(31+l) / d)
+// fits in 32 bits and x / d = (x * mul) >> (31 + l).
+void magic_div(uint32_t d, uint32_t* mul, uint32_t* shift) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  *mul = (uint32_t)(((1ull << (31 + l)) + d - 1) / d);
+  *shift = 31 + l;
+}
+
 struct DeviceInfo {
   int num_sms = 0;
   bool prepared = false;
@@ -362,7 +406,7 @@ cudaError_t device_info(int device, int* num_sms) {
   DeviceInfo& d = g_dev[device];
   if (!d.prepared) {
     cudaError_t e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, device);
-    const int smem_max = kRopeDataOff + kRopeStages * kRopeMaxRowBytes;
+    const int smem_max = kRopeDataOff + kRopeRingBytes;
     if (e == cudaSuccess) e = prepare_one<Bf16, true>(smem_max);
     if (e == cudaSuccess) e = prepare_one<Bf16, false>(smem_max);
     if (e == cudaSuccess) e = prepare_one<Fp16, true>(smem_max);
@@ -455,15 +499,20 @@ extern "C" int paged_decode_attn_rope_kv_write(
     if (prev >= 0 && prev != device) cudaSetDevice(prev);
     return fail(PDA_ECUDA, std::string("rope_kv_write set-up: ") + cudaGetErrorString(e));
   }
-  // Tiles: up to ~24 KB of token rows (<= 32 tokens); fewer tokens per tile
+  // Tiles: up to ~16 KB of token rows (<= 32 tokens); fewer tokens per tile
   // when that still gives every SM two tiles, so short calls spread out.
   const int64_t row_bytes = row_elems * 2;
   int n_max = (int)std::min<int64_t>(pda::kRopeMaxTileTokens,
                                      std::max<int64_t>(1, pda::kRopeStageTarget / row_bytes));
   int n = (int)std::min<int64_t>(n_max, std::max<int64_t>(1, (T + 2 * num_sms - 1) / (2 * num_sms)));
   const int64_t num_tiles = (T + n - 1) / n;
-  const int smem = pda::kRopeDataOff + pda::kRopeStages * n * (int)row_bytes;
-  const int per_sm = std::max(1, std::min(6, 233472 / (smem + 1024)));
+  const uint32_t per_token_items =
+      std::max<uint32_t>(1, (uint32_t)(num_q_heads + num_kv_heads) * (uint32_t)(rot_dim / 16));
+  const int stage_bytes = n * (int)row_bytes;
+  const int stages = std::min(pda::kRopeMaxStages, pda::kRopeRingBytes / stage_bytes);
+  const int lag = stages >= 5 ? 2 : 1;
+  const int smem = pda::kRopeDataOff + stages * stage_bytes;
+  const int per_sm = std::max(1, std::min(3, 233472 / (smem + 1024)));  // 3 by registers
   const int64_t grid = std::min<int64_t>(num_tiles, (int64_t)num_sms * per_sm);
   pda::RopeParams p;
   p.q = static_cast<const uint16_t*>(q);
@@ -490,6 +539,10 @@ extern "C" int paged_decode_attn_rope_kv_write(
   p.row_elems = (int)row_elems;
   p.tile_tokens = n;
   p.num_tiles = (int)num_tiles;
+  pda::magic_div(per_token_items, &p.div_tok_mul, &p.div_tok_shift);
+  pda::magic_div(rot_dim >= 16 ? rot_dim / 16 : 1, &p.div_rot_mul, &p.div_rot_shift);
+  p.stages = stages;
+  p.lag = lag;
   p.fused = (k == p.q + hq_d && v == p.q + hq_d + hkv_d && q_token_stride == row_elems &&
              k_token_stride == row_elems && v_token_stride == row_elems);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
