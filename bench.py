@@ -47,6 +47,8 @@ NCU_TRAFFIC_BYTES = {
     # profiles/paged_partial_tc_kernel_long_b4_l32768.md: 537.07 MB read + 3.78 MB
     # written per launch (captured on the same step over a 1 GiB pool)
     "long_b4_l32768": 540_858_624,
+    # profiles/rope_kv_write_kernel_prefill_t32768.md: 419.90 MB read + 348.27 MB written
+    "rope_prefill_t32768": 768_166_400,
 }
 
 
@@ -609,7 +611,7 @@ def run_rope(args):
                     else "L2-warm: graph replay, no flush"),
                    "timing": timing_desc},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": NCU_TRAFFIC_BYTES.get(args.workload),
                      "peak_source": f"{peak_kind} (hbm_gbs)",
                      "kernel": "rope_kv_write_kernel", "per_launch_ms": avg_ms},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
