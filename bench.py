@@ -74,6 +74,19 @@ def make_workload(name: str, seed: int, device):
     if name == "long_b32_l32768_mqa4":  # same bytes and G as long_b4_l32768, one kv head
         return W.custom(seed=seed, B=32, Hq=4, Hkv=1, D=128, block_size=16, lens=[32768] * 32,
                         num_blocks=4 * 65536, device=device)
+    # other GQA geometries (random pages over exactly the pool they need)
+    if name == "geo_qwen05b_b64_l8192":  # Qwen2.5-0.5B attention: 14/2 heads, D 64
+        return W.custom(seed=seed, B=64, Hq=14, Hkv=2, D=64, block_size=16, lens=[8192] * 64,
+                        device=device)
+    if name == "geo_qwen7b_b16_l8192":  # Qwen2.5-7B attention: 28/4 heads, D 128 (G = 7)
+        return W.custom(seed=seed, B=16, Hq=28, Hkv=4, D=128, block_size=16, lens=[8192] * 16,
+                        device=device)
+    if name == "geo_d256_b16_l8192":  # 16/8 heads, D 256 (G = 2)
+        return W.custom(seed=seed, B=16, Hq=16, Hkv=8, D=256, block_size=16, lens=[8192] * 16,
+                        device=device)
+    if name == "geo_mqa_b64_l8192":  # MQA: 8 query heads on one kv head, D 128
+        return W.custom(seed=seed, B=64, Hq=8, Hkv=1, D=128, block_size=16, lens=[8192] * 64,
+                        device=device)
     if name == "serving_b128":
         return W.serving_mix(seed=seed, batch=128, device=device)
     if name == "mid_ragged_b8":

@@ -64,10 +64,12 @@ int check_config(const pda_config* c) {
   if (c->max_splits < 1 || c->max_splits > pda::kMaxSplits)
     return fail(PDA_EINVAL, "max_splits must be in [1, 64]");
   if (c->device < 0) return fail(PDA_EINVAL, "device must be >= 0");
-  if (c->head_dim != pda::kHeadDim) return fail(PDA_EUNSUPPORTED, "head_dim must be 128");
-  if (!pda::partial_supported(G, c->block_size, c->dtype))
+  if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256)
+    return fail(PDA_EUNSUPPORTED, "head_dim must be 64, 128 or 256");
+  if (!pda::partial_supported(G, c->head_dim, c->block_size, c->dtype))
     return fail(PDA_EUNSUPPORTED,
-                "unsupported geometry: group size must be 1, 2, 4 or 8 and block_size 16 or 32");
+                "unsupported geometry: group size must be 1..8 (1..4 at head_dim 256) and "
+                "block_size 16 or 32");
   return PDA_OK;
 }
 
@@ -117,13 +119,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// A [num_blocks * block_size, Hkv * 128] view of a cache, loaded as boxes of
+// A [num_blocks * block_size, Hkv * D] view of a cache, loaded as boxes of
 // 64 dims x block_size rows with 128-byte swizzle.
-int encode_cache_map(CUtensorMap* m, const void* base, int Hkv, int bs, int64_t num_blocks) {
+int encode_cache_map(CUtensorMap* m, const void* base, int Hkv, int D, int bs,
+                     int64_t num_blocks) {
   auto fn = tensor_map_encoder();
   if (!fn) return fail(PDA_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  cuuint64_t dims[2] = {(cuuint64_t)Hkv * pda::kHeadDim, (cuuint64_t)num_blocks * bs};
-  cuuint64_t strides[1] = {(cuuint64_t)Hkv * pda::kHeadDim * 2};
+  cuuint64_t dims[2] = {(cuuint64_t)Hkv * D, (cuuint64_t)num_blocks * bs};
+  cuuint64_t strides[1] = {(cuuint64_t)Hkv * D * 2};
   cuuint32_t box[2] = {64, (cuuint32_t)bs};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides,
@@ -134,13 +137,13 @@ int encode_cache_map(CUtensorMap* m, const void* base, int Hkv, int bs, int64_t 
   return PDA_OK;
 }
 
-// A [B * Hq, 128] view of q, loaded as boxes of 64 dims x G rows (the G
+// A [B * Hq, D] view of q, loaded as boxes of 64 dims x G rows (the G
 // query heads of one kv head) with 128-byte swizzle.
-int encode_q_map(CUtensorMap* m, const void* q, int64_t rows, int group) {
+int encode_q_map(CUtensorMap* m, const void* q, int64_t rows, int D, int group) {
   auto fn = tensor_map_encoder();
   if (!fn) return fail(PDA_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  cuuint64_t dims[2] = {(cuuint64_t)pda::kHeadDim, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)pda::kHeadDim * 2};
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
   cuuint32_t box[2] = {64, (cuuint32_t)group};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(q), dims, strides, box,
@@ -221,22 +224,23 @@ int paged_decode_attn_create(const pda_config* cfg, pda_handle* out_handle) {
   // The partial kernel: PDA_PARTIAL_KERNEL=tensor_core (groups of 4 or 8
   // query heads) or cuda_core overrides the default; read here, once per
   // handle (A/B measurements and tests).
-  h->kernel = pda::default_partial_kernel(h->group);
+  h->kernel = pda::default_partial_kernel(h->group, cfg->head_dim);
   if (const char* env = std::getenv("PDA_PARTIAL_KERNEL")) {
     if (std::strcmp(env, "cuda_core") == 0) h->kernel = pda::kPartialCudaCore;
     else if (std::strcmp(env, "tensor_core") == 0 &&
-             pda::partial_kernel_supported(pda::kPartialTensorCore, h->group))
+             pda::partial_kernel_supported(pda::kPartialTensorCore, h->group, cfg->head_dim))
       h->kernel = pda::kPartialTensorCore;
   }
-  e = pda::partial_prepare(h->kernel, h->group, cfg->block_size, cfg->dtype);
+  e = pda::partial_prepare(h->kernel, h->group, cfg->head_dim, cfg->block_size, cfg->dtype);
   if (e != cudaSuccess) {
     delete h;
     return cuda_fail("cudaFuncSetAttribute", e);
   }
   // Plan with the residency the kernel is built for, so paged_decode_attn_plan
   // (no GPU) and run agree; fall back to the measured figure if it is lower.
-  const int occ = pda::partial_ctas_per_sm(h->kernel, h->group, cfg->block_size, cfg->dtype);
-  const int hint = pda::partial_ctas_per_sm_hint(h->kernel, h->group);
+  const int occ =
+      pda::partial_ctas_per_sm(h->kernel, h->group, cfg->head_dim, cfg->block_size, cfg->dtype);
+  const int hint = pda::partial_ctas_per_sm_hint(h->kernel, h->group, cfg->head_dim);
   h->ctas_per_sm = occ < hint ? occ : hint;
   const size_t rows = (size_t)cfg->max_batch * cfg->num_q_heads * cfg->max_splits;
   const size_t o_bytes = rows * cfg->head_dim * sizeof(float);
@@ -285,9 +289,9 @@ int paged_decode_attn_plan(const pda_config* cfg, int num_sms, int batch, int ma
     return fail(PDA_EINVAL, "max_blocks out of range");
   if (max_context_len_hint < 0) return fail(PDA_EINVAL, "max_context_len_hint < 0");
   const int G = cfg->num_q_heads / cfg->num_kv_heads;
-  plan_splits(*cfg, num_sms,
-              pda::partial_ctas_per_sm_hint(pda::default_partial_kernel(G), G), batch, max_blocks,
-              max_context_len_hint, 0, num_splits, chunk_pages);
+  const int kernel = pda::default_partial_kernel(G, cfg->head_dim);
+  plan_splits(*cfg, num_sms, pda::partial_ctas_per_sm_hint(kernel, G, cfg->head_dim), batch,
+              max_blocks, max_context_len_hint, 0, num_splits, chunk_pages);
   return PDA_OK;
 }
 
@@ -333,9 +337,11 @@ int paged_decode_attn_run_ex(pda_handle h, const void* q, const void* k_cache,
   if (guard.err != cudaSuccess) return cuda_fail("cudaSetDevice", guard.err);
 
   if (h->tm_k != k_cache || h->tm_v != v_cache || h->tm_nb != num_blocks) {
-    int st = encode_cache_map(&h->tmap_k, k_cache, c.num_kv_heads, c.block_size, num_blocks);
+    int st = encode_cache_map(&h->tmap_k, k_cache, c.num_kv_heads, c.head_dim, c.block_size,
+                              num_blocks);
     if (st == PDA_OK)
-      st = encode_cache_map(&h->tmap_v, v_cache, c.num_kv_heads, c.block_size, num_blocks);
+      st = encode_cache_map(&h->tmap_v, v_cache, c.num_kv_heads, c.head_dim, c.block_size,
+                            num_blocks);
     if (st != PDA_OK) {
       h->tm_k = h->tm_v = nullptr;
       h->tm_nb = -1;
@@ -353,7 +359,7 @@ int paged_decode_attn_run_ex(pda_handle h, const void* q, const void* k_cache,
   if (units > INT_MAX) return fail(PDA_EINVAL, "splits * num_kv_heads * batch exceeds 2^31");
   alignas(64) CUtensorMap tmap_q;
   if (h->kernel == pda::kPartialTensorCore) {
-    int st = encode_q_map(&tmap_q, q, (int64_t)batch * c.num_q_heads, h->group);
+    int st = encode_q_map(&tmap_q, q, (int64_t)batch * c.num_q_heads, c.head_dim, h->group);
     if (st != PDA_OK) return st;
   } else {
     std::memset(&tmap_q, 0, sizeof tmap_q);
@@ -377,8 +383,9 @@ int paged_decode_attn_run_ex(pda_handle h, const void* q, const void* k_cache,
   p.qscale = scale * pda::kLog2e;
   p.num_units = (int)units;
   p.max_ctas = h->num_sms * h->ctas_per_sm;
+  p.out_f32 = out_dtype == PDA_F32;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = pda::launch_partial(h->kernel, h->group, c.block_size, c.dtype,
+  cudaError_t e = pda::launch_partial(h->kernel, h->group, c.head_dim, c.block_size, c.dtype,
                                       out_dtype == PDA_F32, &h->tmap_k, &h->tmap_v, &tmap_q, p,
                                       batch, s);
   if (e != cudaSuccess) return cuda_fail("partial kernel launch", e);

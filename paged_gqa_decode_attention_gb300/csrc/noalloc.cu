@@ -45,7 +45,7 @@ constexpr int kMaxDevices = 128;
 std::mutex g_setup_mu;
 void* g_scratch_addr[kMaxDevices] = {};  // device address of the array, per device
 int g_num_sms[kMaxDevices] = {};
-std::set<std::tuple<int, int, int, int>> g_prepared;  // (device, group, block_size, dtype)
+std::set<std::tuple<int, int, int, int>> g_prepared;  // (device, group * 1024 + head_dim, block_size, dtype)
 
 int fail(int code, const char* msg) { return pda::set_last_error(code, msg); }
 
@@ -76,13 +76,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
-// Same descriptor as the handle path: [num_blocks * block_size, Hkv * 128]
+// Same descriptor as the handle path: [num_blocks * block_size, Hkv * D]
 // view, 64 x block_size boxes, 128-byte swizzle. Fills a host struct only.
-bool encode(CUtensorMap* m, const void* base, int Hkv, int bs, int64_t num_blocks) {
+bool encode(CUtensorMap* m, const void* base, int Hkv, int D, int bs, int64_t num_blocks) {
   auto fn = encoder();
   if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)Hkv * pda::kHeadDim, (cuuint64_t)num_blocks * bs};
-  cuuint64_t strides[1] = {(cuuint64_t)Hkv * pda::kHeadDim * 2};
+  cuuint64_t dims[2] = {(cuuint64_t)Hkv * D, (cuuint64_t)num_blocks * bs};
+  cuuint64_t strides[1] = {(cuuint64_t)Hkv * D * 2};
   cuuint32_t box[2] = {64, (cuuint32_t)bs};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box,
@@ -90,12 +90,12 @@ bool encode(CUtensorMap* m, const void* base, int Hkv, int bs, int64_t num_block
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [B * Hq, 128] view of q, boxes of 64 dims x G rows (tensor-core kernel).
-bool encode_q(CUtensorMap* m, const void* q, int64_t rows, int group) {
+// [B * Hq, D] view of q, boxes of 64 dims x G rows (tensor-core kernel).
+bool encode_q(CUtensorMap* m, const void* q, int64_t rows, int D, int group) {
   auto fn = encoder();
   if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)pda::kHeadDim, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)pda::kHeadDim * 2};
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
   cuuint32_t box[2] = {64, (cuuint32_t)group};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(q), dims, strides, box, estr,
@@ -105,7 +105,8 @@ bool encode_q(CUtensorMap* m, const void* q, int64_t rows, int group) {
 
 // Once per device (with `dev` current): the scratch array's device address,
 // the SM count, and the kernels' shared-memory limit for this geometry.
-int setup_device(int dev, int group, int bs, int dtype, void** scratch, int* num_sms) {
+int setup_device(int dev, int group, int head_dim, int bs, int dtype, void** scratch,
+                 int* num_sms) {
   std::lock_guard<std::mutex> lock(g_setup_mu);
   if (!g_scratch_addr[dev]) {
     void* p = nullptr;
@@ -117,9 +118,10 @@ int setup_device(int dev, int group, int bs, int dtype, void** scratch, int* num
     g_num_sms[dev] = sms;
     g_scratch_addr[dev] = p;
   }
-  const auto key = std::make_tuple(dev, group, bs, dtype);
+  const auto key = std::make_tuple(dev, group * 1024 + head_dim, bs, dtype);
   if (!g_prepared.count(key)) {
-    cudaError_t e = pda::partial_prepare(pda::default_partial_kernel(group), group, bs, dtype);
+    cudaError_t e = pda::partial_prepare(pda::default_partial_kernel(group, head_dim), group,
+                                         head_dim, bs, dtype);
     if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", e);
     g_prepared.insert(key);
   }
@@ -196,7 +198,7 @@ extern "C" int paged_decode_attn_run_noalloc(const void* q, const void* k_cache,
   const int group = num_q_heads / num_kv_heads;
   void* scratch = nullptr;
   int num_sms = 1;
-  st = setup_device(device, group, block_size, dtype, &scratch, &num_sms);
+  st = setup_device(device, group, head_dim, block_size, dtype, &scratch, &num_sms);
   if (st != PDA_OK) return st;
 
   if (num_splits > 0) {
@@ -209,15 +211,15 @@ extern "C" int paged_decode_attn_run_noalloc(const void* q, const void* k_cache,
     if (st != PDA_OK) return st;
   }
 
-  const int kernel = pda::default_partial_kernel(group);
+  const int kernel = pda::default_partial_kernel(group, head_dim);
   const int64_t units = (int64_t)S * num_kv_heads * batch;
   if (units > INT_MAX) return fail(PDA_EINVAL, "splits * num_kv_heads * batch exceeds 2^31");
   alignas(64) CUtensorMap tk, tv, tq;
   std::memset(&tq, 0, sizeof tq);
-  if (!encode(&tk, k_cache, num_kv_heads, block_size, num_blocks) ||
-      !encode(&tv, v_cache, num_kv_heads, block_size, num_blocks) ||
+  if (!encode(&tk, k_cache, num_kv_heads, head_dim, block_size, num_blocks) ||
+      !encode(&tv, v_cache, num_kv_heads, head_dim, block_size, num_blocks) ||
       (kernel == pda::kPartialTensorCore &&
-       !encode_q(&tq, q, (int64_t)batch * num_q_heads, group)))
+       !encode_q(&tq, q, (int64_t)batch * num_q_heads, head_dim, group)))
     return fail(PDA_ECUDA, "cuTensorMapEncodeTiled failed");
 
   float* ws_o = static_cast<float*>(scratch);
@@ -251,8 +253,10 @@ extern "C" int paged_decode_attn_run_noalloc(const void* q, const void* k_cache,
   p.num_splits = S;
   p.qscale = scale * pda::kLog2e;
   p.num_units = (int)units;
-  p.max_ctas = num_sms * pda::partial_ctas_per_sm_hint(kernel, group);
-  e = pda::launch_partial(kernel, group, block_size, dtype, false, &tk, &tv, &tq, p, batch, s);
+  p.max_ctas = num_sms * pda::partial_ctas_per_sm_hint(kernel, group, head_dim);
+  p.out_f32 = 0;
+  e = pda::launch_partial(kernel, group, head_dim, block_size, dtype, false, &tk, &tv, &tq, p,
+                          batch, s);
   if (e != cudaSuccess) return cuda_fail("partial kernel launch", e);
   return PDA_OK;
 }

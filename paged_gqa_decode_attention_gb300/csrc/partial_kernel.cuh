@@ -17,7 +17,10 @@
 //       QK: LPT lanes per token, each holding a slice of the G pre-scaled
 //           query rows in registers, dot products reduced by xor-shuffles;
 //       softmax: chunk max by shuffles, rescale of the running state;
-//       PV: each lane owns 4 of the 128 output dims for all G heads.
+//       PV: each lane owns D / 32 of the output dims for all G heads.
+// Head dims D of 64, 128 and 256 (one, two or four 64-dim boxes per row) and
+// any group size G up to 8 (up to 4 at D = 256, where the query slice would
+// not fit the registers) are instantiated.
 // At the end the consumer warps' (max, sum, acc) states are merged through
 // shared memory; a sequence handled by a single split writes `out` directly,
 // otherwise the split writes its normalised partial and natural-log LSE to
@@ -43,16 +46,27 @@ constexpr int kNW = 4;                    // consumer warps
 constexpr int kTPW = 16;                  // tokens per consumer warp per stage
 constexpr int kChunk = kNW * kTPW;        // tokens per stage
 constexpr int kStages = 3;                // pipeline depth
-constexpr int kRowBytes = 128;            // one 64-element half of a 128-dim row
-constexpr int kHalfBytes = kChunk * kRowBytes;
-constexpr int kStageBytes = 4 * kHalfBytes;  // K lo, K hi, V lo, V hi
+constexpr int kRowBytes = 128;            // one 64-element box of a row
+constexpr int kHalfBytes = kChunk * kRowBytes;  // one box column of a stage
 constexpr int kThreads = (kNW + 1) * 32;
 constexpr int kPBufBytes = kNW * kTPW * 8 * 4;  // probabilities, room for G <= 8
 constexpr int kBarBytes = 2 * kStages * 8;
-constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + kPBufBytes + kBarBytes;
 constexpr unsigned kFull = 0xffffffffu;
 
-static_assert(kHeadDim == 128, "the partial kernel is written for head_dim 128");
+// Bytes of one stage: K and V, D / 64 boxes each.
+__host__ __device__ constexpr int stage_bytes(int D) { return 2 * (D / 64) * kHalfBytes; }
+__host__ __device__ constexpr size_t smem_bytes(int D) {
+  return 1024 + size_t(kStages) * stage_bytes(D) + kPBufBytes + kBarBytes;
+}
+// Lanes per token in QK: enough that each lane's slice of the G query rows
+// (G * D / LPT floats) stays within 128 registers; 8 from G = 4 on, where
+// 4 lanes spilled at D = 128.
+__host__ __device__ constexpr int lpt_for(int G, int D) {
+  return (G >= 4 || G * D / 4 > 128) ? 8 : 4;
+}
+__host__ __device__ constexpr bool geometry_supported(int G, int D) {
+  return G >= 1 && G <= 8 && (D == 64 || D == 128 || D == 256) && G * D / lpt_for(G, D) <= 128;
+}
 
 template <bool FP16>
 __device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
@@ -91,17 +105,22 @@ __device__ __forceinline__ void record_error(int* err, int code, int detail) {
   if (atomicCAS(err, 0, code) == 0) err[1] = detail;
 }
 
-template <int G, int BS, bool FP16, bool OUT_F32>
-__global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCudaCore, G))
+template <int G, int D, int BS, bool FP16>
+__global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCudaCore, G, D))
     paged_partial_kernel(const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v, const PartialParams p) {
-  constexpr int LPT = (G >= 4) ? 8 : 4;  // lanes per token in QK (q slice <= 128 regs)
+  static_assert(geometry_supported(G, D), "unsupported (G, D)");
+  constexpr int NB = D / 64;             // 64-dim boxes per row
+  constexpr int LPT = lpt_for(G, D);     // lanes per token in QK
   constexpr int TPP = 32 / LPT;          // tokens per QK pass
   constexpr int PASSES = kTPW / TPP;
-  constexpr int CPS = 8 / LPT;           // 16-byte chunks per lane per half-row
+  constexpr int CPS = 8 / LPT;           // 16-byte chunks per lane per box
+  constexpr int DPL = D / 32;            // PV: output dims per lane
   constexpr int PPS = kChunk / BS;       // pages per stage
+  constexpr int kStageBytes = stage_bytes(D);
+  constexpr int kVOff = NB * kHalfBytes;  // V boxes follow the K boxes in a stage
   static_assert(kChunk % BS == 0 && PPS <= 32, "stage must hold whole pages");
-  using TOut = std::conditional_t<OUT_F32, float, std::conditional_t<FP16, __half, __nv_bfloat16>>;
+  using TNat = std::conditional_t<FP16, __half, __nv_bfloat16>;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -118,7 +137,6 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int hq0 = h * G;
-  TOut* out = static_cast<TOut*>(p.out);
 
   // The producer's first block-table window depends only on the split index,
   // so its load is issued before the context length arrives.
@@ -136,8 +154,11 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
 
   if (n_splits_b == 0) {  // empty context: zero output rows
     if (split == 0) {
-      for (int i = threadIdx.x; i < G * kHeadDim; i += kThreads)
-        out[((int64_t)b * p.Hq + hq0) * kHeadDim + i] = to_out<TOut>(0.f);
+      for (int i = threadIdx.x; i < G * D; i += kThreads) {
+        const int64_t o = ((int64_t)b * p.Hq + hq0) * D + i;
+        if (p.out_f32) static_cast<float*>(p.out)[o] = 0.f;
+        else static_cast<TNat*>(p.out)[o] = to_out<TNat>(0.f);
+      }
     }
     return;
   }
@@ -159,10 +180,12 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
   __syncthreads();
 
   bool failed = false;
-  float m_run[G], l_run[G], acc[G][4];
-  const int dh = lane >> 4;          // PV: which 64-dim half
-  const int vch = (lane & 15) >> 1;  // PV: 16-byte chunk within the half
-  const int vsub = lane & 1;         // PV: which 8 bytes of the chunk
+  float m_run[G], l_run[G], acc[G][DPL];
+  // PV: this lane's dims [lane * DPL, lane * DPL + DPL): box, 16-byte chunk
+  // within the box, byte offset within the chunk
+  const int vbox = (lane * DPL) >> 6;
+  const int vch = ((lane * DPL) & 63) >> 3;
+  const int vsub = ((lane * DPL) & 7) * 2;
 
   if (warp == kNW) {
     // ------------------------------ producer ------------------------------
@@ -196,17 +219,18 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
       for (int i = 0; i < PPS; ++i) blk[i] = __shfl_sync(kFull, win_blk, (pg0 + i - win_base) & 31);
       if (lane == 0) {
         const uint32_t fb = full_bar(slot);
-        mbar_arrive_expect_tx(fb, (uint32_t)npg * BS * 4 * kRowBytes);
+        mbar_arrive_expect_tx(fb, (uint32_t)npg * BS * 2 * NB * kRowBytes);
         const uint32_t st = base_u32 + slot * kStageBytes;
 #pragma unroll
         for (int i = 0; i < PPS; ++i) {
           if (i < npg) {
             const int y = blk[i] * BS;
             const uint32_t ro = (uint32_t)(i * BS * kRowBytes);
-            tma_load_2d(st + 0 * kHalfBytes + ro, &tmap_k, h * kHeadDim, y, fb);
-            tma_load_2d(st + 1 * kHalfBytes + ro, &tmap_k, h * kHeadDim + 64, y, fb);
-            tma_load_2d(st + 2 * kHalfBytes + ro, &tmap_v, h * kHeadDim, y, fb);
-            tma_load_2d(st + 3 * kHalfBytes + ro, &tmap_v, h * kHeadDim + 64, y, fb);
+#pragma unroll
+            for (int bx = 0; bx < NB; ++bx) {
+              tma_load_2d(st + bx * kHalfBytes + ro, &tmap_k, h * D + bx * 64, y, fb);
+              tma_load_2d(st + kVOff + bx * kHalfBytes + ro, &tmap_v, h * D + bx * 64, y, fb);
+            }
           }
         }
       }
@@ -217,18 +241,17 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
     const int j = lane / LPT;  // token within a QK pass
     const int s = lane % LPT;  // segment: chunks [s*CPS, (s+1)*CPS) of each half-row
 
-    float qf[G][2][CPS][8];
+    float qf[G][NB][CPS][8];
     {
-      const uint8_t* qb = static_cast<const uint8_t*>(p.q) +
-                          (((int64_t)b * p.Hq + hq0) * kHeadDim) * 2;
+      const uint8_t* qb = static_cast<const uint8_t*>(p.q) + (((int64_t)b * p.Hq + hq0) * D) * 2;
 #pragma unroll
       for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
+        for (int hh = 0; hh < NB; ++hh)
 #pragma unroll
           for (int i = 0; i < CPS; ++i) {
             const uint4 u = __ldg(reinterpret_cast<const uint4*>(
-                qb + (g * kHeadDim + hh * 64 + (s * CPS + i) * 8) * 2));
+                qb + (g * D + hh * 64 + (s * CPS + i) * 8) * 2));
             float t[8];
             unpack8<FP16>(u, t);
 #pragma unroll
@@ -240,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
       m_run[g] = -INFINITY;
       l_run[g] = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[g][e] = 0.f;
+      for (int e = 0; e < DPL; ++e) acc[g][e] = 0.f;
     }
     float* pw = pbuf + warp * kTPW * G;
 
@@ -255,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
       const int n_w = min(kTPW, max(0, n_valid - warp * kTPW));
       if (n_w > 0) {
         const uint8_t* kst = base + slot * kStageBytes;
-        const uint8_t* vst = kst + 2 * kHalfBytes;
+        const uint8_t* vst = kst + kVOff;
         float sc[PASSES][G];
 #pragma unroll
         for (int pass = 0; pass < PASSES; ++pass) {
@@ -265,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
 #pragma unroll
           for (int g = 0; g < G; ++g) a[g] = 0.f;
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh)
+          for (int hh = 0; hh < NB; ++hh)
 #pragma unroll
             for (int i = 0; i < CPS; ++i) {
               const int phys = (s * CPS + i) ^ (row & 7);
@@ -304,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
           }
           l_run[g] = l_run[g] * alpha + ls;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) acc[g][e] *= alpha;
+          for (int e = 0; e < DPL; ++e) acc[g][e] *= alpha;
         }
         if (s == 0) {
 #pragma unroll
@@ -316,11 +339,18 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
 #pragma unroll 4
         for (int t = 0; t < n_w; ++t) {
           const int row = warp * kTPW + t;
-          const uint2 u = *reinterpret_cast<const uint2*>(vst + dh * kHalfBytes + row * kRowBytes +
-                                                          ((vch ^ (row & 7)) * 16) + vsub * 8);
-          float vf[4];
-          unpack2<FP16>(u.x, vf[0], vf[1]);
-          unpack2<FP16>(u.y, vf[2], vf[3]);
+          const uint8_t* vp = vst + vbox * kHalfBytes + row * kRowBytes +
+                              ((vch ^ (row & 7)) * 16) + vsub;
+          float vf[DPL];
+          if constexpr (DPL == 2) {
+            unpack2<FP16>(*reinterpret_cast<const uint32_t*>(vp), vf[0], vf[1]);
+          } else if constexpr (DPL == 4) {
+            const uint2 u = *reinterpret_cast<const uint2*>(vp);
+            unpack2<FP16>(u.x, vf[0], vf[1]);
+            unpack2<FP16>(u.y, vf[2], vf[3]);
+          } else {
+            unpack8<FP16>(*reinterpret_cast<const uint4*>(vp), vf);
+          }
           float pp[G];
           if constexpr (G % 4 == 0) {
 #pragma unroll
@@ -338,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
 #pragma unroll
           for (int g = 0; g < G; ++g)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[g][e] = fmaf(pp[g], vf[e], acc[g][e]);
+            for (int e = 0; e < DPL; ++e) acc[g][e] = fmaf(pp[g], vf[e], acc[g][e]);
         }
         __syncwarp();
       }
@@ -361,7 +391,9 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
   named_bar_sync(1, kNW * 32);
   float* mw = reinterpret_cast<float*>(base);  // [kNW][G]
   float* lw = mw + kNW * G;                    // [kNW][G]
-  float* aw = lw + kNW * G;                    // [kNW][G][128]
+  float* aw = lw + kNW * G;                    // [kNW][G][D]
+  static_assert(sizeof(float) * kNW * G * (D + 2) <= 2 * (size_t)stage_bytes(D),
+                "warp states must fit below the merge scratch");
   if (lane == 0) {
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -370,122 +402,138 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
     }
   }
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float4 v4 = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
-    *reinterpret_cast<float4*>(aw + (warp * G + g) * kHeadDim + dh * 64 + vch * 8 + vsub * 4) = v4;
-  }
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) aw[(warp * G + g) * D + lane * DPL + e] = acc[g][e];
   named_bar_sync(1, kNW * 32);
-  const int d = threadIdx.x;  // 0 .. 127
+  const int tid = threadIdx.x;  // 0 .. 127
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kNW; ++w) M = fmaxf(M, mw[w * G + g]);
-    float Ls = 0.f, o = 0.f;
+    float Ls = 0.f;
+    float fw[kNW];
 #pragma unroll
     for (int w = 0; w < kNW; ++w) {
       const float mwv = mw[w * G + g];
-      const float f = (mwv == -INFINITY) ? 0.f : exp2f(mwv - M);
-      Ls += f * lw[w * G + g];
-      o += f * aw[(w * G + g) * kHeadDim + d];
+      fw[w] = (mwv == -INFINITY) ? 0.f : exp2f(mwv - M);
+      Ls += fw[w] * lw[w * G + g];
     }
-    o = o / Ls;
     const int64_t row = (int64_t)b * p.Hq + hq0 + g;
-    if (n_splits_b == 1) {
-      out[row * kHeadDim + d] = to_out<TOut>(o);
-    } else {
-      const int64_t r = row * p.num_splits + split;
-      p.ws_o[r * kHeadDim + d] = o;
-      if (d == 0) p.ws_lse[r] = (M + log2f(Ls)) * kLn2;
+    for (int d = tid; d < D; d += kNW * 32) {
+      float o = 0.f;
+#pragma unroll
+      for (int w = 0; w < kNW; ++w) o += fw[w] * aw[(w * G + g) * D + d];
+      o = o / Ls;
+      if (n_splits_b == 1) {
+        if (p.out_f32) static_cast<float*>(p.out)[row * D + d] = o;
+        else static_cast<TNat*>(p.out)[row * D + d] = to_out<TNat>(o);
+      } else {
+        const int64_t r = row * p.num_splits + split;
+        p.ws_o[r * D + d] = o;
+        if (d == 0) p.ws_lse[r] = (M + log2f(Ls)) * kLn2;
+      }
     }
   }
   // the last split of this (sequence, kv head) merges all of them into `out`
-  if (n_splits_b > 1)
-    finish_split<G, TOut>(p, b, h, n_splits_b, d, reinterpret_cast<float*>(base + 2 * kStageBytes), 1);
+  if (n_splits_b > 1) {
+    float* sw = reinterpret_cast<float*>(base + 2 * kStageBytes);
+    if (p.out_f32) finish_split<G, D, float>(p, b, h, n_splits_b, tid, sw, 1);
+    else finish_split<G, D, TNat>(p, b, h, n_splits_b, tid, sw, 1);
+  }
 }
 
-template <int G, int BS, bool FP16, bool OUT_F32>
+template <int G, int D, int BS, bool FP16>
 cudaError_t launch_one(const CUtensorMap* tk, const CUtensorMap* tv, const PartialParams& p,
                        int batch, cudaStream_t stream) {
   dim3 grid(p.num_splits, p.Hkv, batch);
-  paged_partial_kernel<G, BS, FP16, OUT_F32><<<grid, kThreads, kSmemBytes, stream>>>(*tk, *tv, p);
+  paged_partial_kernel<G, D, BS, FP16><<<grid, kThreads, smem_bytes(D), stream>>>(*tk, *tv, p);
   return cudaGetLastError();
 }
 
-template <int G, int BS, bool FP16, bool OUT_F32>
+template <int G, int D, int BS, bool FP16>
 cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(paged_partial_kernel<G, BS, FP16, OUT_F32>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  return cudaFuncSetAttribute(paged_partial_kernel<G, D, BS, FP16>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(D));
 }
 
-template <int G, int BS, bool FP16>
+template <int G, int D, int BS, bool FP16>
 int occupancy_one() {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_partial_kernel<G, BS, FP16, false>,
-                                                    kThreads, kSmemBytes) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_partial_kernel<G, D, BS, FP16>,
+                                                    kThreads, smem_bytes(D)) != cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }
 
-// Dispatch over (G, block size, out dtype) for one input dtype.
-template <bool FP16>
+// Dispatch over (G, block size) for one head dim and input dtype; each
+// (D, dtype) pair is instantiated in its own translation unit.
+template <int D, bool FP16>
 struct Dispatch {
-  template <int G, int BS>
-  static cudaError_t launch_g(bool f32, const CUtensorMap* tk, const CUtensorMap* tv,
+  template <int G>
+  static cudaError_t launch_g(int BS, const CUtensorMap* tk, const CUtensorMap* tv,
                               const PartialParams& p, int batch, cudaStream_t s) {
-    return f32 ? launch_one<G, BS, FP16, true>(tk, tv, p, batch, s)
-               : launch_one<G, BS, FP16, false>(tk, tv, p, batch, s);
-  }
-  template <int BS>
-  static cudaError_t launch_bs(int G, bool f32, const CUtensorMap* tk, const CUtensorMap* tv,
-                               const PartialParams& p, int batch, cudaStream_t s) {
-    switch (G) {
-      case 1: return launch_g<1, BS>(f32, tk, tv, p, batch, s);
-      case 2: return launch_g<2, BS>(f32, tk, tv, p, batch, s);
-      case 4: return launch_g<4, BS>(f32, tk, tv, p, batch, s);
-      case 8: return launch_g<8, BS>(f32, tk, tv, p, batch, s);
-      default: return cudaErrorInvalidValue;
+    if constexpr (geometry_supported(G, D)) {
+      if (BS == 16) return launch_one<G, D, 16, FP16>(tk, tv, p, batch, s);
+      if (BS == 32) return launch_one<G, D, 32, FP16>(tk, tv, p, batch, s);
     }
-  }
-  static cudaError_t launch(int G, int BS, bool f32, const CUtensorMap* tk, const CUtensorMap* tv,
-                            const PartialParams& p, int batch, cudaStream_t s) {
-    if (BS == 16) return launch_bs<16>(G, f32, tk, tv, p, batch, s);
-    if (BS == 32) return launch_bs<32>(G, f32, tk, tv, p, batch, s);
     return cudaErrorInvalidValue;
   }
-  template <int G, int BS>
-  static cudaError_t prepare_g() {
-    cudaError_t e = prepare_one<G, BS, FP16, false>();
-    if (e != cudaSuccess) return e;
-    return prepare_one<G, BS, FP16, true>();
+  template <int G>
+  static cudaError_t prepare_g(int BS) {
+    if constexpr (geometry_supported(G, D)) {
+      if (BS == 16) return prepare_one<G, D, 16, FP16>();
+      if (BS == 32) return prepare_one<G, D, 32, FP16>();
+    }
+    return cudaErrorInvalidValue;
   }
-  template <int BS>
-  static cudaError_t prepare_bs(int G) {
+  template <int G>
+  static int occupancy_g(int BS) {
+    if constexpr (geometry_supported(G, D)) {
+      return BS == 16 ? occupancy_one<G, D, 16, FP16>() : occupancy_one<G, D, 32, FP16>();
+    }
+    return 1;
+  }
+  static cudaError_t launch(int G, int BS, const CUtensorMap* tk, const CUtensorMap* tv,
+                            const PartialParams& p, int batch, cudaStream_t s) {
     switch (G) {
-      case 1: return prepare_g<1, BS>();
-      case 2: return prepare_g<2, BS>();
-      case 4: return prepare_g<4, BS>();
-      case 8: return prepare_g<8, BS>();
+      case 1: return launch_g<1>(BS, tk, tv, p, batch, s);
+      case 2: return launch_g<2>(BS, tk, tv, p, batch, s);
+      case 3: return launch_g<3>(BS, tk, tv, p, batch, s);
+      case 4: return launch_g<4>(BS, tk, tv, p, batch, s);
+      case 5: return launch_g<5>(BS, tk, tv, p, batch, s);
+      case 6: return launch_g<6>(BS, tk, tv, p, batch, s);
+      case 7: return launch_g<7>(BS, tk, tv, p, batch, s);
+      case 8: return launch_g<8>(BS, tk, tv, p, batch, s);
       default: return cudaErrorInvalidValue;
     }
   }
   static cudaError_t prepare(int G, int BS) {
-    if (BS == 16) return prepare_bs<16>(G);
-    if (BS == 32) return prepare_bs<32>(G);
-    return cudaErrorInvalidValue;
-  }
-  template <int BS>
-  static int occupancy_bs(int G) {
     switch (G) {
-      case 1: return occupancy_one<1, BS, FP16>();
-      case 2: return occupancy_one<2, BS, FP16>();
-      case 4: return occupancy_one<4, BS, FP16>();
-      case 8: return occupancy_one<8, BS, FP16>();
-      default: return 1;
+      case 1: return prepare_g<1>(BS);
+      case 2: return prepare_g<2>(BS);
+      case 3: return prepare_g<3>(BS);
+      case 4: return prepare_g<4>(BS);
+      case 5: return prepare_g<5>(BS);
+      case 6: return prepare_g<6>(BS);
+      case 7: return prepare_g<7>(BS);
+      case 8: return prepare_g<8>(BS);
+      default: return cudaErrorInvalidValue;
     }
   }
   static int occupancy(int G, int BS) {
-    return BS == 16 ? occupancy_bs<16>(G) : occupancy_bs<32>(G);
+    switch (G) {
+      case 1: return occupancy_g<1>(BS);
+      case 2: return occupancy_g<2>(BS);
+      case 3: return occupancy_g<3>(BS);
+      case 4: return occupancy_g<4>(BS);
+      case 5: return occupancy_g<5>(BS);
+      case 6: return occupancy_g<6>(BS);
+      case 7: return occupancy_g<7>(BS);
+      case 8: return occupancy_g<8>(BS);
+      default: return 1;
+    }
   }
 };
 

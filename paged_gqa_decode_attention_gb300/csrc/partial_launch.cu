@@ -1,61 +1,114 @@
 // Host-side entry points of the partial kernels: support checks, shared-memory
-// attributes, occupancy, and dispatch over (kernel, input dtype).
+// attributes, occupancy, and dispatch over (kernel, head dim, input dtype).
 #include "partial_kernel.cuh"
+#include "partial_tc_kernel.cuh"
 
 namespace pda {
 
-cudaError_t launch_partial_bf16(int, int, bool, const CUtensorMap*, const CUtensorMap*,
-                               const PartialParams&, int, cudaStream_t);
-cudaError_t launch_partial_fp16(int, int, bool, const CUtensorMap*, const CUtensorMap*,
-                               const PartialParams&, int, cudaStream_t);
-cudaError_t launch_partial_tc_bf16(int, int, bool, const CUtensorMap*, const CUtensorMap*,
-                                  const CUtensorMap*, const PartialParams&, cudaStream_t);
-cudaError_t launch_partial_tc_fp16(int, int, bool, const CUtensorMap*, const CUtensorMap*,
-                                  const CUtensorMap*, const PartialParams&, cudaStream_t);
-cudaError_t prepare_partial_bf16(int, int);
-cudaError_t prepare_partial_fp16(int, int);
-cudaError_t prepare_partial_tc_bf16(int, int);
-cudaError_t prepare_partial_tc_fp16(int, int);
-int occupancy_partial_bf16(int, int);
-int occupancy_partial_fp16(int, int);
-int occupancy_partial_tc_bf16(int, int);
-int occupancy_partial_tc_fp16(int, int);
+#define PDA_DECLARE_CC(dt, D)                                                                  \
+  cudaError_t launch_partial_cc_##dt##_d##D(int, int, const CUtensorMap*, const CUtensorMap*,  \
+                                            const PartialParams&, int, cudaStream_t);          \
+  cudaError_t prepare_partial_cc_##dt##_d##D(int, int);                                        \
+  int occupancy_partial_cc_##dt##_d##D(int, int);
+PDA_DECLARE_CC(bf16, 64)
+PDA_DECLARE_CC(bf16, 128)
+PDA_DECLARE_CC(bf16, 256)
+PDA_DECLARE_CC(fp16, 64)
+PDA_DECLARE_CC(fp16, 128)
+PDA_DECLARE_CC(fp16, 256)
+#undef PDA_DECLARE_CC
 
-bool partial_supported(int group, int block_size, int dtype) {
-  const bool g_ok = group == 1 || group == 2 || group == 4 || group == 8;
+#define PDA_DECLARE_TC(dt, D)                                                                  \
+  cudaError_t launch_partial_tc_##dt##_d##D(int, int, const CUtensorMap*, const CUtensorMap*,  \
+                                            const CUtensorMap*, const PartialParams&,          \
+                                            cudaStream_t);                                     \
+  cudaError_t prepare_partial_tc_##dt##_d##D(int, int);                                        \
+  int occupancy_partial_tc_##dt##_d##D(int, int);
+PDA_DECLARE_TC(bf16, 64)
+PDA_DECLARE_TC(bf16, 128)
+PDA_DECLARE_TC(fp16, 64)
+PDA_DECLARE_TC(fp16, 128)
+#undef PDA_DECLARE_TC
+
+namespace {
+
+// Calls the CUDA-core function for (dtype, head dim): `f` receives the
+// matching launch, prepare and occupancy entry points.
+template <typename F>
+auto with_cc(int dtype, int head_dim, F f) {
+#define PDA_CC_CASE(dt, D)                                                             \
+  return f(launch_partial_cc_##dt##_d##D, prepare_partial_cc_##dt##_d##D,              \
+           occupancy_partial_cc_##dt##_d##D)
+  if (dtype == 1) {
+    if (head_dim == 64) PDA_CC_CASE(fp16, 64);
+    if (head_dim == 256) PDA_CC_CASE(fp16, 256);
+    PDA_CC_CASE(fp16, 128);
+  }
+  if (head_dim == 64) PDA_CC_CASE(bf16, 64);
+  if (head_dim == 256) PDA_CC_CASE(bf16, 256);
+  PDA_CC_CASE(bf16, 128);
+#undef PDA_CC_CASE
+}
+
+// Same for the tensor-core kernel (head dims 64 and 128).
+template <typename F>
+auto with_tc(int dtype, int head_dim, F f) {
+#define PDA_TC_CASE(dt, D)                                                             \
+  return f(launch_partial_tc_##dt##_d##D, prepare_partial_tc_##dt##_d##D,              \
+           occupancy_partial_tc_##dt##_d##D)
+  if (dtype == 1) {
+    if (head_dim == 64) PDA_TC_CASE(fp16, 64);
+    PDA_TC_CASE(fp16, 128);
+  }
+  if (head_dim == 64) PDA_TC_CASE(bf16, 64);
+  PDA_TC_CASE(bf16, 128);
+#undef PDA_TC_CASE
+}
+
+}  // namespace
+
+bool partial_supported(int group, int head_dim, int block_size, int dtype) {
   const bool bs_ok = block_size == 16 || block_size == 32;
-  return g_ok && bs_ok && (dtype == 0 || dtype == 1);
+  return partial::geometry_supported(group, head_dim) && bs_ok && (dtype == 0 || dtype == 1);
 }
 
-bool partial_kernel_supported(int kernel, int group) {
-  if (kernel == kPartialTensorCore) return group == 4 || group == 8;
-  return kernel == kPartialCudaCore;
+bool partial_kernel_supported(int kernel, int group, int head_dim) {
+  if (kernel == kPartialTensorCore) return tc::geometry_supported(group, head_dim);
+  return kernel == kPartialCudaCore && partial::geometry_supported(group, head_dim);
 }
 
-cudaError_t partial_prepare(int kernel, int group, int block_size, int dtype) {
+cudaError_t partial_prepare(int kernel, int group, int head_dim, int block_size, int dtype) {
   if (kernel == kPartialTensorCore)
-    return dtype == 1 ? prepare_partial_tc_fp16(group, block_size)
-                      : prepare_partial_tc_bf16(group, block_size);
-  return dtype == 1 ? prepare_partial_fp16(group, block_size)
-                    : prepare_partial_bf16(group, block_size);
+    return with_tc(dtype, head_dim, [&](auto, auto prepare, auto) {
+      return prepare(group, block_size);
+    });
+  return with_cc(dtype, head_dim, [&](auto, auto prepare, auto) {
+    return prepare(group, block_size);
+  });
 }
 
-int partial_ctas_per_sm(int kernel, int group, int block_size, int dtype) {
+int partial_ctas_per_sm(int kernel, int group, int head_dim, int block_size, int dtype) {
   if (kernel == kPartialTensorCore)
-    return dtype == 1 ? occupancy_partial_tc_fp16(group, block_size)
-                      : occupancy_partial_tc_bf16(group, block_size);
-  return dtype == 1 ? occupancy_partial_fp16(group, block_size)
-                    : occupancy_partial_bf16(group, block_size);
+    return with_tc(dtype, head_dim, [&](auto, auto, auto occupancy) {
+      return occupancy(group, block_size);
+    });
+  return with_cc(dtype, head_dim, [&](auto, auto, auto occupancy) {
+    return occupancy(group, block_size);
+  });
 }
 
-cudaError_t launch_partial(int kernel, int group, int block_size, int dtype, bool out_f32,
-                           const CUtensorMap* tk, const CUtensorMap* tv, const CUtensorMap* tq,
-                           const PartialParams& p, int batch, cudaStream_t stream) {
+cudaError_t launch_partial(int kernel, int group, int head_dim, int block_size, int dtype,
+                           bool out_f32, const CUtensorMap* tk, const CUtensorMap* tv,
+                           const CUtensorMap* tq, const PartialParams& p, int batch,
+                           cudaStream_t stream) {
+  (void)out_f32;  // both kernels read p.out_f32
   if (kernel == kPartialTensorCore)
-    return dtype == 1 ? launch_partial_tc_fp16(group, block_size, out_f32, tk, tv, tq, p, stream)
-                      : launch_partial_tc_bf16(group, block_size, out_f32, tk, tv, tq, p, stream);
-  return dtype == 1 ? launch_partial_fp16(group, block_size, out_f32, tk, tv, p, batch, stream)
-                    : launch_partial_bf16(group, block_size, out_f32, tk, tv, p, batch, stream);
+    return with_tc(dtype, head_dim, [&](auto launch, auto, auto) {
+      return launch(group, block_size, tk, tv, tq, p, stream);
+    });
+  return with_cc(dtype, head_dim, [&](auto launch, auto, auto) {
+    return launch(group, block_size, tk, tv, p, batch, stream);
+  });
 }
 
 }  // namespace pda

@@ -1,5 +1,6 @@
 // Split-K partial kernel on the 5th-generation tensor cores (tcgen05, TMEM
-// accumulators) for GQA groups of G = 4 or 8 query heads per kv head.
+// accumulators) for GQA groups of G = 3..8 query heads per kv head and head
+// dims D of 128 or 64.
 //
 // Same method and work units as the CUDA-core kernel (partial_kernel.cuh):
 // a unit is one (split, kv head, sequence), split-K with a normalised partial
@@ -14,7 +15,9 @@
 //   S^T [128 tokens x 16]  = K_chunk [128 x 128 dims] . Q^T [128 dims x 16]
 //   O^T [128 dims   x 16]  = V_chunk^T [128 dims x 128 tokens] . P^T [128 x 16]
 //
-// (rows G..15 of Q and P are zero). Both are M=128, N=16, K=128 tcgen05.mma
+// (rows G..15 of Q and P are zero; at D = 64 the QK^T contraction is 64
+// deep and the upper 64 dims of every V slot are zero, so O^T rows 64..127
+// come out zero). Both are M=128, N=16 tcgen05.mma
 // (kind::f16, fp32 accumulate in TMEM) issued by one thread; the K and V
 // tiles are consumed straight from the TMA-written, 128-byte-swizzled stage:
 // K as a K-major A operand, V as an MN-major A operand. The probabilities P
@@ -194,15 +197,18 @@ struct Cursor {
   }
 };
 
-template <int G, int BS, bool FP16, bool OUT_F32>
+template <int G, int D, int BS, bool FP16>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_partial_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v,
                             const __grid_constant__ CUtensorMap tmap_q, const PartialParams p) {
-  static_assert(G == 4 || G == 8, "tensor-core path packs 4 or 8 query heads");
+  static_assert(G >= 3 && G <= 8, "tensor-core path packs 3..8 query heads");
+  static_assert(D == 64 || D == 128, "head dim 64 or 128");
+  constexpr int NB = D / 64;    // 64-dim boxes per row
   constexpr int PPS = kT / BS;  // pages per stage
+  constexpr int GL = G <= 4 ? 4 : 8;  // TMEM columns read per row
   static_assert(kT % BS == 0 && PPS <= 32, "stage must hold whole pages");
-  using TOut = std::conditional_t<OUT_F32, float, std::conditional_t<FP16, __half, __nv_bfloat16>>;
+  using TNat = std::conditional_t<FP16, __half, __nv_bfloat16>;
   using H = Half16<FP16>;
 
   extern __shared__ uint8_t smem_raw[];
@@ -334,9 +340,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp < 4) {
     // Q operands (rows G..15 stay zero; the TMA box fills rows 0..G-1) and
-    // both P operand pairs start zeroed.
+    // both P operand pairs start zeroed; at D = 64 the upper (dims 64..127)
+    // half of every V slot is zero for the whole kernel.
     for (int i = threadIdx.x; i < (2 * kOpBytes + 4 * kOpBytes) / 16; i += 128)
       *reinterpret_cast<uint4*>(base + kOffQ + i * 16) = make_uint4(0, 0, 0, 0);
+    if constexpr (D == 64) {
+      for (int s2 = 0; s2 < kStages; ++s2)
+        for (int i = threadIdx.x; i < kHalf / 16; i += 128)
+          *reinterpret_cast<uint4*>(base + kOffV + s2 * kSlotBytes + kHalf + i * 16) =
+              make_uint4(0, 0, 0, 0);
+    }
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -382,11 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (lane == 0) {
             const uint32_t fb = q_full(qb);
-            mbar_arrive_expect_tx(fb, (uint32_t)G * 2 * kRowBytes);
+            mbar_arrive_expect_tx(fb, (uint32_t)G * NB * kRowBytes);
             const uint32_t qdst = base_u32 + kOffQ + qb * kOpBytes;
             const int row = U.b * p.Hq + U.h * G;
-            tma_load_2d(qdst, &tmap_q, 0, row, fb);
-            tma_load_2d(qdst + kOpHalf, &tmap_q, 64, row, fb);
+#pragma unroll
+            for (int bx = 0; bx < NB; ++bx) tma_load_2d(qdst + bx * kOpHalf, &tmap_q, bx * 64, row, fb);
           }
           __syncwarp();
         }
@@ -412,15 +425,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < PPS; ++i) blk[i] = __shfl_sync(kFull, win_blk, (pg0 + i - win_base) & 31);
       if (lane == 0) {
         const uint32_t fb = full_bar(r, slot);
-        mbar_arrive_expect_tx(fb, (uint32_t)npg * BS * 2 * kRowBytes);
+        mbar_arrive_expect_tx(fb, (uint32_t)npg * BS * NB * kRowBytes);
         const uint32_t st = base_u32 + (r == 0 ? kOffK : kOffV) + slot * kSlotBytes;
 #pragma unroll
         for (int i = 0; i < PPS; ++i) {
           if (i < npg) {
             const int y = blk[i] * BS;
             const uint32_t ro = (uint32_t)(i * BS * kRowBytes);
-            tma_load_2d(st + ro, map, U.h * kHeadDim, y, fb);
-            tma_load_2d(st + kHalf + ro, map, U.h * kHeadDim + 64, y, fb);
+#pragma unroll
+            for (int bx = 0; bx < NB; ++bx)
+              tma_load_2d(st + bx * kHalf + ro, map, U.h * D + bx * 64, y, fb);
           }
         }
       }
@@ -445,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t kb = base_u32 + kOffK + slot * kSlotBytes;
         const uint32_t qa = base_u32 + kOffQ + qb * kOpBytes;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < D / 16; ++k) {
           const uint64_t a = sdesc_sw128(kb + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
           const uint64_t bq = sdesc_sw128(qa + (k >> 2) * kOpHalf + (k & 3) * 32, 16, 1024);
           mma_f16_ss(tS(c & 1), a, bq, idesc_qk, k > 0 ? 1u : 0u);
@@ -513,7 +527,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------ softmax -------------------------------
     const int t = threadIdx.x;  // token row of S; output dim of O
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    TOut* out = static_cast<TOut*>(p.out);
     float* red = reinterpret_cast<float*>(base + kOffRed);
     float* lred = reinterpret_cast<float*>(base + kOffLred);
     float m_run[G], l_th[G], acc[G], alpha_prev[G];
@@ -522,8 +535,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = !failed && mbar_wait(o_full(c & 1), (c >> 1) & 1);
       if (!__all_sync(kFull, ok)) failed = true;
       tc_fence_after();
-      float o[G];
-      if constexpr (G == 4) {
+      float o[GL];
+      if constexpr (GL == 4) {
         tmem_ld_x4(tO(c & 1) + lane_base, o);
       } else {
         tmem_ld_x8(tO(c & 1) + lane_base, o);
@@ -554,8 +567,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Unit U = load_unit<BS>(p, u);
       const int hq0 = U.h * G;
       if (U.zero_fill) {
-        for (int i = t; i < G * kHeadDim; i += 128)
-          out[((int64_t)U.b * p.Hq + hq0) * kHeadDim + i] = to_out<TOut>(0.f);
+        for (int i = t; i < G * D; i += 128) {
+          const int64_t o = ((int64_t)U.b * p.Hq + hq0) * D + i;
+          if (p.out_f32) static_cast<float*>(p.out)[o] = 0.f;
+          else static_cast<TNat*>(p.out)[o] = to_out<TNat>(0.f);
+        }
       }
       if (U.n_chunks == 0) continue;
 #pragma unroll
@@ -570,8 +586,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = !failed && mbar_wait(s_full(c & 1), (c >> 1) & 1);
         if (!__all_sync(kFull, ok)) failed = true;
         tc_fence_after();
-        float s[G];
-        if constexpr (G == 4) {
+        float s[GL];
+        if constexpr (GL == 4) {
           tmem_ld_x4(tS(c & 1) + lane_base, s);
         } else {
           tmem_ld_x8(tS(c & 1) + lane_base, s);
@@ -616,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t >= n_valid) {
           uint8_t* vrow = base + kOffV + slot * kSlotBytes + t * kRowBytes;
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh)
+          for (int hh = 0; hh < NB; ++hh)
 #pragma unroll
             for (int q = 0; q < 8; ++q)
               *reinterpret_cast<uint4*>(vrow + hh * kHalf + q * 16) = make_uint4(0, 0, 0, 0);
@@ -679,7 +695,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------ epilogue ------------------------------
     const int t = threadIdx.x - kWarpEpi0 * 32;  // output dim
     volatile int* flag = reinterpret_cast<volatile int*>(base + kOffEpiFlag);
-    TOut* out = static_cast<TOut*>(p.out);
     for (int je = 0;; ++je) {
       const int es = je & 1;
       const bool ok = !failed && mbar_wait(ep_full(es), (je >> 1) & 1);
@@ -697,22 +712,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (u < 0) break;
       const Unit U = load_unit<BS>(p, u);
       const int hq0 = U.h * G;
+      if (t < D) {
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float Ls = st[8 * kHeadDim + 8 + g];
-        const float o = st[g * kHeadDim + t] / Ls;
-        const int64_t row = (int64_t)U.b * p.Hq + hq0 + g;
-        if (U.n_splits_b == 1) {
-          out[row * kHeadDim + t] = to_out<TOut>(o);
-        } else {
-          const int64_t r = row * p.num_splits + U.split;
-          p.ws_o[r * kHeadDim + t] = o;
-          if (t == 0) p.ws_lse[r] = (st[8 * kHeadDim + g] + log2f(Ls)) * kLn2;
+        for (int g = 0; g < G; ++g) {
+          const float Ls = st[8 * kHeadDim + 8 + g];
+          const float o = st[g * kHeadDim + t] / Ls;
+          const int64_t row = (int64_t)U.b * p.Hq + hq0 + g;
+          if (U.n_splits_b == 1) {
+            if (p.out_f32) static_cast<float*>(p.out)[row * D + t] = o;
+            else static_cast<TNat*>(p.out)[row * D + t] = to_out<TNat>(o);
+          } else {
+            const int64_t r = row * p.num_splits + U.split;
+            p.ws_o[r * D + t] = o;
+            if (t == 0) p.ws_lse[r] = (st[8 * kHeadDim + g] + log2f(Ls)) * kLn2;
+          }
         }
       }
       named_bar_sync(2, 128);  // the state is read; the slot serves as merge scratch
       // the last split of this (sequence, kv head) merges all of them into `out`
-      if (U.n_splits_b > 1) finish_split<G, TOut>(p, U.b, U.h, U.n_splits_b, t, st, 2);
+      if (U.n_splits_b > 1) {
+        if (p.out_f32) finish_split<G, D, float>(p, U.b, U.h, U.n_splits_b, t, st, 2);
+        else finish_split<G, D, TNat>(p, U.b, U.h, U.n_splits_b, t, st, 2);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(ep_empty(es));
     }
@@ -727,62 +748,88 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int G, int BS, bool FP16, bool OUT_F32>
+template <int G, int D, int BS, bool FP16>
 cudaError_t launch_one(const CUtensorMap* tk, const CUtensorMap* tv, const CUtensorMap* tq,
                        const PartialParams& p, cudaStream_t stream) {
   const int ctas = p.num_units < p.max_ctas ? p.num_units : p.max_ctas;
   if (ctas <= 0) return cudaSuccess;
-  paged_partial_tc_kernel<G, BS, FP16, OUT_F32><<<ctas, kThreads, kSmemBytes, stream>>>(
-      *tk, *tv, *tq, p);
+  paged_partial_tc_kernel<G, D, BS, FP16><<<ctas, kThreads, kSmemBytes, stream>>>(*tk, *tv, *tq, p);
   return cudaGetLastError();
 }
 
-template <int G, int BS, bool FP16, bool OUT_F32>
+template <int G, int D, int BS, bool FP16>
 cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(paged_partial_tc_kernel<G, BS, FP16, OUT_F32>,
+  return cudaFuncSetAttribute(paged_partial_tc_kernel<G, D, BS, FP16>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
 }
 
-template <int G, int BS, bool FP16>
+template <int G, int D, int BS, bool FP16>
 int occupancy_one() {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-          &n, paged_partial_tc_kernel<G, BS, FP16, false>, kThreads, kSmemBytes) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_partial_tc_kernel<G, D, BS, FP16>,
+                                                    kThreads, kSmemBytes) != cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }
 
-template <bool FP16>
+__host__ __device__ constexpr bool geometry_supported(int G, int D) {
+  return G >= 3 && G <= 8 && (D == 64 || D == 128);
+}
+
+// Dispatch over (G, block size) for one head dim and input dtype; each
+// (D, dtype) pair is instantiated in its own translation unit.
+template <int D, bool FP16>
 struct Dispatch {
-  template <int G, int BS>
-  static cudaError_t launch_g(bool f32, const CUtensorMap* tk, const CUtensorMap* tv,
+  template <int G>
+  static cudaError_t launch_g(int BS, const CUtensorMap* tk, const CUtensorMap* tv,
                               const CUtensorMap* tq, const PartialParams& p, cudaStream_t s) {
-    return f32 ? launch_one<G, BS, FP16, true>(tk, tv, tq, p, s)
-               : launch_one<G, BS, FP16, false>(tk, tv, tq, p, s);
-  }
-  static cudaError_t launch(int G, int BS, bool f32, const CUtensorMap* tk, const CUtensorMap* tv,
-                            const CUtensorMap* tq, const PartialParams& p, cudaStream_t s) {
-    if (G == 4 && BS == 16) return launch_g<4, 16>(f32, tk, tv, tq, p, s);
-    if (G == 4 && BS == 32) return launch_g<4, 32>(f32, tk, tv, tq, p, s);
-    if (G == 8 && BS == 16) return launch_g<8, 16>(f32, tk, tv, tq, p, s);
-    if (G == 8 && BS == 32) return launch_g<8, 32>(f32, tk, tv, tq, p, s);
+    if (BS == 16) return launch_one<G, D, 16, FP16>(tk, tv, tq, p, s);
+    if (BS == 32) return launch_one<G, D, 32, FP16>(tk, tv, tq, p, s);
     return cudaErrorInvalidValue;
   }
-  template <int G, int BS>
-  static cudaError_t prepare_g() {
-    cudaError_t e = prepare_one<G, BS, FP16, false>();
-    return e != cudaSuccess ? e : prepare_one<G, BS, FP16, true>();
+  template <int G>
+  static cudaError_t prepare_g(int BS) {
+    if (BS == 16) return prepare_one<G, D, 16, FP16>();
+    if (BS == 32) return prepare_one<G, D, 32, FP16>();
+    return cudaErrorInvalidValue;
+  }
+  template <int G>
+  static int occupancy_g(int BS) {
+    return BS == 16 ? occupancy_one<G, D, 16, FP16>() : occupancy_one<G, D, 32, FP16>();
+  }
+  static cudaError_t launch(int G, int BS, const CUtensorMap* tk, const CUtensorMap* tv,
+                            const CUtensorMap* tq, const PartialParams& p, cudaStream_t s) {
+    switch (G) {
+      case 3: return launch_g<3>(BS, tk, tv, tq, p, s);
+      case 4: return launch_g<4>(BS, tk, tv, tq, p, s);
+      case 5: return launch_g<5>(BS, tk, tv, tq, p, s);
+      case 6: return launch_g<6>(BS, tk, tv, tq, p, s);
+      case 7: return launch_g<7>(BS, tk, tv, tq, p, s);
+      case 8: return launch_g<8>(BS, tk, tv, tq, p, s);
+      default: return cudaErrorInvalidValue;
+    }
   }
   static cudaError_t prepare(int G, int BS) {
-    if (G == 4 && BS == 16) return prepare_g<4, 16>();
-    if (G == 4 && BS == 32) return prepare_g<4, 32>();
-    if (G == 8 && BS == 16) return prepare_g<8, 16>();
-    if (G == 8 && BS == 32) return prepare_g<8, 32>();
-    return cudaErrorInvalidValue;
+    switch (G) {
+      case 3: return prepare_g<3>(BS);
+      case 4: return prepare_g<4>(BS);
+      case 5: return prepare_g<5>(BS);
+      case 6: return prepare_g<6>(BS);
+      case 7: return prepare_g<7>(BS);
+      case 8: return prepare_g<8>(BS);
+      default: return cudaErrorInvalidValue;
+    }
   }
   static int occupancy(int G, int BS) {
-    if (G == 4) return BS == 16 ? occupancy_one<4, 16, FP16>() : occupancy_one<4, 32, FP16>();
-    return BS == 16 ? occupancy_one<8, 16, FP16>() : occupancy_one<8, 32, FP16>();
+    switch (G) {
+      case 3: return occupancy_g<3>(BS);
+      case 4: return occupancy_g<4>(BS);
+      case 5: return occupancy_g<5>(BS);
+      case 6: return occupancy_g<6>(BS);
+      case 7: return occupancy_g<7>(BS);
+      case 8: return occupancy_g<8>(BS);
+      default: return 1;
+    }
   }
 };
 

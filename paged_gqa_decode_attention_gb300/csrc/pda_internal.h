@@ -8,7 +8,7 @@
 
 namespace pda {
 
-constexpr int kHeadDim = 128;
+constexpr int kHeadDim = 128;  // the tensor-core kernel's head dim
 constexpr int kMaxSplits = 64;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
@@ -42,6 +42,7 @@ struct PartialParams {
   float qscale;     // scale * log2(e): logits are kept in base-2 units
   int num_units;    // S * Hkv * B work units (persistent tensor-core kernel)
   int max_ctas;     // resident CTAs the persistent kernel launches at most
+  int out_f32;      // out is fp32 (else the input dtype)
 };
 
 struct MergeParams {
@@ -60,34 +61,39 @@ struct MergeParams {
 
 // The two implementations of the split-K partial kernel.
 enum PartialKernel : int {
-  kPartialCudaCore = 0,    // QK/PV on the FMA pipe (partial_kernel.cuh), G in {1, 2, 4, 8}
-  kPartialTensorCore = 1,  // QK/PV with tcgen05 MMAs into TMEM (partial_tc_kernel.cuh), G in {4, 8}
+  kPartialCudaCore = 0,    // QK/PV on the FMA pipe (partial_kernel.cuh): G 1..8 at D 64 and
+                           // 128, G 1..4 at D 256
+  kPartialTensorCore = 1,  // QK/PV with tcgen05 MMAs into TMEM (partial_tc_kernel.cuh):
+                           // G 3..8, D 64 and 128
 };
 
 // The kernel a geometry uses unless overridden (PDA_PARTIAL_KERNEL): the
 // faster one as measured on GB300. With G = 4 or 8 query heads per kv head
 // the packed tile is a real contraction and the tensor-core kernel wins (B=4,
 // L=32768 at G=4: 0.0974 vs 0.1000 ms; the 128-sequence serving mix at G=8:
-// 0.114 vs 0.255 ms); below that the CUDA-core kernel is used.
-constexpr int default_partial_kernel(int group) {
-  return (group == 4 || group == 8) ? kPartialTensorCore : kPartialCudaCore;
+// 0.114 vs 0.255 ms); otherwise the CUDA-core kernel is used.
+constexpr int default_partial_kernel(int group, int head_dim) {
+  return (group >= 3 && group <= 8 && (head_dim == 64 || head_dim == 128)) ? kPartialTensorCore
+                                                                           : kPartialCudaCore;
 }
 
 // CTAs per SM each kernel is built for (its launch bounds and shared memory);
 // the planner's figure when no GPU is queried.
-constexpr int partial_ctas_per_sm_hint(int kernel, int group) {
-  return kernel == kPartialTensorCore ? 1 : (group >= 8 ? 1 : 2);
+constexpr int partial_ctas_per_sm_hint(int kernel, int group, int head_dim) {
+  return kernel == kPartialTensorCore ? 1
+                                      : ((group * head_dim > 512 || head_dim >= 256) ? 1 : 2);
 }
 
-bool partial_supported(int group, int block_size, int dtype);
-bool partial_kernel_supported(int kernel, int group);
-cudaError_t partial_prepare(int kernel, int group, int block_size, int dtype);
-int partial_ctas_per_sm(int kernel, int group, int block_size, int dtype);
+bool partial_supported(int group, int head_dim, int block_size, int dtype);
+bool partial_kernel_supported(int kernel, int group, int head_dim);
+cudaError_t partial_prepare(int kernel, int group, int head_dim, int block_size, int dtype);
+int partial_ctas_per_sm(int kernel, int group, int head_dim, int block_size, int dtype);
 
-// tmap_q (a [B * Hq, 128] view of q, boxes of 64 dims x G rows) is read by
-// the tensor-core kernel only.
-cudaError_t launch_partial(int kernel, int group, int block_size, int dtype, bool out_f32,
-                           const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+// tmap_q (a [B * Hq, D] view of q, boxes of 64 dims x G rows) is read by
+// the tensor-core kernel only; both kernels take the output type from
+// p.out_f32 (`out_f32` must agree with it).
+cudaError_t launch_partial(int kernel, int group, int head_dim, int block_size, int dtype,
+                           bool out_f32, const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
                            const CUtensorMap* tmap_q, const PartialParams& p, int batch,
                            cudaStream_t stream);
 

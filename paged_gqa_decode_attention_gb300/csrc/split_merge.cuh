@@ -33,13 +33,13 @@ __device__ __forceinline__ TOut merge_to_out(float x) {
 }
 
 // Called by 128 threads (tid 0..127) after each has written its part of this
-// split's partial. `sw` is shared scratch
-// of at least G * 64 + 1 floats, `bar_id` a named barrier over exactly these
-// 128 threads.
-template <int G, typename TOut>
+// split's partial (head dim D). `sw` is shared scratch of at least G * 64 + 1
+// floats, `bar_id` a named barrier over exactly these 128 threads.
+template <int G, int D, typename TOut>
 __device__ __forceinline__ void finish_split(const PartialParams& p, int b, int h, int n_splits_b,
                                              int tid, float* sw, int bar_id) {
-  static_assert(kHeadDim == 128, "32 float4 columns per head");
+  static_assert(D % 4 == 0, "float4 columns");
+  constexpr int kCols = D / 4;
   __threadfence();
   named_bar_sync(bar_id, 128);
   int* flag = reinterpret_cast<int*>(sw + G * 64);
@@ -71,19 +71,19 @@ __device__ __forceinline__ void finish_split(const PartialParams& p, int b, int 
     for (int s = 0; s < n_splits_b; ++s) w[s] *= inv;
   }
   named_bar_sync(bar_id, 128);
-  // thread -> (head g, 4 consecutive dims): G * 32 such pairs over 128 threads,
-  // float4 loads, 8 splits in flight per step
+  // thread -> (head g, 4 consecutive dims): G * D / 4 such pairs over 128
+  // threads, float4 loads, 8 splits in flight per step
   TOut* out = static_cast<TOut*>(p.out);
-  for (int pair = tid; pair < G * 32; pair += 128) {
-    const int g = pair >> 5, d4 = (pair & 31) * 4;
-    const float4* o = reinterpret_cast<const float4*>(p.ws_o + ((row0 + g) * p.num_splits) * kHeadDim + d4);
+  for (int pair = tid; pair < G * kCols; pair += 128) {
+    const int g = pair / kCols, d4 = (pair - g * kCols) * 4;
+    const float4* o = reinterpret_cast<const float4*>(p.ws_o + ((row0 + g) * p.num_splits) * D + d4);
     const float* w = sw + g * 64;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     int s = 0;
     for (; s + 8 <= n_splits_b; s += 8) {
       float4 v[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = __ldcg(o + (s + k) * (kHeadDim / 4));
+      for (int k = 0; k < 8; ++k) v[k] = __ldcg(o + (s + k) * kCols);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         acc.x = fmaf(w[s + k], v[k].x, acc.x);
@@ -93,13 +93,13 @@ __device__ __forceinline__ void finish_split(const PartialParams& p, int b, int 
       }
     }
     for (; s < n_splits_b; ++s) {
-      const float4 v = __ldcg(o + s * (kHeadDim / 4));
+      const float4 v = __ldcg(o + s * kCols);
       acc.x = fmaf(w[s], v.x, acc.x);
       acc.y = fmaf(w[s], v.y, acc.y);
       acc.z = fmaf(w[s], v.z, acc.z);
       acc.w = fmaf(w[s], v.w, acc.w);
     }
-    TOut* dst = out + (row0 + g) * kHeadDim + d4;
+    TOut* dst = out + (row0 + g) * D + d4;
     dst[0] = merge_to_out<TOut>(acc.x);
     dst[1] = merge_to_out<TOut>(acc.y);
     dst[2] = merge_to_out<TOut>(acc.z);

@@ -49,8 +49,8 @@ def test_library_needs_no_driver_to_load(lib):
 @pytest.mark.parametrize("field,value,status", [
     ("num_q_heads", 0, pda.PDA_EINVAL),
     ("num_q_heads", 30, pda.PDA_EINVAL),        # not a multiple of Hkv = 8
-    ("num_q_heads", 8 * 3, pda.PDA_EUNSUPPORTED),  # group size 3
-    ("head_dim", 64, pda.PDA_EUNSUPPORTED),
+    ("num_q_heads", 8 * 9, pda.PDA_EUNSUPPORTED),  # group size 9
+    ("head_dim", 96, pda.PDA_EUNSUPPORTED),
     ("head_dim", 0, pda.PDA_EINVAL),
     ("block_size", 8, pda.PDA_EUNSUPPORTED),
     ("dtype", 7, pda.PDA_EINVAL),
@@ -67,6 +67,24 @@ def test_create_rejects_bad_config_before_cuda(lib, field, value, status):
     assert lib.paged_decode_attn_create(ctypes.byref(cfg), ctypes.byref(h)) == status
     assert h.value is None
     assert lib.paged_decode_attn_last_error()
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,ok", [(14, 2, 64, True), (28, 4, 128, True), (40, 8, 128, True),
+                                         (24, 8, 128, True), (8, 1, 256, False), (16, 8, 256, True),
+                                         (32, 8, 256, True), (12, 2, 256, False), (8, 8, 64, True),
+                                         (4, 1, 64, True)])
+def test_create_geometries_before_cuda(lib, Hq, Hkv, D, ok):
+    """Group sizes 1..8 at head dims 64 and 128, 1..4 at 256: accepted by the
+    config checks (creation then needs a GPU), others are unsupported."""
+    cfg = pda.make_config(Hq, Hkv, D, 16)
+    h = ctypes.c_void_p()
+    st = lib.paged_decode_attn_create(ctypes.byref(cfg), ctypes.byref(h))
+    if ok:
+        assert st != pda.PDA_EUNSUPPORTED and st != pda.PDA_EINVAL, lib.paged_decode_attn_last_error()
+        if st == pda.PDA_OK:
+            lib.paged_decode_attn_destroy(h)
+    else:
+        assert st == pda.PDA_EUNSUPPORTED
 
 
 def test_null_arguments(lib):

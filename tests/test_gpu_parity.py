@@ -234,3 +234,53 @@ def test_both_partial_kernels_peaky_and_fp16(kernel, monkeypatch):
     check(workloads.serving_mix(seed=1, batch=24))
     err = check(workloads.mid_ragged(seed=5), out_dtype=torch.float32)
     assert err < 1e-4, err
+
+
+# Other GQA geometries: the Qwen2.5 layouts (14/2 and 28/4 heads: G = 7), odd
+# group sizes 3, 5, 6, MQA (Hkv = 1), head dims 64 and 256.
+GEOMETRIES = [(14, 2, 64), (28, 4, 128), (12, 2, 128), (40, 8, 128), (24, 8, 128), (7, 1, 128),
+              (16, 8, 256), (32, 8, 256), (6, 2, 256), (4, 1, 256), (8, 8, 64), (4, 1, 64),
+              (32, 4, 64), (10, 2, 64)]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", GEOMETRIES)
+@pytest.mark.parametrize("bs", [16, 32])
+def test_geometries_exact(Hq, Hkv, D, bs):
+    lens = [1, bs + 1, 700, 3000, 64, 129]
+    wl = workloads.custom(seed=Hq * 7 + Hkv + D + bs, B=len(lens), Hq=Hq, Hkv=Hkv, D=D,
+                          block_size=bs, lens=lens, num_blocks=600)
+    for splits in (0, 1, 5, 64):
+        check(wl, num_splits=splits)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(14, 2, 64), (16, 8, 256), (28, 4, 128)])
+def test_geometries_fp16_and_fp32_out(Hq, Hkv, D):
+    lens = [900, 17, 2048, 300]
+    wl = workloads.custom(seed=D + Hq, B=4, Hq=Hq, Hkv=Hkv, D=D, block_size=16, lens=lens,
+                          dtype="fp16", num_blocks=300)
+    check(wl)
+    wl = workloads.custom(seed=D + Hq + 1, B=4, Hq=Hq, Hkv=Hkv, D=D, block_size=32, lens=lens)
+    err = check(wl, out_dtype=torch.float32)
+    assert err < 1e-4, err
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("Hq,Hkv,D", [(14, 2, 64), (28, 4, 128), (24, 8, 128), (40, 8, 128),
+                                      (12, 2, 64), (32, 4, 64), (16, 4, 64), (9, 3, 64)])
+def test_both_kernels_on_padded_groups(kernel, Hq, Hkv, D, monkeypatch):
+    """Group sizes 3..8 at head dims 64 and 128 on both implementations (the
+    tensor-core kernel pads the group to 4 or 8 MMA columns, and at D = 64
+    runs a 64-deep QK^T with a zero upper half of V)."""
+    monkeypatch.setenv("PDA_PARTIAL_KERNEL", kernel)
+    lens = [3000, 1, 129, 700, 128, 17]
+    for bs in (16, 32):
+        wl = workloads.custom(seed=Hq + Hkv + D + bs, B=len(lens), Hq=Hq, Hkv=Hkv, D=D,
+                              block_size=bs, lens=lens, num_blocks=700)
+        for splits in (0, 1, 5, 64):
+            check(wl, num_splits=splits)
+    wl = workloads.custom(seed=D, B=3, Hq=Hq, Hkv=Hkv, D=D, block_size=16, lens=[500, 64, 2000],
+                          dtype="fp16")
+    check(wl)
+    err = check(workloads.custom(seed=D + 1, B=3, Hq=Hq, Hkv=Hkv, D=D, block_size=16,
+                                 lens=[500, 64, 2000]), out_dtype=torch.float32)
+    assert err < 1e-4, err
