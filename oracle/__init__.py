@@ -29,6 +29,7 @@ import numpy as np
 
 BF16 = 0
 FP16 = 1
+FP8_E4M3 = 2  # K/V cache elements only
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "paged_attn_oracle.c")
@@ -77,6 +78,11 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_round_array.restype = None
     lib.oracle_decode_array.argtypes = [P, i64, i32, P]
     lib.oracle_decode_array.restype = None
+    lib.oracle_paged_decode_kv.argtypes = [P, P, P, i32, P, P, P, P, i32, i32, i32, i32, i32,
+                                           i32, i64, i32, f64, P, i64, P, i32]
+    lib.oracle_paged_decode_kv.restype = i32
+    lib.oracle_decode_e4m3_array.argtypes = [P, i64, P]
+    lib.oracle_decode_e4m3_array.restype = None
     lib.oracle_rope_kv_write.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                          i64, i32, P, P, P]
     lib.oracle_rope_kv_write.restype = i32
@@ -241,3 +247,49 @@ def rope_kv_write(q, k, v, positions, slot_mapping, cos_sin, rot_dim: int, neox:
                                   dtype, _ptr(q_out), _ptr(kc), _ptr(vc))
     _check(st, "rope_kv_write")
     return q_out, kc, vc
+
+
+def decode_e4m3(bits, lib=None) -> np.ndarray:
+    """Exact float64 values of FP8 E4M3 storage bytes (numpy uint8)."""
+    lib = lib or load()
+    b = np.ascontiguousarray(bits, dtype=np.uint8)
+    out = np.zeros(b.shape, dtype=np.float64)
+    lib.oracle_decode_e4m3_array(_ptr(b), b.size, _ptr(out))
+    return out
+
+
+def paged_decode_kv(q, k_cache, v_cache, block_table, context_lens, q_dtype: int, kv_dtype: int,
+                    scale: float, k_scale=None, v_scale=None, rows=None,
+                    threads: int | None = None, lib=None) -> np.ndarray:
+    """Decode attention with K/V of any element type and per-kv-head
+    dequantisation scales: k_t = k_scale[h] * k_cache[...], likewise v.
+
+    q: uint16 [B, Hq, D]; k_cache/v_cache: uint8 (FP8_E4M3) or uint16
+    [num_blocks, bs, Hkv, D]; k_scale/v_scale: [Hkv] or None (1). Returns
+    float64 [B, Hq, D], or [len(rows), D] for the (b, hq) pairs in rows."""
+    lib = lib or load()
+    q = _as_bits(q)
+    kdt = np.uint8 if kv_dtype == FP8_E4M3 else np.uint16
+    k = np.ascontiguousarray(k_cache)
+    v = np.ascontiguousarray(v_cache)
+    if k.dtype != kdt or v.dtype != kdt:
+        raise TypeError(f"caches must be {np.dtype(kdt).name} storage for kv_dtype {kv_dtype}")
+    bt, cl = _as_i32(block_table), _as_i32(context_lens)
+    B, Hq, D = q.shape
+    nb, bs, Hkv, _ = k.shape
+    ks = None if k_scale is None else np.ascontiguousarray(k_scale, dtype=np.float64).reshape(Hkv)
+    vs = None if v_scale is None else np.ascontiguousarray(v_scale, dtype=np.float64).reshape(Hkv)
+    if rows is None:
+        out = np.zeros((B, Hq, D), dtype=np.float64)
+        rp, nr = None, 0
+    else:
+        rows = _as_i32(rows).reshape(-1, 2)
+        out = np.zeros((rows.shape[0], D), dtype=np.float64)
+        rp, nr = _ptr(rows), rows.shape[0]
+    st = lib.oracle_paged_decode_kv(_ptr(q), _ptr(k), _ptr(v), kv_dtype,
+                                    None if ks is None else _ptr(ks),
+                                    None if vs is None else _ptr(vs), _ptr(bt), _ptr(cl), B, Hq,
+                                    Hkv, D, bs, bt.shape[1], nb, q_dtype, float(scale), rp, nr,
+                                    _ptr(out), threads or default_threads())
+    _check(st, "paged_decode_kv")
+    return out

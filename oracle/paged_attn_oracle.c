@@ -42,6 +42,7 @@
 
 #define ORACLE_BF16 0
 #define ORACLE_FP16 1
+#define ORACLE_FP8_E4M3 2 /* K/V cache elements only */
 
 #define ORACLE_OK 0
 #define ORACLE_EINVAL (-1)
@@ -161,19 +162,38 @@ void oracle_decode_array(const uint16_t* bits, int64_t n, int dtype, double* out
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_to_f64(bits[i], dtype);
 }
 
+/* FP8 E4M3 (the "fn" variant of the OCP 8-bit formats): 1 sign, 4 exponent
+ * (bias 7), 3 fraction bits; exponent 0 holds subnormals m * 2^-9; there is
+ * no infinity, and S.1111.111 is NaN. Largest finite value 448. */
+double oracle_e4m3_to_f64(uint8_t bits) {
+  int sign = bits >> 7, e = (bits >> 3) & 15, m = bits & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) v = ldexp((double)m, -9);
+  else v = ldexp(8.0 + m, e - 7 - 3);
+  return sign ? -v : v;
+}
+
+void oracle_decode_e4m3_array(const uint8_t* bits, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_to_f64(bits[i]);
+}
+
 /* ---------------------------------------------------------------------------
  * Problem description shared by the entry points below.
  * ------------------------------------------------------------------------- */
 typedef struct {
   const uint16_t* q;       /* [B, Hq, D] */
-  const uint16_t* k_cache; /* [num_blocks, bs, Hkv, D] */
-  const uint16_t* v_cache; /* [num_blocks, bs, Hkv, D] */
+  const void* k_cache;     /* [num_blocks, bs, Hkv, D], elements of kv_dtype */
+  const void* v_cache;     /* [num_blocks, bs, Hkv, D] */
   const int32_t* block_table; /* [B, max_blocks] */
   const int32_t* context_lens; /* [B] */
   int B, Hq, Hkv, D, bs, max_blocks;
   int64_t num_blocks;
-  int dtype;
+  int dtype;               /* of q */
   double scale;
+  int kv_dtype;            /* BF16, FP16 or FP8_E4M3 */
+  const double* k_scale;   /* [Hkv] dequantisation scales, NULL = 1 */
+  const double* v_scale;
 } problem;
 
 static int check_problem(const problem* p) {
@@ -183,6 +203,8 @@ static int check_problem(const problem* p) {
     return ORACLE_EINVAL;
   if (p->Hq % p->Hkv != 0) return ORACLE_EINVAL;
   if (p->dtype != ORACLE_BF16 && p->dtype != ORACLE_FP16) return ORACLE_EINVAL;
+  if (p->kv_dtype != ORACLE_BF16 && p->kv_dtype != ORACLE_FP16 && p->kv_dtype != ORACLE_FP8_E4M3)
+    return ORACLE_EINVAL;
   for (int b = 0; b < p->B; ++b) {
     int L = p->context_lens[b];
     if (L < 0 || (int64_t)L > (int64_t)p->max_blocks * p->bs) return ORACLE_ERANGE;
@@ -195,19 +217,30 @@ static int check_problem(const problem* p) {
   return ORACLE_OK;
 }
 
-/* Address of element (token t of sequence b, kv head h, dim 0) in a cache. */
-static const uint16_t* cache_row(const problem* p, const uint16_t* cache, int b, int t, int h) {
+/* Element index of (token t of sequence b, kv head h, dim 0) in a cache. */
+static int64_t cache_row(const problem* p, int b, int t, int h) {
   int32_t blk = p->block_table[(int64_t)b * p->max_blocks + t / p->bs];
   int off = t % p->bs;
-  return cache + (((int64_t)blk * p->bs + off) * p->Hkv + h) * p->D;
+  return (((int64_t)blk * p->bs + off) * p->Hkv + h) * p->D;
+}
+
+/* Element i of a K or V cache of kv head h: its exact value times the head's
+ * dequantisation scale (no scale: the value itself). */
+static double kv_value(const problem* p, const void* cache, const double* head_scale, int h,
+                       int64_t i) {
+  double x = p->kv_dtype == ORACLE_FP8_E4M3
+                 ? oracle_e4m3_to_f64(((const uint8_t*)cache)[i])
+                 : oracle_to_f64(((const uint16_t*)cache)[i], p->kv_dtype);
+  return head_scale ? x * head_scale[h] : x;
 }
 
 /* Scaled logit s_t = scale * q[b,hq,:] . k_t */
 static double logit(const problem* p, int b, int hq, int h, int t) {
   const uint16_t* qrow = p->q + ((int64_t)b * p->Hq + hq) * p->D;
-  const uint16_t* krow = cache_row(p, p->k_cache, b, t, h);
+  const int64_t krow = cache_row(p, b, t, h);
   double dot = 0.0;
-  for (int d = 0; d < p->D; ++d) dot += oracle_to_f64(qrow[d], p->dtype) * oracle_to_f64(krow[d], p->dtype);
+  for (int d = 0; d < p->D; ++d)
+    dot += oracle_to_f64(qrow[d], p->dtype) * kv_value(p, p->k_cache, p->k_scale, h, krow + d);
   return p->scale * dot;
 }
 
@@ -234,8 +267,8 @@ static void attend_range(const problem* p, int b, int hq, int t0, int t1, double
   for (int t = t0; t < t1; ++t) {
     double w = exp(s[t - t0] - m);
     l += w;
-    const uint16_t* vrow = cache_row(p, p->v_cache, b, t, h);
-    for (int d = 0; d < p->D; ++d) o[d] += w * oracle_to_f64(vrow[d], p->dtype);
+    const int64_t vrow = cache_row(p, b, t, h);
+    for (int d = 0; d < p->D; ++d) o[d] += w * kv_value(p, p->v_cache, p->v_scale, h, vrow + d);
   }
   for (int d = 0; d < p->D; ++d) o[d] /= l;
   *m_out = m;
@@ -321,7 +354,7 @@ int oracle_paged_decode(const uint16_t* q, const uint16_t* k_cache, const uint16
                         int Hkv, int D, int block_size, int max_blocks, int64_t num_blocks,
                         int dtype, double scale, double* out, int num_threads) {
   problem p = {q, k_cache, v_cache, block_table, context_lens, B, Hq, Hkv, D,
-               block_size, max_blocks, num_blocks, dtype, scale};
+               block_size, max_blocks, num_blocks, dtype, scale, dtype, NULL, NULL};
   int st = check_problem(&p);
   if (st != ORACLE_OK) return st;
   if (!out) return ORACLE_EINVAL;
@@ -335,10 +368,35 @@ int oracle_paged_decode_rows(const uint16_t* q, const uint16_t* k_cache, const u
                              int64_t num_blocks, int dtype, double scale, const int32_t* rows,
                              int64_t n_rows, double* out_rows, int num_threads) {
   problem p = {q, k_cache, v_cache, block_table, context_lens, B, Hq, Hkv, D,
-               block_size, max_blocks, num_blocks, dtype, scale};
+               block_size, max_blocks, num_blocks, dtype, scale, dtype, NULL, NULL};
   int st = check_problem(&p);
   if (st != ORACLE_OK) return st;
   if (!rows || !out_rows || n_rows < 0) return ORACLE_EINVAL;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[2 * r] < 0 || rows[2 * r] >= B || rows[2 * r + 1] < 0 || rows[2 * r + 1] >= Hq)
+      return ORACLE_EINVAL;
+  return run_parallel(&p, rows, n_rows, out_rows, num_threads);
+}
+
+/* Any K/V element type with per-kv-head dequantisation scales (FP8 KV
+ * cache; the pages leave the scale granularity open, so per kv head is the
+ * reading and a per-tensor scale is the case of equal entries):
+ *   k_t[d] = k_scale[h] * decode(k_cache element), likewise v_t with v_scale.
+ * q is bf16/fp16 (q_dtype). rows: n_rows pairs (b, hq), or NULL for all
+ * B * Hq rows in order (n_rows ignored). out_rows[rows, D]. */
+int oracle_paged_decode_kv(const uint16_t* q, const void* k_cache, const void* v_cache,
+                           int kv_dtype, const double* k_scale, const double* v_scale,
+                           const int32_t* block_table, const int32_t* context_lens, int B,
+                           int Hq, int Hkv, int D, int block_size, int max_blocks,
+                           int64_t num_blocks, int q_dtype, double scale, const int32_t* rows,
+                           int64_t n_rows, double* out_rows, int num_threads) {
+  problem p = {q, k_cache, v_cache, block_table, context_lens, B, Hq, Hkv, D,
+               block_size, max_blocks, num_blocks, q_dtype, scale, kv_dtype, k_scale, v_scale};
+  int st = check_problem(&p);
+  if (st != ORACLE_OK) return st;
+  if (!out_rows) return ORACLE_EINVAL;
+  if (!rows) return run_parallel(&p, NULL, (int64_t)B * Hq, out_rows, num_threads);
+  if (n_rows < 0) return ORACLE_EINVAL;
   for (int64_t r = 0; r < n_rows; ++r)
     if (rows[2 * r] < 0 || rows[2 * r] >= B || rows[2 * r + 1] < 0 || rows[2 * r + 1] >= Hq)
       return ORACLE_EINVAL;
@@ -358,7 +416,7 @@ int oracle_split_partials(const uint16_t* q, const uint16_t* k_cache, const uint
                           int dtype, double scale, int chunk_pages, int num_splits,
                           double* lse, double* o) {
   problem p = {q, k_cache, v_cache, block_table, context_lens, B, Hq, Hkv, D,
-               block_size, max_blocks, num_blocks, dtype, scale};
+               block_size, max_blocks, num_blocks, dtype, scale, dtype, NULL, NULL};
   int st = check_problem(&p);
   if (st != ORACLE_OK) return st;
   if (chunk_pages < 1 || num_splits < 1 || !lse || !o) return ORACLE_EINVAL;

@@ -446,6 +446,62 @@ def pin_rope_exact_turns(lib):
         np.testing.assert_array_equal(yk[:, a], -xk[:, b])
 
 
+# ---------------------------------------------------------------------------
+# FP8 E4M3 KV cache with per-kv-head scales
+# ---------------------------------------------------------------------------
+
+def pin_e4m3_decode(lib):
+    """All 256 E4M3 codes decode to torch's float8_e4m3fn values (NaN codes
+    to NaN), including subnormals (m * 2^-9) and the largest finite 448."""
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.decode_e4m3(codes, lib=lib)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2
+    np.testing.assert_array_equal(got[~nan], ref[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+
+
+def pin_fp8_kv_equals_dequantised_bf16(lib):
+    """FP8 K/V with per-kv-head scales equals the bf16 oracle on the same
+    values converted to bf16 (exact: E4M3 values are bf16 values), with each
+    head's K scale folded into the logit scale and its V scale into the
+    output: rows of kv head h of out_fp8 = v_scale[h] * out_bf16(scale *
+    k_scale[h]). Also a per-tensor case (all scales equal)."""
+    rng = np.random.default_rng(17)
+    B, Hq, Hkv, D, bs = 3, 8, 4, 16, 4
+    G = Hq // Hkv
+    lens = [1, 9, 23]
+    nb = 20
+    kf = (torch.randn(nb, bs, Hkv, D, generator=torch.Generator().manual_seed(3)) * 3)
+    vf = (torch.randn(nb, bs, Hkv, D, generator=torch.Generator().manual_seed(4)) * 3)
+    k8 = kf.to(torch.float8_e4m3fn)
+    v8 = vf.to(torch.float8_e4m3fn)
+    kb = _bits(k8.to(torch.float32).to(torch.bfloat16))
+    vb = _bits(v8.to(torch.float32).to(torch.bfloat16))
+    k8n, v8n = k8.view(torch.uint8).numpy(), v8.view(torch.uint8).numpy()
+    q = _bits(torch.randn(B, Hq, D, generator=torch.Generator().manual_seed(5)).bfloat16())
+    table = rng.permutation(nb)[: B * 6].reshape(B, 6).astype(np.int32)
+    cl = np.array(lens, dtype=np.int32)
+    scale = D ** -0.5
+    for ks, vs in ((np.array([0.5, 2.0, 0.125, 3.0]), np.array([4.0, 0.25, 1.5, 0.75])),
+                   (np.full(Hkv, 0.3), np.full(Hkv, 1.7))):
+        got = oracle.paged_decode_kv(q, k8n, v8n, table, cl, BF16, oracle.FP8_E4M3, scale, ks, vs,
+                                     lib=lib)
+        for h in range(Hkv):
+            ref = oracle.paged_decode(q, kb, vb, table, cl, BF16, scale * ks[h], lib=lib)
+            rows = slice(h * G, (h + 1) * G)
+            np.testing.assert_allclose(got[:, rows], vs[h] * ref[:, rows], rtol=1e-12,
+                                       atol=1e-12)
+    # no scales = unit scales; bf16 caches through the same entry = paged_decode
+    got = oracle.paged_decode_kv(q, k8n, v8n, table, cl, BF16, oracle.FP8_E4M3, scale, lib=lib)
+    ref = oracle.paged_decode(q, kb, vb, table, cl, BF16, scale, lib=lib)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    got = oracle.paged_decode_kv(q, kb, vb, table, cl, BF16, BF16, scale, lib=lib)
+    np.testing.assert_array_equal(got, ref)
+
+
 ALL_PINS = [pin_brute_force, pin_closed_forms, pin_block_table_invariance, pin_gqa_reductions,
             pin_split_merge, pin_merge_special_cases, pin_dtype_conversions,
-            pin_rope_complex_form, pin_rope_exact_turns]
+            pin_rope_complex_form, pin_rope_exact_turns, pin_e4m3_decode,
+            pin_fp8_kv_equals_dequantised_bf16]

@@ -31,7 +31,7 @@ MUTANTS = {
     "softmax_sign": ("double w = exp(s[t - t0] - m);", "double w = exp(m - s[t - t0]);"),
     "no_max_shift": ("double w = exp(s[t - t0] - m);", "double w = exp(s[t - t0]);"),
     "no_normalisation": ("for (int d = 0; d < p->D; ++d) o[d] /= l;", "(void)l;"),
-    "v_reads_k": ("cache_row(p, p->v_cache, b, t, h)", "cache_row(p, p->k_cache, b, t, h)"),
+    "v_reads_k": ("kv_value(p, p->v_cache, p->v_scale", "kv_value(p, p->k_cache, p->v_scale"),
     "off_by_one_context": ("attend_range(p, b, hq, 0, p->context_lens[b],",
                            "attend_range(p, b, hq, 0, p->context_lens[b] - (p->context_lens[b] > 1),"),
     "split_lse_drops_log": ("lse[idx] = (l > 0.0) ? m + log(l) : -INFINITY;",
@@ -41,6 +41,11 @@ MUTANTS = {
     "bf16_exponent_bias": ("exp - 127 - 7", "exp - 127 - 8"),
     "fp16_subnormal_scale": ("ldexp((double)frac, -14 - 10)", "ldexp((double)frac, -15 - 10)"),
     "rne_ties_away": ("r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;", "r = fl + 1.0;"),
+    "e4m3_bias": ("else v = ldexp(8.0 + m, e - 7 - 3);", "else v = ldexp(8.0 + m, e - 8 - 3);"),
+    "e4m3_subnormal": ("if (e == 0) v = ldexp((double)m, -9);", "if (e == 0) v = ldexp((double)m, -10);"),
+    "kv_scale_wrong_head": ("return head_scale ? x * head_scale[h] : x;",
+                            "return head_scale ? x * head_scale[(h + 1) % p->Hkv] : x;"),
+    "k_uses_v_scale": ("kv_value(p, p->k_cache, p->k_scale", "kv_value(p, p->k_cache, p->v_scale"),
     "rope_second_sign": ("double yb = xb * c + xa * s;", "double yb = xb * c - xa * s;"),
     "rope_first_sign": ("double ya = xa * c - xb * s;", "double ya = xa * c + xb * s;"),
     "rope_neox_pairing": ("int b = neox ? j + half : 2 * j + 1;",
