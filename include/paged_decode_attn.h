@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define PDA_ABI_VERSION 1
+#define PDA_ABI_VERSION 2
 
 typedef enum {
   PDA_OK = 0,
@@ -75,17 +75,25 @@ typedef enum {
   PDA_F32 = 2 /* output only: fp32 out for accuracy checks */
 } pda_dtype;
 
-/* Fixed at create time. */
+/* Fixed at create time. Supported geometries: G = Hq / Hkv from 1 to 8 at
+ * head_dim 64 or 128, 1 to 4 at head_dim 256; with kv_fp8, any G up to 8 at
+ * head_dim 128 and dtype PDA_BF16. */
 typedef struct {
   int num_q_heads;        /* Hq; a multiple of num_kv_heads */
-  int num_kv_heads;       /* Hkv; G = Hq / Hkv must be 1, 2, 4 or 8 */
-  int head_dim;           /* D; 128 */
+  int num_kv_heads;       /* Hkv */
+  int head_dim;           /* D; 64, 128 or 256 */
   int block_size;         /* tokens per page; 16 or 32 */
-  int dtype;              /* pda_dtype of q, k_cache, v_cache: PDA_BF16 or PDA_FP16 */
+  int dtype;              /* pda_dtype of q and out (and of the caches unless kv_fp8):
+                             PDA_BF16 or PDA_FP16 */
   int max_batch;          /* largest batch a run may pass (1 .. 65535) */
   int max_blocks_per_seq; /* largest max_blocks a run may pass */
   int max_splits;         /* largest split count (1 .. 64); sizes the workspace */
   int device;             /* CUDA device ordinal the handle and its launches use */
+  int kv_fp8;             /* 0: k_cache/v_cache hold dtype values; 1: they hold FP8 E4M3
+                             bytes (OCP "e4m3fn": bias 7, no infinities, max 448) that
+                             paged_decode_attn_run_scaled dequantises with per-kv-head
+                             scales (landing page, "Next boundaries": FP8 KV-cache
+                             compression) */
 } pda_config;
 
 typedef struct pda_handle_s* pda_handle;
@@ -141,6 +149,20 @@ int paged_decode_attn_run_ex(pda_handle handle, const void* q, const void* k_cac
                              const int32_t* context_lens, int batch, int max_blocks,
                              int64_t num_blocks, float scale, void* out, void* stream,
                              int num_splits, int max_context_len_hint, int out_dtype);
+
+/* As paged_decode_attn_run_ex, with K/V dequantisation scales:
+ *   k_t = k_scale[h] * k_cache[...],  v_t = v_scale[h] * v_cache[...]
+ * for kv head h (scale_per_head = 1: arrays of Hkv fp32 values; 0: one fp32
+ * value each, a per-tensor scale). Device pointers; NULL means 1. Any cache
+ * type may be scaled; FP8 caches (cfg->kv_fp8) are 1-byte elements with the
+ * same [num_blocks, block_size, Hkv, D] layout. */
+int paged_decode_attn_run_scaled(pda_handle handle, const void* q, const void* k_cache,
+                                 const void* v_cache, const int32_t* block_table,
+                                 const int32_t* context_lens, int batch, int max_blocks,
+                                 int64_t num_blocks, float scale, const float* k_scale,
+                                 const float* v_scale, int scale_per_head, void* out,
+                                 void* stream, int num_splits, int max_context_len_hint,
+                                 int out_dtype);
 
 /* The split plan the heuristic picks (host only, no CUDA call): for a
  * problem of `batch` sequences, `max_blocks` table columns and an optional

@@ -17,7 +17,7 @@ import torch
 PDA_OK, PDA_EINVAL, PDA_EUNSUPPORTED, PDA_ENOMEM, PDA_ECUDA, PDA_EALIAS, PDA_EDEVICE = (
     0, -1, -2, -3, -4, -5, -6)
 PDA_BF16, PDA_FP16, PDA_F32 = 0, 1, 2
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 _STATUS_NAMES = {0: "PDA_OK", -1: "PDA_EINVAL", -2: "PDA_EUNSUPPORTED", -3: "PDA_ENOMEM",
                  -4: "PDA_ECUDA", -5: "PDA_EALIAS", -6: "PDA_EDEVICE"}
@@ -34,6 +34,7 @@ EXPORTS = [
     "paged_decode_attn_destroy",
     "paged_decode_attn_run",
     "paged_decode_attn_run_ex",
+    "paged_decode_attn_run_scaled",
     "paged_decode_attn_plan",
     "paged_decode_attn_merge",
     "paged_decode_attn_validate",
@@ -54,7 +55,7 @@ class Config(ctypes.Structure):
                 ("head_dim", ctypes.c_int), ("block_size", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("max_batch", ctypes.c_int),
                 ("max_blocks_per_seq", ctypes.c_int), ("max_splits", ctypes.c_int),
-                ("device", ctypes.c_int)]
+                ("device", ctypes.c_int), ("kv_fp8", ctypes.c_int)]
 
 
 _lib = None
@@ -85,6 +86,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.paged_decode_attn_run.restype = I
         lib.paged_decode_attn_run_ex.argtypes = [P, P, P, P, P, P, I, I, I64, F, P, P, I, I, I]
         lib.paged_decode_attn_run_ex.restype = I
+        lib.paged_decode_attn_run_scaled.argtypes = [P, P, P, P, P, P, I, I, I64, F, P, P, I, P,
+                                                     P, I, I, I]
+        lib.paged_decode_attn_run_scaled.restype = I
         lib.paged_decode_attn_plan.argtypes = [ctypes.POINTER(Config), I, I, I, I,
                                                ctypes.POINTER(I), ctypes.POINTER(I)]
         lib.paged_decode_attn_plan.restype = I
@@ -132,9 +136,9 @@ def _dev_ptr(t: torch.Tensor, name: str, dtype=None) -> int:
 
 def make_config(num_q_heads: int, num_kv_heads: int, head_dim: int = 128, block_size: int = 16,
                 dtype=torch.bfloat16, max_batch: int = 256, max_blocks_per_seq: int = 4096,
-                max_splits: int = 64, device: int = 0) -> Config:
+                max_splits: int = 64, device: int = 0, kv_fp8: bool = False) -> Config:
     return Config(num_q_heads, num_kv_heads, head_dim, block_size, _DT[dtype], max_batch,
-                  max_blocks_per_seq, max_splits, device)
+                  max_blocks_per_seq, max_splits, device, int(bool(kv_fp8)))
 
 
 def plan(config: Config, num_sms: int, batch: int, max_blocks: int,
@@ -153,7 +157,8 @@ class PagedDecodeAttention:
 
     def __init__(self, num_q_heads: int, num_kv_heads: int, head_dim: int = 128,
                  block_size: int = 16, dtype=torch.bfloat16, max_batch: int = 256,
-                 max_blocks_per_seq: int = 4096, max_splits: int = 64, device=None):
+                 max_blocks_per_seq: int = 4096, max_splits: int = 64, device=None,
+                 kv_fp8: bool = False):
         self.lib = load_library()
         if device is None:
             device = torch.cuda.current_device()
@@ -161,8 +166,10 @@ class PagedDecodeAttention:
             device = device.index if device.index is not None else torch.cuda.current_device()
         self.device = int(device)
         self.dtype = dtype
+        self.kv_fp8 = bool(kv_fp8)
         self.config = make_config(num_q_heads, num_kv_heads, head_dim, block_size, dtype,
-                                  max_batch, max_blocks_per_seq, max_splits, self.device)
+                                  max_batch, max_blocks_per_seq, max_splits, self.device,
+                                  self.kv_fp8)
         h = ctypes.c_void_p(None)
         _check(self.lib, self.lib.paged_decode_attn_create(ctypes.byref(self.config),
                                                            ctypes.byref(h)))
@@ -187,9 +194,11 @@ class PagedDecodeAttention:
 
     def run(self, q, k_cache, v_cache, block_table, context_lens, scale: float | None = None,
             out=None, num_splits: int = 0, max_context_len_hint: int = 0, out_dtype=None,
-            stream=None):
+            stream=None, k_scale=None, v_scale=None):
         """out[B, Hq, D] = paged decode attention; asynchronous on ``stream``
-        (default: torch's current stream)."""
+        (default: torch's current stream). With FP8 caches (kv_fp8), k_cache
+        and v_cache are torch.float8_e4m3fn (or uint8) tensors; k_scale and
+        v_scale are fp32 device tensors of Hkv (per kv head) or 1 values."""
         c = self.config
         B = q.shape[0]
         if scale is None:
@@ -198,15 +207,33 @@ class PagedDecodeAttention:
             out_dtype = self.dtype
         if out is None:
             out = torch.empty((B, c.num_q_heads, c.head_dim), dtype=out_dtype, device=q.device)
+        if self.kv_fp8:
+            for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+                if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+                    raise ValueError(f"{name} must be float8_e4m3fn or uint8 for an FP8 cache")
+            kp, vp = _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache")
+        else:
+            kp = _dev_ptr(k_cache, "k_cache", self.dtype)
+            vp = _dev_ptr(v_cache, "v_cache", self.dtype)
+        per_head = 0
+        for t in (k_scale, v_scale):
+            if t is not None:
+                if t.numel() not in (1, c.num_kv_heads):
+                    raise ValueError("k_scale / v_scale must hold 1 or Hkv values")
+                per_head = int(t.numel() == c.num_kv_heads and c.num_kv_heads > 1)
+        if (k_scale is not None and v_scale is not None and
+                k_scale.numel() != v_scale.numel()):
+            raise ValueError("k_scale and v_scale must have the same size")
         args = (self.handle,
-                _dev_ptr(q, "q", self.dtype), _dev_ptr(k_cache, "k_cache", self.dtype),
-                _dev_ptr(v_cache, "v_cache", self.dtype),
+                _dev_ptr(q, "q", self.dtype), kp, vp,
                 _dev_ptr(block_table, "block_table", torch.int32),
                 _dev_ptr(context_lens, "context_lens", torch.int32),
                 B, block_table.shape[1], k_cache.shape[0], float(scale),
-                _dev_ptr(out, "out", out_dtype), _stream_ptr(stream),
+                _dev_ptr(k_scale, "k_scale", torch.float32) if k_scale is not None else None,
+                _dev_ptr(v_scale, "v_scale", torch.float32) if v_scale is not None else None,
+                per_head, _dev_ptr(out, "out", out_dtype), _stream_ptr(stream),
                 int(num_splits), int(max_context_len_hint), _DT[out_dtype])
-        _check(self.lib, self.lib.paged_decode_attn_run_ex(*args))
+        _check(self.lib, self.lib.paged_decode_attn_run_scaled(*args))
         return out
 
     def run_raw(self, q_ptr: int, k_ptr: int, v_ptr: int, table_ptr: int, lens_ptr: int,

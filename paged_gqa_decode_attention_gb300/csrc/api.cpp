@@ -64,9 +64,14 @@ int check_config(const pda_config* c) {
   if (c->max_splits < 1 || c->max_splits > pda::kMaxSplits)
     return fail(PDA_EINVAL, "max_splits must be in [1, 64]");
   if (c->device < 0) return fail(PDA_EINVAL, "device must be >= 0");
+  if (c->kv_fp8 != 0 && c->kv_fp8 != 1) return fail(PDA_EINVAL, "kv_fp8 must be 0 or 1");
   if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256)
     return fail(PDA_EUNSUPPORTED, "head_dim must be 64, 128 or 256");
-  if (!pda::partial_supported(G, c->head_dim, c->block_size, c->dtype))
+  if (c->kv_fp8 && !pda::partial_supported(G, c->head_dim, c->block_size, c->dtype, true))
+    return fail(PDA_EUNSUPPORTED,
+                "FP8 K/V caches need head_dim 128, group size 1..8, dtype PDA_BF16 and "
+                "block_size 16 or 32");
+  if (!pda::partial_supported(G, c->head_dim, c->block_size, c->dtype, c->kv_fp8 != 0))
     return fail(PDA_EUNSUPPORTED,
                 "unsupported geometry: group size must be 1..8 (1..4 at head_dim 256) and "
                 "block_size 16 or 32");
@@ -120,16 +125,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // A [num_blocks * block_size, Hkv * D] view of a cache, loaded as boxes of
-// 64 dims x block_size rows with 128-byte swizzle.
+// 128 bytes (64 16-bit dims or 128 fp8 dims) x block_size rows with 128-byte
+// swizzle.
 int encode_cache_map(CUtensorMap* m, const void* base, int Hkv, int D, int bs,
-                     int64_t num_blocks) {
+                     int64_t num_blocks, bool fp8 = false) {
   auto fn = tensor_map_encoder();
   if (!fn) return fail(PDA_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const int esz = fp8 ? 1 : 2;
   cuuint64_t dims[2] = {(cuuint64_t)Hkv * D, (cuuint64_t)num_blocks * bs};
-  cuuint64_t strides[1] = {(cuuint64_t)Hkv * D * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)bs};
+  cuuint64_t strides[1] = {(cuuint64_t)Hkv * D * esz};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / esz), (cuuint32_t)bs};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides,
+  CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+                  const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
@@ -224,14 +232,17 @@ int paged_decode_attn_create(const pda_config* cfg, pda_handle* out_handle) {
   // The partial kernel: PDA_PARTIAL_KERNEL=tensor_core (groups of 4 or 8
   // query heads) or cuda_core overrides the default; read here, once per
   // handle (A/B measurements and tests).
-  h->kernel = pda::default_partial_kernel(h->group, cfg->head_dim);
+  const bool kv8 = cfg->kv_fp8 != 0;
+  h->kernel = pda::default_partial_kernel(h->group, cfg->head_dim, kv8);
   if (const char* env = std::getenv("PDA_PARTIAL_KERNEL")) {
-    if (std::strcmp(env, "cuda_core") == 0) h->kernel = pda::kPartialCudaCore;
+    if (std::strcmp(env, "cuda_core") == 0 &&
+        pda::partial_kernel_supported(pda::kPartialCudaCore, h->group, cfg->head_dim, kv8))
+      h->kernel = pda::kPartialCudaCore;
     else if (std::strcmp(env, "tensor_core") == 0 &&
-             pda::partial_kernel_supported(pda::kPartialTensorCore, h->group, cfg->head_dim))
+             pda::partial_kernel_supported(pda::kPartialTensorCore, h->group, cfg->head_dim, kv8))
       h->kernel = pda::kPartialTensorCore;
   }
-  e = pda::partial_prepare(h->kernel, h->group, cfg->head_dim, cfg->block_size, cfg->dtype);
+  e = pda::partial_prepare(h->kernel, h->group, cfg->head_dim, cfg->block_size, cfg->dtype, kv8);
   if (e != cudaSuccess) {
     delete h;
     return cuda_fail("cudaFuncSetAttribute", e);
@@ -239,7 +250,8 @@ int paged_decode_attn_create(const pda_config* cfg, pda_handle* out_handle) {
   // Plan with the residency the kernel is built for, so paged_decode_attn_plan
   // (no GPU) and run agree; fall back to the measured figure if it is lower.
   const int occ =
-      pda::partial_ctas_per_sm(h->kernel, h->group, cfg->head_dim, cfg->block_size, cfg->dtype);
+      pda::partial_ctas_per_sm(h->kernel, h->group, cfg->head_dim, cfg->block_size, cfg->dtype,
+                               kv8);
   const int hint = pda::partial_ctas_per_sm_hint(h->kernel, h->group, cfg->head_dim);
   h->ctas_per_sm = occ < hint ? occ : hint;
   const size_t rows = (size_t)cfg->max_batch * cfg->num_q_heads * cfg->max_splits;
@@ -289,7 +301,7 @@ int paged_decode_attn_plan(const pda_config* cfg, int num_sms, int batch, int ma
     return fail(PDA_EINVAL, "max_blocks out of range");
   if (max_context_len_hint < 0) return fail(PDA_EINVAL, "max_context_len_hint < 0");
   const int G = cfg->num_q_heads / cfg->num_kv_heads;
-  const int kernel = pda::default_partial_kernel(G, cfg->head_dim);
+  const int kernel = pda::default_partial_kernel(G, cfg->head_dim, cfg->kv_fp8 != 0);
   plan_splits(*cfg, num_sms, pda::partial_ctas_per_sm_hint(kernel, G, cfg->head_dim), batch,
               max_blocks, max_context_len_hint, 0, num_splits, chunk_pages);
   return PDA_OK;
@@ -300,6 +312,18 @@ int paged_decode_attn_run_ex(pda_handle h, const void* q, const void* k_cache,
                              const int32_t* context_lens, int batch, int max_blocks,
                              int64_t num_blocks, float scale, void* out, void* stream,
                              int num_splits, int max_context_len_hint, int out_dtype) {
+  return paged_decode_attn_run_scaled(h, q, k_cache, v_cache, block_table, context_lens, batch,
+                                      max_blocks, num_blocks, scale, nullptr, nullptr, 0, out,
+                                      stream, num_splits, max_context_len_hint, out_dtype);
+}
+
+int paged_decode_attn_run_scaled(pda_handle h, const void* q, const void* k_cache,
+                                 const void* v_cache, const int32_t* block_table,
+                                 const int32_t* context_lens, int batch, int max_blocks,
+                                 int64_t num_blocks, float scale, const float* k_scale,
+                                 const float* v_scale, int scale_per_head, void* out,
+                                 void* stream, int num_splits, int max_context_len_hint,
+                                 int out_dtype) {
   if (!h) return fail(PDA_EINVAL, "handle is NULL");
   const pda_config& c = h->cfg;
   if (batch < 0 || batch > c.max_batch) return fail(PDA_EINVAL, "batch out of [0, max_batch]");
@@ -322,15 +346,24 @@ int paged_decode_attn_run_ex(pda_handle h, const void* q, const void* k_cache,
   if ((reinterpret_cast<uintptr_t>(block_table) | reinterpret_cast<uintptr_t>(context_lens)) & 3u)
     return fail(PDA_EINVAL, "block_table and context_lens must be 4-byte aligned");
 
+  if (scale_per_head != 0 && scale_per_head != 1)
+    return fail(PDA_EINVAL, "scale_per_head must be 0 or 1");
+  if ((reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) & 3u)
+    return fail(PDA_EINVAL, "k_scale and v_scale must be 4-byte aligned");
   const size_t esz = 2;
+  const size_t kv_esz = c.kv_fp8 ? 1 : 2;
   const size_t out_esz = out_dtype == PDA_F32 ? 4 : 2;
   const size_t n_q = (size_t)batch * c.num_q_heads * c.head_dim;
-  const size_t cache_bytes = (size_t)num_blocks * c.block_size * c.num_kv_heads * c.head_dim * esz;
+  const size_t cache_bytes =
+      (size_t)num_blocks * c.block_size * c.num_kv_heads * c.head_dim * kv_esz;
+  const size_t scale_bytes = (scale_per_head ? (size_t)c.num_kv_heads : 1) * 4;
   const size_t out_bytes = n_q * out_esz;
   if (overlaps(out, out_bytes, q, n_q * esz) || overlaps(out, out_bytes, k_cache, cache_bytes) ||
       overlaps(out, out_bytes, v_cache, cache_bytes) ||
       overlaps(out, out_bytes, block_table, (size_t)batch * max_blocks * 4) ||
-      overlaps(out, out_bytes, context_lens, (size_t)batch * 4))
+      overlaps(out, out_bytes, context_lens, (size_t)batch * 4) ||
+      overlaps(out, out_bytes, k_scale, k_scale ? scale_bytes : 0) ||
+      overlaps(out, out_bytes, v_scale, v_scale ? scale_bytes : 0))
     return fail(PDA_EALIAS, "out overlaps an input");
 
   DeviceGuard guard(c.device);
@@ -338,10 +371,10 @@ int paged_decode_attn_run_ex(pda_handle h, const void* q, const void* k_cache,
 
   if (h->tm_k != k_cache || h->tm_v != v_cache || h->tm_nb != num_blocks) {
     int st = encode_cache_map(&h->tmap_k, k_cache, c.num_kv_heads, c.head_dim, c.block_size,
-                              num_blocks);
+                              num_blocks, c.kv_fp8 != 0);
     if (st == PDA_OK)
       st = encode_cache_map(&h->tmap_v, v_cache, c.num_kv_heads, c.head_dim, c.block_size,
-                            num_blocks);
+                            num_blocks, c.kv_fp8 != 0);
     if (st != PDA_OK) {
       h->tm_k = h->tm_v = nullptr;
       h->tm_nb = -1;
@@ -384,10 +417,13 @@ int paged_decode_attn_run_ex(pda_handle h, const void* q, const void* k_cache,
   p.num_units = (int)units;
   p.max_ctas = h->num_sms * h->ctas_per_sm;
   p.out_f32 = out_dtype == PDA_F32;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.scale_per_head = scale_per_head;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = pda::launch_partial(h->kernel, h->group, c.head_dim, c.block_size, c.dtype,
-                                      out_dtype == PDA_F32, &h->tmap_k, &h->tmap_v, &tmap_q, p,
-                                      batch, s);
+                                      c.kv_fp8 != 0, &h->tmap_k, &h->tmap_v, &tmap_q, p, batch,
+                                      s);
   if (e != cudaSuccess) return cuda_fail("partial kernel launch", e);
   return PDA_OK;
 }

@@ -121,7 +121,7 @@ int setup_device(int dev, int group, int head_dim, int bs, int dtype, void** scr
   const auto key = std::make_tuple(dev, group * 1024 + head_dim, bs, dtype);
   if (!g_prepared.count(key)) {
     cudaError_t e = pda::partial_prepare(pda::default_partial_kernel(group, head_dim), group,
-                                         head_dim, bs, dtype);
+                                         head_dim, bs, dtype, false);
     if (e != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", e);
     g_prepared.insert(key);
   }
@@ -255,6 +255,9 @@ extern "C" int paged_decode_attn_run_noalloc(const void* q, const void* k_cache,
   p.num_units = (int)units;
   p.max_ctas = num_sms * pda::partial_ctas_per_sm_hint(kernel, group, head_dim);
   p.out_f32 = 0;
+  p.k_scale = nullptr;
+  p.v_scale = nullptr;
+  p.scale_per_head = 0;
   e = pda::launch_partial(kernel, group, head_dim, block_size, dtype, false, &tk, &tv, &tq, p,
                           batch, s);
   if (e != cudaSuccess) return cuda_fail("partial kernel launch", e);

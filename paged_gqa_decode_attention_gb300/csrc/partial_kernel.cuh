@@ -243,6 +243,8 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
 
     float qf[G][NB][CPS][8];
     {
+      // logit scale: softmax scale (base 2) x the kv head's K dequantisation scale
+      const float qsc = p.qscale * (p.k_scale ? __ldg(p.k_scale + (p.scale_per_head ? h : 0)) : 1.f);
       const uint8_t* qb = static_cast<const uint8_t*>(p.q) + (((int64_t)b * p.Hq + hq0) * D) * 2;
 #pragma unroll
       for (int g = 0; g < G; ++g)
@@ -255,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
             float t[8];
             unpack8<FP16>(u, t);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) qf[g][hh][i][e] = t[e] * p.qscale;
+            for (int e = 0; e < 8; ++e) qf[g][hh][i][e] = t[e] * qsc;
           }
     }
 #pragma unroll
@@ -407,6 +409,7 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
     for (int e = 0; e < DPL; ++e) aw[(warp * G + g) * D + lane * DPL + e] = acc[g][e];
   named_bar_sync(1, kNW * 32);
   const int tid = threadIdx.x;  // 0 .. 127
+  const float vsc = p.v_scale ? __ldg(p.v_scale + (p.scale_per_head ? h : 0)) : 1.f;
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     float M = -INFINITY;
@@ -425,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, partial_ctas_per_sm_hint(kPartialCud
       float o = 0.f;
 #pragma unroll
       for (int w = 0; w < kNW; ++w) o += fw[w] * aw[(w * G + g) * D + d];
-      o = o / Ls;
+      o = o / Ls * vsc;
       if (n_splits_b == 1) {
         if (p.out_f32) static_cast<float*>(p.out)[row * D + d] = o;
         else static_cast<TNat*>(p.out)[row * D + d] = to_out<TNat>(o);

@@ -28,6 +28,7 @@ PDA_DECLARE_TC(bf16, 64)
 PDA_DECLARE_TC(bf16, 128)
 PDA_DECLARE_TC(fp16, 64)
 PDA_DECLARE_TC(fp16, 128)
+PDA_DECLARE_TC(kv8_bf16, 128)
 #undef PDA_DECLARE_TC
 
 namespace {
@@ -50,12 +51,13 @@ auto with_cc(int dtype, int head_dim, F f) {
 #undef PDA_CC_CASE
 }
 
-// Same for the tensor-core kernel (head dims 64 and 128).
+// Same for the tensor-core kernel (head dims 64 and 128; FP8 K/V at 128).
 template <typename F>
-auto with_tc(int dtype, int head_dim, F f) {
+auto with_tc(int dtype, int head_dim, bool kv_fp8, F f) {
 #define PDA_TC_CASE(dt, D)                                                             \
   return f(launch_partial_tc_##dt##_d##D, prepare_partial_tc_##dt##_d##D,              \
            occupancy_partial_tc_##dt##_d##D)
+  if (kv_fp8) PDA_TC_CASE(kv8_bf16, 128);
   if (dtype == 1) {
     if (head_dim == 64) PDA_TC_CASE(fp16, 64);
     PDA_TC_CASE(fp16, 128);
@@ -67,19 +69,21 @@ auto with_tc(int dtype, int head_dim, F f) {
 
 }  // namespace
 
-bool partial_supported(int group, int head_dim, int block_size, int dtype) {
+bool partial_supported(int group, int head_dim, int block_size, int dtype, bool kv_fp8) {
   const bool bs_ok = block_size == 16 || block_size == 32;
+  if (kv_fp8) return tc::geometry_supported(group, head_dim, true) && bs_ok && dtype == 0;
   return partial::geometry_supported(group, head_dim) && bs_ok && (dtype == 0 || dtype == 1);
 }
 
-bool partial_kernel_supported(int kernel, int group, int head_dim) {
-  if (kernel == kPartialTensorCore) return tc::geometry_supported(group, head_dim);
-  return kernel == kPartialCudaCore && partial::geometry_supported(group, head_dim);
+bool partial_kernel_supported(int kernel, int group, int head_dim, bool kv_fp8) {
+  if (kernel == kPartialTensorCore) return tc::geometry_supported(group, head_dim, kv_fp8);
+  return kernel == kPartialCudaCore && !kv_fp8 && partial::geometry_supported(group, head_dim);
 }
 
-cudaError_t partial_prepare(int kernel, int group, int head_dim, int block_size, int dtype) {
+cudaError_t partial_prepare(int kernel, int group, int head_dim, int block_size, int dtype,
+                            bool kv_fp8) {
   if (kernel == kPartialTensorCore)
-    return with_tc(dtype, head_dim, [&](auto, auto prepare, auto) {
+    return with_tc(dtype, head_dim, kv_fp8, [&](auto, auto prepare, auto) {
       return prepare(group, block_size);
     });
   return with_cc(dtype, head_dim, [&](auto, auto prepare, auto) {
@@ -87,9 +91,10 @@ cudaError_t partial_prepare(int kernel, int group, int head_dim, int block_size,
   });
 }
 
-int partial_ctas_per_sm(int kernel, int group, int head_dim, int block_size, int dtype) {
+int partial_ctas_per_sm(int kernel, int group, int head_dim, int block_size, int dtype,
+                        bool kv_fp8) {
   if (kernel == kPartialTensorCore)
-    return with_tc(dtype, head_dim, [&](auto, auto, auto occupancy) {
+    return with_tc(dtype, head_dim, kv_fp8, [&](auto, auto, auto occupancy) {
       return occupancy(group, block_size);
     });
   return with_cc(dtype, head_dim, [&](auto, auto, auto occupancy) {
@@ -98,12 +103,11 @@ int partial_ctas_per_sm(int kernel, int group, int head_dim, int block_size, int
 }
 
 cudaError_t launch_partial(int kernel, int group, int head_dim, int block_size, int dtype,
-                           bool out_f32, const CUtensorMap* tk, const CUtensorMap* tv,
+                           bool kv_fp8, const CUtensorMap* tk, const CUtensorMap* tv,
                            const CUtensorMap* tq, const PartialParams& p, int batch,
                            cudaStream_t stream) {
-  (void)out_f32;  // both kernels read p.out_f32
   if (kernel == kPartialTensorCore)
-    return with_tc(dtype, head_dim, [&](auto launch, auto, auto) {
+    return with_tc(dtype, head_dim, kv_fp8, [&](auto launch, auto, auto) {
       return launch(group, block_size, tk, tv, tq, p, stream);
     });
   return with_cc(dtype, head_dim, [&](auto launch, auto, auto) {

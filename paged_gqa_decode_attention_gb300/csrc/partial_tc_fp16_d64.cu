@@ -7,15 +7,15 @@ namespace pda {
 cudaError_t launch_partial_tc_fp16_d64(int G, int BS, const CUtensorMap* tk,
                                          const CUtensorMap* tv, const CUtensorMap* tq,
                                          const PartialParams& p, cudaStream_t s) {
-  return tc::Dispatch<64, true>::launch(G, BS, tk, tv, tq, p, s);
+  return tc::Dispatch<64, true, false>::launch(G, BS, tk, tv, tq, p, s);
 }
 
 cudaError_t prepare_partial_tc_fp16_d64(int G, int BS) {
-  return tc::Dispatch<64, true>::prepare(G, BS);
+  return tc::Dispatch<64, true, false>::prepare(G, BS);
 }
 
 int occupancy_partial_tc_fp16_d64(int G, int BS) {
-  return tc::Dispatch<64, true>::occupancy(G, BS);
+  return tc::Dispatch<64, true, false>::occupancy(G, BS);
 }
 
 }  // namespace pda

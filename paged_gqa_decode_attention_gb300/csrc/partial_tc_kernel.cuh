@@ -55,6 +55,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <type_traits>
 
@@ -66,10 +67,8 @@ namespace pda {
 namespace tc {
 
 constexpr int kT = 128;                    // tokens per stage = MMA M of QK^T
-constexpr int kStages = 3;                 // slots per ring (K and V each)
 constexpr int kRowBytes = 128;             // one 64-element half of a 128-dim row
 constexpr int kHalf = kT * kRowBytes;      // one half tile: 16 KiB
-constexpr int kSlotBytes = 2 * kHalf;      // lo, hi halves of a K or V tile: 32 KiB
 constexpr int kN = 16;                     // MMA N: the group's query heads, padded
 constexpr int kOpHalf = 2048;              // 16 rows x 128 B of a K-major operand half
 constexpr int kOpBytes = 2 * kOpHalf;      // Q, P_hi or P_lo operand
@@ -80,27 +79,39 @@ constexpr int kWarpMma = 6;
 constexpr int kWarpEpi0 = 7;               // warps 7-10: epilogue group
 constexpr uint32_t kTmemCols = 64;
 constexpr unsigned kFull = 0xffffffffu;
-
-constexpr int kOffK = 0;
-constexpr int kOffV = kStages * kSlotBytes;
-constexpr int kOffQ = 2 * kStages * kSlotBytes;  // [2 buffers] Q operands
-constexpr int kOffP = kOffQ + 2 * kOpBytes;      // [2 buffers][hi, lo] operands
-constexpr int kOffRed = kOffP + 4 * kOpBytes;    // 2 x [4 warps][8] floats (chunk maxima)
-constexpr int kOffLred = kOffRed + 2 * 4 * 8 * 4;  // [4 warps][8] floats (final sums)
-constexpr int kOffBar = kOffLred + 4 * 8 * 4;
 constexpr int kUnitRing = 4;               // slots of the shared unit queue
 constexpr int kUnitConsumers = 3;          // V producer, MMA warp, softmax warp 0
-constexpr int kNumBars = 4 * kStages + 14 + 2 * kUnitRing + 4;
-constexpr int kOffTmem = kOffBar + kNumBars * 8;
-constexpr int kOffURing = kOffTmem + 16;          // [kUnitRing] unit indices
-constexpr int kOffUBcast = kOffURing + kUnitRing * 4;  // unit index, softmax warp 0 -> 1..3
-constexpr int kOffEpiFlag = kOffUBcast + 4;            // epilogue group's shared wait outcome
 // A finished unit's state, softmax -> epilogue, double-buffered:
 // acc[8][128], max[8], sum[8], unit index (floats; the index as int).
 constexpr int kEpiFloats = 8 * 128 + 8 + 8 + 4;
-constexpr int kOffEpi = (kOffEpiFlag + 4 + 15) & ~15;
-constexpr size_t kSmemBytes = 1024 + kOffEpi + 2 * kEpiFloats * 4;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+constexpr float kP8Scale = 256.f;          // FP8 K/V: P is split at p * 256
+
+// Shared-memory layout. 16-bit K/V: 3-slot rings of 32 KiB slots (two
+// 64-dim halves of 128 tokens). FP8 K/V (KV8): 5-slot rings of 16 KiB slots
+// (one 128-byte row per token), two fp8 terms of Q next to the 16-bit Q
+// tile, three fp8 terms of P in the P buffers.
+template <bool KV8>
+struct Layout {
+  static constexpr int kStages = KV8 ? 5 : 3;
+  static constexpr int kSlotBytes = KV8 ? kT * 128 : 2 * kHalf;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kStages * kSlotBytes;
+  static constexpr int kOffQ = 2 * kStages * kSlotBytes;  // [2 buffers] Q tiles (TMA)
+  static constexpr int kOffQ8 = kOffQ + 2 * kOpBytes;     // [2 buffers] fp8 Q terms (KV8)
+  static constexpr int kOffP = kOffQ8 + (KV8 ? 2 * kOpBytes : 0);  // [2 buffers] P operands
+  static constexpr int kOffQs = kOffP + 4 * kOpBytes;     // [2 buffers][8] 1/sigma per row (KV8)
+  static constexpr int kOffRed = kOffQs + 2 * 8 * 4;      // 2 x [4 warps][8] floats (chunk maxima)
+  static constexpr int kOffLred = kOffRed + 2 * 4 * 8 * 4;  // [4 warps][8] floats (final sums)
+  static constexpr int kOffBar = kOffLred + 4 * 8 * 4;
+  static constexpr int kNumBars = 4 * kStages + 14 + 2 * kUnitRing + 4 + 2;
+  static constexpr int kOffTmem = kOffBar + kNumBars * 8;
+  static constexpr int kOffURing = kOffTmem + 16;              // [kUnitRing] unit indices
+  static constexpr int kOffUBcast = kOffURing + kUnitRing * 4;  // unit index, warp 0 -> 1..3
+  static constexpr int kOffEpiFlag = kOffUBcast + 4;           // epilogue group's wait outcome
+  static constexpr int kOffEpi = (kOffEpiFlag + 4 + 15) & ~15;
+  static constexpr size_t kSmemBytes = 1024 + kOffEpi + 2 * kEpiFloats * 4;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
 
 template <bool FP16>
 struct Half16 {
@@ -131,6 +142,21 @@ __device__ __forceinline__ uint32_t op_offset(int n, int k) {
   const int half = k >> 6, col = k & 63;
   return half * kOpHalf + (n >> 3) * 1024 + (n & 7) * 128 + (((col >> 3) ^ (n & 7)) << 4) +
          (col & 7) * 2;
+}
+
+// Byte offset of element (row n, column k) of a 16 x 128 K-major fp8 operand
+// (one 128-byte row per n, 128-byte swizzle).
+__device__ __forceinline__ uint32_t op8_offset(int n, int k) {
+  return (n >> 3) * 1024 + (n & 7) * 128 + ((((k >> 4) ^ (n & 7))) << 4) + (k & 15);
+}
+
+__device__ __forceinline__ uint8_t to_e4m3(float x) {
+  return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ float e4m3_to_float(uint8_t b) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3);
+  return __half2float(__half(h));
 }
 
 // One work unit: (split, kv head, sequence) and its page / token / chunk range.
@@ -197,13 +223,31 @@ struct Cursor {
   }
 };
 
-template <int G, int D, int BS, bool FP16>
+template <int G, int D, int BS, bool FP16, bool KV8>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_partial_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v,
                             const __grid_constant__ CUtensorMap tmap_q, const PartialParams p) {
-  static_assert(G >= 3 && G <= 8, "tensor-core path packs 3..8 query heads");
+  static_assert(G >= 1 && G <= 8, "tensor-core path packs up to 8 query heads");
   static_assert(D == 64 || D == 128, "head dim 64 or 128");
+  static_assert(!KV8 || (D == 128 && !FP16), "FP8 K/V: head dim 128, bf16 queries");
+  using L = Layout<KV8>;
+  constexpr int kStages = L::kStages;
+  constexpr int kSlotBytes = L::kSlotBytes;
+  constexpr int kOffK = L::kOffK;
+  constexpr int kOffV = L::kOffV;
+  constexpr int kOffQ = L::kOffQ;
+  constexpr int kOffQ8 = L::kOffQ8;
+  constexpr int kOffP = L::kOffP;
+  constexpr int kOffQs = L::kOffQs;
+  constexpr int kOffRed = L::kOffRed;
+  constexpr int kOffLred = L::kOffLred;
+  constexpr int kOffBar = L::kOffBar;
+  constexpr int kOffTmem = L::kOffTmem;
+  constexpr int kOffURing = L::kOffURing;
+  constexpr int kOffUBcast = L::kOffUBcast;
+  constexpr int kOffEpiFlag = L::kOffEpiFlag;
+  constexpr int kOffEpi = L::kOffEpi;
   constexpr int NB = D / 64;    // 64-dim boxes per row
   constexpr int PPS = kT / BS;  // pages per stage
   constexpr int GL = G <= 4 ? 4 : 8;  // TMEM columns read per row
@@ -232,6 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto uring_empty = [&](int s) { return bar0 + 8u * (4 * kStages + 14 + kUnitRing + s); };
   auto ep_full = [&](int s) { return bar0 + 8u * (4 * kStages + 14 + 2 * kUnitRing + s); };
   auto ep_empty = [&](int s) { return bar0 + 8u * (4 * kStages + 16 + 2 * kUnitRing + s); };
+  // FP8 K/V: the unit's fp8 Q terms and row scales are ready (buffer b)
+  auto q8_full = [&](int b) { return bar0 + 8u * (4 * kStages + 18 + 2 * kUnitRing + b); };
   volatile int* uring = reinterpret_cast<volatile int*>(base + kOffURing);
 
   const int warp = threadIdx.x >> 5;
@@ -330,7 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(o_full(b2), 1);
       mbar_init(o_free(b2), 4);
       mbar_init(q_full(b2), 1);
-      mbar_init(q_empty(b2), 1);
+      // FP8 K/V: also released by the softmax warps once they have read the
+      // buffer's row scales
+      mbar_init(q_empty(b2), KV8 ? 2 : 1);
+      mbar_init(q8_full(b2), 1);
     }
     fence_mbar_init();
   }
@@ -342,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Q operands (rows G..15 stay zero; the TMA box fills rows 0..G-1) and
     // both P operand pairs start zeroed; at D = 64 the upper (dims 64..127)
     // half of every V slot is zero for the whole kernel.
-    for (int i = threadIdx.x; i < (2 * kOpBytes + 4 * kOpBytes) / 16; i += 128)
+    for (int i = threadIdx.x; i < (kOffQs - kOffQ) / 16; i += 128)
       *reinterpret_cast<uint4*>(base + kOffQ + i * 16) = make_uint4(0, 0, 0, 0);
     if constexpr (D == 64) {
       for (int s2 = 0; s2 < kStages; ++s2)
@@ -425,7 +474,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < PPS; ++i) blk[i] = __shfl_sync(kFull, win_blk, (pg0 + i - win_base) & 31);
       if (lane == 0) {
         const uint32_t fb = full_bar(r, slot);
-        mbar_arrive_expect_tx(fb, (uint32_t)npg * BS * NB * kRowBytes);
+        // 16-bit K/V: D / 64 boxes of 64 dims per page; FP8: one box of D bytes
+        constexpr int kBoxes = KV8 ? 1 : NB;
+        constexpr int kBoxElems = KV8 ? D : 64;
+        mbar_arrive_expect_tx(fb, (uint32_t)npg * BS * kBoxes * kRowBytes);
         const uint32_t st = base_u32 + (r == 0 ? kOffK : kOffV) + slot * kSlotBytes;
 #pragma unroll
         for (int i = 0; i < PPS; ++i) {
@@ -433,36 +485,95 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int y = blk[i] * BS;
             const uint32_t ro = (uint32_t)(i * BS * kRowBytes);
 #pragma unroll
-            for (int bx = 0; bx < NB; ++bx)
-              tma_load_2d(st + bx * kHalf + ro, map, U.h * D + bx * 64, y, fb);
+            for (int bx = 0; bx < kBoxes; ++bx)
+              tma_load_2d(st + bx * kHalf + ro, map, U.h * D + bx * kBoxElems, y, fb);
           }
         }
       }
       __syncwarp();
+      if constexpr (KV8) {
+        if (r == 0 && cu_i == 0) {
+          // The unit's q rows (16-bit tile from TMA) become two fp8 terms,
+          // q * sigma = hi + lo, with a power-of-two sigma per row that puts
+          // the row's largest |q| in [128, 256): the fp8 QK^T then sees q
+          // exactly except for elements below 2^-10 of the row maximum.
+          const int qb = cu_j & 1;
+          const bool okq = mbar_wait(q_full(qb), (cu_j >> 1) & 1);
+          if (!__all_sync(kFull, okq)) {
+            failed = true;
+            break;
+          }
+          const uint8_t* qt = base + kOffQ + qb * kOpBytes;
+          uint8_t* q8 = base + kOffQ8 + qb * kOpBytes;
+          float* qs = reinterpret_cast<float*>(base + kOffQs) + qb * 8;
+          const int d0 = 4 * lane;
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const uint2 w = *reinterpret_cast<const uint2*>(qt + op_offset(g, d0));
+            const float x[4] = {__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                                __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u)};
+            float mx = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+            int e = 0;
+            if (mx > 0.f) frexpf(mx, &e);
+            const float sig = ldexpf(1.f, 8 - e);
+            uint32_t hw = 0, lw = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float y = x[i] * sig;
+              const uint8_t hb = to_e4m3(y);
+              const uint8_t lb = to_e4m3(y - e4m3_to_float(hb));
+              hw |= (uint32_t)hb << (8 * i);
+              lw |= (uint32_t)lb << (8 * i);
+            }
+            *reinterpret_cast<uint32_t*>(q8 + op8_offset(g, d0)) = hw;
+            *reinterpret_cast<uint32_t*>(q8 + kOpHalf + op8_offset(g, d0)) = lw;
+            if (lane == 0) qs[g] = 1.f / sig;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(q8_full(qb));
+        }
+      }
       if (r == 0) cur_k.advance(p, fetch); else cur_v.advance(p, ring);
     }
   } else if (warp == kWarpMma) {
     // ------------------------------ MMA issue -----------------------------
-    constexpr uint32_t idesc_qk = idesc_f16(128, kN, !FP16, false, false);
-    constexpr uint32_t idesc_pv = idesc_f16(128, kN, !FP16, true, false);
+    // kind::f16: type fields 1 = bf16, 0 = f16; kind::f8f6f4: 0 = E4M3
+    constexpr uint32_t idesc_qk = idesc_f16(128, kN, !FP16 && !KV8, false, false);
+    constexpr uint32_t idesc_pv = idesc_f16(128, kN, !FP16 && !KV8, true, false);
     // S(c) = K(c) . Q^T into S[c & 1]; needs the K slot, the unit's Q and the
     // softmax's read of S(c-2)
     auto issue_qk = [&](const Cursor<BS, RingSource>& cur) {
       const int c = cur.c, slot = c % kStages, qb = cur.j & 1;
       bool ok = !failed && mbar_wait(full_bar(0, slot), (c / kStages) & 1);
       if (ok && c >= 2) ok = mbar_wait(s_free(c & 1), ((c - 2) >> 1) & 1);
-      if (ok && cur.i == 0) ok = mbar_wait(q_full(qb), (cur.j >> 1) & 1);
+      if (ok && cur.i == 0) ok = mbar_wait(KV8 ? q8_full(qb) : q_full(qb), (cur.j >> 1) & 1);
       if (!__all_sync(kFull, ok)) failed = true;
       if (failed) return;
       tc_fence_after();
       if (lane == 0) {
         const uint32_t kb = base_u32 + kOffK + slot * kSlotBytes;
-        const uint32_t qa = base_u32 + kOffQ + qb * kOpBytes;
+        if constexpr (KV8) {
+          // S = K . (Q_hi + Q_lo)^T: 32 fp8 dims (32 bytes) per step
+          const uint32_t q8 = base_u32 + kOffQ8 + qb * kOpBytes;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint64_t a = sdesc_sw128(kb + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
-          const uint64_t bq = sdesc_sw128(qa + (k >> 2) * kOpHalf + (k & 3) * 32, 16, 1024);
-          mma_f16_ss(tS(c & 1), a, bq, idesc_qk, k > 0 ? 1u : 0u);
+          for (int term = 0; term < 2; ++term)
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k) {
+              const uint64_t a = sdesc_sw128(kb + k * 32, 16, 1024);
+              const uint64_t bq = sdesc_sw128(q8 + term * kOpHalf + k * 32, 16, 1024);
+              mma_f8_ss(tS(c & 1), a, bq, idesc_qk, (term | k) > 0 ? 1u : 0u);
+            }
+        } else {
+          const uint32_t qa = base_u32 + kOffQ + qb * kOpBytes;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint64_t a = sdesc_sw128(kb + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
+            const uint64_t bq = sdesc_sw128(qa + (k >> 2) * kOpHalf + (k & 3) * 32, 16, 1024);
+            mma_f16_ss(tS(c & 1), a, bq, idesc_qk, k > 0 ? 1u : 0u);
+          }
         }
         mma_commit(s_full(c & 1));
         mma_commit(empty_bar(0, slot));                          // K slot read
@@ -482,10 +593,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (lane == 0) {
         const uint32_t vb = base_u32 + kOffV + slot * kSlotBytes;
+        if constexpr (KV8) {
+          // O = V^T . (P_0 + P_1 + P_2)^T: V^T as an MN-major fp8 A operand (all
+          // 128 dims in one 128-byte row per token), 32 tokens per step
+          const uint32_t p8 = base_u32 + kOffP + (c & 1) * 3 * kOpHalf;
+#pragma unroll
+          for (int k = 0; k < kT / 32; ++k) {
+            const uint64_t a = sdesc_sw128(vb + k * 32 * 128, kSlotBytes, 1024);
+#pragma unroll
+            for (int term = 0; term < 3; ++term)
+              mma_f8_ss(tO(c & 1), a, sdesc_sw128(p8 + term * kOpHalf + k * 32, 16, 1024),
+                        idesc_pv, (k | term) > 0 ? 1u : 0u);
+          }
+        }
         const uint32_t phi = base_u32 + kOffP + (c & 1) * 2 * kOpBytes;
         const uint32_t plo = phi + kOpBytes;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < (KV8 ? 0 : 8); ++k) {
           // V^T as an MN-major A operand: 64-dim halves kHalf apart (LBO),
           // 8-token row groups 1 KiB apart (SBO); 16 tokens per step
           const uint64_t a = sdesc_sw128(vb + k * 2048, kHalf, 1024);
@@ -563,6 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return u;
     };
     int c = 0, je = 0;  // je: units handed to the epilogue group
+    int jq = 0;         // units with chunks (the Q buffer sequence)
     for (int u = next_unit(); u >= 0; u = next_unit()) {
       const Unit U = load_unit<BS>(p, u);
       const int hq0 = U.h * G;
@@ -579,6 +704,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_run[g] = -INFINITY;
         l_th[g] = 0.f;
         acc[g] = 0.f;
+      }
+      // logit scale per row: softmax scale (base 2) x K dequantisation scale
+      // (x 1 / sigma of the row's fp8 q terms)
+      const float ksc = p.k_scale ? __ldg(p.k_scale + (p.scale_per_head ? U.h : 0)) : 1.f;
+      float qsc[G];
+      if constexpr (KV8) {
+        const bool okq = !failed && mbar_wait(q8_full(jq & 1), (jq >> 1) & 1);
+        if (!__all_sync(kFull, okq)) failed = true;
+        const float* qs = reinterpret_cast<const float*>(base + kOffQs) + (jq & 1) * 8;
+#pragma unroll
+        for (int g = 0; g < G; ++g) qsc[g] = p.qscale * ksc * qs[g];
+      } else {
+#pragma unroll
+        for (int g = 0; g < G; ++g) qsc[g] = p.qscale * ksc;
       }
       for (int i = 0; i < U.n_chunks; ++i, ++c) {
         const int slot = c % kStages;
@@ -597,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(s_free(c & 1));
 #pragma unroll
-        for (int g = 0; g < G; ++g) s[g] = (t < n_valid) ? s[g] * p.qscale : -INFINITY;
+        for (int g = 0; g < G; ++g) s[g] = (t < n_valid) ? s[g] * qsc[g] : -INFINITY;
         float* rb = red + (c & 1) * 32;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -607,8 +746,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) rb[warp * 8 + g] = mx;
         }
         named_bar_sync(1, 128);
+        // every softmax thread has read the row scales of this unit's Q buffer
+        if (KV8 && i == 0 && t == 0) mbar_arrive(q_empty(jq & 1));
         float alpha[G];
-        uint8_t* pb = base + kOffP + (c & 1) * 2 * kOpBytes;
+        uint8_t* pb = base + kOffP + (c & 1) * (KV8 ? 3 * kOpHalf : 2 * kOpBytes);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           const float mx = fmaxf(fmaxf(rb[g], rb[8 + g]), fmaxf(rb[16 + g], rb[24 + g]));
@@ -617,11 +758,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_run[g] = mn;
           const float pr = exp2f(s[g] - mn);
           l_th[g] = l_th[g] * alpha[g] + pr;
-          const typename H::T hi = H::from(pr);
-          const typename H::T lo = H::from(pr - H::to(hi));
-          const uint32_t off = op_offset(g, t);
-          *reinterpret_cast<typename H::T*>(pb + off) = hi;
-          *reinterpret_cast<typename H::T*>(pb + kOpBytes + off) = lo;
+          if constexpr (KV8) {
+            // p * 256 = t0 + t1 + t2 in fp8 (about 12 significant bits)
+            const float x = pr * kP8Scale;
+            const uint8_t b0 = to_e4m3(x);
+            const float r0 = x - e4m3_to_float(b0);
+            const uint8_t b1 = to_e4m3(r0);
+            const uint8_t b2 = to_e4m3(r0 - e4m3_to_float(b1));
+            const uint32_t off = op8_offset(g, t);
+            pb[off] = b0;
+            pb[kOpHalf + off] = b1;
+            pb[2 * kOpHalf + off] = b2;
+          } else {
+            const typename H::T hi = H::from(pr);
+            const typename H::T lo = H::from(pr - H::to(hi));
+            const uint32_t off = op_offset(g, t);
+            *reinterpret_cast<typename H::T*>(pb + off) = hi;
+            *reinterpret_cast<typename H::T*>(pb + kOpBytes + off) = lo;
+          }
         }
         if (n_valid < kT) {
           // keep stale or out-of-context V rows out of the MMA; the V tile of
@@ -632,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t >= n_valid) {
           uint8_t* vrow = base + kOffV + slot * kSlotBytes + t * kRowBytes;
 #pragma unroll
-          for (int hh = 0; hh < NB; ++hh)
+          for (int hh = 0; hh < (KV8 ? 1 : NB); ++hh)
 #pragma unroll
             for (int q = 0; q < 8; ++q)
               *reinterpret_cast<uint4*>(vrow + hh * kHalf + q * 16) = make_uint4(0, 0, 0, 0);
@@ -679,6 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(ep_full(es));
         ++je;
       }
+      ++jq;
     }
     // end of work: an empty state tells the epilogue group to stop
     {
@@ -712,11 +867,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (u < 0) break;
       const Unit U = load_unit<BS>(p, u);
       const int hq0 = U.h * G;
+      // V dequantisation scale (and the fp8 split factor of P)
+      const float vsc = (p.v_scale ? __ldg(p.v_scale + (p.scale_per_head ? U.h : 0)) : 1.f) *
+                        (KV8 ? 1.f / kP8Scale : 1.f);
       if (t < D) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           const float Ls = st[8 * kHeadDim + 8 + g];
-          const float o = st[g * kHeadDim + t] / Ls;
+          const float o = st[g * kHeadDim + t] / Ls * vsc;
           const int64_t row = (int64_t)U.b * p.Hq + hq0 + g;
           if (U.n_splits_b == 1) {
             if (p.out_f32) static_cast<float*>(p.out)[row * D + t] = o;
@@ -748,58 +906,83 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int G, int D, int BS, bool FP16>
+template <int G, int D, int BS, bool FP16, bool KV8>
 cudaError_t launch_one(const CUtensorMap* tk, const CUtensorMap* tv, const CUtensorMap* tq,
                        const PartialParams& p, cudaStream_t stream) {
   const int ctas = p.num_units < p.max_ctas ? p.num_units : p.max_ctas;
   if (ctas <= 0) return cudaSuccess;
-  paged_partial_tc_kernel<G, D, BS, FP16><<<ctas, kThreads, kSmemBytes, stream>>>(*tk, *tv, *tq, p);
+  paged_partial_tc_kernel<G, D, BS, FP16, KV8>
+      <<<ctas, kThreads, Layout<KV8>::kSmemBytes, stream>>>(*tk, *tv, *tq, p);
   return cudaGetLastError();
 }
 
-template <int G, int D, int BS, bool FP16>
+template <int G, int D, int BS, bool FP16, bool KV8>
 cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(paged_partial_tc_kernel<G, D, BS, FP16>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  return cudaFuncSetAttribute(paged_partial_tc_kernel<G, D, BS, FP16, KV8>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)Layout<KV8>::kSmemBytes);
 }
 
-template <int G, int D, int BS, bool FP16>
+template <int G, int D, int BS, bool FP16, bool KV8>
 int occupancy_one() {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_partial_tc_kernel<G, D, BS, FP16>,
-                                                    kThreads, kSmemBytes) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &n, paged_partial_tc_kernel<G, D, BS, FP16, KV8>, kThreads,
+          Layout<KV8>::kSmemBytes) != cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }
 
-__host__ __device__ constexpr bool geometry_supported(int G, int D) {
-  return G >= 3 && G <= 8 && (D == 64 || D == 128);
+// 16-bit K/V: G 3..8 (G 1 and 2 go to the CUDA-core kernel), D 64 or 128.
+// FP8 K/V: any G up to 8, D 128, bf16 queries.
+__host__ __device__ constexpr bool geometry_supported(int G, int D, bool kv8 = false) {
+  return kv8 ? (G >= 1 && G <= 8 && D == 128) : (G >= 3 && G <= 8 && (D == 64 || D == 128));
 }
 
-// Dispatch over (G, block size) for one head dim and input dtype; each
-// (D, dtype) pair is instantiated in its own translation unit.
-template <int D, bool FP16>
+// Dispatch over (G, block size) for one head dim, input dtype and K/V type;
+// each combination is instantiated in its own translation unit.
+template <int D, bool FP16, bool KV8>
 struct Dispatch {
   template <int G>
   static cudaError_t launch_g(int BS, const CUtensorMap* tk, const CUtensorMap* tv,
                               const CUtensorMap* tq, const PartialParams& p, cudaStream_t s) {
-    if (BS == 16) return launch_one<G, D, 16, FP16>(tk, tv, tq, p, s);
-    if (BS == 32) return launch_one<G, D, 32, FP16>(tk, tv, tq, p, s);
+    if constexpr (geometry_supported(G, D, KV8)) {
+      if (BS == 16) return launch_one<G, D, 16, FP16, KV8>(tk, tv, tq, p, s);
+      if (BS == 32) return launch_one<G, D, 32, FP16, KV8>(tk, tv, tq, p, s);
+    }
     return cudaErrorInvalidValue;
   }
   template <int G>
   static cudaError_t prepare_g(int BS) {
-    if (BS == 16) return prepare_one<G, D, 16, FP16>();
-    if (BS == 32) return prepare_one<G, D, 32, FP16>();
+    if constexpr (geometry_supported(G, D, KV8)) {
+      if (BS == 16) return prepare_one<G, D, 16, FP16, KV8>();
+      if (BS == 32) return prepare_one<G, D, 32, FP16, KV8>();
+    }
     return cudaErrorInvalidValue;
   }
   template <int G>
   static int occupancy_g(int BS) {
-    return BS == 16 ? occupancy_one<G, D, 16, FP16>() : occupancy_one<G, D, 32, FP16>();
+    if constexpr (geometry_supported(G, D, KV8)) {
+      return BS == 16 ? occupancy_one<G, D, 16, FP16, KV8>() : occupancy_one<G, D, 32, FP16, KV8>();
+    }
+    return 1;
+  }
+#define PDA_TC_SWITCH(call)      \\
+  switch (G) {                   \\
+    case 1: return call<1>;      \\
+    case 2: return call<2>;      \\
+    case 3: return call<3>;      \\
+    case 4: return call<4>;      \\
+    case 5: return call<5>;      \\
+    case 6: return call<6>;      \\
+    case 7: return call<7>;      \\
+    case 8: return call<8>;      \\
   }
   static cudaError_t launch(int G, int BS, const CUtensorMap* tk, const CUtensorMap* tv,
                             const CUtensorMap* tq, const PartialParams& p, cudaStream_t s) {
     switch (G) {
+      case 1: return launch_g<1>(BS, tk, tv, tq, p, s);
+      case 2: return launch_g<2>(BS, tk, tv, tq, p, s);
       case 3: return launch_g<3>(BS, tk, tv, tq, p, s);
       case 4: return launch_g<4>(BS, tk, tv, tq, p, s);
       case 5: return launch_g<5>(BS, tk, tv, tq, p, s);
@@ -811,6 +994,8 @@ struct Dispatch {
   }
   static cudaError_t prepare(int G, int BS) {
     switch (G) {
+      case 1: return prepare_g<1>(BS);
+      case 2: return prepare_g<2>(BS);
       case 3: return prepare_g<3>(BS);
       case 4: return prepare_g<4>(BS);
       case 5: return prepare_g<5>(BS);
@@ -822,6 +1007,8 @@ struct Dispatch {
   }
   static int occupancy(int G, int BS) {
     switch (G) {
+      case 1: return occupancy_g<1>(BS);
+      case 2: return occupancy_g<2>(BS);
       case 3: return occupancy_g<3>(BS);
       case 4: return occupancy_g<4>(BS);
       case 5: return occupancy_g<5>(BS);

@@ -43,6 +43,9 @@ struct PartialParams {
   int num_units;    // S * Hkv * B work units (persistent tensor-core kernel)
   int max_ctas;     // resident CTAs the persistent kernel launches at most
   int out_f32;      // out is fp32 (else the input dtype)
+  const float* k_scale;  // K/V dequantisation scales: [Hkv] (scale_per_head) or [1];
+  const float* v_scale;  // NULL = 1
+  int scale_per_head;
 };
 
 struct MergeParams {
@@ -72,9 +75,10 @@ enum PartialKernel : int {
 // the packed tile is a real contraction and the tensor-core kernel wins (B=4,
 // L=32768 at G=4: 0.0974 vs 0.1000 ms; the 128-sequence serving mix at G=8:
 // 0.114 vs 0.255 ms); otherwise the CUDA-core kernel is used.
-constexpr int default_partial_kernel(int group, int head_dim) {
-  return (group >= 3 && group <= 8 && (head_dim == 64 || head_dim == 128)) ? kPartialTensorCore
-                                                                           : kPartialCudaCore;
+constexpr int default_partial_kernel(int group, int head_dim, bool kv_fp8 = false) {
+  return (kv_fp8 || (group >= 3 && group <= 8 && (head_dim == 64 || head_dim == 128)))
+             ? kPartialTensorCore
+             : kPartialCudaCore;
 }
 
 // CTAs per SM each kernel is built for (its launch bounds and shared memory);
@@ -84,16 +88,19 @@ constexpr int partial_ctas_per_sm_hint(int kernel, int group, int head_dim) {
                                       : ((group * head_dim > 512 || head_dim >= 256) ? 1 : 2);
 }
 
-bool partial_supported(int group, int head_dim, int block_size, int dtype);
-bool partial_kernel_supported(int kernel, int group, int head_dim);
-cudaError_t partial_prepare(int kernel, int group, int head_dim, int block_size, int dtype);
-int partial_ctas_per_sm(int kernel, int group, int head_dim, int block_size, int dtype);
+// kv_fp8: K/V caches hold FP8 E4M3 (tensor-core kernel, D 128, bf16 q).
+bool partial_supported(int group, int head_dim, int block_size, int dtype, bool kv_fp8);
+bool partial_kernel_supported(int kernel, int group, int head_dim, bool kv_fp8);
+cudaError_t partial_prepare(int kernel, int group, int head_dim, int block_size, int dtype,
+                            bool kv_fp8);
+int partial_ctas_per_sm(int kernel, int group, int head_dim, int block_size, int dtype,
+                        bool kv_fp8);
 
 // tmap_q (a [B * Hq, D] view of q, boxes of 64 dims x G rows) is read by
 // the tensor-core kernel only; both kernels take the output type from
-// p.out_f32 (`out_f32` must agree with it).
+// p.out_f32.
 cudaError_t launch_partial(int kernel, int group, int head_dim, int block_size, int dtype,
-                           bool out_f32, const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                           bool kv_fp8, const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
                            const CUtensorMap* tmap_q, const PartialParams& p, int batch,
                            cudaStream_t stream);
 

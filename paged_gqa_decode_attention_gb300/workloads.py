@@ -83,8 +83,12 @@ class Workload:
         """Algorithmic KV bytes one call reads: sum_b L_b * 2 * Hkv * D * esz
         (no padding of partial pages, no re-reads, shared pages counted once
         per sequence that reads them)."""
-        esz = self.q.element_size()
+        esz = self.k_cache.element_size()
         return sum(self.lens_list()) * 2 * self.num_kv_heads * self.head_dim * esz
+
+    @property
+    def kv_fp8(self) -> bool:
+        return self.k_cache.element_size() == 1
 
     def unique_kv_bytes(self) -> int:
         """KV bytes of the distinct physical token slots read by one call."""
@@ -97,13 +101,15 @@ class Workload:
                 blk = int(bt[b, p])
                 used = min(bs, L - p * bs)
                 seen[blk] = max(seen.get(blk, 0), used)
-        esz = self.q.element_size()
+        esz = self.k_cache.element_size()
         return sum(seen.values()) * 2 * self.num_kv_heads * self.head_dim * esz
 
     def to(self, device) -> "Workload":
+        meta = {k: (v.to(device) if isinstance(v, torch.Tensor) else v)
+                for k, v in self.meta.items()}
         return Workload(self.name, self.q.to(device), self.k_cache.to(device),
                         self.v_cache.to(device), self.block_table.to(device),
-                        self.context_lens.to(device), self.scale, dict(self.meta))
+                        self.context_lens.to(device), self.scale, meta)
 
 
 # ---------------------------------------------------------------------------
@@ -226,17 +232,46 @@ LONG_POOL_BLOCKS = 655_360  # 40 GiB of K+V at block 16, Hkv 8, D 128, bf16
 
 
 def long_context(seed: int = 0, batch: int = 4, context: int = 32768,
-                 num_blocks: int = LONG_POOL_BLOCKS, device="cpu") -> Workload:
+                 num_blocks: int = LONG_POOL_BLOCKS, device="cpu",
+                 kv_fp8: bool = False) -> Workload:
     """Long-context split-K case: B in {1, 4} x context in {8192, 32768},
     32/8/128, block 16, bf16; random tables over a pool of ``num_blocks``
-    blocks (the full-size pool is 40 GiB of K+V)."""
+    blocks (the full-size pool is 40 GiB of K+V, 20 GiB as FP8)."""
     rng = _rng(seed, 3)
     Hq, Hkv, D, bs = 32, 8, 128, 16
     lens = [context] * batch
     max_blocks = (context + bs - 1) // bs
     tables = _tables_without_replacement(rng, lens, bs, max_blocks, num_blocks)
-    return _assemble(f"long_b{batch}_l{context}", batch, Hq, Hkv, D, bs, num_blocks, tables,
-                     lens, "bf16", 1.0, seed, device, meta={"pool_blocks": num_blocks})
+    wl = _assemble(f"long_b{batch}_l{context}", batch, Hq, Hkv, D, bs, num_blocks, tables,
+                   lens, "bf16", 1.0, seed, device, meta={"pool_blocks": num_blocks})
+    return to_fp8_kv(wl) if kv_fp8 else wl
+
+
+def to_fp8_kv(wl: Workload) -> Workload:
+    """The same workload with FP8 (E4M3) K/V caches: per kv head h, scale_h =
+    max |x| over the pool / 448 (so the largest value maps to the largest
+    E4M3 value) and the cache holds RNE(x / scale_h) (torch's saturating
+    conversion). The scales go to meta["k_scale"], meta["v_scale"] (fp32
+    [Hkv]). Works in row chunks so multi-GiB pools need no fp32 copy."""
+    Hkv, D = wl.num_kv_heads, wl.head_dim
+    out = {}
+    for name, cache in (("k", wl.k_cache), ("v", wl.v_cache)):
+        flat = cache.view(-1, Hkv, D)
+        rows = flat.shape[0]
+        step = max(1, (1 << 26) // (Hkv * D))
+        amax = torch.zeros(Hkv, dtype=torch.float32, device=cache.device)
+        for r0 in range(0, rows, step):
+            amax = torch.maximum(amax, flat[r0:r0 + step].float().abs().amax(dim=(0, 2)))
+        sc = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+        q8 = torch.empty(flat.shape, dtype=torch.float8_e4m3fn, device=cache.device)
+        for r0 in range(0, rows, step):
+            q8[r0:r0 + step] = (flat[r0:r0 + step].float() / sc.view(1, Hkv, 1)).to(
+                torch.float8_e4m3fn)
+        out[name] = (q8.view(cache.shape), sc)
+    meta = dict(wl.meta)
+    meta["k_scale"], meta["v_scale"] = out["k"][1], out["v"][1]
+    return Workload(wl.name + "_fp8", wl.q, out["k"][0], out["v"][0], wl.block_table,
+                    wl.context_lens, wl.scale, meta)
 
 
 def serving_mix(seed: int = 0, batch: int = 128, max_context: int = 4096,
@@ -289,8 +324,12 @@ def custom(seed: int, B: int, Hq: int, Hkv: int, D: int, block_size: int, lens,
 # ---------------------------------------------------------------------------
 
 def bits(t: torch.Tensor) -> np.ndarray:
-    """Raw 16-bit storage patterns of a bf16/fp16 tensor as numpy uint16."""
-    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+    """Raw storage patterns: numpy uint16 for bf16/fp16 tensors, uint8 for
+    FP8 tensors."""
+    t = t.detach().contiguous().cpu()
+    if t.element_size() == 1:
+        return t.view(torch.uint8).numpy()
+    return t.view(torch.int16).numpy().view(np.uint16)
 
 
 def host_arrays(wl: Workload):

@@ -47,6 +47,16 @@ def assert_close(out: torch.Tensor, ref: np.ndarray, what: str = "") -> float:
 
 def oracle_ref(wl: workloads.Workload) -> np.ndarray:
     dt = oracle.BF16 if wl.q.dtype == torch.bfloat16 else oracle.FP16
+    if wl.kv_fp8 or "k_scale" in wl.meta:
+        q, k, v, bt, cl = workloads.host_arrays(wl)
+        ks = wl.meta.get("k_scale")
+        vs = wl.meta.get("v_scale")
+        return oracle.paged_decode_kv(
+            q, k, v, bt, cl, dt, oracle.FP8_E4M3 if wl.kv_fp8 else dt, wl.scale,
+            None if ks is None else ks.double().cpu().numpy().repeat(
+                wl.num_kv_heads // ks.numel()),
+            None if vs is None else vs.double().cpu().numpy().repeat(
+                wl.num_kv_heads // vs.numel()))
     return oracle.paged_decode(*workloads.host_arrays(wl), dt, wl.scale)
 
 
@@ -55,10 +65,13 @@ def make_attn(wl: workloads.Workload, max_splits: int = 64, max_batch: int | Non
     return PagedDecodeAttention(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size,
                                 wl.q.dtype, max_batch=max_batch or max(1, wl.batch),
                                 max_blocks_per_seq=max_blocks or wl.max_blocks,
-                                max_splits=max_splits, device=torch.cuda.current_device())
+                                max_splits=max_splits, device=torch.cuda.current_device(),
+                                kv_fp8=wl.kv_fp8)
 
 
 def run_gpu(attn: PagedDecodeAttention, wl: workloads.Workload, **kw) -> torch.Tensor:
+    kw.setdefault("k_scale", wl.meta.get("k_scale"))
+    kw.setdefault("v_scale", wl.meta.get("v_scale"))
     out = attn.run(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.context_lens, wl.scale, **kw)
     torch.cuda.synchronize()
     return out

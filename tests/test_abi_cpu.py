@@ -38,7 +38,7 @@ def test_exports_every_header_function(lib):
 
 
 def test_abi_version(lib):
-    assert lib.paged_decode_attn_abi_version() == pda.ABI_VERSION == 1
+    assert lib.paged_decode_attn_abi_version() == pda.ABI_VERSION == 2
 
 
 def test_library_needs_no_driver_to_load(lib):

@@ -1,0 +1,101 @@
+"""GPU parity of the FP8 (E4M3) KV-cache path against the FP64 oracle with
+per-kv-head (and per-tensor) dequantisation scales, and of scaled 16-bit
+caches. Calls go through the C ABI (ctypes binding)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_gqa_decode_attention_gb300 import PDAError, PDA_EUNSUPPORTED, workloads
+from parity import assert_close, make_attn, oracle_ref, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+DEV = torch.device("cuda", torch.cuda.current_device())
+
+
+def check(wl_host, **kw):
+    wl = wl_host.to(DEV)
+    attn = make_attn(wl)
+    out = run_gpu(attn, wl, **kw)
+    attn.close()
+    return assert_close(out, oracle_ref(wl_host), wl.name)
+
+
+@pytest.mark.parametrize("G,Hkv", [(1, 8), (2, 4), (4, 8), (7, 4), (8, 1), (8, 8), (3, 2)])
+@pytest.mark.parametrize("bs", [16, 32])
+def test_fp8_geometries_exact(G, Hkv, bs):
+    lens = [1, bs + 1, 700, 3000, 64, 129]
+    wl = workloads.to_fp8_kv(workloads.custom(seed=G * 11 + Hkv + bs, B=len(lens), Hq=G * Hkv,
+                                              Hkv=Hkv, D=128, block_size=bs, lens=lens,
+                                              num_blocks=700))
+    for splits in (0, 1, 5, 64):
+        check(wl, num_splits=splits)
+
+
+def test_fp8_per_tensor_and_unit_scales():
+    base = workloads.custom(seed=3, B=4, Hq=32, Hkv=8, D=128, block_size=16,
+                            lens=[900, 17, 2048, 300])
+    wl = workloads.to_fp8_kv(base)
+    # one scale for the whole tensor (the largest per-head one)
+    wl.meta["k_scale"] = wl.meta["k_scale"].max().reshape(1)
+    wl.meta["v_scale"] = wl.meta["v_scale"].max().reshape(1)
+    check(wl)
+    # no scales at all: the raw E4M3 values
+    del wl.meta["k_scale"], wl.meta["v_scale"]
+    check(wl)
+
+
+def test_fp8_peaky_rows_and_fp32_out():
+    wl = workloads.to_fp8_kv(workloads.mid_ragged(seed=2))
+    check(wl)
+    err = check(workloads.to_fp8_kv(workloads.mid_ragged(seed=3)), out_dtype=torch.float32)
+    assert err < 2e-3, err
+
+
+def test_fp8_full_size_long_context_sampled_rows():
+    """The FP8 bench workload (B=4, L=32768, 20 GiB FP8 pool): sampled rows
+    against the oracle on the pages those rows read."""
+    wl = workloads.long_context(seed=0, batch=4, context=32768, device=DEV, kv_fp8=True)
+    attn = make_attn(wl)
+    out = run_gpu(attn, wl)
+    attn.close()
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(1)
+    ks = wl.meta["k_scale"].double().cpu().numpy()
+    vs = wl.meta["v_scale"].double().cpu().numpy()
+    for b in (0, 2):
+        q, k, v, bt, cl = workloads.compact_for_rows(wl, [b])
+        hqs = rng.choice(32, size=6, replace=False)
+        rows = np.array([[0, int(h)] for h in hqs], dtype=np.int32)
+        ref = oracle.paged_decode_kv(q, k, v, bt, cl, oracle.BF16, oracle.FP8_E4M3, wl.scale,
+                                     ks, vs, rows=rows)
+        assert_close(out[b, torch.from_numpy(hqs).to(DEV)], ref, f"fp8 b={b}")
+    del wl
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("kernel", ["cuda_core", "tensor_core"])
+def test_scaled_16bit_caches(kernel, monkeypatch):
+    """Dequantisation scales on bf16 caches (both kernels)."""
+    monkeypatch.setenv("PDA_PARTIAL_KERNEL", kernel)
+    wl = workloads.custom(seed=9, B=3, Hq=32, Hkv=8, D=128, block_size=16, lens=[500, 64, 2000])
+    g = torch.Generator().manual_seed(0)
+    wl.meta["k_scale"] = torch.rand(8, generator=g) * 2 + 0.25
+    wl.meta["v_scale"] = torch.rand(8, generator=g) * 2 + 0.25
+    check(wl)
+    check(wl, num_splits=7)
+
+
+def test_fp8_unsupported_geometries_rejected():
+    from paged_gqa_decode_attention_gb300 import PagedDecodeAttention
+    for kw in (dict(head_dim=64), dict(dtype=torch.float16)):
+        args = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                    dtype=torch.bfloat16)
+        args.update(kw)
+        with pytest.raises(PDAError) as e:
+            PagedDecodeAttention(**args, kv_fp8=True)
+        assert e.value.status == PDA_EUNSUPPORTED
