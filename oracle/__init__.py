@@ -83,6 +83,14 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_paged_decode_kv.restype = i32
     lib.oracle_decode_e4m3_array.argtypes = [P, i64, P]
     lib.oracle_decode_e4m3_array.restype = None
+    lib.oracle_copy_blocks.argtypes = [P, P, i64, i64, P, i64]
+    lib.oracle_copy_blocks.restype = i32
+    lib.oracle_gather_kv.argtypes = [P, P, i64, i32, i64, P, i32, P, i32, P, P]
+    lib.oracle_gather_kv.restype = i32
+    lib.oracle_scatter_kv.argtypes = [P, P, i64, i64, P, P, P, i64]
+    lib.oracle_scatter_kv.restype = i32
+    lib.oracle_remap_table.argtypes = [P, i32, i32, P, i32, P, i64]
+    lib.oracle_remap_table.restype = i32
     lib.oracle_rope_kv_write.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                          i64, i32, P, P, P]
     lib.oracle_rope_kv_write.restype = i32
@@ -293,3 +301,64 @@ def paged_decode_kv(q, k_cache, v_cache, block_table, context_lens, q_dtype: int
                                     _ptr(out), threads or default_threads())
     _check(st, "paged_decode_kv")
     return out
+
+
+def _raw_rows(cache) -> np.ndarray:
+    """Any numpy cache [num_blocks, bs, Hkv, D] as contiguous bytes."""
+    return np.ascontiguousarray(cache).view(np.uint8)
+
+
+def copy_blocks(k_cache, v_cache, pairs, lib=None):
+    """Copies of the caches with block pairs[i][1] := block pairs[i][0]."""
+    lib = lib or load()
+    k = np.array(k_cache, copy=True, order="C")
+    v = np.array(v_cache, copy=True, order="C")
+    nb = k.shape[0]
+    block_bytes = k.nbytes // max(nb, 1)
+    pr = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
+    _check(lib.oracle_copy_blocks(_ptr(k.view(np.uint8)), _ptr(v.view(np.uint8)), nb,
+                                  block_bytes, _ptr(pr), pr.shape[0]), "copy_blocks")
+    return k, v
+
+
+def gather_kv(k_cache, v_cache, block_table, lens, lib=None):
+    """(k_out, v_out) [sum(lens), Hkv, D]: each sequence's tokens in order."""
+    lib = lib or load()
+    k, v = np.ascontiguousarray(k_cache), np.ascontiguousarray(v_cache)
+    nb, bs = k.shape[0], k.shape[1]
+    row_shape = k.shape[2:]
+    row_bytes = k.nbytes // max(nb * bs, 1)
+    bt, cl = _as_i32(block_table), _as_i32(lens)
+    total = int(cl.sum())
+    ko = np.zeros((total,) + row_shape, dtype=k.dtype)
+    vo = np.zeros((total,) + row_shape, dtype=k.dtype)
+    _check(lib.oracle_gather_kv(_ptr(_raw_rows(k)), _ptr(_raw_rows(v)), nb, bs, row_bytes,
+                                _ptr(bt), bt.shape[1], _ptr(cl), cl.shape[0],
+                                _ptr(ko.view(np.uint8)), _ptr(vo.view(np.uint8))), "gather_kv")
+    return ko, vo
+
+
+def scatter_kv(k_rows, v_rows, slot_mapping, k_cache, v_cache, lib=None):
+    """Copies of the caches with row t written to slot slot_mapping[t] (< 0 skipped)."""
+    lib = lib or load()
+    kr, vr = np.ascontiguousarray(k_rows), np.ascontiguousarray(v_rows)
+    k = np.array(k_cache, copy=True, order="C")
+    v = np.array(v_cache, copy=True, order="C")
+    n = kr.shape[0]
+    row_bytes = kr.nbytes // max(n, 1) if n else k.nbytes // max(k.shape[0] * k.shape[1], 1)
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    _check(lib.oracle_scatter_kv(_ptr(kr.view(np.uint8)), _ptr(vr.view(np.uint8)), n, row_bytes,
+                                 _ptr(sm), _ptr(k.view(np.uint8)), _ptr(v.view(np.uint8)),
+                                 k.shape[0] * k.shape[1]), "scatter_kv")
+    return k, v
+
+
+def remap_table(block_table, lens, block_size: int, new_id, lib=None) -> np.ndarray:
+    """A copy of the table with every used entry e replaced by new_id[e]."""
+    lib = lib or load()
+    bt = np.array(block_table, dtype=np.int32, copy=True, order="C")
+    cl = _as_i32(lens)
+    nid = _as_i32(new_id)
+    _check(lib.oracle_remap_table(_ptr(bt), bt.shape[0], bt.shape[1], _ptr(cl), block_size,
+                                  _ptr(nid), nid.shape[0]), "remap_table")
+    return bt

@@ -532,3 +532,93 @@ int oracle_rope_kv_write(const uint16_t* q, const uint16_t* k, const uint16_t* v
   }
   return ORACLE_OK;
 }
+
+/* ---------------------------------------------------------------------------
+ * KV-cache movement (landing page, "Next boundaries": KV-cache movement,
+ * "scheduler-facing block copy, gather, scatter, and compact work for prefix
+ * reuse and preemption"). The pages name the operations only; the readings:
+ * a cache is [num_blocks, block_size, Hkv, D] of any element type, moved as
+ * raw bytes (row_bytes = Hkv * D * element size per token slot), so every
+ * operation is an exact copy.
+ *   copy_blocks: for each pair i, block pairs[2i+1] of both caches becomes a
+ *     copy of block pairs[2i] (destinations distinct and not sources, so the
+ *     order of the pairs does not matter);
+ *   gather: the tokens t < lens[b] of each sequence, in order, through its
+ *     block table, into a contiguous [sum(lens), row] buffer (sequence b
+ *     starts at row lens[0] + ... + lens[b-1]);
+ *   scatter: contiguous rows into the cache slots slot_mapping[t] (slot =
+ *     block * block_size + offset; negative = skip);
+ *   remap_table: table[b, p] = new_id[table[b, p]] for the pages p <
+ *     ceil(lens[b] / block_size) a sequence uses (compaction's table update).
+ * ------------------------------------------------------------------------- */
+int oracle_copy_blocks(uint8_t* k_cache, uint8_t* v_cache, int64_t num_blocks,
+                       int64_t block_bytes, const int64_t* pairs, int64_t n_pairs) {
+  if (!k_cache || !v_cache || num_blocks < 0 || block_bytes < 0 || n_pairs < 0)
+    return ORACLE_EINVAL;
+  if (n_pairs > 0 && !pairs) return ORACLE_EINVAL;
+  for (int64_t i = 0; i < n_pairs; ++i) {
+    int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) return ORACLE_ERANGE;
+    for (int64_t j = 0; j < block_bytes; ++j) {
+      k_cache[dst * block_bytes + j] = k_cache[src * block_bytes + j];
+      v_cache[dst * block_bytes + j] = v_cache[src * block_bytes + j];
+    }
+  }
+  return ORACLE_OK;
+}
+
+int oracle_gather_kv(const uint8_t* k_cache, const uint8_t* v_cache, int64_t num_blocks,
+                     int block_size, int64_t row_bytes, const int32_t* block_table,
+                     int max_blocks, const int32_t* lens, int B, uint8_t* k_out,
+                     uint8_t* v_out) {
+  if (!k_cache || !v_cache || !block_table || !lens || !k_out || !v_out) return ORACLE_EINVAL;
+  if (block_size < 1 || row_bytes < 0 || B < 0 || max_blocks < 0) return ORACLE_EINVAL;
+  int64_t row = 0;
+  for (int b = 0; b < B; ++b) {
+    if (lens[b] < 0 || (int64_t)lens[b] > (int64_t)max_blocks * block_size) return ORACLE_ERANGE;
+    for (int t = 0; t < lens[b]; ++t) {
+      int32_t blk = block_table[(int64_t)b * max_blocks + t / block_size];
+      if (blk < 0 || blk >= num_blocks) return ORACLE_ERANGE;
+      int64_t slot = (int64_t)blk * block_size + t % block_size;
+      for (int64_t j = 0; j < row_bytes; ++j) {
+        k_out[row * row_bytes + j] = k_cache[slot * row_bytes + j];
+        v_out[row * row_bytes + j] = v_cache[slot * row_bytes + j];
+      }
+      ++row;
+    }
+  }
+  return ORACLE_OK;
+}
+
+int oracle_scatter_kv(const uint8_t* k_in, const uint8_t* v_in, int64_t n_rows,
+                      int64_t row_bytes, const int64_t* slot_mapping, uint8_t* k_cache,
+                      uint8_t* v_cache, int64_t num_slots) {
+  if (!k_in || !v_in || !slot_mapping || !k_cache || !v_cache || n_rows < 0 || row_bytes < 0)
+    return ORACLE_EINVAL;
+  for (int64_t t = 0; t < n_rows; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= num_slots) return ORACLE_ERANGE;
+    for (int64_t j = 0; j < row_bytes; ++j) {
+      k_cache[slot * row_bytes + j] = k_in[t * row_bytes + j];
+      v_cache[slot * row_bytes + j] = v_in[t * row_bytes + j];
+    }
+  }
+  return ORACLE_OK;
+}
+
+int oracle_remap_table(int32_t* block_table, int B, int max_blocks, const int32_t* lens,
+                       int block_size, const int32_t* new_id, int64_t num_blocks) {
+  if (!block_table || !lens || !new_id || B < 0 || max_blocks < 0 || block_size < 1)
+    return ORACLE_EINVAL;
+  for (int b = 0; b < B; ++b) {
+    int pages = (lens[b] + block_size - 1) / block_size;
+    if (lens[b] < 0 || pages > max_blocks) return ORACLE_ERANGE;
+    for (int p = 0; p < pages; ++p) {
+      int32_t* e = block_table + (int64_t)b * max_blocks + p;
+      if (*e < 0 || *e >= num_blocks) return ORACLE_ERANGE;
+      *e = new_id[*e];
+    }
+  }
+  return ORACLE_OK;
+}

@@ -501,7 +501,99 @@ def pin_fp8_kv_equals_dequantised_bf16(lib):
     np.testing.assert_array_equal(got, ref)
 
 
+# ---------------------------------------------------------------------------
+# KV-cache movement
+# ---------------------------------------------------------------------------
+
+def _kv_problem(seed):
+    d = Dense(seed, B=3, Hq=4, Hkv=2, D=8, bs=4, lens=[5, 12, 1], spare_blocks=9)
+    d.kc, d.vc, d.q_bits = _bits(d.k_cache), _bits(d.v_cache), _bits(d.q)
+    return d
+
+
+def pin_gather_matches_attention_addressing(lib):
+    """Gathered rows are the tokens attention reads: decode attention over
+    the gathered contiguous K/V (as a cache of 1-token blocks with an
+    identity table) equals decode attention over the paged cache, bit for
+    bit in FP64; the gathered K equals the dense K the pages were built from."""
+    d = _kv_problem(31)
+    kg, vg = oracle.gather_kv(d.kc, d.vc, d.table, d.lens, lib=lib)
+    total = int(d.lens.sum())
+    assert kg.shape[0] == total
+    off = np.concatenate([[0], np.cumsum(d.lens)[:-1]])
+    for b in range(d.B):
+        np.testing.assert_array_equal(kg[off[b]:off[b] + d.lens[b]], _bits(d.k[b, : d.lens[b]]))
+        np.testing.assert_array_equal(vg[off[b]:off[b] + d.lens[b]], _bits(d.v[b, : d.lens[b]]))
+    t1 = np.zeros((d.B, int(d.lens.max())), dtype=np.int32)
+    for b in range(d.B):
+        t1[b, : d.lens[b]] = off[b] + np.arange(d.lens[b])
+    ref = oracle.paged_decode(d.q_bits, d.kc, d.vc, d.table, d.lens, BF16, 0.3, lib=lib)
+    got = oracle.paged_decode(d.q_bits, kg.reshape(total, 1, d.Hkv, d.D),
+                              vg.reshape(total, 1, d.Hkv, d.D), t1, d.lens, BF16, 0.3, lib=lib)
+    np.testing.assert_array_equal(got, ref)
+
+
+def pin_scatter_then_gather_roundtrip(lib):
+    """Rows scattered into the slots a block table names come back unchanged
+    from a gather through that table; padding rows (slot -1) write nothing;
+    slots nobody names keep their bytes."""
+    rng = np.random.default_rng(5)
+    nb, bs, Hkv, D = 12, 4, 2, 8
+    lens = np.array([6, 9], dtype=np.int32)
+    table = rng.permutation(nb)[:6].reshape(2, 3).astype(np.int32)
+    slots = np.concatenate([table[b, np.arange(L) // bs] * bs + np.arange(L) % bs
+                            for b, L in enumerate(lens)]).astype(np.int64)
+    rows = rng.integers(0, 65535, size=(slots.size, Hkv, D)).astype(np.uint16)
+    rows_v = rng.integers(0, 65535, size=(slots.size, Hkv, D)).astype(np.uint16)
+    pad_rows = np.concatenate([rows, rows[:1] ^ 1])
+    pad_v = np.concatenate([rows_v, rows_v[:1] ^ 1])
+    pad_slots = np.concatenate([slots, [-1]])
+    k0 = rng.integers(0, 65535, size=(nb, bs, Hkv, D)).astype(np.uint16)
+    v0 = rng.integers(0, 65535, size=(nb, bs, Hkv, D)).astype(np.uint16)
+    k1, v1 = oracle.scatter_kv(pad_rows, pad_v, pad_slots, k0, v0, lib=lib)
+    kg, vg = oracle.gather_kv(k1, v1, table, lens, lib=lib)
+    np.testing.assert_array_equal(kg, rows)
+    np.testing.assert_array_equal(vg, rows_v)
+    untouched = np.ones(nb * bs, dtype=bool)
+    untouched[slots] = False
+    np.testing.assert_array_equal(k1.reshape(nb * bs, Hkv, D)[untouched],
+                                  k0.reshape(nb * bs, Hkv, D)[untouched])
+    np.testing.assert_array_equal(v1.reshape(nb * bs, Hkv, D)[untouched],
+                                  v0.reshape(nb * bs, Hkv, D)[untouched])
+
+
+def pin_compaction_preserves_attention(lib):
+    """Compaction: copy every used block to a free block, remap the table
+    through the same old -> new map; attention over the moved cache equals
+    attention over the original bit for bit, blocks not written keep their
+    bytes, and an empty pair list or remapping through the identity changes
+    nothing."""
+    d = _kv_problem(41)
+    used = sorted({int(x) for b in range(d.B)
+                   for x in d.table[b, : (int(d.lens[b]) + d.bs - 1) // d.bs]})
+    free = [i for i in range(d.kc.shape[0]) if i not in used]
+    assert len(free) >= len(used)
+    pairs = np.array([[u, free[i]] for i, u in enumerate(used)], dtype=np.int64)
+    k1, v1 = oracle.copy_blocks(d.kc, d.vc, pairs, lib=lib)
+    new_id = np.arange(d.kc.shape[0], dtype=np.int32)
+    new_id[pairs[:, 0]] = pairs[:, 1]
+    t1 = oracle.remap_table(d.table, d.lens, d.bs, new_id, lib=lib)
+    ref = oracle.paged_decode(d.q_bits, d.kc, d.vc, d.table, d.lens, BF16, 0.2, lib=lib)
+    got = oracle.paged_decode(d.q_bits, k1, v1, t1, d.lens, BF16, 0.2, lib=lib)
+    np.testing.assert_array_equal(got, ref)
+    written = set(int(x) for x in pairs[:, 1])
+    for i in range(d.kc.shape[0]):
+        if i not in written:
+            np.testing.assert_array_equal(k1[i], d.kc[i])
+            np.testing.assert_array_equal(v1[i], d.vc[i])
+    k2, v2 = oracle.copy_blocks(d.kc, d.vc, np.zeros((0, 2), dtype=np.int64), lib=lib)
+    np.testing.assert_array_equal(k2, d.kc)
+    np.testing.assert_array_equal(
+        oracle.remap_table(d.table, d.lens, d.bs, np.arange(d.kc.shape[0]), lib=lib), d.table)
+
+
 ALL_PINS = [pin_brute_force, pin_closed_forms, pin_block_table_invariance, pin_gqa_reductions,
             pin_split_merge, pin_merge_special_cases, pin_dtype_conversions,
             pin_rope_complex_form, pin_rope_exact_turns, pin_e4m3_decode,
-            pin_fp8_kv_equals_dequantised_bf16]
+            pin_fp8_kv_equals_dequantised_bf16, pin_gather_matches_attention_addressing,
+            pin_scatter_then_gather_roundtrip, pin_compaction_preserves_attention]

@@ -46,6 +46,14 @@ MUTANTS = {
     "kv_scale_wrong_head": ("return head_scale ? x * head_scale[h] : x;",
                             "return head_scale ? x * head_scale[(h + 1) % p->Hkv] : x;"),
     "k_uses_v_scale": ("kv_value(p, p->k_cache, p->k_scale", "kv_value(p, p->k_cache, p->v_scale"),
+    "copy_direction": ("k_cache[dst * block_bytes + j] = k_cache[src * block_bytes + j];",
+                       "k_cache[src * block_bytes + j] = k_cache[dst * block_bytes + j];"),
+    "gather_page_index": ("int32_t blk = block_table[(int64_t)b * max_blocks + t / block_size];",
+                          "int32_t blk = block_table[(int64_t)b * max_blocks + t % block_size];"),
+    "gather_no_advance": ("      ++row;\n", "\n"),
+    "scatter_writes_padding": ("    if (slot < 0) continue;\n    if (slot >= num_slots)",
+                               "    if (slot < 0) slot = 0;\n    if (slot >= num_slots)"),
+    "remap_by_position": ("*e = new_id[*e];", "*e = new_id[p];"),
     "rope_second_sign": ("double yb = xb * c + xa * s;", "double yb = xb * c - xa * s;"),
     "rope_first_sign": ("double ya = xa * c - xb * s;", "double ya = xa * c + xb * s;"),
     "rope_neox_pairing": ("int b = neox ? j + half : 2 * j + 1;",
