@@ -62,6 +62,10 @@ def make_workload(name: str, seed: int, device):
         return W.long_context(seed=seed, batch=4, context=32768, device=device)
     if name == "long_b4_l32768_pool1g":  # same step over a 1 GiB pool (for ncu captures)
         return W.long_context(seed=seed, batch=4, context=32768, num_blocks=16384, device=device)
+    if name == "long_b4_l32768_fp8":  # the headline step with an FP8 (E4M3) K/V cache
+        return W.long_context(seed=seed, batch=4, context=32768, device=device, kv_fp8=True)
+    if name == "long_b8_l32768_fp8":  # FP8 cache, the headline's KV bytes per step
+        return W.long_context(seed=seed, batch=8, context=32768, device=device, kv_fp8=True)
     if name == "long_b1_l32768":
         return W.long_context(seed=seed, batch=1, context=32768, device=device)
     if name == "long_b4_l8192":
@@ -112,6 +116,12 @@ ROPE_WORKLOADS = {
                                 mode="prefill"),
 }
 ROPE_METRIC = "RoPE + paged-KV write tokens/s and HBM GB/s (% of GB300 peak), 1 GPU"
+
+# KV-cache movement workloads (32/8/128 bf16 caches, block 16, 40 GiB pool):
+# gather the headline step's 4 x 32768 tokens into contiguous rows; copy
+# 4096 random blocks to other blocks; scatter 32768 rows into random slots.
+MOVE_WORKLOADS = ("move_gather_b4_l32768", "move_copy_blocks_4096", "move_scatter_t32768")
+MOVE_METRIC = "KV-cache movement GB/s moved (read + write, % of GB300 peak), 1 GPU"
 
 
 # ---------------------------------------------------------------------------
@@ -234,6 +244,19 @@ def measured_peaks() -> tuple[float, str]:
 # CPU baseline: the FP64 oracle on a bounded sample
 # ---------------------------------------------------------------------------
 
+def _oracle_rows(wl, q, k, v, bt, cl, rows, threads):
+    """The oracle on rows (b, hq) of host arrays from compact_for_rows."""
+    import oracle
+    dt = oracle.BF16 if wl.q.dtype == torch.bfloat16 else oracle.FP16
+    if wl.kv_fp8 or "k_scale" in wl.meta:
+        ks, vs = wl.meta.get("k_scale"), wl.meta.get("v_scale")
+        return oracle.paged_decode_kv(
+            q, k, v, bt, cl, dt, oracle.FP8_E4M3 if wl.kv_fp8 else dt, wl.scale,
+            None if ks is None else ks.double().cpu().numpy(),
+            None if vs is None else vs.double().cpu().numpy(), rows=rows, threads=threads)
+    return oracle.paged_decode_rows(q, k, v, bt, cl, dt, wl.scale, rows, threads=threads)
+
+
 def oracle_sample(wl, target_s: float = 10.0):
     """Time the FP64 oracle on whole sequences of ``wl`` (all query heads of
     every sequence, passes repeated until about ``target_s`` of wall time).
@@ -248,7 +271,7 @@ def oracle_sample(wl, target_s: float = 10.0):
     passes, elapsed = 0, 0.0
     while elapsed < target_s and passes < 1000:
         t0 = time.perf_counter()
-        oracle.paged_decode_rows(q, k, v, bt, cl, dt, wl.scale, rows, threads=threads)
+        _oracle_rows(wl, q, k, v, bt, cl, rows, threads)
         elapsed += time.perf_counter() - t0
         passes += 1
     seqs = passes * q.shape[0]
@@ -270,10 +293,10 @@ def run_reference(args):
     if dev.type == "cpu" and args.workload.startswith("long_"):
         # without a GPU, draw the same shapes over a pool just large enough
         from paged_gqa_decode_attention_gb300 import workloads as W
-        B = 4 if "_b4_" in args.workload else 1
-        L = int(args.workload.split("_l")[-1])
+        B = 8 if "_b8_" in args.workload else (4 if "_b4_" in args.workload else 1)
+        L = int(args.workload.split("_l")[-1].split("_")[0])
         wl = W.long_context(seed=args.seed, batch=B, context=L,
-                            num_blocks=B * (L // 16) + 64)
+                            num_blocks=B * (L // 16) + 64, kv_fp8="fp8" in args.workload)
     else:
         wl = make_workload(args.workload, args.seed, dev)
     import oracle
@@ -283,10 +306,10 @@ def run_reference(args):
     q, k, v, bt, cl = W.compact_for_rows(wl, [0])
     rows = np.array([[0, h] for h in range(q.shape[1])], dtype=np.int32)
     for _ in range(args.warmup):
-        oracle.paged_decode_rows(q, k, v, bt, cl, dt, wl.scale, rows, threads=threads)
+        _oracle_rows(wl, q, k, v, bt, cl, rows, threads)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.paged_decode_rows(q, k, v, bt, cl, dt, wl.scale, rows, threads=threads)
+        _oracle_rows(wl, q, k, v, bt, cl, rows, threads)
     el = time.perf_counter() - t0
     value = args.steps / el  # one sequence (all query heads) per step
     sample = (f"per step: sequence 0 (all {q.shape[1]} query heads, {int(cl[0])} tokens) of "
@@ -322,7 +345,8 @@ def run_ours(args):
     B, Hq, D = wl.batch, wl.num_q_heads, wl.head_dim
     attn = PagedDecodeAttention(Hq, wl.num_kv_heads, D, wl.block_size, wl.q.dtype,
                                 max_batch=B, max_blocks_per_seq=wl.max_blocks, max_splits=64,
-                                device=dev)
+                                device=dev, kv_fp8=wl.kv_fp8)
+    ksc, vsc = wl.meta.get("k_scale"), wl.meta.get("v_scale")
     out = torch.empty((B, Hq, D), dtype=wl.q.dtype, device=dev)
     kv_bytes = wl.kv_bytes()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -337,7 +361,7 @@ def run_ours(args):
 
     def step():
         attn.run(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.context_lens, wl.scale, out=out,
-                 num_splits=args.splits)
+                 num_splits=args.splits, k_scale=ksc, v_scale=vsc)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -429,7 +453,8 @@ def run_ours(args):
         q_d.copy_(q_h, non_blocking=True)
         bt_d.copy_(bt_h, non_blocking=True)
         cl_d.copy_(cl_h, non_blocking=True)
-        attn.run(q_d, wl.k_cache, wl.v_cache, bt_d, cl_d, wl.scale, out=out, num_splits=args.splits)
+        attn.run(q_d, wl.k_cache, wl.v_cache, bt_d, cl_d, wl.scale, out=out, num_splits=args.splits,
+                 k_scale=ksc, v_scale=vsc)
         out_h.copy_(out, non_blocking=True)
         stream.synchronize()
     e2e_s = reduce_max(time.perf_counter() - t0, dev)
@@ -441,7 +466,8 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": timed_ms_max / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 q / fp8-e4m3 kv" if wl.kv_fp8 else "bf16",
         "data": "synthetic",
         "config": {"workload": args.workload, "desc": WORKLOAD_DESC.get(args.workload, ""),
                    "batch_per_gpu": B, "global_batch": B * world,
@@ -640,6 +666,93 @@ def run_rope(args):
     return 0
 
 
+def run_move(args):
+    """One step = one KV-cache movement call (gather, block copy or scatter)."""
+    from paged_gqa_decode_attention_gb300 import build as pda_build
+    from paged_gqa_decode_attention_gb300 import copy_blocks, gather_kv, scatter_kv
+    from paged_gqa_decode_attention_gb300 import workloads as W
+    world, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pda_build.build()
+    wl = W.long_context(seed=args.seed, batch=4, context=32768, device=dev)
+    nb, bs = wl.k_cache.shape[0], wl.block_size
+    row_bytes = wl.num_kv_heads * wl.head_dim * 2
+    rng = np.random.default_rng(args.seed)
+    if args.workload == "move_gather_b4_l32768":
+        lens = wl.context_lens
+        cu = (torch.cumsum(lens.to(torch.int64), 0) - lens.to(torch.int64))
+        total = int(lens.sum())
+        ko = torch.empty((total, wl.num_kv_heads, wl.head_dim), dtype=torch.bfloat16, device=dev)
+        vo = torch.empty_like(ko)
+        max_len = int(lens.max())
+
+        def step():
+            gather_kv(wl.k_cache, wl.v_cache, wl.block_table, lens, cu, max_len, ko, vo)
+        units, unit, moved = total, "tokens/s", 2 * 2 * total * row_bytes
+    elif args.workload == "move_copy_blocks_4096":
+        perm = rng.permutation(nb)[: 2 * 4096].reshape(4096, 2)
+        pairs = torch.from_numpy(perm.astype(np.int64)).to(dev)
+
+        def step():
+            copy_blocks(wl.k_cache, wl.v_cache, pairs)
+        units, unit, moved = 4096, "blocks/s", 2 * 2 * 4096 * bs * row_bytes
+    else:
+        n = 32768
+        rows_k = torch.randn((n, wl.num_kv_heads, wl.head_dim), device=dev).to(torch.bfloat16)
+        rows_v = torch.randn_like(rows_k)
+        slots = torch.from_numpy(rng.permutation(nb * bs)[:n].astype(np.int64)).to(dev)
+
+        def step():
+            scatter_kv(rows_k, rows_v, slots, wl.k_cache, wl.v_cache)
+        units, unit, moved = n, "tokens/s", 2 * 2 * n * row_bytes
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    n_inner = max(d for d in range(1, min(args.steps, 100) + 1) if args.steps % d == 0)
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        for _ in range(n_inner):
+            step()
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with sampler:
+        e0.record(stream)
+        for _ in range(args.steps // n_inner):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    peak, peak_kind = measured_peaks()
+    achieved = moved / (ms / 1e3) / 1e9
+    line = {
+        "metric": MOVE_METRIC, "value": units / (ms / 1e3), "unit": unit, "n_gpus": 1,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bytes",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "bytes_moved_per_step": moved,
+                   "l2": "inputs larger than L2 (>= 2x L2 per step, no flush)",
+                   "timing": f"CUDA graph of {n_inner} calls replayed {args.steps // n_inner}x"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_kind} (hbm_gbs)", "per_launch_ms": ms},
+        "gpu_launches": args.steps, "clocks": sampler.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -654,6 +767,12 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.workload in ROPE_WORKLOADS:
         return run_rope(args)
+    if args.workload in MOVE_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "KV-cache movement has no timed oracle arm (byte copies)"}))
+            return 0
+        return run_move(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

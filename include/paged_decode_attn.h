@@ -200,7 +200,8 @@ int paged_decode_attn_validate(pda_handle handle, const int32_t* block_table,
  * *code receives 0 (no error) or a nonzero code:
  *   1 = context length out of range, 2 = block id out of range (validator);
  *   3 = a pipeline wait inside a kernel gave up after its time limit.
- * (Codes 4 and 5 belong to paged_decode_attn_rope_kv_write's own error word.)
+ * (Codes 4 and 5 belong to the error words of paged_decode_attn_rope_kv_write and of
+ * the KV-cache movement calls.)
  * *detail receives the sequence index (codes 1, 2) or the split index (3).
  * Returns PDA_OK, or PDA_ECUDA if the synchronisation or the copy failed. */
 int paged_decode_attn_check_device_error(pda_handle handle, int* code, int* detail,
@@ -253,6 +254,57 @@ int paged_decode_attn_rope_kv_write(const void* q, int64_t q_token_stride, const
                                     int head_dim, int dtype, void* q_out,
                                     int64_t q_out_token_stride, void* k_cache, void* v_cache,
                                     int64_t num_slots, int* err, int device, void* stream);
+
+/* KV-cache movement (landing page, "Next boundaries": KV-cache movement -
+ * block copy, gather, scatter and compact work for prefix reuse and
+ * preemption). Caches are [num_blocks, block_size, Hkv, D] of any element
+ * type and are moved as raw bytes, so results are exact copies. All pointers
+ * are device memory, calls are asynchronous on `stream`, allocate nothing
+ * and may be captured in a CUDA graph. `err` is an optional device int[2]
+ * (NULL = none) that receives the first out-of-range id found: code 1
+ * (a length above max_len), 2 (a block id outside [0, num_blocks)) or 5 (a
+ * slot past the cache), and its index; such entries are skipped, never
+ * dereferenced. Sizes in bytes must be multiples of 16 and buffers 16-byte
+ * aligned (index arrays: their element size). */
+
+/* For i < n_pairs (<= 65535): block pairs[2i+1] of k_cache and of v_cache
+ * becomes a copy of block pairs[2i] (int64 pairs). block_bytes =
+ * block_size * Hkv * D * element size. Destinations must be distinct and
+ * must not also be sources (then the pairs' order does not matter; a
+ * compaction's moves into free blocks satisfy this). */
+int paged_decode_attn_copy_blocks(void* k_cache, void* v_cache, int64_t num_blocks,
+                                  int64_t block_bytes, const int64_t* pairs, int n_pairs,
+                                  int* err, int device, void* stream);
+
+/* Gather: for each sequence b < batch (<= 65535), its tokens t < lens[b]
+ * (int32; read through block_table [batch, max_blocks] int32) are copied in
+ * order to rows cu_rows[b] + t of k_out / v_out ([rows, Hkv, D], row_bytes =
+ * Hkv * D * element size each); cu_rows [batch] int64 holds each sequence's
+ * first row (e.g. exclusive prefix sums of lens), and the outputs must hold
+ * every row it implies. max_len >= every lens[b] (<= max_blocks *
+ * block_size) sizes the grid; a longer length is flagged (code 1) and cut. */
+int paged_decode_attn_gather_kv(const void* k_cache, const void* v_cache, int64_t num_blocks,
+                                int block_size, int64_t row_bytes, const int32_t* block_table,
+                                int max_blocks, const int32_t* lens, const int64_t* cu_rows,
+                                int batch, int max_len, void* k_out, void* v_out, int* err,
+                                int device, void* stream);
+
+/* Scatter: row r < n_rows of k_rows / v_rows ([n_rows, Hkv, D], row_bytes
+ * each) is copied to cache slot slot_mapping[r] (int64; slot = block *
+ * block_size + offset, num_slots = num_blocks * block_size); slot < 0 skips
+ * the row. Two rows with the same slot race. */
+int paged_decode_attn_scatter_kv(const void* k_rows, const void* v_rows, int64_t n_rows,
+                                 int64_t row_bytes, const int64_t* slot_mapping, void* k_cache,
+                                 void* v_cache, int64_t num_slots, int* err, int device,
+                                 void* stream);
+
+/* In place: block_table[b, p] := new_id[block_table[b, p]] for b < batch and
+ * the pages p < ceil(lens[b] / block_size) a sequence uses (entries past
+ * them are left alone); new_id has num_blocks int32 entries. With
+ * copy_blocks this is a compaction: move the live blocks, then remap. */
+int paged_decode_attn_remap_table(int32_t* block_table, int batch, int max_blocks,
+                                  const int32_t* lens, int block_size, const int32_t* new_id,
+                                  int64_t num_blocks, int* err, int device, void* stream);
 
 /* Decode attention for callers that cannot allocate device memory.
  * (No counterpart in the paper: this entry point exists for integration.)

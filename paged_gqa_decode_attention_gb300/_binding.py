@@ -41,6 +41,10 @@ EXPORTS = [
     "paged_decode_attn_check_device_error",
     "paged_decode_attn_run_noalloc",
     "paged_decode_attn_rope_kv_write",
+    "paged_decode_attn_copy_blocks",
+    "paged_decode_attn_gather_kv",
+    "paged_decode_attn_scatter_kv",
+    "paged_decode_attn_remap_table",
 ]
 
 
@@ -106,6 +110,15 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                                         I, I, I, I, I, P, I64, P, P, I64, P, I,
                                                         P]
         lib.paged_decode_attn_rope_kv_write.restype = I
+        lib.paged_decode_attn_copy_blocks.argtypes = [P, P, I64, I64, P, I, P, I, P]
+        lib.paged_decode_attn_copy_blocks.restype = I
+        lib.paged_decode_attn_gather_kv.argtypes = [P, P, I64, I, I64, P, I, P, P, I, I, P, P, P,
+                                                    I, P]
+        lib.paged_decode_attn_gather_kv.restype = I
+        lib.paged_decode_attn_scatter_kv.argtypes = [P, P, I64, I64, P, P, P, I64, P, I, P]
+        lib.paged_decode_attn_scatter_kv.restype = I
+        lib.paged_decode_attn_remap_table.argtypes = [P, I, I, P, I, P, I64, P, I, P]
+        lib.paged_decode_attn_remap_table.restype = I
         if lib.paged_decode_attn_abi_version() != ABI_VERSION:
             raise RuntimeError("ABI version mismatch between binding and library")
         if path is None:
@@ -334,3 +347,88 @@ def rope_kv_write(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, positions: 
         _dev_ptr(err, "err", torch.int32) if err is not None else None, dev,
         _stream_ptr(stream)))
     return q_out
+
+
+# ------------------------------ KV-cache movement ------------------------------
+
+def _cache_geometry(k_cache: torch.Tensor, v_cache: torch.Tensor):
+    if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype or k_cache.dim() != 4:
+        raise ValueError("k_cache and v_cache must be [num_blocks, block_size, Hkv, D] alike")
+    nb, bs = k_cache.shape[0], k_cache.shape[1]
+    row_bytes = k_cache.shape[2] * k_cache.shape[3] * k_cache.element_size()
+    return nb, bs, row_bytes
+
+
+def _opt_err(err):
+    return _dev_ptr(err, "err", torch.int32) if err is not None else None
+
+
+def _device_of(t: torch.Tensor) -> int:
+    return t.device.index if t.device.index is not None else torch.cuda.current_device()
+
+
+def copy_blocks(k_cache, v_cache, pairs: torch.Tensor, err=None, stream=None):
+    """Block pairs[i, 1] := block pairs[i, 0] in both caches (in place);
+    pairs is an int64 [n, 2] device tensor."""
+    lib = load_library()
+    nb, bs, row_bytes = _cache_geometry(k_cache, v_cache)
+    n = pairs.shape[0] if pairs.numel() else 0
+    _check(lib, lib.paged_decode_attn_copy_blocks(
+        _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), nb, bs * row_bytes,
+        _dev_ptr(pairs, "pairs", torch.int64) if n else None, n, _opt_err(err),
+        _device_of(k_cache), _stream_ptr(stream)))
+
+
+def gather_kv(k_cache, v_cache, block_table, lens, cu_rows=None, max_len: int | None = None,
+              k_out=None, v_out=None, err=None, stream=None):
+    """Each sequence's tokens, in order, into contiguous [rows, Hkv, D] buffers
+    (sequence b from row cu_rows[b]; default: exclusive prefix sums of lens,
+    computed on the host from lens). Returns (k_out, v_out)."""
+    lib = load_library()
+    nb, bs, row_bytes = _cache_geometry(k_cache, v_cache)
+    B = lens.shape[0]
+    if cu_rows is None or max_len is None or k_out is None:
+        lens_h = lens.cpu().to(torch.int64)
+        if cu_rows is None:
+            cu_rows = (torch.cumsum(lens_h, 0) - lens_h).to(k_cache.device)
+        if max_len is None:
+            max_len = int(lens_h.max()) if B else 0
+        total = int(lens_h.sum())
+    else:
+        total = k_out.shape[0]
+    shape = (total,) + tuple(k_cache.shape[2:])
+    if k_out is None:
+        k_out = torch.empty(shape, dtype=k_cache.dtype, device=k_cache.device)
+        v_out = torch.empty(shape, dtype=k_cache.dtype, device=k_cache.device)
+    _check(lib, lib.paged_decode_attn_gather_kv(
+        _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), nb, bs, row_bytes,
+        _dev_ptr(block_table, "block_table", torch.int32), block_table.shape[1],
+        _dev_ptr(lens, "lens", torch.int32), _dev_ptr(cu_rows, "cu_rows", torch.int64), B,
+        int(max_len), _dev_ptr(k_out, "k_out"), _dev_ptr(v_out, "v_out"), _opt_err(err),
+        _device_of(k_cache), _stream_ptr(stream)))
+    return k_out, v_out
+
+
+def scatter_kv(k_rows, v_rows, slot_mapping, k_cache, v_cache, err=None, stream=None):
+    """Row r of k_rows / v_rows ([n, Hkv, D]) into cache slot slot_mapping[r]
+    (int64; < 0 skips), in place."""
+    lib = load_library()
+    nb, bs, row_bytes = _cache_geometry(k_cache, v_cache)
+    if k_rows.dtype != k_cache.dtype or v_rows.dtype != k_cache.dtype:
+        raise ValueError("rows and caches must share a dtype")
+    n = k_rows.shape[0]
+    _check(lib, lib.paged_decode_attn_scatter_kv(
+        _dev_ptr(k_rows, "k_rows"), _dev_ptr(v_rows, "v_rows"), n, row_bytes,
+        _dev_ptr(slot_mapping, "slot_mapping", torch.int64), _dev_ptr(k_cache, "k_cache"),
+        _dev_ptr(v_cache, "v_cache"), nb * bs, _opt_err(err), _device_of(k_cache),
+        _stream_ptr(stream)))
+
+
+def remap_table(block_table, lens, block_size: int, new_id, err=None, stream=None):
+    """In place: every used entry e of block_table becomes new_id[e]."""
+    lib = load_library()
+    _check(lib, lib.paged_decode_attn_remap_table(
+        _dev_ptr(block_table, "block_table", torch.int32), block_table.shape[0],
+        block_table.shape[1], _dev_ptr(lens, "lens", torch.int32), int(block_size),
+        _dev_ptr(new_id, "new_id", torch.int32), new_id.shape[0], _opt_err(err),
+        _device_of(block_table), _stream_ptr(stream)))
