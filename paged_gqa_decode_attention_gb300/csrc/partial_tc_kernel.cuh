@@ -13,32 +13,40 @@
 // run on the tensor cores, with the G query rows packed as the N side:
 //
 //   S^T [128 tokens x 16]  = K_chunk [128 x 128 dims] . Q^T [128 dims x 16]
-//   O^T [128 dims   x 16]  = V_chunk^T [128 dims x 128 tokens] . P^T [128 x 16]
+//   O^T [128 dims   x 32]  = V_chunk^T [128 dims x 128 tokens] . [P_hi; P_lo]^T
 //
-// (rows G..15 of Q and P are zero; at D = 64 the QK^T contraction is 64
-// deep and the upper 64 dims of every V slot are zero, so O^T rows 64..127
-// come out zero). Both are M=128, N=16 tcgen05.mma
-// (kind::f16, fp32 accumulate in TMEM) issued by one thread; the K and V
-// tiles are consumed straight from the TMA-written, 128-byte-swizzled stage:
-// K as a K-major A operand, V as an MN-major A operand. The probabilities P
-// are written to shared memory as two bf16 (or fp16) operands, hi = rn(p) and
-// lo = rn(p - hi), both multiplied into O, so P keeps about 16 significant
-// bits (one 8-bit operand would cost up to 2^-9 relative error per weight).
+// (rows G..15 of each 16-row block of Q and P are zero; at D = 64 the QK^T
+// contraction is 64 deep and the upper 64 dims of every V slot are zero, so
+// O^T rows 64..127 come out zero). Both are M=128 tcgen05.mma (kind::f16,
+// fp32 accumulate in TMEM) issued by one thread; the K and V tiles are
+// consumed straight from the TMA-written, 128-byte-swizzled stage: K as a
+// K-major A operand, V as an MN-major A operand. The probabilities P are
+// written to shared memory as two bf16 (or fp16) terms, hi = rn(p) and
+// lo = rn(p - hi), stacked as one 32-row operand so a single MMA multiplies
+// both into O (columns g and 16 + g, added by the softmax); P keeps about
+// 16 significant bits (one 8-bit operand would cost up to 2^-9 relative
+// error per weight). At these small N the tensor pipe's cost is per
+// instruction, so stacking the terms halves the PV instructions.
 //
-// Warp roles (192 threads):
-//   warps 0-3: softmax and epilogue. Thread t reads TMEM lane t of S (token t
-//     of the chunk), scales and masks it, joins a CTA-wide max per head
-//     (shuffles + shared memory), writes p_hi/p_lo and, for tokens past the
-//     context, zeroes that token's V row (so 0 * stale data never enters the
-//     MMA); then reads TMEM lane t of O (dim t) and folds it into a running
-//     fp32 accumulator with the online-softmax rescale.
+// Warp roles (480 threads):
+//   warps 0-3 and 11-14: softmax, two groups of four that split the G query
+//     heads' columns (group 0 the first ceil(G/2), group 1 the rest; G = 1
+//     uses one group). Thread t of a group reads TMEM lane t of S (token t of
+//     the chunk) for its columns, scales and masks it, joins a CTA-wide max
+//     per head (shuffles + shared memory), writes p_hi/p_lo and, in group 0,
+//     zeroes the V rows of tokens past the context (so 0 * stale data never
+//     enters the MMA); then reads TMEM lane t of O (dim t) for its columns
+//     and folds it into a running fp32 accumulator with the online-softmax
+//     rescale. The two groups run the same chunk side by side.
 //   warps 4 and 5: producers, TMA page loads of K and of V into two separate
 //     3-slot rings (a slot is 128 tokens, 32 KiB): a K slot is released as
 //     soon as its QK^T completes, a V slot after its PV, so K loads run ahead.
 //     The K producer also loads each unit's G query rows (a TMA box) into one
 //     of two Q operand buffers.
-//   warp 6: allocates 64 TMEM columns (S0, S1, O0, O1, 16 each), issues the
-//     MMAs and commits their completion to mbarriers.
+//   warp 6: allocates 256 TMEM columns (S and O, double-buffered), issues
+//     the MMAs and commits their completion to mbarriers. The terms of a
+//     split operand (P_hi / P_lo; with FP8, q_hi / q_lo and the three P
+//     terms) are stacked along N, so each contraction step is one MMA.
 // S, O and P are double-buffered by chunk parity so the chunks overlap: the
 // MMA warp issues QK^T of chunk c+1 as soon as its K tile lands (while the
 // softmax warps work on chunk c), then PV of chunk c once its P is written;
@@ -72,12 +80,18 @@ constexpr int kHalf = kT * kRowBytes;      // one half tile: 16 KiB
 constexpr int kN = 16;                     // MMA N: the group's query heads, padded
 constexpr int kOpHalf = 2048;              // 16 rows x 128 B of a K-major operand half
 constexpr int kOpBytes = 2 * kOpHalf;      // Q, P_hi or P_lo operand
-constexpr int kThreads = 352;
+constexpr int kThreads = 480;
 constexpr int kWarpProducerK = 4;
 constexpr int kWarpProducerV = 5;
 constexpr int kWarpMma = 6;
 constexpr int kWarpEpi0 = 7;               // warps 7-10: epilogue group
-constexpr uint32_t kTmemCols = 64;
+constexpr int kWarpSmxB0 = 11;             // warps 11-14: second softmax group
+// TMEM columns: S and O, double-buffered. The terms of a split operand are
+// stacked along N so one MMA carries all of them (the tensor pipe's cost
+// is per instruction at these small N): S holds 16 columns (32 with FP8
+// K/V: q_hi and q_lo), O 32 (P_hi, P_lo; 48 with FP8: three P terms); the
+// softmax adds the stacked columns of a head.
+constexpr uint32_t kTmemCols = 256;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kUnitRing = 4;               // slots of the shared unit queue
 constexpr int kUnitConsumers = 3;          // V producer, MMA warp, softmax warp 0
@@ -100,9 +114,10 @@ struct Layout {
   static constexpr int kOffQ8 = kOffQ + 2 * kOpBytes;     // [2 buffers] fp8 Q terms (KV8)
   static constexpr int kOffP = kOffQ8 + (KV8 ? 2 * kOpBytes : 0);  // [2 buffers] P operands
   static constexpr int kOffQs = kOffP + 4 * kOpBytes;     // [2 buffers][8] 1/sigma per row (KV8)
-  static constexpr int kOffRed = kOffQs + 2 * 8 * 4;      // 2 x [4 warps][8] floats (chunk maxima)
-  static constexpr int kOffLred = kOffRed + 2 * 4 * 8 * 4;  // [4 warps][8] floats (final sums)
-  static constexpr int kOffBar = kOffLred + 4 * 8 * 4;
+  // per softmax group: 2 x [4 warps][8] floats (chunk maxima), [4 warps][8] (final sums)
+  static constexpr int kOffRed = kOffQs + 2 * 8 * 4;
+  static constexpr int kOffLred = kOffRed + 2 * 2 * 4 * 8 * 4;
+  static constexpr int kOffBar = kOffLred + 2 * 4 * 8 * 4;
   static constexpr int kNumBars = 4 * kStages + 14 + 2 * kUnitRing + 4 + 2;
   static constexpr int kOffTmem = kOffBar + kNumBars * 8;
   static constexpr int kOffURing = kOffTmem + 16;              // [kUnitRing] unit indices
@@ -142,6 +157,14 @@ __device__ __forceinline__ uint32_t op_offset(int n, int k) {
   const int half = k >> 6, col = k & 63;
   return half * kOpHalf + (n >> 3) * 1024 + (n & 7) * 128 + (((col >> 3) ^ (n & 7)) << 4) +
          (col & 7) * 2;
+}
+
+// Same for a 32 x 128 16-bit operand (two stacked 16-row terms): 64-column
+// halves of 4 KiB, each four 8-row atoms.
+__device__ __forceinline__ uint32_t op32_offset(int n, int k) {
+  const int half = k >> 6, col = k & 63;
+  return half * (2 * kOpHalf) + (n >> 3) * 1024 + (n & 7) * 128 +
+         (((col >> 3) ^ (n & 7)) << 4) + (col & 7) * 2;
 }
 
 // Byte offset of element (row n, column k) of a 16 x 128 K-major fp8 operand
@@ -250,7 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kOffEpi = L::kOffEpi;
   constexpr int NB = D / 64;    // 64-dim boxes per row
   constexpr int PPS = kT / BS;  // pages per stage
-  constexpr int GL = G <= 4 ? 4 : 8;  // TMEM columns read per row
+  constexpr int kGroups = G >= 2 ? 2 : 1;  // softmax warp groups (query-head columns split)
+  constexpr int kGA = (G + 1) / 2 > 0 ? (G + 1) / 2 : 1;  // columns of group 0 (group 1: G - kGA)
   static_assert(kT % BS == 0 && PPS <= 32, "stage must hold whole pages");
   using TNat = std::conditional_t<FP16, __half, __nv_bfloat16>;
   using H = Half16<FP16>;
@@ -361,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(uring_empty(s2), kUnitConsumers);
     }
     for (int s2 = 0; s2 < 2; ++s2) {
-      mbar_init(ep_full(s2), 4);
+      mbar_init(ep_full(s2), 4 * kGroups);
       mbar_init(ep_empty(s2), 4);
     }
     for (int r = 0; r < 2; ++r)
@@ -371,14 +395,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     for (int b2 = 0; b2 < 2; ++b2) {
       mbar_init(s_full(b2), 1);
-      mbar_init(s_free(b2), 4);
-      mbar_init(p_full(b2), 4);
+      mbar_init(s_free(b2), 4 * kGroups);
+      mbar_init(p_full(b2), 4 * kGroups);
       mbar_init(o_full(b2), 1);
-      mbar_init(o_free(b2), 4);
+      mbar_init(o_free(b2), 4 * kGroups);
       mbar_init(q_full(b2), 1);
-      // FP8 K/V: also released by the softmax warps once they have read the
+      // FP8 K/V: also released by each softmax group once it has read the
       // buffer's row scales
-      mbar_init(q_empty(b2), KV8 ? 2 : 1);
+      mbar_init(q_empty(b2), KV8 ? 1 + kGroups : 1);
       mbar_init(q8_full(b2), 1);
     }
     fence_mbar_init();
@@ -405,8 +429,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + kOffTmem);
-  auto tS = [&](int b2) { return tmem + (uint32_t)(b2 * kN); };
-  auto tO = [&](int b2) { return tmem + (uint32_t)((2 + b2) * kN); };
+  constexpr int kSCols = KV8 ? 2 * kN : kN;  // S columns per buffer
+  constexpr int kOCols = KV8 ? 3 * kN : 2 * kN;  // O columns per buffer
+  auto tS = [&](int b2) { return tmem + (uint32_t)(b2 * kSCols); };
+  auto tO = [&](int b2) { return tmem + (uint32_t)(2 * kSCols + b2 * kOCols); };
 
   if (warp == kWarpProducerK || warp == kWarpProducerV) {
     // ------------------- producers: K ring (warp 4), V ring (warp 5) -------------------
@@ -541,8 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma) {
     // ------------------------------ MMA issue -----------------------------
     // kind::f16: type fields 1 = bf16, 0 = f16; kind::f8f6f4: 0 = E4M3
-    constexpr uint32_t idesc_qk = idesc_f16(128, kN, !FP16 && !KV8, false, false);
-    constexpr uint32_t idesc_pv = idesc_f16(128, kN, !FP16 && !KV8, true, false);
+    constexpr uint32_t idesc_qk = idesc_f16(128, kSCols, !FP16 && !KV8, false, false);
+    constexpr uint32_t idesc_pv = idesc_f16(128, kOCols, !FP16 && !KV8, true, false);
     // S(c) = K(c) . Q^T into S[c & 1]; needs the K slot, the unit's Q and the
     // softmax's read of S(c-2)
     auto issue_qk = [&](const Cursor<BS, RingSource>& cur) {
@@ -556,16 +582,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         const uint32_t kb = base_u32 + kOffK + slot * kSlotBytes;
         if constexpr (KV8) {
-          // S = K . (Q_hi + Q_lo)^T: 32 fp8 dims (32 bytes) per step
+          // S = K . [Q_hi; Q_lo]^T (N = 32: rows 16..31 of the operand are q_lo):
+          // 32 fp8 dims (32 bytes) per step
           const uint32_t q8 = base_u32 + kOffQ8 + qb * kOpBytes;
 #pragma unroll
-          for (int term = 0; term < 2; ++term)
-#pragma unroll
-            for (int k = 0; k < D / 32; ++k) {
-              const uint64_t a = sdesc_sw128(kb + k * 32, 16, 1024);
-              const uint64_t bq = sdesc_sw128(q8 + term * kOpHalf + k * 32, 16, 1024);
-              mma_f8_ss(tS(c & 1), a, bq, idesc_qk, (term | k) > 0 ? 1u : 0u);
-            }
+          for (int k = 0; k < D / 32; ++k) {
+            const uint64_t a = sdesc_sw128(kb + k * 32, 16, 1024);
+            const uint64_t bq = sdesc_sw128(q8 + k * 32, 16, 1024);
+            mma_f8_ss(tS(c & 1), a, bq, idesc_qk, k > 0 ? 1u : 0u);
+          }
         } else {
           const uint32_t qa = base_u32 + kOffQ + qb * kOpBytes;
 #pragma unroll
@@ -594,28 +619,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         const uint32_t vb = base_u32 + kOffV + slot * kSlotBytes;
         if constexpr (KV8) {
-          // O = V^T . (P_0 + P_1 + P_2)^T: V^T as an MN-major fp8 A operand (all
-          // 128 dims in one 128-byte row per token), 32 tokens per step
+          // O = V^T . [P_0; P_1; P_2]^T (N = 48, one 16-row block per term): V^T
+          // as an MN-major fp8 A operand (all 128 dims in one 128-byte row per
+          // token), 32 tokens per step
           const uint32_t p8 = base_u32 + kOffP + (c & 1) * 3 * kOpHalf;
 #pragma unroll
           for (int k = 0; k < kT / 32; ++k) {
             const uint64_t a = sdesc_sw128(vb + k * 32 * 128, kSlotBytes, 1024);
-#pragma unroll
-            for (int term = 0; term < 3; ++term)
-              mma_f8_ss(tO(c & 1), a, sdesc_sw128(p8 + term * kOpHalf + k * 32, 16, 1024),
-                        idesc_pv, (k | term) > 0 ? 1u : 0u);
+            mma_f8_ss(tO(c & 1), a, sdesc_sw128(p8 + k * 32, 16, 1024), idesc_pv,
+                      k > 0 ? 1u : 0u);
           }
         }
-        const uint32_t phi = base_u32 + kOffP + (c & 1) * 2 * kOpBytes;
-        const uint32_t plo = phi + kOpBytes;
+        // O = V^T . [P_hi; P_lo]^T (N = 32): V^T as an MN-major A operand with
+        // 64-dim halves kHalf apart (LBO) and 8-token row groups 1 KiB apart
+        // (SBO); P as a 32-row K-major operand (64-token halves 4 KiB apart);
+        // 16 tokens per step
+        const uint32_t pb16 = base_u32 + kOffP + (c & 1) * 2 * kOpBytes;
 #pragma unroll
         for (int k = 0; k < (KV8 ? 0 : 8); ++k) {
-          // V^T as an MN-major A operand: 64-dim halves kHalf apart (LBO),
-          // 8-token row groups 1 KiB apart (SBO); 16 tokens per step
           const uint64_t a = sdesc_sw128(vb + k * 2048, kHalf, 1024);
-          const uint32_t po = (k >> 2) * kOpHalf + (k & 3) * 32;
-          mma_f16_ss(tO(c & 1), a, sdesc_sw128(phi + po, 16, 1024), idesc_pv, k > 0 ? 1u : 0u);
-          mma_f16_ss(tO(c & 1), a, sdesc_sw128(plo + po, 16, 1024), idesc_pv, 1u);
+          const uint32_t po = (k >> 2) * (2 * kOpHalf) + (k & 3) * 32;
+          mma_f16_ss(tO(c & 1), a, sdesc_sw128(pb16 + po, 16, 1024), idesc_pv, k > 0 ? 1u : 0u);
         }
         mma_commit(o_full(c & 1));
         mma_commit(empty_bar(1, slot));  // V slot read
@@ -647,204 +671,222 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = mbar_wait(empty_bar(1, c % kStages), (c / kStages) & 1);
       if (!__all_sync(kFull, ok)) failed = true;
     }
-  } else if (warp < 4) {
+  } else if (warp < 4 || warp >= kWarpSmxB0) {
     // ------------------------------ softmax -------------------------------
-    const int t = threadIdx.x;  // token row of S; output dim of O
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float* red = reinterpret_cast<float*>(base + kOffRed);
-    float* lred = reinterpret_cast<float*>(base + kOffLred);
-    float m_run[G], l_th[G], acc[G], alpha_prev[G];
-    // acc = acc * alpha(c) + O(c)
-    auto fold = [&](int c) {
-      bool ok = !failed && mbar_wait(o_full(c & 1), (c >> 1) & 1);
-      if (!__all_sync(kFull, ok)) failed = true;
-      tc_fence_after();
-      float o[GL];
-      if constexpr (GL == 4) {
-        tmem_ld_x4(tO(c & 1) + lane_base, o);
-      } else {
-        tmem_ld_x8(tO(c & 1) + lane_base, o);
-      }
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_free(c & 1));
-#pragma unroll
-      for (int g = 0; g < G; ++g) acc[g] = acc[g] * alpha_prev[g] + o[g];
-    };
-    // Softmax warp 0 alone reads the unit ring and hands the index to warps
-    // 1-3, so the four always walk the same units through the same named
-    // barriers (a late timeout in one warp cannot split them).
-    RingSource ring = ring_source();
-    volatile int* ubc = reinterpret_cast<volatile int*>(base + kOffUBcast);
-    auto next_unit = [&]() {
-      int u = -1;
-      if (warp == 0) u = ring.next();
-      if (warp == 0 && lane == 0) *ubc = u;
-      named_bar_sync(1, 128);
-      u = *ubc;
-      named_bar_sync(1, 128);  // before warp 0 overwrites it
-      return u;
-    };
-    int c = 0, je = 0;  // je: units handed to the epilogue group
-    int jq = 0;         // units with chunks (the Q buffer sequence)
-    for (int u = next_unit(); u >= 0; u = next_unit()) {
-      const Unit U = load_unit<BS>(p, u);
-      const int hq0 = U.h * G;
-      if (U.zero_fill) {
-        for (int i = t; i < G * D; i += 128) {
-          const int64_t o = ((int64_t)U.b * p.Hq + hq0) * D + i;
-          if (p.out_f32) static_cast<float*>(p.out)[o] = 0.f;
-          else static_cast<TNat*>(p.out)[o] = to_out<TNat>(0.f);
-        }
-      }
-      if (U.n_chunks == 0) continue;
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        m_run[g] = -INFINITY;
-        l_th[g] = 0.f;
-        acc[g] = 0.f;
-      }
-      // logit scale per row: softmax scale (base 2) x K dequantisation scale
-      // (x 1 / sigma of the row's fp8 q terms)
-      const float ksc = p.k_scale ? __ldg(p.k_scale + (p.scale_per_head ? U.h : 0)) : 1.f;
-      float qsc[G];
-      if constexpr (KV8) {
-        const bool okq = !failed && mbar_wait(q8_full(jq & 1), (jq >> 1) & 1);
-        if (!__all_sync(kFull, okq)) failed = true;
-        const float* qs = reinterpret_cast<const float*>(base + kOffQs) + (jq & 1) * 8;
-#pragma unroll
-        for (int g = 0; g < G; ++g) qsc[g] = p.qscale * ksc * qs[g];
-      } else {
-#pragma unroll
-        for (int g = 0; g < G; ++g) qsc[g] = p.qscale * ksc;
-      }
-      for (int i = 0; i < U.n_chunks; ++i, ++c) {
-        const int slot = c % kStages;
-        const int n_valid = min(kT, U.t1 - (U.t0 + i * kT));
-        bool ok = !failed && mbar_wait(s_full(c & 1), (c >> 1) & 1);
+    // Group 0 (warps 0-3) takes query-head columns [0, kGA), group 1 (warps
+    // 11-14, when G >= 2) columns [kGA, G). Each group has the CTA-wide max,
+    // P rows and O columns of its heads to itself, so the two run the same
+    // chunk side by side; they meet only at unit boundaries.
+    const int grp = warp >= kWarpSmxB0 ? 1 : 0;
+    if (grp < kGroups) {
+      const int wq = warp & 3;        // TMEM lane quadrant: warp w reads lanes 32 (w % 4) ..
+      const int t = wq * 32 + lane;   // token row of S; output dim of O
+      const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+      const int g0 = grp ? kGA : 0;   // first column of this group
+      const int ng = grp ? G - kGA : kGA;
+      const int bar = grp ? 3 : 1;    // the group's named barrier
+      float* red = reinterpret_cast<float*>(base + kOffRed) + grp * 64;
+      float* lred = reinterpret_cast<float*>(base + kOffLred) + grp * 32;
+      float m_run[kGA], l_th[kGA], acc[kGA], alpha_prev[kGA];
+      // acc = acc * alpha(c) + O(c), this group's columns
+      auto fold = [&](int c) {
+        bool ok = !failed && mbar_wait(o_full(c & 1), (c >> 1) & 1);
         if (!__all_sync(kFull, ok)) failed = true;
         tc_fence_after();
-        float s[GL];
-        if constexpr (GL == 4) {
-          tmem_ld_x4(tS(c & 1) + lane_base, s);
-        } else {
-          tmem_ld_x8(tS(c & 1) + lane_base, s);
-        }
+        // the stacked term columns of each head: g, 16 + g (, 32 + g)
+        float o[4], o2[4], o3[4];
+        tmem_ld_x4(tO(c & 1) + lane_base + (uint32_t)g0, o);
+        tmem_ld_x4(tO(c & 1) + lane_base + (uint32_t)(kN + g0), o2);
+        if constexpr (KV8) tmem_ld_x4(tO(c & 1) + lane_base + (uint32_t)(2 * kN + g0), o3);
         tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] += KV8 ? o2[j] + o3[j] : o2[j];
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(s_free(c & 1));
+        if (lane == 0) mbar_arrive(o_free(c & 1));
 #pragma unroll
-        for (int g = 0; g < G; ++g) s[g] = (t < n_valid) ? s[g] * qsc[g] : -INFINITY;
-        float* rb = red + (c & 1) * 32;
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float mx = s[g];
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
-          if (lane == 0) rb[warp * 8 + g] = mx;
-        }
-        named_bar_sync(1, 128);
-        // every softmax thread has read the row scales of this unit's Q buffer
-        if (KV8 && i == 0 && t == 0) mbar_arrive(q_empty(jq & 1));
-        float alpha[G];
-        uint8_t* pb = base + kOffP + (c & 1) * (KV8 ? 3 * kOpHalf : 2 * kOpBytes);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float mx = fmaxf(fmaxf(rb[g], rb[8 + g]), fmaxf(rb[16 + g], rb[24 + g]));
-          const float mn = fmaxf(m_run[g], mx);  // finite: every chunk holds a valid token
-          alpha[g] = exp2f(m_run[g] - mn);
-          m_run[g] = mn;
-          const float pr = exp2f(s[g] - mn);
-          l_th[g] = l_th[g] * alpha[g] + pr;
-          if constexpr (KV8) {
-            // p * 256 = t0 + t1 + t2 in fp8 (about 12 significant bits)
-            const float x = pr * kP8Scale;
-            const uint8_t b0 = to_e4m3(x);
-            const float r0 = x - e4m3_to_float(b0);
-            const uint8_t b1 = to_e4m3(r0);
-            const uint8_t b2 = to_e4m3(r0 - e4m3_to_float(b1));
-            const uint32_t off = op8_offset(g, t);
-            pb[off] = b0;
-            pb[kOpHalf + off] = b1;
-            pb[2 * kOpHalf + off] = b2;
-          } else {
-            const typename H::T hi = H::from(pr);
-            const typename H::T lo = H::from(pr - H::to(hi));
-            const uint32_t off = op_offset(g, t);
-            *reinterpret_cast<typename H::T*>(pb + off) = hi;
-            *reinterpret_cast<typename H::T*>(pb + kOpBytes + off) = lo;
+        for (int j = 0; j < kGA; ++j) acc[j] = acc[j] * alpha_prev[j] + o[j];
+      };
+      // Softmax warp 0 alone reads the unit ring and hands the index to the
+      // other softmax warps, so all walk the same units through the same
+      // named barriers (a late timeout in one warp cannot split them).
+      RingSource ring = ring_source();
+      volatile int* ubc = reinterpret_cast<volatile int*>(base + kOffUBcast);
+      auto next_unit = [&]() {
+        int u = -1;
+        if (warp == 0) u = ring.next();
+        if (warp == 0 && lane == 0) *ubc = u;
+        named_bar_sync(4, 128 * kGroups);
+        u = *ubc;
+        named_bar_sync(4, 128 * kGroups);  // before warp 0 overwrites it
+        return u;
+      };
+      int c = 0, je = 0;  // je: units handed to the epilogue group
+      int jq = 0;         // units with chunks (the Q buffer sequence)
+      for (int u = next_unit(); u >= 0; u = next_unit()) {
+        const Unit U = load_unit<BS>(p, u);
+        const int hq0 = U.h * G;
+        if (U.zero_fill && grp == 0) {
+          for (int i = t; i < G * D; i += 128) {
+            const int64_t o = ((int64_t)U.b * p.Hq + hq0) * D + i;
+            if (p.out_f32) static_cast<float*>(p.out)[o] = 0.f;
+            else static_cast<TNat*>(p.out)[o] = to_out<TNat>(0.f);
           }
         }
-        if (n_valid < kT) {
-          // keep stale or out-of-context V rows out of the MMA; the V tile of
-          // this chunk must have landed first (its last page may be partial)
-          ok = !failed && mbar_wait(full_bar(1, slot), (c / kStages) & 1);
+        if (U.n_chunks == 0) continue;
+#pragma unroll
+        for (int j = 0; j < kGA; ++j) {
+          m_run[j] = -INFINITY;
+          l_th[j] = 0.f;
+          acc[j] = 0.f;
+        }
+        // logit scale per row: softmax scale (base 2) x K dequantisation
+        // scale (x 1 / sigma of the row's fp8 q terms)
+        const float ksc = p.k_scale ? __ldg(p.k_scale + (p.scale_per_head ? U.h : 0)) : 1.f;
+        float qsc[kGA];
+        if constexpr (KV8) {
+          const bool okq = !failed && mbar_wait(q8_full(jq & 1), (jq >> 1) & 1);
+          if (!__all_sync(kFull, okq)) failed = true;
+          const float* qs = reinterpret_cast<const float*>(base + kOffQs) + (jq & 1) * 8;
+#pragma unroll
+          for (int j = 0; j < kGA; ++j) qsc[j] = j < ng ? p.qscale * ksc * qs[g0 + j] : 0.f;
+        } else {
+#pragma unroll
+          for (int j = 0; j < kGA; ++j) qsc[j] = p.qscale * ksc;
+        }
+        for (int i = 0; i < U.n_chunks; ++i, ++c) {
+          const int slot = c % kStages;
+          const int n_valid = min(kT, U.t1 - (U.t0 + i * kT));
+          bool ok = !failed && mbar_wait(s_full(c & 1), (c >> 1) & 1);
           if (!__all_sync(kFull, ok)) failed = true;
+          tc_fence_after();
+          float s[4], s2[4];
+          tmem_ld_x4(tS(c & 1) + lane_base + (uint32_t)g0, s);
+          if constexpr (KV8) tmem_ld_x4(tS(c & 1) + lane_base + (uint32_t)(kN + g0), s2);
+          tmem_ld_wait();
+          if constexpr (KV8) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) s[j] += s2[j];
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(s_free(c & 1));
+#pragma unroll
+          for (int j = 0; j < kGA; ++j) s[j] = (t < n_valid) ? s[j] * qsc[j] : -INFINITY;
+          float* rb = red + (c & 1) * 32;
+#pragma unroll
+          for (int j = 0; j < kGA; ++j) {
+            float mx = s[j];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+            if (lane == 0) rb[wq * 8 + j] = mx;
+          }
+          named_bar_sync(bar, 128);
+          // every softmax thread has read the row scales of this unit's Q buffer
+          if (KV8 && i == 0 && t == 0) mbar_arrive(q_empty(jq & 1));
+          float alpha[kGA];
+          uint8_t* pb = base + kOffP + (c & 1) * (KV8 ? 3 * kOpHalf : 2 * kOpBytes);
+#pragma unroll
+          for (int j = 0; j < kGA; ++j) {
+            const float mx = fmaxf(fmaxf(rb[j], rb[8 + j]), fmaxf(rb[16 + j], rb[24 + j]));
+            const float mn = fmaxf(m_run[j], mx);  // finite: every chunk holds a valid token
+            alpha[j] = exp2f(m_run[j] - mn);
+            m_run[j] = mn;
+            const float pr = exp2f(s[j] - mn);
+            l_th[j] = l_th[j] * alpha[j] + pr;
+            if (j < ng) {  // rows of padding heads stay zero
+              const int g = g0 + j;
+              if constexpr (KV8) {
+                // p * 256 = t0 + t1 + t2 in fp8 (about 12 significant bits)
+                const float x = pr * kP8Scale;
+                const uint8_t b0 = to_e4m3(x);
+                const float r0 = x - e4m3_to_float(b0);
+                const uint8_t b1 = to_e4m3(r0);
+                const uint8_t b2 = to_e4m3(r0 - e4m3_to_float(b1));
+                const uint32_t off = op8_offset(g, t);
+                pb[off] = b0;
+                pb[kOpHalf + off] = b1;
+                pb[2 * kOpHalf + off] = b2;
+              } else {
+                const typename H::T hi = H::from(pr);
+                const typename H::T lo = H::from(pr - H::to(hi));
+                *reinterpret_cast<typename H::T*>(pb + op32_offset(g, t)) = hi;
+                *reinterpret_cast<typename H::T*>(pb + op32_offset(kN + g, t)) = lo;
+              }
+            }
+          }
+          if (grp == 0 && n_valid < kT) {
+            // keep stale or out-of-context V rows out of the MMA; the V tile
+            // of this chunk must have landed first (its last page may be partial)
+            ok = !failed && mbar_wait(full_bar(1, slot), (c / kStages) & 1);
+            if (!__all_sync(kFull, ok)) failed = true;
+            if (t >= n_valid) {
+              uint8_t* vrow = base + kOffV + slot * kSlotBytes + t * kRowBytes;
+#pragma unroll
+              for (int hh = 0; hh < (KV8 ? 1 : NB); ++hh)
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                  *reinterpret_cast<uint4*>(vrow + hh * kHalf + q * 16) = make_uint4(0, 0, 0, 0);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(p_full(c & 1));
+          if (i > 0) fold(c - 1);
+#pragma unroll
+          for (int j = 0; j < kGA; ++j) alpha_prev[j] = alpha[j];
         }
-        if (t >= n_valid) {
-          uint8_t* vrow = base + kOffV + slot * kSlotBytes + t * kRowBytes;
+        fold(c - 1);
+        // softmax denominators: sum the per-token partial sums over the group
 #pragma unroll
-          for (int hh = 0; hh < (KV8 ? 1 : NB); ++hh)
+        for (int j = 0; j < kGA; ++j) {
+          float v = l_th[j];
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              *reinterpret_cast<uint4*>(vrow + hh * kHalf + q * 16) = make_uint4(0, 0, 0, 0);
+          for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+          if (lane == 0) lred[wq * 8 + j] = v;
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(p_full(c & 1));
-        if (i > 0) fold(c - 1);
+        named_bar_sync(bar, 128);
+        float Ls[kGA];
 #pragma unroll
-        for (int g = 0; g < G; ++g) alpha_prev[g] = alpha[g];
+        for (int j = 0; j < kGA; ++j) Ls[j] = lred[j] + lred[8 + j] + lred[16 + j] + lred[24 + j];
+        named_bar_sync(bar, 128);  // lred is rewritten by the next unit
+        // hand this group's part of the unit's state to the epilogue group
+        {
+          const int es = je & 1;
+          bool ok2 = !failed;
+          if (ok2 && je >= 2) ok2 = mbar_wait(ep_empty(es), ((je - 2) >> 1) & 1);
+          if (!__all_sync(kFull, ok2)) failed = true;
+          float* st = reinterpret_cast<float*>(base + kOffEpi) + es * kEpiFloats;
+#pragma unroll
+          for (int j = 0; j < kGA; ++j)
+            if (j < ng) st[(g0 + j) * kHeadDim + t] = acc[j];
+          if (t == 0) {
+#pragma unroll
+            for (int j = 0; j < kGA; ++j) {
+              if (j < ng) {
+                st[8 * kHeadDim + g0 + j] = m_run[j];
+                st[8 * kHeadDim + 8 + g0 + j] = Ls[j];
+              }
+            }
+            if (grp == 0) reinterpret_cast<int*>(st)[8 * kHeadDim + 16] = u;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ep_full(es));
+          ++je;
+        }
+        ++jq;
       }
-      fold(c - 1);
-      // softmax denominators: sum the per-token partial sums over 128 threads
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float v = l_th[g];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
-        if (lane == 0) lred[warp * 8 + g] = v;
-      }
-      named_bar_sync(1, 128);
-      float Ls[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) Ls[g] = lred[g] + lred[8 + g] + lred[16 + g] + lred[24 + g];
-      named_bar_sync(1, 128);  // lred is rewritten by the next unit
-      // hand the unit's state to the epilogue group
+      // end of work: an empty state tells the epilogue group to stop
       {
         const int es = je & 1;
         bool ok2 = !failed;
         if (ok2 && je >= 2) ok2 = mbar_wait(ep_empty(es), ((je - 2) >> 1) & 1);
         if (!__all_sync(kFull, ok2)) failed = true;
         float* st = reinterpret_cast<float*>(base + kOffEpi) + es * kEpiFloats;
-#pragma unroll
-        for (int g = 0; g < G; ++g) st[g * kHeadDim + t] = acc[g];
-        if (t == 0) {
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            st[8 * kHeadDim + g] = m_run[g];
-            st[8 * kHeadDim + 8 + g] = Ls[g];
-          }
-          reinterpret_cast<int*>(st)[8 * kHeadDim + 16] = u;
-        }
+        if (grp == 0 && t == 0) reinterpret_cast<int*>(st)[8 * kHeadDim + 16] = -1;
         __syncwarp();
         if (lane == 0) mbar_arrive(ep_full(es));
-        ++je;
       }
-      ++jq;
-    }
-    // end of work: an empty state tells the epilogue group to stop
-    {
-      const int es = je & 1;
-      bool ok2 = !failed;
-      if (ok2 && je >= 2) ok2 = mbar_wait(ep_empty(es), ((je - 2) >> 1) & 1);
-      if (!__all_sync(kFull, ok2)) failed = true;
-      float* st = reinterpret_cast<float*>(base + kOffEpi) + es * kEpiFloats;
-      if (t == 0) reinterpret_cast<int*>(st)[8 * kHeadDim + 16] = -1;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(ep_full(es));
     }
   } else {
     // ------------------------------ epilogue ------------------------------
