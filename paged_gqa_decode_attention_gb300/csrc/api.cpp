@@ -33,12 +33,16 @@ int cuda_fail(const char* what, cudaError_t e) {
 }
 
 // Planner cost constants, in token-equivalents of one CTA's streaming time:
-// the fixed cost of a CTA (launch, barrier set-up, q and first-page latency,
-// the final merge of its warps) and of merging split partials. Chosen from a
-// split-count sweep on GB300 (B=1 L=32768, B=4 L=8192, B=4 L=32768, the
-// 128-sequence serving mix): with these the planner picks the measured
-// fastest split count on all four.
-constexpr int kOverheadTokens = 256;
+// the fixed cost of a work unit (q and first-page latency, the unit's state
+// hand-off, partial write and merge ticket) and of merging split partials.
+// Chosen from split-count sweeps on GB300 (B=1 L=32768, B=4 L=8192,
+// B=4 / B=8 L=32768, the 128-sequence serving mix, 28/4-head B=16 L=8192):
+// a unit of the persistent tensor-core kernel costs about 512 tokens, a CTA
+// of the CUDA-core kernel about 256; with these the planner's pick is the
+// fastest measured split count or within 2% of it on every case but the
+// ragged serving mix (planned from its longest sequence).
+constexpr int kOverheadTokensCudaCore = 256;
+constexpr int kOverheadTokensTensorCore = 512;
 constexpr int kMergeTokens = 96;
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
@@ -78,8 +82,10 @@ int check_config(const pda_config* c) {
   return PDA_OK;
 }
 
-void plan_splits(const pda_config& c, int num_sms, int ctas_per_sm, int batch, int max_blocks,
-                 int hint, int forced, int* S_out, int* chunk_out) {
+void plan_splits(const pda_config& c, int kernel, int num_sms, int ctas_per_sm, int batch,
+                 int max_blocks, int hint, int forced, int* S_out, int* chunk_out) {
+  const int overhead = kernel == pda::kPartialTensorCore ? kOverheadTokensTensorCore
+                                                         : kOverheadTokensCudaCore;
   const int bs = c.block_size;
   int64_t max_len = (int64_t)max_blocks * bs;
   if (hint > 0 && hint < max_len) max_len = hint;
@@ -97,7 +103,7 @@ void plan_splits(const pda_config& c, int num_sms, int ctas_per_sm, int batch, i
       const int s_eff = ceil_div(max_pages, chunk);
       if (s_eff != s) continue;  // identical to a smaller split count
       const int64_t waves = (base * s_eff + slots - 1) / slots;
-      const double cost = (double)waves * ((double)chunk * bs + kOverheadTokens) +
+      const double cost = (double)waves * ((double)chunk * bs + overhead) +
                           (s_eff > 1 ? kMergeTokens : 0);
       if (cost < best * (1.0 - 1e-9)) {
         best = cost;
@@ -186,6 +192,14 @@ struct DeviceGuard {
 }  // namespace
 
 int pda::set_last_error(int code, const char* msg) { return fail(code, msg); }
+
+bool pda::pdl_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("PDA_PDL");
+    return !(e && std::strcmp(e, "0") == 0);
+  }();
+  return on;
+}
 
 struct pda_handle_s {
   pda_config cfg;
@@ -302,8 +316,8 @@ int paged_decode_attn_plan(const pda_config* cfg, int num_sms, int batch, int ma
   if (max_context_len_hint < 0) return fail(PDA_EINVAL, "max_context_len_hint < 0");
   const int G = cfg->num_q_heads / cfg->num_kv_heads;
   const int kernel = pda::default_partial_kernel(G, cfg->head_dim, cfg->kv_fp8 != 0);
-  plan_splits(*cfg, num_sms, pda::partial_ctas_per_sm_hint(kernel, G, cfg->head_dim), batch,
-              max_blocks, max_context_len_hint, 0, num_splits, chunk_pages);
+  plan_splits(*cfg, kernel, num_sms, pda::partial_ctas_per_sm_hint(kernel, G, cfg->head_dim),
+              batch, max_blocks, max_context_len_hint, 0, num_splits, chunk_pages);
   return PDA_OK;
 }
 
@@ -386,8 +400,8 @@ int paged_decode_attn_run_scaled(pda_handle h, const void* q, const void* k_cach
   }
 
   int S = 1, chunk = 1;
-  plan_splits(c, h->num_sms, h->ctas_per_sm, batch, max_blocks, max_context_len_hint, num_splits,
-              &S, &chunk);
+  plan_splits(c, h->kernel, h->num_sms, h->ctas_per_sm, batch, max_blocks, max_context_len_hint,
+              num_splits, &S, &chunk);
   const int64_t units = (int64_t)S * c.num_kv_heads * batch;
   if (units > INT_MAX) return fail(PDA_EINVAL, "splits * num_kv_heads * batch exceeds 2^31");
   alignas(64) CUtensorMap tmap_q;

@@ -344,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++k;
         if (pub < 0) {
           if (lane == 0) {
+            griddep_launch_dependents();  // no more units: the next grid may start launching
             __threadfence();  // this CTA's last fetch is ordered before its done count
             if (atomicAdd(p->sched + 1, 1) == (int)gridDim.x - 1) {
               p->sched[0] = 0;
@@ -428,6 +429,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Everything above touches only this CTA's resources; from here on the
+  // kernel reads the inputs and the shared counters, which the previous
+  // grid in the stream may still be writing (programmatic dependent launch).
+  griddep_wait();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + kOffTmem);
   constexpr int kSCols = KV8 ? 2 * kN : kN;  // S columns per buffer
   constexpr int kOCols = KV8 ? 3 * kN : 2 * kN;  // O columns per buffer
@@ -953,9 +958,20 @@ cudaError_t launch_one(const CUtensorMap* tk, const CUtensorMap* tv, const CUten
                        const PartialParams& p, cudaStream_t stream) {
   const int ctas = p.num_units < p.max_ctas ? p.num_units : p.max_ctas;
   if (ctas <= 0) return cudaSuccess;
-  paged_partial_tc_kernel<G, D, BS, FP16, KV8>
-      <<<ctas, kThreads, Layout<KV8>::kSmemBytes, stream>>>(*tk, *tv, *tq, p);
-  return cudaGetLastError();
+  // Programmatic dependent launch (off with PDA_PDL=0): the CTAs may start
+  // their set-up while the previous grid in the stream finishes; the kernel
+  // waits for that grid before reading any input.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Layout<KV8>::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, paged_partial_tc_kernel<G, D, BS, FP16, KV8>, *tk, *tv, *tq, p);
 }
 
 template <int G, int D, int BS, bool FP16, bool KV8>

@@ -111,6 +111,10 @@ cudaError_t launch_validate(const int32_t* block_table, const int32_t* context_l
                             int max_blocks, int block_size, int64_t num_blocks, int* err,
                             cudaStream_t stream);
 
+// Whether kernels are launched with programmatic dependent launch (default
+// on; the environment variable PDA_PDL=0 turns it off, read once).
+bool pdl_enabled();
+
 // Records `msg` as this thread's last error (paged_decode_attn_last_error)
 // and returns `code`.
 int set_last_error(int code, const char* msg);

@@ -55,30 +55,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
+// Programmatic dependent launch: wait until the preceding grid in the stream
+// has completed and its memory is visible (returns at once when the launch
+// has no such dependency).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-// mbar_wait for latency-critical hand-offs: polls with the non-blocking
-// test_wait, so the waiter resumes as soon as the phase completes; false
-// after kWaitLimitNs without completion.
-__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity) {
-  if (mbar_test_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_test_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-  }
+// Let the next grid in the stream start launching; its griddep_wait() still
+// waits for this grid to complete.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // try_wait with a suspend-time hint: the thread may sleep up to `hint_ns`
