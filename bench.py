@@ -44,7 +44,9 @@ FALLBACK_HBM_GBS = 6800.0
 # capture of this workload (profiles/); None when not measured for the
 # current kernel.
 NCU_TRAFFIC_BYTES = {
-    "long_b4_l32768": None,  # kernel changed since the last capture
+    # profiles/paged_partial_tc_kernel_long_b4_l32768.md: 537.15 MB read + 3.38 MB
+    # written per launch (captured on the same step over a 1 GiB pool)
+    "long_b4_l32768": 540_526_336,
     # profiles/rope_kv_write_kernel_prefill_t32768.md: 419.90 MB read + 348.27 MB written
     "rope_prefill_t32768": 768_166_400,
 }
