@@ -25,10 +25,13 @@
 // lo = rn(p - hi), stacked as one 32-row operand so a single MMA multiplies
 // both into O (columns g and 16 + g, added by the softmax); P keeps about
 // 16 significant bits (one 8-bit operand would cost up to 2^-9 relative
-// error per weight). At these small N the tensor pipe's cost is per
-// instruction, so stacking the terms halves the PV instructions.
+// error per weight). At these small N an MMA's cost is per instruction,
+// not per FLOP: one issuing thread needs ~170-185 cycles per shared-memory
+// operand MMA whatever N (16 to 256), while MMAs from two issuing warps
+// overlap. So the terms are stacked (half the PV instructions), and QK^T
+// and PV are issued by two different warps.
 //
-// Warp roles (480 threads):
+// Warp roles (512 threads):
 //   warps 0-3 and 11-14: softmax, two groups of four that split the G query
 //     heads' columns (group 0 the first ceil(G/2), group 1 the rest; G = 1
 //     uses one group). Thread t of a group reads TMEM lane t of S (token t of
@@ -44,14 +47,15 @@
 //     The K producer also loads each unit's G query rows (a TMA box) into one
 //     of two Q operand buffers.
 //   warp 6: allocates 256 TMEM columns (S and O, double-buffered), issues
-//     the MMAs and commits their completion to mbarriers. The terms of a
+//     the QK^T MMAs and commits their completion to mbarriers.
+//   warp 15: issues the PV MMAs and commits their completion. The terms of a
 //     split operand (P_hi / P_lo; with FP8, q_hi / q_lo and the three P
 //     terms) are stacked along N, so each contraction step is one MMA.
-// S, O and P are double-buffered by chunk parity so the chunks overlap: the
-// MMA warp issues QK^T of chunk c+1 as soon as its K tile lands (while the
-// softmax warps work on chunk c), then PV of chunk c once its P is written;
-// the softmax warps fold O of chunk c-1 into the running output after
-// writing P of chunk c.
+// S, O and P are double-buffered by chunk parity so the chunks overlap:
+// QK^T of chunk c+1 is issued as soon as its K tile lands (while the
+// softmax warps work on chunk c), PV of chunk c once its P is written; the
+// softmax warps fold O of chunk c-1 into the running output after writing P
+// of chunk c.
 //   warps 7-10: epilogue. A finished unit's state (accumulators, max, sum)
 //     comes through a double-buffered shared-memory slot; this group
 //     normalises it, stores the output or the split partial, and runs the
@@ -80,12 +84,13 @@ constexpr int kHalf = kT * kRowBytes;      // one half tile: 16 KiB
 constexpr int kN = 16;                     // MMA N: the group's query heads, padded
 constexpr int kOpHalf = 2048;              // 16 rows x 128 B of a K-major operand half
 constexpr int kOpBytes = 2 * kOpHalf;      // Q, P_hi or P_lo operand
-constexpr int kThreads = 480;
+constexpr int kThreads = 512;
 constexpr int kWarpProducerK = 4;
 constexpr int kWarpProducerV = 5;
-constexpr int kWarpMma = 6;
+constexpr int kWarpMma = 6;                // issues QK^T (and owns the TMEM allocation)
 constexpr int kWarpEpi0 = 7;               // warps 7-10: epilogue group
 constexpr int kWarpSmxB0 = 11;             // warps 11-14: second softmax group
+constexpr int kWarpMmaPV = 15;             // issues PV
 // TMEM columns: S and O, double-buffered. The terms of a split operand are
 // stacked along N so one MMA carries all of them (the tensor pipe's cost
 // is per instruction at these small N): S holds 16 columns (32 with FP8
@@ -94,7 +99,7 @@ constexpr int kWarpSmxB0 = 11;             // warps 11-14: second softmax group
 constexpr uint32_t kTmemCols = 256;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kUnitRing = 4;               // slots of the shared unit queue
-constexpr int kUnitConsumers = 3;          // V producer, MMA warp, softmax warp 0
+constexpr int kUnitConsumers = 4;          // V producer, both MMA warps, softmax warp 0
 // A finished unit's state, softmax -> epilogue, double-buffered:
 // acc[8][128], max[8], sum[8], unit index (floats; the index as int).
 constexpr int kEpiFloats = 8 * 128 + 8 + 8 + 4;
@@ -569,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (r == 0) cur_k.advance(p, fetch); else cur_v.advance(p, ring);
     }
-  } else if (warp == kWarpMma) {
+  } else if (warp == kWarpMma || warp == kWarpMmaPV) {
     // ------------------------------ MMA issue -----------------------------
     // kind::f16: type fields 1 = bf16, 0 = f16; kind::f8f6f4: 0 = E4M3
     constexpr uint32_t idesc_qk = idesc_f16(128, kSCols, !FP16 && !KV8, false, false);
@@ -651,32 +656,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
+    // Each issuing warp walks the same chunk sequence: warp 6 issues QK^T,
+    // warp 15 PV. Their MMAs overlap in the tensor pipe.
+    const bool is_qk = warp == kWarpMma;
     RingSource ring = ring_source();
-    Cursor<BS, RingSource> qk;
-    qk.start(p, ring);
-    if (qk.valid()) {
-      issue_qk(qk);
-      qk.advance(p, ring);
+    Cursor<BS, RingSource> cur;
+    cur.start(p, ring);
+    int last_c = -1;
+    while (!failed && cur.valid()) {
+      if (is_qk) issue_qk(cur); else issue_pv(cur.c);
+      last_c = cur.c;
+      cur.advance(p, ring);
     }
-    // PV trails QK^T by one chunk: QK^T of chunk c+1 is issued before PV of c
-    int c_pv = 0, last_c = -1;
-    while (!failed) {
-      if (qk.valid()) {
-        issue_qk(qk);
-        qk.advance(p, ring);
-      }
-      if (c_pv >= qk.c) break;
-      issue_pv(c_pv);
-      last_c = c_pv++;
-    }
-    // Drain the last slots' completion arrivals so that no MMA commit lands on
-    // this CTA's shared memory after it exits.
+    // Drain the last slots' completion arrivals of this warp's ring so that
+    // no MMA commit lands on this CTA's shared memory after it exits.
+    const int r = is_qk ? 0 : 1;
     for (int c = last_c - kStages + 1 > 0 ? last_c - kStages + 1 : 0; c <= last_c && !failed; ++c) {
-      bool ok = mbar_wait(empty_bar(0, c % kStages), (c / kStages) & 1);
-      if (ok) ok = mbar_wait(empty_bar(1, c % kStages), (c / kStages) & 1);
+      const bool ok = mbar_wait(empty_bar(r, c % kStages), (c / kStages) & 1);
       if (!__all_sync(kFull, ok)) failed = true;
     }
-  } else if (warp < 4 || warp >= kWarpSmxB0) {
+  } else if (warp < 4 || (warp >= kWarpSmxB0 && warp < kWarpSmxB0 + 4)) {
     // ------------------------------ softmax -------------------------------
     // Group 0 (warps 0-3) takes query-head columns [0, kGA), group 1 (warps
     // 11-14, when G >= 2) columns [kGA, G). Each group has the CTA-wide max,
@@ -1024,17 +1023,6 @@ struct Dispatch {
       return BS == 16 ? occupancy_one<G, D, 16, FP16, KV8>() : occupancy_one<G, D, 32, FP16, KV8>();
     }
     return 1;
-  }
-#define PDA_TC_SWITCH(call)      \\
-  switch (G) {                   \\
-    case 1: return call<1>;      \\
-    case 2: return call<2>;      \\
-    case 3: return call<3>;      \\
-    case 4: return call<4>;      \\
-    case 5: return call<5>;      \\
-    case 6: return call<6>;      \\
-    case 7: return call<7>;      \\
-    case 8: return call<8>;      \\
   }
   static cudaError_t launch(int G, int BS, const CUtensorMap* tk, const CUtensorMap* tv,
                             const CUtensorMap* tq, const PartialParams& p, cudaStream_t s) {
