@@ -40,7 +40,10 @@
 //     zeroes the V rows of tokens past the context (so 0 * stale data never
 //     enters the MMA); then reads TMEM lane t of O (dim t) for its columns
 //     and folds it into a running fp32 accumulator with the online-softmax
-//     rescale. The two groups run the same chunk side by side.
+//     rescale. The two groups run the same chunk side by side. A unit's last
+//     chunk is folded after the next unit's first P is written, so a unit
+//     boundary does not wait for the last PV. The unit ring carries each
+//     unit decoded, so no role repeats its global loads.
 //   warps 4 and 5: producers, TMA page loads of K and of V into two separate
 //     3-slot rings (a slot is 128 tokens, 32 KiB): a K slot is released as
 //     soon as its QK^T completes, a V slot after its PV, so K loads run ahead.
@@ -100,6 +103,7 @@ constexpr uint32_t kTmemCols = 256;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kUnitRing = 4;               // slots of the shared unit queue
 constexpr int kUnitConsumers = 4;          // V producer, both MMA warps, softmax warp 0
+constexpr int kUnitInts = 12;              // a unit ring entry: index + decoded Unit
 // A finished unit's state, softmax -> epilogue, double-buffered:
 // acc[8][128], max[8], sum[8], unit index (floats; the index as int).
 constexpr int kEpiFloats = 8 * 128 + 8 + 8 + 4;
@@ -125,9 +129,10 @@ struct Layout {
   static constexpr int kOffBar = kOffLred + 2 * 4 * 8 * 4;
   static constexpr int kNumBars = 4 * kStages + 14 + 2 * kUnitRing + 4 + 2;
   static constexpr int kOffTmem = kOffBar + kNumBars * 8;
-  static constexpr int kOffURing = kOffTmem + 16;              // [kUnitRing] unit indices
-  static constexpr int kOffUBcast = kOffURing + kUnitRing * 4;  // unit index, warp 0 -> 1..3
-  static constexpr int kOffEpiFlag = kOffUBcast + 4;           // epilogue group's wait outcome
+  // [kUnitRing] unit index + decoded unit, so no reader repeats its global loads
+  static constexpr int kOffURing = kOffTmem + 16;
+  static constexpr int kOffUBcast = kOffURing + kUnitRing * kUnitInts * 4;  // same, softmax warp 0 -> rest
+  static constexpr int kOffEpiFlag = kOffUBcast + kUnitInts * 4;  // epilogue group's wait outcome
   static constexpr int kOffEpi = (kOffEpiFlag + 4 + 15) & ~15;
   static constexpr size_t kSmemBytes = 1024 + kOffEpi + 2 * kEpiFloats * 4;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -194,6 +199,35 @@ struct Unit {
   bool zero_fill;  // an empty context whose output rows this unit writes as zeros
 };
 
+// A unit index and its decoded Unit as kUnitInts ints in shared memory
+// (written by one thread, read by a whole warp).
+__device__ __forceinline__ void unit_put(volatile int* d, int u, const Unit& U) {
+  d[0] = u;
+  d[1] = U.b;
+  d[2] = U.h;
+  d[3] = U.split;
+  d[4] = U.n_splits_b;
+  d[5] = U.p0;
+  d[6] = U.p1;
+  d[7] = U.t0;
+  d[8] = U.t1;
+  d[9] = U.n_chunks;
+  d[10] = U.zero_fill ? 1 : 0;
+}
+__device__ __forceinline__ int unit_get(const volatile int* d, Unit& U) {
+  U.b = d[1];
+  U.h = d[2];
+  U.split = d[3];
+  U.n_splits_b = d[4];
+  U.p0 = d[5];
+  U.p1 = d[6];
+  U.t0 = d[7];
+  U.t1 = d[8];
+  U.n_chunks = d[9];
+  U.zero_fill = d[10] != 0;
+  return d[0];
+}
+
 template <int BS>
 __device__ __forceinline__ Unit load_unit(const PartialParams& p, int u) {
   constexpr int PPS = kT / BS;
@@ -230,11 +264,9 @@ template <int BS, typename Source>
 struct Cursor {
   int u, i, c, j;
   Unit U;
-  __device__ __forceinline__ void seek(const PartialParams& p, Source& src) {
-    while ((u = src.next()) >= 0) {
-      U = load_unit<BS>(p, u);
+  __device__ __forceinline__ void seek(const PartialParams&, Source& src) {
+    while ((u = src.next(U)) >= 0)
       if (U.n_chunks > 0) return;
-    }
   }
   __device__ __forceinline__ void start(const PartialParams& p, Source& src) {
     i = c = j = 0;
@@ -324,14 +356,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t full0, empty0;
     int lane, k;
     bool* failed;
-    __device__ __forceinline__ int next() {
+    __device__ __forceinline__ int next(Unit& U) {
       while (true) {
         int u = 0;
         if (lane == 0) u = atomicAdd(p->sched, 1);
         u = __shfl_sync(kFull, u, 0);
         const int pub = u < p->num_units ? u : -1;
         if (pub >= 0) {
-          const Unit U = load_unit<BS>(*p, pub);
+          U = load_unit<BS>(*p, pub);
           if (U.n_chunks == 0 && !U.zero_fill) continue;  // nothing to do for this unit
         }
         const int slot = k % kUnitRing;
@@ -342,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           return -1;
         }
         if (lane == 0) {
-          ring[slot] = pub;
+          unit_put(ring + slot * kUnitInts, pub, U);
           mbar_arrive(full0 + 8u * slot);
         }
         __syncwarp();
@@ -367,14 +399,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t full0, empty0;
     int lane, k;
     bool* failed;
-    __device__ __forceinline__ int next() {
+    __device__ __forceinline__ int next(Unit& U) {
       const int slot = k % kUnitRing;
       const bool ok = !*failed && mbar_wait(full0 + 8u * slot, (k / kUnitRing) & 1);
       if (!__all_sync(kFull, ok)) {
         *failed = true;
         return -1;
       }
-      const int u = ring[slot];
+      const int u = unit_get(ring + slot * kUnitInts, U);
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8u * slot);
       ++k;
@@ -692,8 +724,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* red = reinterpret_cast<float*>(base + kOffRed) + grp * 64;
       float* lred = reinterpret_cast<float*>(base + kOffLred) + grp * 32;
       float m_run[kGA], l_th[kGA], acc[kGA], alpha_prev[kGA];
-      // acc = acc * alpha(c) + O(c), this group's columns
-      auto fold = [&](int c) {
+      // A unit whose last chunk is not folded yet (u_pd >= 0): its state
+      // waits until the next unit's first P is written, so the unit boundary
+      // does not wait for the last PV to complete.
+      float m_pd[kGA], l_pd[kGA], acc_pd[kGA], alpha_pd[kGA];
+      int u_pd = -1;
+      // a = a * al + O(c), this group's columns
+      auto fold = [&](int c, float (&a)[kGA], const float (&al)[kGA]) {
         bool ok = !failed && mbar_wait(o_full(c & 1), (c >> 1) & 1);
         if (!__all_sync(kFull, ok)) failed = true;
         tc_fence_after();
@@ -709,26 +746,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(o_free(c & 1));
 #pragma unroll
-        for (int j = 0; j < kGA; ++j) acc[j] = acc[j] * alpha_prev[j] + o[j];
+        for (int j = 0; j < kGA; ++j) a[j] = a[j] * al[j] + o[j];
       };
       // Softmax warp 0 alone reads the unit ring and hands the index to the
       // other softmax warps, so all walk the same units through the same
       // named barriers (a late timeout in one warp cannot split them).
       RingSource ring = ring_source();
       volatile int* ubc = reinterpret_cast<volatile int*>(base + kOffUBcast);
+      Unit U;
       auto next_unit = [&]() {
         int u = -1;
-        if (warp == 0) u = ring.next();
-        if (warp == 0 && lane == 0) *ubc = u;
+        if (warp == 0) u = ring.next(U);
+        if (warp == 0 && lane == 0) unit_put(ubc, u, U);
         named_bar_sync(4, 128 * kGroups);
-        u = *ubc;
+        u = unit_get(ubc, U);
         named_bar_sync(4, 128 * kGroups);  // before warp 0 overwrites it
         return u;
       };
       int c = 0, je = 0;  // je: units handed to the epilogue group
       int jq = 0;         // units with chunks (the Q buffer sequence)
+      // Hands a finished unit's state (this group's columns) to the epilogue
+      // group: the softmax denominators are the per-token partial sums added
+      // over the group.
+      auto finish = [&](int uf, const float (&mf)[kGA], const float (&lf)[kGA],
+                        const float (&af)[kGA]) {
+#pragma unroll
+        for (int j = 0; j < kGA; ++j) {
+          float v = lf[j];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+          if (lane == 0) lred[wq * 8 + j] = v;
+        }
+        named_bar_sync(bar, 128);
+        float Ls[kGA];
+#pragma unroll
+        for (int j = 0; j < kGA; ++j) Ls[j] = lred[j] + lred[8 + j] + lred[16 + j] + lred[24 + j];
+        named_bar_sync(bar, 128);  // lred is rewritten by the next unit
+        const int es = je & 1;
+        bool ok2 = !failed;
+        if (ok2 && je >= 2) ok2 = mbar_wait(ep_empty(es), ((je - 2) >> 1) & 1);
+        if (!__all_sync(kFull, ok2)) failed = true;
+        float* st = reinterpret_cast<float*>(base + kOffEpi) + es * kEpiFloats;
+#pragma unroll
+        for (int j = 0; j < kGA; ++j)
+          if (j < ng) st[(g0 + j) * kHeadDim + t] = af[j];
+        if (t == 0) {
+#pragma unroll
+          for (int j = 0; j < kGA; ++j) {
+            if (j < ng) {
+              st[8 * kHeadDim + g0 + j] = mf[j];
+              st[8 * kHeadDim + 8 + g0 + j] = Ls[j];
+            }
+          }
+          if (grp == 0) reinterpret_cast<int*>(st)[8 * kHeadDim + 16] = uf;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ep_full(es));
+        ++je;
+      };
       for (int u = next_unit(); u >= 0; u = next_unit()) {
-        const Unit U = load_unit<BS>(p, u);
         const int hq0 = U.h * G;
         if (U.zero_fill && grp == 0) {
           for (int i = t; i < G * D; i += 128) {
@@ -836,49 +912,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(p_full(c & 1));
-          if (i > 0) fold(c - 1);
+          if (i > 0) {
+            fold(c - 1, acc, alpha_prev);
+          } else if (u_pd >= 0) {
+            // the previous unit's last chunk
+            fold(c - 1, acc_pd, alpha_pd);
+            finish(u_pd, m_pd, l_pd, acc_pd);
+            u_pd = -1;
+          }
 #pragma unroll
           for (int j = 0; j < kGA; ++j) alpha_prev[j] = alpha[j];
         }
-        fold(c - 1);
-        // softmax denominators: sum the per-token partial sums over the group
 #pragma unroll
         for (int j = 0; j < kGA; ++j) {
-          float v = l_th[j];
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
-          if (lane == 0) lred[wq * 8 + j] = v;
+          m_pd[j] = m_run[j];
+          l_pd[j] = l_th[j];
+          acc_pd[j] = acc[j];
+          alpha_pd[j] = alpha_prev[j];
         }
-        named_bar_sync(bar, 128);
-        float Ls[kGA];
-#pragma unroll
-        for (int j = 0; j < kGA; ++j) Ls[j] = lred[j] + lred[8 + j] + lred[16 + j] + lred[24 + j];
-        named_bar_sync(bar, 128);  // lred is rewritten by the next unit
-        // hand this group's part of the unit's state to the epilogue group
-        {
-          const int es = je & 1;
-          bool ok2 = !failed;
-          if (ok2 && je >= 2) ok2 = mbar_wait(ep_empty(es), ((je - 2) >> 1) & 1);
-          if (!__all_sync(kFull, ok2)) failed = true;
-          float* st = reinterpret_cast<float*>(base + kOffEpi) + es * kEpiFloats;
-#pragma unroll
-          for (int j = 0; j < kGA; ++j)
-            if (j < ng) st[(g0 + j) * kHeadDim + t] = acc[j];
-          if (t == 0) {
-#pragma unroll
-            for (int j = 0; j < kGA; ++j) {
-              if (j < ng) {
-                st[8 * kHeadDim + g0 + j] = m_run[j];
-                st[8 * kHeadDim + 8 + g0 + j] = Ls[j];
-              }
-            }
-            if (grp == 0) reinterpret_cast<int*>(st)[8 * kHeadDim + 16] = u;
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(ep_full(es));
-          ++je;
-        }
+        u_pd = u;
         ++jq;
+      }
+      if (u_pd >= 0) {
+        fold(c - 1, acc_pd, alpha_pd);
+        finish(u_pd, m_pd, l_pd, acc_pd);
       }
       // end of work: an empty state tells the epilogue group to stop
       {
