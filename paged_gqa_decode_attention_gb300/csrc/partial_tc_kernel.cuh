@@ -50,7 +50,8 @@
 //     The K producer also loads each unit's G query rows (a TMA box) into one
 //     of two Q operand buffers.
 //   warp 6: allocates 256 TMEM columns (S and O, double-buffered), issues
-//     the QK^T MMAs and commits their completion to mbarriers.
+//     the QK^T MMAs and commits their completion to mbarriers; with FP8 K/V
+//     it also turns each unit's 16-bit q tile into the two fp8 q terms.
 //   warp 15: issues the PV MMAs and commits their completion. The terms of a
 //     split operand (P_hi / P_lo; with FP8, q_hi / q_lo and the three P
 //     terms) are stacked along N, so each contraction step is one MMA.
@@ -559,18 +560,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
+      if (r == 0) cur_k.advance(p, fetch); else cur_v.advance(p, ring);
+    }
+  } else if (warp == kWarpMma || warp == kWarpMmaPV) {
+    // ------------------------------ MMA issue -----------------------------
+    // kind::f16: type fields 1 = bf16, 0 = f16; kind::f8f6f4: 0 = E4M3
+    constexpr uint32_t idesc_qk = idesc_f16(128, kSCols, !FP16 && !KV8, false, false);
+    constexpr uint32_t idesc_pv = idesc_f16(128, kOCols, !FP16 && !KV8, true, false);
+    // S(c) = K(c) . Q^T into S[c & 1]; needs the K slot, the unit's Q and the
+    // softmax's read of S(c-2)
+    auto issue_qk = [&](const Cursor<BS, RingSource>& cur) {
+      const int c = cur.c, slot = c % kStages, qb = cur.j & 1;
+      bool ok = !failed;
+      if (ok && cur.i == 0) ok = mbar_wait(q_full(qb), (cur.j >> 1) & 1);
+      if (!__all_sync(kFull, ok)) failed = true;
+      if (failed) return;
       if constexpr (KV8) {
-        if (r == 0 && cu_i == 0) {
+        if (cur.i == 0) {
           // The unit's q rows (16-bit tile from TMA) become two fp8 terms,
           // q * sigma = hi + lo, with a power-of-two sigma per row that puts
           // the row's largest |q| in [128, 256): the fp8 QK^T then sees q
           // exactly except for elements below 2^-10 of the row maximum.
-          const int qb = cu_j & 1;
-          const bool okq = mbar_wait(q_full(qb), (cu_j >> 1) & 1);
-          if (!__all_sync(kFull, okq)) {
-            failed = true;
-            break;
-          }
+          // Done here, not in the K producer, so the TMA rings never wait for
+          // a unit's Q.
           const uint8_t* qt = base + kOffQ + qb * kOpBytes;
           uint8_t* q8 = base + kOffQ8 + qb * kOpBytes;
           float* qs = reinterpret_cast<float*>(base + kOffQs) + qb * 8;
@@ -601,23 +613,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(q8_full(qb));
+          if (lane == 0) mbar_arrive(q8_full(qb));  // the row scales, for the softmax
         }
       }
-      if (r == 0) cur_k.advance(p, fetch); else cur_v.advance(p, ring);
-    }
-  } else if (warp == kWarpMma || warp == kWarpMmaPV) {
-    // ------------------------------ MMA issue -----------------------------
-    // kind::f16: type fields 1 = bf16, 0 = f16; kind::f8f6f4: 0 = E4M3
-    constexpr uint32_t idesc_qk = idesc_f16(128, kSCols, !FP16 && !KV8, false, false);
-    constexpr uint32_t idesc_pv = idesc_f16(128, kOCols, !FP16 && !KV8, true, false);
-    // S(c) = K(c) . Q^T into S[c & 1]; needs the K slot, the unit's Q and the
-    // softmax's read of S(c-2)
-    auto issue_qk = [&](const Cursor<BS, RingSource>& cur) {
-      const int c = cur.c, slot = c % kStages, qb = cur.j & 1;
-      bool ok = !failed && mbar_wait(full_bar(0, slot), (c / kStages) & 1);
+      ok = mbar_wait(full_bar(0, slot), (c / kStages) & 1);
       if (ok && c >= 2) ok = mbar_wait(s_free(c & 1), ((c - 2) >> 1) & 1);
-      if (ok && cur.i == 0) ok = mbar_wait(KV8 ? q8_full(qb) : q_full(qb), (cur.j >> 1) & 1);
       if (!__all_sync(kFull, ok)) failed = true;
       if (failed) return;
       tc_fence_after();
