@@ -96,7 +96,7 @@ void plan_splits(const pda_config& c, int kernel, int num_sms, int ctas_per_sm, 
     S = forced < cap ? forced : cap;
   } else {
     const int64_t base = (int64_t)(batch > 0 ? batch : 1) * c.num_kv_heads;
-    const int64_t slots = (int64_t)(num_sms > 0 ? num_sms : 1) * (ctas_per_sm > 0 ? ctas_per_sm : 1);
+    const int64_t slots = pda::planning_slots(kernel, c.kv_fp8 != 0, num_sms, ctas_per_sm);
     double best = INFINITY;
     for (int s = 1; s <= cap; ++s) {
       const int chunk = ceil_div(max_pages, s);
@@ -192,6 +192,18 @@ struct DeviceGuard {
 }  // namespace
 
 int pda::set_last_error(int code, const char* msg) { return fail(code, msg); }
+
+int pda::planning_slots(int kernel, bool kv_fp8, int num_sms, int ctas_per_sm) {
+  static const int forced = [] {
+    const char* e = std::getenv("PDA_PLAN_SLOTS");
+    return e ? std::atoi(e) : 0;
+  }();
+  const int slots = (num_sms > 0 ? num_sms : 1) * (ctas_per_sm > 0 ? ctas_per_sm : 1);
+  int n = slots;
+  if (kernel == kPartialTensorCore && !kv_fp8) n = (slots * 27) / 32;
+  if (forced > 0) n = forced;
+  return n < 1 ? 1 : (n > slots ? slots : n);
+}
 
 bool pda::pdl_enabled() {
   static const bool on = [] {

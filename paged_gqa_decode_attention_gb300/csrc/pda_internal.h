@@ -88,6 +88,17 @@ constexpr int partial_ctas_per_sm_hint(int kernel, int group, int head_dim) {
                                       : ((group * head_dim > 512 || head_dim >= 256) ? 1 : 2);
 }
 
+// Work slots per wave the split planner counts on. Measured on GB300
+// (split-count sweeps of the B=4 L=32768, B=1 L=32768 and B=1 / B=4 L=8192
+// steps): a few long streams per SM do best when one wave covers the whole
+// step, and the tensor-core kernel with 16-bit K/V saturates HBM with about
+// 27/32 of the SMs (128 of 152). So it plans for 128 units of one wave (B=4
+// L=32768: 0.932-0.945 of peak, against 0.912-0.925 with two units on each
+// of 152 CTAs). The launch still uses every SM, so steps of many short units
+// balance over all of them. FP8 K/V is limited per SM and plans for every
+// SM, as does the CUDA-core kernel. PDA_PLAN_SLOTS overrides (experiments).
+int planning_slots(int kernel, bool kv_fp8, int num_sms, int ctas_per_sm);
+
 // kv_fp8: K/V caches hold FP8 E4M3 (tensor-core kernel, D 128, bf16 q).
 bool partial_supported(int group, int head_dim, int block_size, int dtype, bool kv_fp8);
 bool partial_kernel_supported(int kernel, int group, int head_dim, bool kv_fp8);

@@ -132,9 +132,11 @@ def test_plan_no_split_when_grid_is_full(lib):
 
 
 def test_plan_splits_long_contexts_to_fill_the_gpu(lib):
+    # the 16-bit tensor-core kernel plans one wave over 27/32 of the SMs (128 of 152)
     S1, _ = plan(1, 512)    # B=1, L=8192: 8 CTAs without splitting
     S4, _ = plan(4, 2048)   # B=4, L=32768
-    assert S1 * 8 >= 152 and S4 * 32 >= 152
+    assert S1 * 8 >= 128 and S4 * 32 >= 128
+    assert S1 * 8 <= 152 and S4 * 32 <= 152    # one wave: no CTA takes a second unit
     assert plan(1, 2048)[0] >= plan(4, 2048)[0]
 
 
