@@ -46,7 +46,9 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC_BYTES = {
     # profiles/paged_partial_tc_kernel_long_b4_l32768.md: 537.15 MB read + 3.38 MB
     # written per launch (captured on the same step over a 1 GiB pool)
-    "long_b4_l32768": None,  # kernel changed since the last capture
+    # profiles/paged_partial_tc_kernel_long_b4_l32768.md: 537.04 MB read + 3.74 MB
+    # written per launch (captured on the same step over a 1 GiB pool)
+    "long_b4_l32768": 540_774_912,
     # profiles/rope_kv_write_kernel_prefill_t32768.md: 419.90 MB read + 348.27 MB written
     "rope_prefill_t32768": 768_166_400,
 }
