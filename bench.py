@@ -333,6 +333,18 @@ def run_reference(args):
     return 0
 
 
+def partial_kernel_label(wl) -> str:
+    """Which partial kernel the library runs for this geometry: tensor cores
+    for FP8 K/V and for groups of 3..8 at head dim 64/128, CUDA cores
+    otherwise (PDA_PARTIAL_KERNEL overrides)."""
+    env = os.environ.get("PDA_PARTIAL_KERNEL", "")
+    G = wl.num_q_heads // wl.num_kv_heads
+    tc = env == "tensor_core" or (env != "cuda_core" and (
+        wl.kv_fp8 or (3 <= G <= 8 and wl.head_dim in (64, 128))))
+    return ("paged_partial_tc_kernel (tcgen05 split-K partials + fused LSE merge)" if tc else
+            "paged_partial_kernel (CUDA-core split-K partials + fused LSE merge)")
+
+
 def e2e_graph(attn, wl, out, args, ksc, vsc, dev, world):
     """End-to-end tokens/s through the public API with host-resident inputs
     and output: per step one graph (H2D copy of the packed inputs, run, D2H
@@ -537,7 +549,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} (hbm_gbs)",
-                     "kernel": "paged_partial_tc_kernel (tcgen05 split-K partials + fused LSE merge)",
+                     "kernel": partial_kernel_label(wl),
                      "per_launch_ms": avg_launch_ms},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "mode": e2e_mode},
