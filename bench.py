@@ -93,6 +93,22 @@ def make_workload(name: str, seed: int, device):
     if name == "geo_d256_b16_l8192":  # 16/8 heads, D 256 (G = 2)
         return W.custom(seed=seed, B=16, Hq=16, Hkv=8, D=256, block_size=16, lens=[8192] * 16,
                         device=device)
+    # the headline's bytes (B x L x 8 kv heads) at other group sizes / head dims
+    if name == "geo_g1_b4_l32768":  # 8/8 heads (G = 1), D 128
+        return W.custom(seed=seed, B=4, Hq=8, Hkv=8, D=128, block_size=16, lens=[32768] * 4,
+                        device=device)
+    if name == "geo_g2_b4_l32768":  # 16/8 heads (G = 2), D 128
+        return W.custom(seed=seed, B=4, Hq=16, Hkv=8, D=128, block_size=16, lens=[32768] * 4,
+                        device=device)
+    if name == "geo_g8_b4_l32768":  # 64/8 heads (G = 8), D 128
+        return W.custom(seed=seed, B=4, Hq=64, Hkv=8, D=128, block_size=16, lens=[32768] * 4,
+                        device=device)
+    if name == "geo_d64_b8_l32768":  # 32/8 heads, D 64 (B = 8: the same bytes)
+        return W.custom(seed=seed, B=8, Hq=32, Hkv=8, D=64, block_size=16, lens=[32768] * 8,
+                        device=device)
+    if name == "long_b8_l32768_fp8_g8":  # FP8 cache, 64/8 heads
+        return W.to_fp8_kv(W.custom(seed=seed, B=8, Hq=64, Hkv=8, D=128, block_size=16,
+                                    lens=[32768] * 8, device=device))
     if name == "geo_mqa_b64_l8192":  # MQA: 8 query heads on one kv head, D 128
         return W.custom(seed=seed, B=64, Hq=8, Hkv=1, D=128, block_size=16, lens=[8192] * 64,
                         device=device)
