@@ -35,12 +35,12 @@ int cuda_fail(const char* what, cudaError_t e) {
 // Planner cost constants, in token-equivalents of one CTA's streaming time:
 // the fixed cost of a work unit (q and first-page latency, the unit's state
 // hand-off, partial write and merge ticket) and of merging split partials.
-// Chosen from split-count sweeps on GB300 (B=1 L=32768, B=4 L=8192,
-// B=4 / B=8 L=32768, the 128-sequence serving mix, 28/4-head B=16 L=8192):
-// a unit of the persistent tensor-core kernel costs about 512 tokens, a CTA
-// of the CUDA-core kernel about 256; with these the planner's pick is the
-// fastest measured split count or within 2% of it on every case but the
-// ragged serving mix (planned from its longest sequence).
+// Chosen from split-count sweeps on GB300 (B=1 and B=4 at L=8192 and
+// L=32768, FP8 B=8 L=32768, the 128-sequence serving mix, 28/4-head B=16
+// L=8192): a unit of the persistent tensor-core kernel costs about 512
+// tokens, a CTA of the CUDA-core kernel about 256; with these (and the
+// planning slots below) the planner's pick is the fastest measured split
+// count or within 2% of it on every one of those cases.
 constexpr int kOverheadTokensCudaCore = 256;
 constexpr int kOverheadTokensTensorCore = 512;
 constexpr int kMergeTokens = 96;
