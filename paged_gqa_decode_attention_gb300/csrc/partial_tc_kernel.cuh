@@ -16,8 +16,8 @@
 //   O^T [128 dims   x 32]  = V_chunk^T [128 dims x 128 tokens] . [P_hi; P_lo]^T
 //
 // (rows G..15 of each 16-row block of Q and P are zero; at D = 64 the QK^T
-// contraction is 64 deep and the upper 64 dims of every V slot are zero, so
-// O^T rows 64..127 come out zero). Both are M=128 tcgen05.mma (kind::f16,
+// contraction is 64 deep and PV is an M = 64 MMA over 16 KiB slots, so the
+// rings hold six chunks). Both are tcgen05.mma (kind::f16,
 // fp32 accumulate in TMEM) issued by one thread; the K and V tiles are
 // consumed straight from the TMA-written, 128-byte-swizzled stage: K as a
 // K-major A operand, V as an MN-major A operand. The probabilities P are
@@ -110,14 +110,15 @@ constexpr int kUnitInts = 12;              // a unit ring entry: index + decoded
 constexpr int kEpiFloats = 8 * 128 + 8 + 8 + 4;
 constexpr float kP8Scale = 256.f;          // FP8 K/V: P is split at p * 256
 
-// Shared-memory layout. 16-bit K/V: 3-slot rings of 32 KiB slots (two
-// 64-dim halves of 128 tokens). FP8 K/V (KV8): 5-slot rings of 16 KiB slots
-// (one 128-byte row per token), two fp8 terms of Q next to the 16-bit Q
-// tile, three fp8 terms of P in the P buffers.
-template <bool KV8>
+// Shared-memory layout. 16-bit K/V at D 128: 3-slot rings of 32 KiB slots
+// (two 64-dim halves of 128 tokens). 16-bit K/V at D 64: 6-slot rings of
+// 16 KiB slots (one 64-dim half), the same bytes in flight. FP8 K/V (KV8):
+// 5-slot rings of 16 KiB slots (one 128-byte row per token), two fp8 terms
+// of Q next to the 16-bit Q tile, three fp8 terms of P in the P buffers.
+template <bool KV8, int D = 128>
 struct Layout {
-  static constexpr int kStages = KV8 ? 5 : 3;
-  static constexpr int kSlotBytes = KV8 ? kT * 128 : 2 * kHalf;
+  static constexpr int kStages = KV8 ? 5 : (D == 64 ? 6 : 3);
+  static constexpr int kSlotBytes = KV8 ? kT * 128 : (D / 64) * kHalf;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kStages * kSlotBytes;
   static constexpr int kOffQ = 2 * kStages * kSlotBytes;  // [2 buffers] Q tiles (TMA)
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(G >= 1 && G <= 8, "tensor-core path packs up to 8 query heads");
   static_assert(D == 64 || D == 128, "head dim 64 or 128");
   static_assert(!KV8 || (D == 128 && !FP16), "FP8 K/V: head dim 128, bf16 queries");
-  using L = Layout<KV8>;
+  using L = Layout<KV8, D>;
   constexpr int kStages = L::kStages;
   constexpr int kSlotBytes = L::kSlotBytes;
   constexpr int kOffK = L::kOffK;
@@ -452,16 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp < 4) {
     // Q operands (rows G..15 stay zero; the TMA box fills rows 0..G-1) and
-    // both P operand pairs start zeroed; at D = 64 the upper (dims 64..127)
-    // half of every V slot is zero for the whole kernel.
+    // both P operand pairs start zeroed.
     for (int i = threadIdx.x; i < (kOffQs - kOffQ) / 16; i += 128)
       *reinterpret_cast<uint4*>(base + kOffQ + i * 16) = make_uint4(0, 0, 0, 0);
-    if constexpr (D == 64) {
-      for (int s2 = 0; s2 < kStages; ++s2)
-        for (int i = threadIdx.x; i < kHalf / 16; i += 128)
-          *reinterpret_cast<uint4*>(base + kOffV + s2 * kSlotBytes + kHalf + i * 16) =
-              make_uint4(0, 0, 0, 0);
-    }
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -566,7 +560,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------ MMA issue -----------------------------
     // kind::f16: type fields 1 = bf16, 0 = f16; kind::f8f6f4: 0 = E4M3
     constexpr uint32_t idesc_qk = idesc_f16(128, kSCols, !FP16 && !KV8, false, false);
-    constexpr uint32_t idesc_pv = idesc_f16(128, kOCols, !FP16 && !KV8, true, false);
+    // PV has M = D: at D 64 an M = 64 MMA, whose accumulator rows 16 q .. 16 q + 15
+    // sit in TMEM lanes 32 q .. 32 q + 15
+    constexpr uint32_t idesc_pv = idesc_f16(D, kOCols, !FP16 && !KV8, true, false);
     // S(c) = K(c) . Q^T into S[c & 1]; needs the K slot, the unit's Q and the
     // softmax's read of S(c-2)
     auto issue_qk = [&](const Cursor<BS, RingSource>& cur) {
@@ -716,7 +712,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int grp = warp >= kWarpSmxB0 ? 1 : 0;
     if (grp < kGroups) {
       const int wq = warp & 3;        // TMEM lane quadrant: warp w reads lanes 32 (w % 4) ..
-      const int t = wq * 32 + lane;   // token row of S; output dim of O
+      const int t = wq * 32 + lane;   // token row of S; output dim of O (D 128)
+      // D 64 (M = 64 PV): lanes 0-15 of quadrant q hold output dims 16 q .. 16 q + 15
+      const int od = D == 64 ? 16 * wq + lane : t;
+      const bool od_ok = D != 64 || lane < 16;
       const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
       const int g0 = grp ? kGA : 0;   // first column of this group
       const int ng = grp ? G - kGA : kGA;
@@ -789,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* st = reinterpret_cast<float*>(base + kOffEpi) + es * kEpiFloats;
 #pragma unroll
         for (int j = 0; j < kGA; ++j)
-          if (j < ng) st[(g0 + j) * kHeadDim + t] = af[j];
+          if (j < ng && od_ok) st[(g0 + j) * kHeadDim + od] = af[j];
         if (t == 0) {
 #pragma unroll
           for (int j = 0; j < kGA; ++j) {
@@ -1020,7 +1019,7 @@ cudaError_t launch_one(const CUtensorMap* tk, const CUtensorMap* tv, const CUten
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ctas);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Layout<KV8>::kSmemBytes;
+  cfg.dynamicSmemBytes = Layout<KV8, D>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1034,7 +1033,7 @@ template <int G, int D, int BS, bool FP16, bool KV8>
 cudaError_t prepare_one() {
   return cudaFuncSetAttribute(paged_partial_tc_kernel<G, D, BS, FP16, KV8>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)Layout<KV8>::kSmemBytes);
+                              (int)Layout<KV8, D>::kSmemBytes);
 }
 
 template <int G, int D, int BS, bool FP16, bool KV8>
@@ -1042,7 +1041,7 @@ int occupancy_one() {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
           &n, paged_partial_tc_kernel<G, D, BS, FP16, KV8>, kThreads,
-          Layout<KV8>::kSmemBytes) != cudaSuccess)
+          Layout<KV8, D>::kSmemBytes) != cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }
