@@ -31,7 +31,7 @@
 // overlap. So the terms are stacked (half the PV instructions), and QK^T
 // and PV are issued by two different warps.
 //
-// Warp roles (512 threads):
+// Warp roles (576 threads):
 //   warps 0-3 and 11-14: softmax, two groups of four that split the G query
 //     heads' columns (group 0 the first ceil(G/2), group 1 the rest; G = 1
 //     uses one group). Thread t of a group reads TMEM lane t of S (token t of
@@ -44,11 +44,14 @@
 //     chunk is folded after the next unit's first P is written, so a unit
 //     boundary does not wait for the last PV. The unit ring carries each
 //     unit decoded, so no role repeats its global loads.
-//   warps 4 and 5: producers, TMA page loads of K and of V into two separate
-//     3-slot rings (a slot is 128 tokens, 32 KiB): a K slot is released as
-//     soon as its QK^T completes, a V slot after its PV, so K loads run ahead.
-//     The K producer also loads each unit's G query rows (a TMA box) into one
-//     of two Q operand buffers.
+//   warps 4 (K) and 5 (V): producers, TMA page loads of K and of V into two
+//     separate 3-slot rings (a slot is 128 tokens, 32 KiB). A K slot is
+//     released as soon as its QK^T completes, a V slot after its PV, so K
+//     loads run ahead. Warp 4 also takes the work units and loads each
+//     unit's G query rows (a TMA box) into one of two Q operand buffers.
+//     With FP8 K/V or D 64 (half the bytes per chunk) warps 16 (K) and 17
+//     (V) are second producers and the two warps of a ring take alternate
+//     chunks; otherwise they idle.
 //   warp 6: allocates 256 TMEM columns (S and O, double-buffered), issues
 //     the QK^T MMAs and commits their completion to mbarriers; with FP8 K/V
 //     it also turns each unit's 16-bit q tile into the two fp8 q terms.
@@ -88,13 +91,15 @@ constexpr int kHalf = kT * kRowBytes;      // one half tile: 16 KiB
 constexpr int kN = 16;                     // MMA N: the group's query heads, padded
 constexpr int kOpHalf = 2048;              // 16 rows x 128 B of a K-major operand half
 constexpr int kOpBytes = 2 * kOpHalf;      // Q, P_hi or P_lo operand
-constexpr int kThreads = 512;
+constexpr int kThreads = 576;
 constexpr int kWarpProducerK = 4;
 constexpr int kWarpProducerV = 5;
 constexpr int kWarpMma = 6;                // issues QK^T (and owns the TMEM allocation)
 constexpr int kWarpEpi0 = 7;               // warps 7-10: epilogue group
 constexpr int kWarpSmxB0 = 11;             // warps 11-14: second softmax group
 constexpr int kWarpMmaPV = 15;             // issues PV
+constexpr int kWarpProducerK2 = 16;        // second K producer (odd chunks)
+constexpr int kWarpProducerV2 = 17;        // second V producer (odd chunks)
 // TMEM columns: S and O, double-buffered. The terms of a split operand are
 // stacked along N so one MMA carries all of them (the tensor pipe's cost
 // is per instruction at these small N): S holds 16 columns (32 with FP8
@@ -103,7 +108,9 @@ constexpr int kWarpMmaPV = 15;             // issues PV
 constexpr uint32_t kTmemCols = 256;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kUnitRing = 4;               // slots of the shared unit queue
-constexpr int kUnitConsumers = 4;          // V producer, both MMA warps, softmax warp 0
+// unit ring readers: V producer, both MMA warps, softmax warp 0 (+ the two
+// second producers when a ring has two)
+constexpr int kUnitConsumers = 4;
 constexpr int kUnitInts = 12;              // a unit ring entry: index + decoded Unit
 // A finished unit's state, softmax -> epilogue, double-buffered:
 // acc[8][128], max[8], sum[8], unit index (floats; the index as int).
@@ -313,6 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NB = D / 64;    // 64-dim boxes per row
   constexpr int PPS = kT / BS;  // pages per stage
   constexpr int kGroups = G >= 2 ? 2 : 1;  // softmax warp groups (query-head columns split)
+  // Two producer warps per ring for the half-byte chunks (FP8 K/V, D 64),
+  // whose per-chunk TMA issue kept one warp per ring busy most of the time;
+  // at 16-bit D 128 one warp per ring measured as fast or faster.
+  constexpr bool kDual = KV8 || D == 64;
   constexpr int kGA = (G + 1) / 2 > 0 ? (G + 1) / 2 : 1;  // columns of group 0 (group 1: G - kGA)
   static_assert(kT % BS == 0 && PPS <= 32, "stage must hold whole pages");
   using TNat = std::conditional_t<FP16, __half, __nv_bfloat16>;
@@ -422,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s2 = 0; s2 < kUnitRing; ++s2) {
       mbar_init(uring_full(s2), 1);
-      mbar_init(uring_empty(s2), kUnitConsumers);
+      mbar_init(uring_empty(s2), kUnitConsumers + (kDual ? 2 : 0));
     }
     for (int s2 = 0; s2 < 2; ++s2) {
       mbar_init(ep_full(s2), 4 * kGroups);
@@ -471,32 +482,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tS = [&](int b2) { return tmem + (uint32_t)(b2 * kSCols); };
   auto tO = [&](int b2) { return tmem + (uint32_t)(2 * kSCols + b2 * kOCols); };
 
-  if (warp == kWarpProducerK || warp == kWarpProducerV) {
-    // ------------------- producers: K ring (warp 4), V ring (warp 5) -------------------
-    const int r = warp - kWarpProducerK;
+  if (warp == kWarpProducerK || warp == kWarpProducerV || (kDual && warp >= kWarpProducerK2)) {
+    // ------- producers: K ring (warps 4, 16), V ring (warps 5, 17) -------
+    // With kDual each ring has two producer warps that take alternate
+    // chunks: one thread issues a TMA box in ~80 cycles, so a single warp
+    // per ring spent most of a half-byte chunk's time issuing its boxes.
+    // Warp 4 also takes units from the counter and loads each unit's Q; the
+    // others follow the unit ring.
+    const int r = (warp == kWarpProducerV || warp == kWarpProducerV2) ? 1 : 0;
+    const int par = warp >= kWarpProducerK2 ? 1 : 0;  // this warp's chunks: c % 2 == par
+    const bool fetcher = warp == kWarpProducerK;
     const CUtensorMap* map = r == 0 ? &tmap_k : &tmap_v;
     if (lane == 0) {
       prefetch_tensormap(map);
-      if (r == 0) prefetch_tensormap(&tmap_q);
+      if (fetcher) prefetch_tensormap(&tmap_q);
     }
     FetchSource fetch{&p, uring, uring_full(0), uring_empty(0), lane, 0, &failed};
     RingSource ring = ring_source();
     Cursor<BS, FetchSource> cur_k;
     Cursor<BS, RingSource> cur_v;
-    if (r == 0) cur_k.start(p, fetch); else cur_v.start(p, ring);
+    if (fetcher) cur_k.start(p, fetch); else cur_v.start(p, ring);
     // block-table entries in windows of 32 pages, the next window prefetched
     int win_base = 0, win_blk = 0, nxt_blk = 0;
-    while (!failed && (r == 0 ? cur_k.valid() : cur_v.valid())) {
-      const int cu_i = r == 0 ? cur_k.i : cur_v.i;
-      const int cu_c = r == 0 ? cur_k.c : cur_v.c;
-      const int cu_j = r == 0 ? cur_k.j : cur_v.j;
-      const Unit& U = r == 0 ? cur_k.U : cur_v.U;
+    while (!failed && (fetcher ? cur_k.valid() : cur_v.valid())) {
+      const int cu_i = fetcher ? cur_k.i : cur_v.i;
+      const int cu_c = fetcher ? cur_k.c : cur_v.c;
+      const int cu_j = fetcher ? cur_k.j : cur_v.j;
+      const Unit& U = fetcher ? cur_k.U : cur_v.U;
       const int32_t* table = p.block_table + (int64_t)U.b * p.max_blocks;
       if (cu_i == 0) {
         win_base = U.p0;
         win_blk = (U.p0 + lane < U.p1) ? __ldg(table + U.p0 + lane) : 0;
         nxt_blk = (U.p0 + 32 + lane < U.p1) ? __ldg(table + U.p0 + 32 + lane) : 0;
-        if (r == 0) {
+        if (fetcher) {
           // this unit's G query rows -> Q operand buffer j & 1
           const int qb = cu_j & 1;
           bool ok = true;
@@ -517,14 +535,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const int c = cu_c;
-      const int slot = c % kStages;
-      if (c >= kStages) {
-        const bool ok = mbar_wait(empty_bar(r, slot), ((c / kStages) - 1) & 1);
-        if (!__all_sync(kFull, ok)) {
-          failed = true;
-          break;
-        }
-      }
       const int pg0 = U.p0 + cu_i * PPS;
       const int npg = min(PPS, U.p1 - pg0);
       if (pg0 + PPS > win_base + 32) {  // pg0 == win_base + 32: PPS divides 32
@@ -532,30 +542,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         win_blk = nxt_blk;
         nxt_blk = (win_base + 32 + lane < U.p1) ? __ldg(table + win_base + 32 + lane) : 0;
       }
-      int blk[PPS];
-#pragma unroll
-      for (int i = 0; i < PPS; ++i) blk[i] = __shfl_sync(kFull, win_blk, (pg0 + i - win_base) & 31);
-      if (lane == 0) {
-        const uint32_t fb = full_bar(r, slot);
-        // 16-bit K/V: D / 64 boxes of 64 dims per page; FP8: one box of D bytes
-        constexpr int kBoxes = KV8 ? 1 : NB;
-        constexpr int kBoxElems = KV8 ? D : 64;
-        mbar_arrive_expect_tx(fb, (uint32_t)npg * BS * kBoxes * kRowBytes);
-        const uint32_t st = base_u32 + (r == 0 ? kOffK : kOffV) + slot * kSlotBytes;
-#pragma unroll
-        for (int i = 0; i < PPS; ++i) {
-          if (i < npg) {
-            const int y = blk[i] * BS;
-            const uint32_t ro = (uint32_t)(i * BS * kRowBytes);
-#pragma unroll
-            for (int bx = 0; bx < kBoxes; ++bx)
-              tma_load_2d(st + bx * kHalf + ro, map, U.h * D + bx * kBoxElems, y, fb);
+      if (!kDual || (c & 1) == par) {  // this warp's chunk
+        const int slot = c % kStages;
+        if (c >= kStages) {
+          const bool ok = mbar_wait(empty_bar(r, slot), ((c / kStages) - 1) & 1);
+          if (!__all_sync(kFull, ok)) {
+            failed = true;
+            break;
           }
         }
+        int blk[PPS];
+#pragma unroll
+        for (int i = 0; i < PPS; ++i) blk[i] = __shfl_sync(kFull, win_blk, (pg0 + i - win_base) & 31);
+        if (lane == 0) {
+          const uint32_t fb = full_bar(r, slot);
+          // 16-bit K/V: D / 64 boxes of 64 dims per page; FP8: one box of D bytes
+          constexpr int kBoxes = KV8 ? 1 : NB;
+          constexpr int kBoxElems = KV8 ? D : 64;
+          mbar_arrive_expect_tx(fb, (uint32_t)npg * BS * kBoxes * kRowBytes);
+          const uint32_t st = base_u32 + (r == 0 ? kOffK : kOffV) + slot * kSlotBytes;
+#pragma unroll
+          for (int i = 0; i < PPS; ++i) {
+            if (i < npg) {
+              const int y = blk[i] * BS;
+              const uint32_t ro = (uint32_t)(i * BS * kRowBytes);
+#pragma unroll
+              for (int bx = 0; bx < kBoxes; ++bx)
+                tma_load_2d(st + bx * kHalf + ro, map, U.h * D + bx * kBoxElems, y, fb);
+            }
+          }
+        }
+        __syncwarp();
       }
-      __syncwarp();
-      if (r == 0) cur_k.advance(p, fetch); else cur_v.advance(p, ring);
+      if (fetcher) cur_k.advance(p, fetch); else cur_v.advance(p, ring);
     }
+  } else if (warp >= kWarpProducerK2) {
+    // second producers: idle unless kDual
   } else if (warp == kWarpMma || warp == kWarpMmaPV) {
     // ------------------------------ MMA issue -----------------------------
     // kind::f16: type fields 1 = bf16, 0 = f16; kind::f8f6f4: 0 = E4M3
