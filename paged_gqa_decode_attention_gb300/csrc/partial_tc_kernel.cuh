@@ -31,7 +31,7 @@
 // overlap. So the terms are stacked (half the PV instructions), and QK^T
 // and PV are issued by two different warps.
 //
-// Warp roles (576 threads):
+// Warp roles (512 threads; 576 with second producers):
 //   warps 0-3 and 11-14: softmax, two groups of four that split the G query
 //     heads' columns (group 0 the first ceil(G/2), group 1 the rest; G = 1
 //     uses one group). Thread t of a group reads TMEM lane t of S (token t of
@@ -49,9 +49,9 @@
 //     released as soon as its QK^T completes, a V slot after its PV, so K
 //     loads run ahead. Warp 4 also takes the work units and loads each
 //     unit's G query rows (a TMA box) into one of two Q operand buffers.
-//     With FP8 K/V or D 64 (half the bytes per chunk) warps 16 (K) and 17
-//     (V) are second producers and the two warps of a ring take alternate
-//     chunks; otherwise they idle.
+//     With FP8 K/V or D 64 (half the bytes per chunk) at G <= 4, warps 16
+//     (K) and 17 (V) are second producers and the two warps of a ring take
+//     alternate chunks (the CTA has 18 warps then, else 16).
 //   warp 6: allocates 256 TMEM columns (S and O, double-buffered), issues
 //     the QK^T MMAs and commits their completion to mbarriers; with FP8 K/V
 //     it also turns each unit's 16-bit q tile into the two fp8 q terms.
@@ -91,7 +91,16 @@ constexpr int kHalf = kT * kRowBytes;      // one half tile: 16 KiB
 constexpr int kN = 16;                     // MMA N: the group's query heads, padded
 constexpr int kOpHalf = 2048;              // 16 rows x 128 B of a K-major operand half
 constexpr int kOpBytes = 2 * kOpHalf;      // Q, P_hi or P_lo operand
-constexpr int kThreads = 576;
+// Two producer warps per ring for the half-byte chunks (FP8 K/V, D 64) at
+// G <= 4, whose per-chunk TMA issue kept one warp per ring busy most of the
+// time; elsewhere one warp per ring measured as fast or faster, and the
+// extra warps' launch size (and register cap) slowed G >= 7.
+__host__ __device__ constexpr bool dual_producers(int G, int D, bool kv8) {
+  return (kv8 || D == 64) && G <= 4;
+}
+__host__ __device__ constexpr int tc_threads(int G, int D, bool kv8) {
+  return dual_producers(G, D, kv8) ? 576 : 512;
+}
 constexpr int kWarpProducerK = 4;
 constexpr int kWarpProducerV = 5;
 constexpr int kWarpMma = 6;                // issues QK^T (and owns the TMEM allocation)
@@ -293,7 +302,7 @@ struct Cursor {
 };
 
 template <int G, int D, int BS, bool FP16, bool KV8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     paged_partial_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v,
                             const __grid_constant__ CUtensorMap tmap_q, const PartialParams p) {
@@ -320,10 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NB = D / 64;    // 64-dim boxes per row
   constexpr int PPS = kT / BS;  // pages per stage
   constexpr int kGroups = G >= 2 ? 2 : 1;  // softmax warp groups (query-head columns split)
-  // Two producer warps per ring for the half-byte chunks (FP8 K/V, D 64),
-  // whose per-chunk TMA issue kept one warp per ring busy most of the time;
-  // at 16-bit D 128 one warp per ring measured as fast or faster.
-  constexpr bool kDual = KV8 || D == 64;
+  constexpr bool kDual = dual_producers(G, D, KV8);
   constexpr int kGA = (G + 1) / 2 > 0 ? (G + 1) / 2 : 1;  // columns of group 0 (group 1: G - kGA)
   static_assert(kT % BS == 0 && PPS <= 32, "stage must hold whole pages");
   using TNat = std::conditional_t<FP16, __half, __nv_bfloat16>;
@@ -482,7 +488,95 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tS = [&](int b2) { return tmem + (uint32_t)(b2 * kSCols); };
   auto tO = [&](int b2) { return tmem + (uint32_t)(2 * kSCols + b2 * kOCols); };
 
-  if (warp == kWarpProducerK || warp == kWarpProducerV || (kDual && warp >= kWarpProducerK2)) {
+  if (!kDual && (warp == kWarpProducerK || warp == kWarpProducerV)) {
+    // one producer warp per ring (this loop measured a few percent faster
+    // here than the two-warp loop below run with one warp per ring)
+    // ------------------- producers: K ring (warp 4), V ring (warp 5) -------------------
+    const int r = warp - kWarpProducerK;
+    const CUtensorMap* map = r == 0 ? &tmap_k : &tmap_v;
+    if (lane == 0) {
+      prefetch_tensormap(map);
+      if (r == 0) prefetch_tensormap(&tmap_q);
+    }
+    FetchSource fetch{&p, uring, uring_full(0), uring_empty(0), lane, 0, &failed};
+    RingSource ring = ring_source();
+    Cursor<BS, FetchSource> cur_k;
+    Cursor<BS, RingSource> cur_v;
+    if (r == 0) cur_k.start(p, fetch); else cur_v.start(p, ring);
+    // block-table entries in windows of 32 pages, the next window prefetched
+    int win_base = 0, win_blk = 0, nxt_blk = 0;
+    while (!failed && (r == 0 ? cur_k.valid() : cur_v.valid())) {
+      const int cu_i = r == 0 ? cur_k.i : cur_v.i;
+      const int cu_c = r == 0 ? cur_k.c : cur_v.c;
+      const int cu_j = r == 0 ? cur_k.j : cur_v.j;
+      const Unit& U = r == 0 ? cur_k.U : cur_v.U;
+      const int32_t* table = p.block_table + (int64_t)U.b * p.max_blocks;
+      if (cu_i == 0) {
+        win_base = U.p0;
+        win_blk = (U.p0 + lane < U.p1) ? __ldg(table + U.p0 + lane) : 0;
+        nxt_blk = (U.p0 + 32 + lane < U.p1) ? __ldg(table + U.p0 + 32 + lane) : 0;
+        if (r == 0) {
+          // this unit's G query rows -> Q operand buffer j & 1
+          const int qb = cu_j & 1;
+          bool ok = true;
+          if (cu_j >= 2) ok = mbar_wait(q_empty(qb), ((cu_j - 2) >> 1) & 1);
+          if (!__all_sync(kFull, ok)) {
+            failed = true;
+            break;
+          }
+          if (lane == 0) {
+            const uint32_t fb = q_full(qb);
+            mbar_arrive_expect_tx(fb, (uint32_t)G * NB * kRowBytes);
+            const uint32_t qdst = base_u32 + kOffQ + qb * kOpBytes;
+            const int row = U.b * p.Hq + U.h * G;
+#pragma unroll
+            for (int bx = 0; bx < NB; ++bx) tma_load_2d(qdst + bx * kOpHalf, &tmap_q, bx * 64, row, fb);
+          }
+          __syncwarp();
+        }
+      }
+      const int c = cu_c;
+      const int slot = c % kStages;
+      if (c >= kStages) {
+        const bool ok = mbar_wait(empty_bar(r, slot), ((c / kStages) - 1) & 1);
+        if (!__all_sync(kFull, ok)) {
+          failed = true;
+          break;
+        }
+      }
+      const int pg0 = U.p0 + cu_i * PPS;
+      const int npg = min(PPS, U.p1 - pg0);
+      if (pg0 + PPS > win_base + 32) {  // pg0 == win_base + 32: PPS divides 32
+        win_base += 32;
+        win_blk = nxt_blk;
+        nxt_blk = (win_base + 32 + lane < U.p1) ? __ldg(table + win_base + 32 + lane) : 0;
+      }
+      int blk[PPS];
+#pragma unroll
+      for (int i = 0; i < PPS; ++i) blk[i] = __shfl_sync(kFull, win_blk, (pg0 + i - win_base) & 31);
+      if (lane == 0) {
+        const uint32_t fb = full_bar(r, slot);
+        // 16-bit K/V: D / 64 boxes of 64 dims per page; FP8: one box of D bytes
+        constexpr int kBoxes = KV8 ? 1 : NB;
+        constexpr int kBoxElems = KV8 ? D : 64;
+        mbar_arrive_expect_tx(fb, (uint32_t)npg * BS * kBoxes * kRowBytes);
+        const uint32_t st = base_u32 + (r == 0 ? kOffK : kOffV) + slot * kSlotBytes;
+#pragma unroll
+        for (int i = 0; i < PPS; ++i) {
+          if (i < npg) {
+            const int y = blk[i] * BS;
+            const uint32_t ro = (uint32_t)(i * BS * kRowBytes);
+#pragma unroll
+            for (int bx = 0; bx < kBoxes; ++bx)
+              tma_load_2d(st + bx * kHalf + ro, map, U.h * D + bx * kBoxElems, y, fb);
+          }
+        }
+      }
+      __syncwarp();
+      if (r == 0) cur_k.advance(p, fetch); else cur_v.advance(p, ring);
+    }
+  } else if (kDual && (warp == kWarpProducerK || warp == kWarpProducerV ||
+                        warp >= kWarpProducerK2)) {
     // ------- producers: K ring (warps 4, 16), V ring (warps 5, 17) -------
     // With kDual each ring has two producer warps that take alternate
     // chunks: one thread issues a TMA box in ~80 cycles, so a single warp
@@ -535,6 +629,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const int c = cu_c;
+      const bool mine = !kDual || (c & 1) == par;  // this warp's chunk
+      if (mine && c >= kStages) {
+        const bool ok = mbar_wait(empty_bar(r, c % kStages), ((c / kStages) - 1) & 1);
+        if (!__all_sync(kFull, ok)) {
+          failed = true;
+          break;
+        }
+      }
       const int pg0 = U.p0 + cu_i * PPS;
       const int npg = min(PPS, U.p1 - pg0);
       if (pg0 + PPS > win_base + 32) {  // pg0 == win_base + 32: PPS divides 32
@@ -542,15 +644,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         win_blk = nxt_blk;
         nxt_blk = (win_base + 32 + lane < U.p1) ? __ldg(table + win_base + 32 + lane) : 0;
       }
-      if (!kDual || (c & 1) == par) {  // this warp's chunk
+      if (mine) {
         const int slot = c % kStages;
-        if (c >= kStages) {
-          const bool ok = mbar_wait(empty_bar(r, slot), ((c / kStages) - 1) & 1);
-          if (!__all_sync(kFull, ok)) {
-            failed = true;
-            break;
-          }
-        }
         int blk[PPS];
 #pragma unroll
         for (int i = 0; i < PPS; ++i) blk[i] = __shfl_sync(kFull, win_blk, (pg0 + i - win_base) & 31);
@@ -576,8 +671,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (fetcher) cur_k.advance(p, fetch); else cur_v.advance(p, ring);
     }
-  } else if (warp >= kWarpProducerK2) {
-    // second producers: idle unless kDual
   } else if (warp == kWarpMma || warp == kWarpMmaPV) {
     // ------------------------------ MMA issue -----------------------------
     // kind::f16: type fields 1 = bf16, 0 = f16; kind::f8f6f4: 0 = E4M3
@@ -1040,7 +1133,7 @@ cudaError_t launch_one(const CUtensorMap* tk, const CUtensorMap* tv, const CUten
   // waits for that grid before reading any input.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ctas);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(tc_threads(G, D, KV8));
   cfg.dynamicSmemBytes = Layout<KV8, D>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1062,7 +1155,7 @@ template <int G, int D, int BS, bool FP16, bool KV8>
 int occupancy_one() {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-          &n, paged_partial_tc_kernel<G, D, BS, FP16, KV8>, kThreads,
+          &n, paged_partial_tc_kernel<G, D, BS, FP16, KV8>, tc_threads(G, D, KV8),
           Layout<KV8, D>::kSmemBytes) != cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
