@@ -140,6 +140,20 @@ def test_plan_splits_long_contexts_to_fill_the_gpu(lib):
     assert plan(1, 2048)[0] >= plan(4, 2048)[0]
 
 
+def test_plan_slots_by_kernel(lib):
+    """The 16-bit tensor-core kernel plans one wave over 128 of 152 SMs; FP8
+    caches (limited per SM) and the CUDA-core kernel (G 1, 2) plan over every
+    SM and CTA slot."""
+    B, pages = 8, 2048                    # 64 (sequence, kv head) pairs, L = 32768
+    S16, _ = plan(B, pages)
+    assert S16 * 64 <= 128
+    cfg8 = pda.make_config(32, 8, 128, 16, max_batch=B, max_blocks_per_seq=pages, kv_fp8=True)
+    S8, _ = pda.plan(cfg8, 152, B, pages)
+    assert S8 * 64 > 152                  # several units per SM, balanced dynamically
+    Sg2, _ = plan(4, pages, Hq=16)        # G = 2: CUDA-core kernel, 2 CTAs per SM
+    assert Sg2 * 32 > 128
+
+
 def test_plan_respects_hint_and_caps(lib):
     assert plan(1, 2048, hint=64)[0] <= 4
     assert plan(1, 4096, max_splits=8)[0] <= 8
