@@ -269,8 +269,8 @@ def test_geometries_fp16_and_fp32_out(Hq, Hkv, D):
                                       (12, 2, 64), (32, 4, 64), (16, 4, 64), (9, 3, 64)])
 def test_both_kernels_on_padded_groups(kernel, Hq, Hkv, D, monkeypatch):
     """Group sizes 3..8 at head dims 64 and 128 on both implementations (the
-    tensor-core kernel pads the group to 4 or 8 MMA columns, and at D = 64
-    runs a 64-deep QK^T with a zero upper half of V)."""
+    tensor-core kernel pads the group to 16 MMA columns; at D = 64 it runs a
+    64-deep QK^T and an M = 64 PV, with two producer warps per ring at G <= 4)."""
     monkeypatch.setenv("PDA_PARTIAL_KERNEL", kernel)
     lens = [3000, 1, 129, 700, 128, 17]
     for bs in (16, 32):
