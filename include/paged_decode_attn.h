@@ -169,7 +169,9 @@ int paged_decode_attn_run_scaled(pda_handle handle, const void* q, const void* k
  * length hint (0 = max_blocks * block_size), on a GPU with `num_sms` SMs.
  * *num_splits receives S (1 .. cfg->max_splits) and *chunk_pages the pages
  * each split covers; sequence b then uses min(S, ceil(ceil(L_b / block_size)
- * / chunk_pages)) splits. */
+ * / chunk_pages)) splits. Waves of work units are counted over 27/32 of the
+ * SMs for the 16-bit tensor-core kernel (G 3..8 at head_dim 64/128) and over
+ * every SM (times CTAs per SM) otherwise. */
 int paged_decode_attn_plan(const pda_config* cfg, int num_sms, int batch, int max_blocks,
                            int max_context_len_hint, int* num_splits, int* chunk_pages);
 
