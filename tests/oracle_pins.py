@@ -592,8 +592,60 @@ def pin_compaction_preserves_attention(lib):
         oracle.remap_table(d.table, d.lens, d.bs, np.arange(d.kc.shape[0]), lib=lib), d.table)
 
 
+
+# ---------------------------------------------------------------------------
+# row selection (the entry points the full-size GPU checks and the CPU
+# baseline use)
+# ---------------------------------------------------------------------------
+
+def pin_row_selection(lib):
+    """Selected rows equal the matching rows of the full output, bit for bit,
+    and the brute force: shuffled rows, repeated rows and a single row, through
+    paged_decode_rows (bf16 and fp16) and paged_decode_kv(rows=...) (bf16 and
+    FP8 caches with per-head scales). B = Hq, so a selection that swapped b and
+    hq would still address valid rows and could only be caught by its values."""
+    rng = np.random.default_rng(23)
+    for seed, dt in ((51, BF16), (52, FP16)):
+        dn = Dense(seed, B=8, Hq=8, Hkv=2, D=8, bs=4, lens=[5, 12, 1, 7, 3, 9, 16, 2], dtype=dt)
+        full = dn.run(lib)
+        every = np.array([(b, h) for b in range(8) for h in range(8)], dtype=np.int32)
+        selections = [every[rng.permutation(len(every))],
+                      every[rng.integers(0, len(every), size=23)],  # repeats
+                      np.array([[6, 3]], dtype=np.int32),
+                      np.array([[3, 6], [6, 3], [0, 7], [7, 0]], dtype=np.int32)]
+        for rows in selections:
+            got = oracle.paged_decode_rows(*dn.args(), dt, dn.scale, rows, threads=3, lib=lib)
+            np.testing.assert_array_equal(got, full[rows[:, 0], rows[:, 1]])
+            got_kv = oracle.paged_decode_kv(*dn.args(), dt, dt, dn.scale, rows=rows, threads=2,
+                                            lib=lib)
+            np.testing.assert_array_equal(got_kv, full[rows[:, 0], rows[:, 1]])
+        bf = brute_force(dn, dn.scale)
+        rows = selections[3]
+        got = oracle.paged_decode_rows(*dn.args(), dt, dn.scale, rows, lib=lib)
+        assert np.max(np.abs(got - bf[rows[:, 0], rows[:, 1]])) < 1e-12
+    # FP8 caches with per-head scales: rows of the full FP8 output
+    B, Hq, Hkv, D, bs, nb = 6, 6, 3, 16, 4, 30
+    g = torch.Generator().manual_seed(61)
+    k8 = (torch.randn(nb, bs, Hkv, D, generator=g) * 3).to(torch.float8_e4m3fn)
+    v8 = (torch.randn(nb, bs, Hkv, D, generator=g) * 3).to(torch.float8_e4m3fn)
+    q = _bits(torch.randn(B, Hq, D, generator=g).bfloat16())
+    table = rng.permutation(nb)[: B * 5].reshape(B, 5).astype(np.int32)
+    cl = np.array([20, 1, 7, 13, 4, 17], dtype=np.int32)
+    ks, vs = np.array([0.5, 2.0, 0.25]), np.array([1.5, 0.75, 3.0])
+    k8n, v8n = k8.view(torch.uint8).numpy(), v8.view(torch.uint8).numpy()
+    full = oracle.paged_decode_kv(q, k8n, v8n, table, cl, BF16, oracle.FP8_E4M3, 0.25, ks, vs,
+                                  lib=lib)
+    every = np.array([(b, h) for b in range(B) for h in range(Hq)], dtype=np.int32)
+    for rows in (every[rng.permutation(len(every))], every[rng.integers(0, len(every), 9)],
+                 np.array([[4, 1]], dtype=np.int32)):
+        got = oracle.paged_decode_kv(q, k8n, v8n, table, cl, BF16, oracle.FP8_E4M3, 0.25, ks, vs,
+                                     rows=rows, threads=4, lib=lib)
+        np.testing.assert_array_equal(got, full[rows[:, 0], rows[:, 1]])
+
+
 ALL_PINS = [pin_brute_force, pin_closed_forms, pin_block_table_invariance, pin_gqa_reductions,
             pin_split_merge, pin_merge_special_cases, pin_dtype_conversions,
             pin_rope_complex_form, pin_rope_exact_turns, pin_e4m3_decode,
             pin_fp8_kv_equals_dequantised_bf16, pin_gather_matches_attention_addressing,
-            pin_scatter_then_gather_roundtrip, pin_compaction_preserves_attention]
+            pin_scatter_then_gather_roundtrip, pin_compaction_preserves_attention,
+            pin_row_selection]

@@ -54,6 +54,10 @@ MUTANTS = {
     "scatter_writes_padding": ("    if (slot < 0) continue;\n    if (slot >= num_slots)",
                                "    if (slot < 0) slot = 0;\n    if (slot >= num_slots)"),
     "remap_by_position": ("*e = new_id[*e];", "*e = new_id[p];"),
+    "rows_b_hq_swapped": ("      b = j->rows[2 * r];\n      hq = j->rows[2 * r + 1];",
+                          "      b = j->rows[2 * r + 1];\n      hq = j->rows[2 * r];"),
+    "rows_pair_stride": ("      b = j->rows[2 * r];\n", "      b = j->rows[r];\n"),
+    "rows_ignored": ("    if (j->rows) {\n      b = j->rows", "    if (0) {\n      b = j->rows"),
     "rope_second_sign": ("double yb = xb * c + xa * s;", "double yb = xb * c - xa * s;"),
     "rope_first_sign": ("double ya = xa * c - xb * s;", "double ya = xa * c + xb * s;"),
     "rope_neox_pairing": ("int b = neox ? j + half : 2 * j + 1;",
