@@ -324,8 +324,12 @@ int paged_decode_attn_remap_table(int32_t* block_table, int batch, int max_block
  * the process exits. The split count the heuristic picks is lowered until
  * the partials fit (batch * Hq * S * head_dim <= 2^21, batch * Hq * S <= 2^16,
  * and no splitting at all if batch * Hkv > 2^16); a sequence with a single
- * split needs no scratch. An explicit num_splits > 1 that does not fit is
- * rejected with PDA_EINVAL. Each call clears the tickets it uses.
+ * split needs no scratch. An explicit num_splits runs as
+ * S = ceil(max_blocks / chunk) splits of chunk = ceil(max_blocks /
+ * min(num_splits, max_blocks)) pages, as in paged_decode_attn_run_ex; if that
+ * S is above 1 and does not fit, the call is rejected with PDA_EINVAL and the
+ * message names S and the largest split count that fits. Each call clears the
+ * tickets it uses.
  *
  * Set-up: the first call on a device looks up the scratch array's device
  * address and sets the kernels' shared-memory limits for that device; make

@@ -173,14 +173,21 @@ extern "C" int paged_decode_attn_run_noalloc(const void* q, const void* k_cache,
   size_t fit = kPartialFloats / (rows * head_dim);
   if (kLseFloats / rows < fit) fit = kLseFloats / rows;
   if ((size_t)batch * num_kv_heads > kCounterInts) fit = 1;  // no room for split tickets
-  if (num_splits > 1 && (size_t)num_splits > fit) {
-    char buf[256];
-    snprintf(buf, sizeof buf,
-             "num_splits %d needs %zu bytes of split partials; the built-in scratch holds %zu "
-             "(at most %zu splits for this batch)",
-             num_splits, rows * (size_t)num_splits * (head_dim + 1) * 4,
-             (kPartialFloats + kLseFloats) * 4, fit);
-    return fail(PDA_EINVAL, buf);
+  // An explicit request runs as S = ceil(max_blocks / chunk) splits of chunk
+  // pages (the handle path's rule); only that S has to fit.
+  if (num_splits > 0) {
+    const int cap = num_splits < max_blocks ? num_splits : max_blocks;
+    chunk = (max_blocks + cap - 1) / cap;
+    S = (max_blocks + chunk - 1) / chunk;
+    if (S > 1 && (size_t)S > fit) {
+      char buf[320];
+      snprintf(buf, sizeof buf,
+               "num_splits %d runs as %d splits, which need %zu bytes of split partials; the "
+               "built-in scratch holds %zu (at most %zu splits for this batch)",
+               num_splits, S, rows * (size_t)S * (head_dim + 1) * 4,
+               (kPartialFloats + kLseFloats) * 4, fit);
+      return fail(PDA_EINVAL, buf);
+    }
   }
 
   int prev = -1;
@@ -201,11 +208,7 @@ extern "C" int paged_decode_attn_run_noalloc(const void* q, const void* k_cache,
   st = setup_device(device, group, head_dim, block_size, dtype, &scratch, &num_sms);
   if (st != PDA_OK) return st;
 
-  if (num_splits > 0) {
-    const int cap = num_splits < max_blocks ? num_splits : max_blocks;
-    chunk = (max_blocks + cap - 1) / cap;
-    S = (max_blocks + chunk - 1) / chunk;
-  } else {
+  if (num_splits == 0) {
     cfg.max_splits = fit < 1 ? 1 : (fit > (size_t)pda::kMaxSplits ? pda::kMaxSplits : (int)fit);
     st = paged_decode_attn_plan(&cfg, num_sms, batch, max_blocks, 0, &S, &chunk);
     if (st != PDA_OK) return st;
