@@ -247,6 +247,20 @@ def long_context(seed: int = 0, batch: int = 4, context: int = 32768,
     return to_fp8_kv(wl) if kv_fp8 else wl
 
 
+def leading(wl: Workload, batch: int, context: int) -> Workload:
+    """The first ``batch`` sequences of ``wl`` cut to their first ``context``
+    tokens, over the same cache pool (views, no copies): the smaller
+    long-context shapes taken from one full-size pool."""
+    bs = wl.block_size
+    pages = (context + bs - 1) // bs
+    if batch > wl.batch or pages > wl.max_blocks:
+        raise ValueError("leading(): larger than the workload it is cut from")
+    lens = torch.clamp(wl.context_lens[:batch], max=context).contiguous()
+    name = wl.name.split("_b")[0] + f"_b{batch}_l{context}" + ("_fp8" if wl.kv_fp8 else "")
+    return Workload(name, wl.q[:batch].contiguous(), wl.k_cache, wl.v_cache,
+                    wl.block_table[:batch, :pages].contiguous(), lens, wl.scale, dict(wl.meta))
+
+
 def to_fp8_kv(wl: Workload) -> Workload:
     """The same workload with FP8 (E4M3) K/V caches: per kv head h, scale_h =
     max |x| over the pool / 448 (so the largest value maps to the largest

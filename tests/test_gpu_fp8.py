@@ -1,7 +1,6 @@
 """GPU parity of the FP8 (E4M3) KV-cache path against the FP64 oracle with
 per-kv-head (and per-tensor) dequantisation scales, and of scaled 16-bit
 caches. Calls go through the C ABI (ctypes binding)."""
-import numpy as np
 import pytest
 import torch
 
@@ -56,24 +55,23 @@ def test_fp8_peaky_rows_and_fp32_out():
     assert err < 2e-3, err
 
 
-def test_fp8_full_size_long_context_sampled_rows():
-    """The FP8 bench workload (B=4, L=32768, 20 GiB FP8 pool): sampled rows
-    against the oracle on the pages those rows read."""
-    wl = workloads.long_context(seed=0, batch=4, context=32768, device=DEV, kv_fp8=True)
-    attn = make_attn(wl)
-    out = run_gpu(attn, wl)
-    attn.close()
-    torch.cuda.synchronize()
-    rng = np.random.default_rng(1)
+def test_fp8_full_size_long_context_every_split_count():
+    """The FP8 bench workload (B=8, L=32768, the headline's bytes, random
+    tables over a 20 GiB FP8 pool): every row against the oracle on the
+    pages those rows read, at every split count of the sweep and the
+    heuristic's, and in fp32 output."""
+    wl = workloads.long_context(seed=0, batch=8, context=32768, device=DEV, kv_fp8=True)
     ks = wl.meta["k_scale"].double().cpu().numpy()
     vs = wl.meta["v_scale"].double().cpu().numpy()
-    for b in (0, 2):
-        q, k, v, bt, cl = workloads.compact_for_rows(wl, [b])
-        hqs = rng.choice(32, size=6, replace=False)
-        rows = np.array([[0, int(h)] for h in hqs], dtype=np.int32)
-        ref = oracle.paged_decode_kv(q, k, v, bt, cl, oracle.BF16, oracle.FP8_E4M3, wl.scale,
-                                     ks, vs, rows=rows)
-        assert_close(out[b, torch.from_numpy(hqs).to(DEV)], ref, f"fp8 b={b}")
+    q, k, v, bt, cl = workloads.compact_for_rows(wl, range(wl.batch))
+    ref = oracle.paged_decode_kv(q, k, v, bt, cl, oracle.BF16, oracle.FP8_E4M3, wl.scale, ks, vs)
+    del q, k, v
+    attn = make_attn(wl)
+    for splits in (0, 1, 2, 4, 8, 16, 32, 64):
+        assert_close(run_gpu(attn, wl, num_splits=splits), ref, f"fp8 splits={splits}")
+    err = assert_close(run_gpu(attn, wl, out_dtype=torch.float32), ref, "fp8 fp32 out")
+    assert err < 2e-3, err
+    attn.close()
     del wl
     torch.cuda.empty_cache()
 

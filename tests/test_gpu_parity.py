@@ -83,22 +83,45 @@ def test_context_hint_below_actual_is_still_exact():
     check(wl, max_context_len_hint=64)
 
 
-def test_full_size_long_context_sampled_rows():
-    """The bench workload itself (B=4, L=32768, 40 GiB pool, heuristic splits):
-    sampled rows against the oracle run on the pages those rows read."""
+# The long-context split-K shapes at full size (B in {1, 4} x L in {8192,
+# 32768}, random tables over the 40 GiB pool), every split count the sweep
+# covers plus the heuristic's (0), every row against the oracle.
+LONG_SPLITS = [0, 1, 2, 4, 8, 16, 32, 64]
+
+
+@pytest.fixture(scope="module")
+def long_pool():
     wl = workloads.long_context(seed=0, batch=4, context=32768, device=DEV)
-    attn = make_attn(wl)
-    out = run_gpu(attn, wl)
-    attn.close()
-    rng = np.random.default_rng(0)
-    for b in (0, 3):
-        q, k, v, bt, cl = workloads.compact_for_rows(wl, [b])
-        hqs = rng.choice(32, size=6, replace=False)
-        rows = np.array([[0, int(h)] for h in hqs], dtype=np.int32)
-        ref = oracle.paged_decode_rows(q, k, v, bt, cl, oracle.BF16, wl.scale, rows)
-        assert_close(out[b, torch.from_numpy(hqs).to(DEV)], ref, f"b={b}")
+    yield wl
     del wl
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("batch,context", [(1, 8192), (4, 8192), (1, 32768), (4, 32768)])
+def test_full_size_long_context_every_split_count(long_pool, batch, context):
+    wl = workloads.leading(long_pool, batch, context)
+    ref = oracle.paged_decode(*workloads.compact_for_rows(wl, range(batch)), oracle.BF16,
+                              wl.scale)
+    attn = make_attn(wl)
+    for splits in LONG_SPLITS:
+        out = run_gpu(attn, wl, num_splits=splits)
+        assert_close(out, ref, f"{wl.name} splits={splits}")
+    err = assert_close(run_gpu(attn, wl, out_dtype=torch.float32), ref, f"{wl.name} fp32 out")
+    assert err < 1e-4, err
+    attn.close()
+
+
+def test_fp32_output_mode_every_config():
+    """The kernel's own accuracy (fp32 out) on the tiny, short-batch (both
+    dtypes, both block sizes), mid-ragged and serving-mix configs: within the
+    flat 2e-3 bar, and in fact below 1e-4."""
+    cases = [workloads.tiny(seed=0), workloads.mid_ragged(seed=2),
+             workloads.serving_mix(seed=2, batch=128)]
+    cases += [workloads.short_batch(seed=5, block_size=bs, dtype=dt)
+              for bs in (16, 32) for dt in ("bf16", "fp16")]
+    for wl in cases:
+        err = check(wl, out_dtype=torch.float32)
+        assert err < 1e-4, (wl.name, err)
 
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16, torch.float16])
@@ -284,3 +307,31 @@ def test_both_kernels_on_padded_groups(kernel, Hq, Hkv, D, monkeypatch):
     err = check(workloads.custom(seed=D + 1, B=3, Hq=Hq, Hkv=Hkv, D=D, block_size=16,
                                  lens=[500, 64, 2000]), out_dtype=torch.float32)
     assert err < 1e-4, err
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (32, 8, 64)])
+def test_timed_out_call_reports_and_next_call_is_exact(Hq, Hkv, D, monkeypatch):
+    """Failure detection without a GPU fault. PDA_TEST_STALL_RUNS=1 (read when
+    the handle is created) makes the handle's first run publish no work unit
+    and shortens every pipeline wait to 1 ms: no page load, MMA or store is
+    ever issued, so the waits run out with nothing in flight. That run
+    records error code 3; the next run of the same handle, with no
+    check_device_error in between, is exact (the timed-out CTAs still counted
+    themselves done, so the work counters were reset); the error word reports
+    the timeout and is clear after the next exact run. Both producer
+    layouts of the tensor-core kernel (one and two producer warps per ring)."""
+    monkeypatch.setenv("PDA_PARTIAL_KERNEL", "tensor_core")
+    monkeypatch.setenv("PDA_TEST_STALL_RUNS", "1")
+    wl_host = workloads.custom(seed=D + 3, B=3, Hq=Hq, Hkv=Hkv, D=D, block_size=16,
+                               lens=[3000, 17, 900], num_blocks=400)
+    ref = oracle_ref(wl_host)
+    wl = wl_host.to(DEV)
+    attn = make_attn(wl)
+    monkeypatch.delenv("PDA_TEST_STALL_RUNS")
+    run_gpu(attn, wl, num_splits=4)  # stalled: nothing is written
+    assert_close(run_gpu(attn, wl, num_splits=4), ref, "first run after a timed-out run")
+    code, _ = attn.check_device_error()
+    assert code == 3
+    assert_close(run_gpu(attn, wl), ref, "heuristic splits after the error was read")
+    assert attn.check_device_error() == (0, 0)
+    attn.close()
