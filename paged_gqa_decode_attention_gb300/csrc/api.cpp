@@ -225,6 +225,7 @@ struct pda_handle_s {
   int* err = nullptr;
   int* counters = nullptr;  // [max_batch, Hkv] split tickets
   size_t counter_bytes = 0;
+  int test_stall_runs = 0;  // timeout tests: this many first runs publish no unit
   // TMA descriptors for the last (k_cache, v_cache, num_blocks) seen
   const void* tm_k = nullptr;
   const void* tm_v = nullptr;
@@ -268,6 +269,12 @@ int paged_decode_attn_create(const pda_config* cfg, pda_handle* out_handle) {
              pda::partial_kernel_supported(pda::kPartialTensorCore, h->group, cfg->head_dim, kv8))
       h->kernel = pda::kPartialTensorCore;
   }
+  // Timeout tests (tensor-core kernel only): PDA_TEST_STALL_RUNS=n makes the
+  // first n runs of this handle publish no work unit with a 1 ms wait limit,
+  // so every pipeline wait runs out while nothing is in flight; the run
+  // records error code 3 and the next run must be exact.
+  if (const char* env = std::getenv("PDA_TEST_STALL_RUNS"))
+    if (h->kernel == pda::kPartialTensorCore) h->test_stall_runs = std::atoi(env);
   e = pda::partial_prepare(h->kernel, h->group, cfg->head_dim, cfg->block_size, cfg->dtype, kv8);
   if (e != cudaSuccess) {
     delete h;
@@ -446,6 +453,11 @@ int paged_decode_attn_run_scaled(pda_handle h, const void* q, const void* k_cach
   p.k_scale = k_scale;
   p.v_scale = v_scale;
   p.scale_per_head = scale_per_head;
+  if (h->test_stall_runs > 0) {
+    --h->test_stall_runs;
+    p.stall_units = 1;
+    p.wait_ns = 1000ull * 1000ull;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = pda::launch_partial(h->kernel, h->group, c.head_dim, c.block_size, c.dtype,
                                       c.kv_fp8 != 0, &h->tmap_k, &h->tmap_v, &tmap_q, p, batch,

@@ -69,7 +69,8 @@
 //     split ticket and merge, while the softmax warps go on with the next
 //     unit (the unit boundary does not stall the pipeline).
 // Every wait is bounded; a timed-out CTA records error code 3, stops issuing
-// work, still passes every barrier, and frees its TMEM.
+// work, still passes every barrier, counts itself done with the work counter
+// (so the counters are reset for the next call) and frees its TMEM.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -363,6 +364,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   bool failed = false;
+  const uint64_t wlim = p.wait_ns ? (uint64_t)p.wait_ns : kWaitLimitNs;
 
   // Work units are handed out dynamically: the K-producer warp takes unit
   // indices from a global counter (p.sched[0]) and publishes every one that
@@ -375,7 +377,29 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     uint32_t full0, empty0;
     int lane, k;
     bool* failed;
+    uint64_t wlim;
+    bool counted;
+    // This CTA takes no more units: count it done exactly once (also after a
+    // timed-out wait), so the CTA that finishes last resets the counters and
+    // the next call starts from zero.
+    __device__ __forceinline__ void done() {
+      if (counted) return;
+      counted = true;
+      if (lane == 0) {
+        griddep_launch_dependents();  // no more units: the next grid may start launching
+        __threadfence();  // this CTA's last fetch is ordered before its done count
+        if (atomicAdd(p->sched + 1, 1) == (int)gridDim.x - 1) {
+          p->sched[0] = 0;
+          p->sched[1] = 0;
+        }
+      }
+      __syncwarp();
+    }
     __device__ __forceinline__ int next(Unit& U) {
+      if (p->stall_units) {  // fault injection: publish nothing, let every wait run out
+        done();
+        return -1;
+      }
       while (true) {
         int u = 0;
         if (lane == 0) u = atomicAdd(p->sched, 1);
@@ -387,9 +411,10 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
         }
         const int slot = k % kUnitRing;
         bool ok = true;
-        if (k >= kUnitRing) ok = mbar_wait(empty0 + 8u * slot, ((k / kUnitRing) - 1) & 1);
+        if (k >= kUnitRing) ok = mbar_wait(empty0 + 8u * slot, ((k / kUnitRing) - 1) & 1, wlim);
         if (!__all_sync(kFull, ok)) {
           *failed = true;
+          done();
           return -1;
         }
         if (lane == 0) {
@@ -399,14 +424,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
         __syncwarp();
         ++k;
         if (pub < 0) {
-          if (lane == 0) {
-            griddep_launch_dependents();  // no more units: the next grid may start launching
-            __threadfence();  // this CTA's last fetch is ordered before its done count
-            if (atomicAdd(p->sched + 1, 1) == (int)gridDim.x - 1) {
-              p->sched[0] = 0;
-              p->sched[1] = 0;
-            }
-          }
+          done();
           return -1;
         }
         return pub;
@@ -418,9 +436,10 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     uint32_t full0, empty0;
     int lane, k;
     bool* failed;
+    uint64_t wlim;
     __device__ __forceinline__ int next(Unit& U) {
       const int slot = k % kUnitRing;
-      const bool ok = !*failed && mbar_wait(full0 + 8u * slot, (k / kUnitRing) & 1);
+      const bool ok = !*failed && mbar_wait(full0 + 8u * slot, (k / kUnitRing) & 1, wlim);
       if (!__all_sync(kFull, ok)) {
         *failed = true;
         return -1;
@@ -433,7 +452,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     }
   };
   auto ring_source = [&]() {
-    return RingSource{uring, uring_full(0), uring_empty(0), lane, 0, &failed};
+    return RingSource{uring, uring_full(0), uring_empty(0), lane, 0, &failed, wlim};
   };
 
   if (threadIdx.x == 0) {
@@ -498,7 +517,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       prefetch_tensormap(map);
       if (r == 0) prefetch_tensormap(&tmap_q);
     }
-    FetchSource fetch{&p, uring, uring_full(0), uring_empty(0), lane, 0, &failed};
+    FetchSource fetch{&p, uring, uring_full(0), uring_empty(0), lane, 0, &failed, wlim, false};
     RingSource ring = ring_source();
     Cursor<BS, FetchSource> cur_k;
     Cursor<BS, RingSource> cur_v;
@@ -519,7 +538,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
           // this unit's G query rows -> Q operand buffer j & 1
           const int qb = cu_j & 1;
           bool ok = true;
-          if (cu_j >= 2) ok = mbar_wait(q_empty(qb), ((cu_j - 2) >> 1) & 1);
+          if (cu_j >= 2) ok = mbar_wait(q_empty(qb), ((cu_j - 2) >> 1) & 1, wlim);
           if (!__all_sync(kFull, ok)) {
             failed = true;
             break;
@@ -538,7 +557,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       const int c = cu_c;
       const int slot = c % kStages;
       if (c >= kStages) {
-        const bool ok = mbar_wait(empty_bar(r, slot), ((c / kStages) - 1) & 1);
+        const bool ok = mbar_wait(empty_bar(r, slot), ((c / kStages) - 1) & 1, wlim);
         if (!__all_sync(kFull, ok)) {
           failed = true;
           break;
@@ -575,6 +594,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       __syncwarp();
       if (r == 0) cur_k.advance(p, fetch); else cur_v.advance(p, ring);
     }
+    if (r == 0) fetch.done();  // counted already unless a wait timed out
   } else if (kDual && (warp == kWarpProducerK || warp == kWarpProducerV ||
                         warp >= kWarpProducerK2)) {
     // ------- producers: K ring (warps 4, 16), V ring (warps 5, 17) -------
@@ -591,7 +611,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       prefetch_tensormap(map);
       if (fetcher) prefetch_tensormap(&tmap_q);
     }
-    FetchSource fetch{&p, uring, uring_full(0), uring_empty(0), lane, 0, &failed};
+    FetchSource fetch{&p, uring, uring_full(0), uring_empty(0), lane, 0, &failed, wlim, false};
     RingSource ring = ring_source();
     Cursor<BS, FetchSource> cur_k;
     Cursor<BS, RingSource> cur_v;
@@ -612,7 +632,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
           // this unit's G query rows -> Q operand buffer j & 1
           const int qb = cu_j & 1;
           bool ok = true;
-          if (cu_j >= 2) ok = mbar_wait(q_empty(qb), ((cu_j - 2) >> 1) & 1);
+          if (cu_j >= 2) ok = mbar_wait(q_empty(qb), ((cu_j - 2) >> 1) & 1, wlim);
           if (!__all_sync(kFull, ok)) {
             failed = true;
             break;
@@ -631,7 +651,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       const int c = cu_c;
       const bool mine = !kDual || (c & 1) == par;  // this warp's chunk
       if (mine && c >= kStages) {
-        const bool ok = mbar_wait(empty_bar(r, c % kStages), ((c / kStages) - 1) & 1);
+        const bool ok = mbar_wait(empty_bar(r, c % kStages), ((c / kStages) - 1) & 1, wlim);
         if (!__all_sync(kFull, ok)) {
           failed = true;
           break;
@@ -671,6 +691,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       }
       if (fetcher) cur_k.advance(p, fetch); else cur_v.advance(p, ring);
     }
+    if (fetcher) fetch.done();  // counted already unless a wait timed out
   } else if (warp == kWarpMma || warp == kWarpMmaPV) {
     // ------------------------------ MMA issue -----------------------------
     // kind::f16: type fields 1 = bf16, 0 = f16; kind::f8f6f4: 0 = E4M3
@@ -683,7 +704,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     auto issue_qk = [&](const Cursor<BS, RingSource>& cur) {
       const int c = cur.c, slot = c % kStages, qb = cur.j & 1;
       bool ok = !failed;
-      if (ok && cur.i == 0) ok = mbar_wait(q_full(qb), (cur.j >> 1) & 1);
+      if (ok && cur.i == 0) ok = mbar_wait(q_full(qb), (cur.j >> 1) & 1, wlim);
       if (!__all_sync(kFull, ok)) failed = true;
       if (failed) return;
       if constexpr (KV8) {
@@ -727,8 +748,8 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
           if (lane == 0) mbar_arrive(q8_full(qb));  // the row scales, for the softmax
         }
       }
-      ok = mbar_wait(full_bar(0, slot), (c / kStages) & 1);
-      if (ok && c >= 2) ok = mbar_wait(s_free(c & 1), ((c - 2) >> 1) & 1);
+      ok = mbar_wait(full_bar(0, slot), (c / kStages) & 1, wlim);
+      if (ok && c >= 2) ok = mbar_wait(s_free(c & 1), ((c - 2) >> 1) & 1, wlim);
       if (!__all_sync(kFull, ok)) failed = true;
       if (failed) return;
       tc_fence_after();
@@ -763,9 +784,9 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     // fold of O(c-2)
     auto issue_pv = [&](int c) {
       const int slot = c % kStages;
-      bool ok = !failed && mbar_wait(full_bar(1, slot), (c / kStages) & 1);
-      if (ok) ok = mbar_wait(p_full(c & 1), (c >> 1) & 1);
-      if (ok && c >= 2) ok = mbar_wait(o_free(c & 1), ((c - 2) >> 1) & 1);
+      bool ok = !failed && mbar_wait(full_bar(1, slot), (c / kStages) & 1, wlim);
+      if (ok) ok = mbar_wait(p_full(c & 1), (c >> 1) & 1, wlim);
+      if (ok && c >= 2) ok = mbar_wait(o_free(c & 1), ((c - 2) >> 1) & 1, wlim);
       if (!__all_sync(kFull, ok)) failed = true;
       if (failed) return;
       tc_fence_after();
@@ -815,7 +836,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     // no MMA commit lands on this CTA's shared memory after it exits.
     const int r = is_qk ? 0 : 1;
     for (int c = last_c - kStages + 1 > 0 ? last_c - kStages + 1 : 0; c <= last_c && !failed; ++c) {
-      const bool ok = mbar_wait(empty_bar(r, c % kStages), (c / kStages) & 1);
+      const bool ok = mbar_wait(empty_bar(r, c % kStages), (c / kStages) & 1, wlim);
       if (!__all_sync(kFull, ok)) failed = true;
     }
   } else if (warp < 4 || (warp >= kWarpSmxB0 && warp < kWarpSmxB0 + 4)) {
@@ -845,7 +866,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       int u_pd = -1;
       // a = a * al + O(c), this group's columns
       auto fold = [&](int c, float (&a)[kGA], const float (&al)[kGA]) {
-        bool ok = !failed && mbar_wait(o_full(c & 1), (c >> 1) & 1);
+        bool ok = !failed && mbar_wait(o_full(c & 1), (c >> 1) & 1, wlim);
         if (!__all_sync(kFull, ok)) failed = true;
         tc_fence_after();
         // the stacked term columns of each head: g, 16 + g (, 32 + g)
@@ -898,7 +919,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
         named_bar_sync(bar, 128);  // lred is rewritten by the next unit
         const int es = je & 1;
         bool ok2 = !failed;
-        if (ok2 && je >= 2) ok2 = mbar_wait(ep_empty(es), ((je - 2) >> 1) & 1);
+        if (ok2 && je >= 2) ok2 = mbar_wait(ep_empty(es), ((je - 2) >> 1) & 1, wlim);
         if (!__all_sync(kFull, ok2)) failed = true;
         float* st = reinterpret_cast<float*>(base + kOffEpi) + es * kEpiFloats;
 #pragma unroll
@@ -939,7 +960,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
         const float ksc = p.k_scale ? __ldg(p.k_scale + (p.scale_per_head ? U.h : 0)) : 1.f;
         float qsc[kGA];
         if constexpr (KV8) {
-          const bool okq = !failed && mbar_wait(q8_full(jq & 1), (jq >> 1) & 1);
+          const bool okq = !failed && mbar_wait(q8_full(jq & 1), (jq >> 1) & 1, wlim);
           if (!__all_sync(kFull, okq)) failed = true;
           const float* qs = reinterpret_cast<const float*>(base + kOffQs) + (jq & 1) * 8;
 #pragma unroll
@@ -951,7 +972,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
         for (int i = 0; i < U.n_chunks; ++i, ++c) {
           const int slot = c % kStages;
           const int n_valid = min(kT, U.t1 - (U.t0 + i * kT));
-          bool ok = !failed && mbar_wait(s_full(c & 1), (c >> 1) & 1);
+          bool ok = !failed && mbar_wait(s_full(c & 1), (c >> 1) & 1, wlim);
           if (!__all_sync(kFull, ok)) failed = true;
           tc_fence_after();
           float s[4], s2[4];
@@ -1012,7 +1033,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
           if (grp == 0 && n_valid < kT) {
             // keep stale or out-of-context V rows out of the MMA; the V tile
             // of this chunk must have landed first (its last page may be partial)
-            ok = !failed && mbar_wait(full_bar(1, slot), (c / kStages) & 1);
+            ok = !failed && mbar_wait(full_bar(1, slot), (c / kStages) & 1, wlim);
             if (!__all_sync(kFull, ok)) failed = true;
             if (t >= n_valid) {
               uint8_t* vrow = base + kOffV + slot * kSlotBytes + t * kRowBytes;
@@ -1055,7 +1076,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       {
         const int es = je & 1;
         bool ok2 = !failed;
-        if (ok2 && je >= 2) ok2 = mbar_wait(ep_empty(es), ((je - 2) >> 1) & 1);
+        if (ok2 && je >= 2) ok2 = mbar_wait(ep_empty(es), ((je - 2) >> 1) & 1, wlim);
         if (!__all_sync(kFull, ok2)) failed = true;
         float* st = reinterpret_cast<float*>(base + kOffEpi) + es * kEpiFloats;
         if (grp == 0 && t == 0) reinterpret_cast<int*>(st)[8 * kHeadDim + 16] = -1;
@@ -1069,7 +1090,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     volatile int* flag = reinterpret_cast<volatile int*>(base + kOffEpiFlag);
     for (int je = 0;; ++je) {
       const int es = je & 1;
-      const bool ok = !failed && mbar_wait(ep_full(es), (je >> 1) & 1);
+      const bool ok = !failed && mbar_wait(ep_full(es), (je >> 1) & 1, wlim);
       // the four warps agree on the outcome before acting on it
       if (t == 0) *flag = 0;
       named_bar_sync(2, 128);

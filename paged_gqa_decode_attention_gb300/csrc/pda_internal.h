@@ -46,6 +46,12 @@ struct PartialParams {
   const float* k_scale;  // K/V dequantisation scales: [Hkv] (scale_per_head) or [1];
   const float* v_scale;  // NULL = 1
   int scale_per_head;
+  // Fault injection for the timeout tests (tensor-core kernel): stall_units
+  // makes the unit-fetching warp publish no unit, so every other role's
+  // first wait runs out with nothing issued or in flight; wait_ns (0 = the
+  // default kWaitLimitNs) shortens every pipeline wait.
+  int stall_units = 0;
+  unsigned long long wait_ns = 0;
 };
 
 struct MergeParams {

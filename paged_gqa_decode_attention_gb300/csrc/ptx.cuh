@@ -85,25 +85,27 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 // mbar_wait for waiters that have nothing else to do: sleeps in the
 // barrier instead of polling, so idle warps leave issue slots to the rest.
-__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity,
+                                                uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
 // Wait for the phase with the given parity to complete; false after
-// kWaitLimitNs without completion.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// `limit_ns` (default kWaitLimitNs) without completion.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
