@@ -40,18 +40,41 @@ METRIC = "decode tokens/s and KV-read HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes (read + write) per launch of the partial kernel from one ncu
-# capture of this workload (profiles/); None when not measured for the
-# current kernel.
-NCU_TRAFFIC_BYTES = {
-    # profiles/paged_partial_tc_kernel_long_b4_l32768.md: 537.15 MB read + 3.38 MB
-    # written per launch (captured on the same step over a 1 GiB pool)
-    # profiles/paged_partial_tc_kernel_long_b4_l32768.md: 537.04 MB read + 3.74 MB
-    # written per launch (captured on the same step over a 1 GiB pool)
-    "long_b4_l32768": 540_774_912,
-    # profiles/rope_kv_write_kernel_prefill_t32768.md: 419.90 MB read + 348.27 MB written
-    "rope_prefill_t32768": 768_166_400,
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal (~8 TB/s)
+
+# DRAM bytes (read + write) per launch from one ncu capture of the workload's
+# kernel, and the SHA-256 of the kernel sources that capture ran on. When the
+# sources no longer hash to that value the figure is stale and the bench
+# reports null traffic.
+_CSRC = os.path.join(ROOT, "paged_gqa_decode_attention_gb300", "csrc")
+TC_KERNEL_SOURCES = ("partial_tc_kernel.cuh", "ptx.cuh", "split_merge.cuh", "pda_internal.h",
+                     "partial_tc_bf16_d128.cu", "partial_launch.cu")
+ROPE_KERNEL_SOURCES = ("rope_kv_write.cu", "ptx.cuh", "pda_internal.h")
+NCU_TRAFFIC = {
+    # workload: (bytes per launch, kernel sources, their SHA-256 at capture)
+    "long_b4_l32768": (None, TC_KERNEL_SOURCES, None),
+    "rope_prefill_t32768": (768_166_400, ROPE_KERNEL_SOURCES, None),
 }
+
+
+def sources_digest(files) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in files:
+        with open(os.path.join(_CSRC, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(workload: str):
+    """(bytes per launch or None, note)."""
+    entry = NCU_TRAFFIC.get(workload)
+    if entry is None:
+        return None, "no ncu capture for this workload"
+    nbytes, files, digest = entry
+    if nbytes is None or digest is None or sources_digest(files) != digest:
+        return None, "kernel sources changed since the last ncu capture"
+    return nbytes, "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch"
 
 
 # ---------------------------------------------------------------------------
@@ -229,6 +252,7 @@ class ClockSampler:
             time.sleep(self.period)
 
     def __enter__(self):
+        self._stop.clear()
         if self._nvml is not None:
             self._thr = threading.Thread(target=self._run, daemon=True)
             self._thr.start()
@@ -347,6 +371,60 @@ def run_reference(args):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def back_to_back_samples(step, dev, samples: int = 7, launches: int = 200) -> list[float]:
+    """Per-launch device time (ms) of ``samples`` replays of one CUDA graph of
+    ``launches`` calls, CUDA events on the replay stream around each replay
+    (consecutive calls overlap their set-up with the previous call's tail)."""
+    stream = torch.cuda.current_stream(dev)
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        for _ in range(launches):
+            step()
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    out = []
+    for _ in range(samples):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        out.append(e0.elapsed_time(e1) / launches)
+    del graph
+    return out
+
+
+def cold_calls(step, dev, calls: int = 30) -> list[float]:
+    """Device time (ms) of ``calls`` single calls, each preceded by an L2
+    flush (a write of twice the L2 size, then a read of another such buffer so
+    the dirty lines drain before the call), CUDA events around each call on
+    the launching stream."""
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    wbuf = torch.empty(2 * max(l2, 1 << 27), dtype=torch.uint8, device=dev)
+    rbuf = torch.empty(2 * max(l2, 1 << 27) // 4, dtype=torch.int32, device=dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(calls)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(calls)]
+    for i in range(calls):
+        wbuf.zero_()
+        rbuf.max()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+
+def sample_summary(ms: list[float], nbytes: int, peak: float, **extra) -> dict:
+    med = statistics.median(ms)
+    return {**extra, "per_call_ms_median": med, "per_call_ms_min": min(ms),
+            "per_call_ms_max": max(ms), "kv_gbs_median": nbytes / (med / 1e3) / 1e9,
+            "frac_of_measured_median": nbytes / (med / 1e3) / 1e9 / peak,
+            "frac_of_nominal_median": nbytes / (med / 1e3) / 1e9 / NOMINAL_HBM_GBS}
 
 
 def partial_kernel_label(wl) -> str:
@@ -532,6 +610,13 @@ def run_ours(args):
     print(f"[bench] timed {timed_ms:.3f} ms for {args.steps} steps; host submit "
           f"{1e3 * cpu_submit:.3f} ms; {timing_desc}", file=sys.stderr)
     timed_ms_max = reduce_max(timed_ms, dev)
+
+    # ---- repeated samples of the same step, outside the K-step region ----
+    # back to back: 7 replays of a 200-call graph; cold: single calls after an
+    # L2 flush. The clock sampler keeps running across both.
+    with sampler:
+        b2b_ms = back_to_back_samples(step, dev)
+        cold_ms = cold_calls(step, dev)
     value = (B * world * args.steps) / (timed_ms_max / 1e3)
 
     # ---- end to end: host buffers, copies inside the timed region ----
@@ -544,7 +629,8 @@ def run_ours(args):
 
     peak, peak_kind = measured_peaks()
     achieved = kv_bytes / (avg_launch_ms / 1e3) / 1e9
-    traffic = NCU_TRAFFIC_BYTES.get(args.workload)
+    traffic, traffic_note = ncu_traffic(args.workload)
+    unique_bytes = wl.unique_kv_bytes()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": timed_ms_max / args.steps,
@@ -554,6 +640,7 @@ def run_ours(args):
         "config": {"workload": args.workload, "desc": WORKLOAD_DESC.get(args.workload, ""),
                    "batch_per_gpu": B, "global_batch": B * world,
                    "kv_bytes_per_step": kv_bytes,
+                   "unique_kv_bytes_per_step": unique_bytes,
                    "l2": "inputs larger than L2 (KV per step >= 2x L2, no flush)" if not flush
                    else ("L2 flushed between steps (write + read of 2x L2, outside the step "
                          "events)" if not use_graph else
@@ -562,16 +649,30 @@ def run_ours(args):
                    "timing": timing_desc},
         "kv_gbs": achieved,
         "kv_frac_of_peak": achieved / peak,
+        "kv_frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+        "samples": {
+            "back_to_back": sample_summary(b2b_ms, kv_bytes, peak, samples=len(b2b_ms),
+                                           launches_per_sample=200),
+            "cold": sample_summary(cold_ms, kv_bytes, peak, calls=len(cold_ms),
+                                   l2="flushed before each call"),
+        },
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
+                     "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_note,
                      "peak_source": f"{peak_kind} (hbm_gbs)",
                      "kernel": partial_kernel_label(wl),
-                     "per_launch_ms": avg_launch_ms},
+                     "per_launch_ms": avg_launch_ms,
+                     "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+                     "nominal_peak": NOMINAL_HBM_GBS},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "mode": e2e_mode},
         "gpu_launches": args.steps * launches_per_step(attn, wl),
         "clocks": sampler.summary(),
     }
+    if unique_bytes != kv_bytes:
+        # shared prefix pages: bytes of the distinct slots read (aliased pages
+        # may be served from L2 for all but their first reader)
+        line["kv_gbs_unique"] = unique_bytes / (avg_launch_ms / 1e3) / 1e9
+        line["kv_frac_of_peak_unique"] = line["kv_gbs_unique"] / peak
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, desc, cores, secs = oracle_sample(wl)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -581,6 +682,53 @@ def run_ours(args):
     attn.close()
     if world > 1:
         dist.destroy_process_group()
+    return 0
+
+
+def run_split_sweep(args):
+    """The long-context split-count sweep: B in {1, 4} x L in {8192, 32768}
+    cut from one full-size pool (random tables over 40 GiB; FP8 workloads use
+    B in {1, 8} over the 20 GiB FP8 pool), every split count in 1..64 plus the
+    planner's pick. Per (shape, S) one JSON line with the cold per-call time
+    (L2 flushed before each call) and the back-to-back time (graph replay)."""
+    from paged_gqa_decode_attention_gb300 import PagedDecodeAttention, make_config, plan
+    from paged_gqa_decode_attention_gb300 import build as pda_build
+    from paged_gqa_decode_attention_gb300 import workloads as W
+    world, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pda_build.build()
+    fp8 = "fp8" in args.workload
+    big = 8 if fp8 else 4
+    pool = W.long_context(seed=args.seed, batch=big, context=32768, device=dev, kv_fp8=fp8)
+    peak, _ = measured_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ksc, vsc = pool.meta.get("k_scale"), pool.meta.get("v_scale")
+    for B, L in ((1, 8192), (big, 8192), (1, 32768), (big, 32768)):
+        wl = W.leading(pool, B, L)
+        attn = PagedDecodeAttention(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size,
+                                    wl.q.dtype, max_batch=B, max_blocks_per_seq=wl.max_blocks,
+                                    max_splits=64, device=dev, kv_fp8=fp8)
+        cfg = make_config(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size,
+                          wl.q.dtype, max_batch=B, max_blocks_per_seq=wl.max_blocks,
+                          max_splits=64, device=dev.index, kv_fp8=fp8)
+        picked = plan(cfg, sms, B, wl.max_blocks)[0]
+        out = torch.empty_like(wl.q)
+        for S in sorted({1, 2, 4, 8, 16, 32, 64, picked}):
+            def step(S=S):
+                attn.run(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.context_lens,
+                         wl.scale, out=out, num_splits=S, k_scale=ksc, v_scale=vsc)
+            for _ in range(max(3, args.warmup)):
+                step()
+            torch.cuda.synchronize(dev)
+            cold = sample_summary(cold_calls(step, dev, 20), wl.kv_bytes(), peak, calls=20)
+            b2b = sample_summary(back_to_back_samples(step, dev, 5, 100), wl.kv_bytes(), peak,
+                                 samples=5, launches_per_sample=100)
+            print(json.dumps({"workload": wl.name, "batch": B, "context": L, "splits": S,
+                              "planner_pick": S == picked, "kv_bytes": wl.kv_bytes(),
+                              "cold": cold, "back_to_back": b2b}), flush=True)
+        attn.close()
     return 0
 
 
@@ -734,7 +882,8 @@ def run_rope(args):
                     else "L2-warm: graph replay, no flush"),
                    "timing": timing_desc},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": NCU_TRAFFIC_BYTES.get(args.workload),
+                     "frac": achieved / peak, "traffic": ncu_traffic(args.workload)[0],
+                     "traffic_source": ncu_traffic(args.workload)[1],
                      "peak_source": f"{peak_kind} (hbm_gbs)",
                      "kernel": "rope_kv_write_kernel", "per_launch_ms": avg_ms},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -848,7 +997,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--timing", choices=["auto", "graph", "eager"], default="auto")
     ap.add_argument("--splits", type=int, default=0, help="split count (0 = the planner's)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="long-context split-count sweep (one JSON line per shape and count)")
     args = ap.parse_args(argv)
+    if args.sweep:
+        return run_split_sweep(args)
     if args.workload in ROPE_WORKLOADS:
         return run_rope(args)
     if args.workload in MOVE_WORKLOADS:
