@@ -525,6 +525,7 @@ def run_ours(args):
     ksc, vsc = wl.meta.get("k_scale"), wl.meta.get("v_scale")
     out = torch.empty((B, Hq, D), dtype=wl.q.dtype, device=dev)
     kv_bytes = wl.kv_bytes()
+    launch = attn.launch_shape(B, wl.max_blocks, num_splits=args.splits)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     # Inputs of at least twice the L2 size evict each other between steps. For
     # smaller ones the L2 is flushed between steps: a write of a buffer larger
@@ -645,6 +646,7 @@ def run_ours(args):
                    else ("L2 flushed between steps (write + read of 2x L2, outside the step "
                          "events)" if not use_graph else
                          "graph replay without flush: KV per step < 2x L2, partly L2-resident"),
+                   "launch": launch,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "timing": timing_desc},
         "kv_gbs": achieved,
@@ -727,6 +729,7 @@ def run_split_sweep(args):
                                  samples=5, launches_per_sample=100)
             print(json.dumps({"workload": wl.name, "batch": B, "context": L, "splits": S,
                               "planner_pick": S == picked, "kv_bytes": wl.kv_bytes(),
+                              "launch": attn.launch_shape(B, wl.max_blocks, num_splits=S),
                               "cold": cold, "back_to_back": b2b}), flush=True)
         attn.close()
     return 0

@@ -175,6 +175,21 @@ int paged_decode_attn_run_scaled(pda_handle handle, const void* q, const void* k
 int paged_decode_attn_plan(const pda_config* cfg, int num_sms, int batch, int max_blocks,
                            int max_context_len_hint, int* num_splits, int* chunk_pages);
 
+/* How paged_decode_attn_run_ex with these arguments is launched on this
+ * handle's GPU (host only, no CUDA call): *splits and *chunk_pages as in
+ * paged_decode_attn_plan (num_splits 0 = the heuristic), *ctas the CTAs of
+ * the partial kernel, and *cluster the CTAs per thread-block cluster. With
+ * the tensor-core kernel, a split count of 2..16 whose batch * Hkv
+ * (sequence, kv head) pairs all fit on the GPU at once as clusters of that
+ * many CTAs runs as one cluster per pair, one CTA per split, and the splits
+ * merge through distributed shared memory (*cluster = splits); otherwise
+ * *cluster = 1 and the last split of a pair merges through the handle's
+ * workspace. (Landing page, "Supported now": split-K with log-sum-exp
+ * merge; the cluster layout is this library's GB300 design.) */
+int paged_decode_attn_launch_shape(pda_handle handle, int batch, int max_blocks,
+                                   int max_context_len_hint, int num_splits, int* splits,
+                                   int* chunk_pages, int* ctas, int* cluster);
+
 /* Log-sum-exp merge of split partials (the split-K merge step on its own,
  * e.g. for partials computed elsewhere):
  *   partial_o   [rows, num_splits, head_dim] fp32, each split's normalised output

@@ -36,6 +36,7 @@ EXPORTS = [
     "paged_decode_attn_run_ex",
     "paged_decode_attn_run_scaled",
     "paged_decode_attn_plan",
+    "paged_decode_attn_launch_shape",
     "paged_decode_attn_merge",
     "paged_decode_attn_validate",
     "paged_decode_attn_check_device_error",
@@ -96,6 +97,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.paged_decode_attn_plan.argtypes = [ctypes.POINTER(Config), I, I, I, I,
                                                ctypes.POINTER(I), ctypes.POINTER(I)]
         lib.paged_decode_attn_plan.restype = I
+        lib.paged_decode_attn_launch_shape.argtypes = [P, I, I, I, I] + [ctypes.POINTER(I)] * 4
+        lib.paged_decode_attn_launch_shape.restype = I
         lib.paged_decode_attn_merge.argtypes = [P, P, I, I, I, P, I, I, P]
         lib.paged_decode_attn_merge.restype = I
         lib.paged_decode_attn_validate.argtypes = [P, P, P, I, I, I64, P]
@@ -256,6 +259,16 @@ class PagedDecodeAttention:
         return self.lib.paged_decode_attn_run(self.handle, q_ptr, k_ptr, v_ptr, table_ptr,
                                               lens_ptr, batch, max_blocks, num_blocks,
                                               float(scale), out_ptr, stream)
+
+    def launch_shape(self, batch: int, max_blocks: int, num_splits: int = 0,
+                     max_context_len_hint: int = 0) -> dict:
+        """How a run with these sizes is launched: splits, chunk_pages, ctas,
+        cluster (CTAs per thread-block cluster; 1 = no clusters)."""
+        out = [ctypes.c_int(0) for _ in range(4)]
+        _check(self.lib, self.lib.paged_decode_attn_launch_shape(
+            self.handle, batch, max_blocks, max_context_len_hint, num_splits,
+            *[ctypes.byref(o) for o in out]))
+        return dict(zip(("splits", "chunk_pages", "ctas", "cluster"), (o.value for o in out)))
 
     def validate(self, block_table, context_lens, num_blocks: int, stream=None):
         B = context_lens.shape[0]

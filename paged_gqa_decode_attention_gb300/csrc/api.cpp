@@ -226,6 +226,12 @@ struct pda_handle_s {
   int* counters = nullptr;  // [max_batch, Hkv] split tickets
   size_t counter_bytes = 0;
   int test_stall_runs = 0;  // timeout tests: this many first runs publish no unit
+  // Tensor-core kernel: clusters of c CTAs (c = 2..16) that can be resident
+  // at once, so a step of groups <= max_clusters[S] (sequence, kv head) pairs
+  // runs as clusters that merge their splits in distributed shared memory;
+  // 0 = that cluster size is not available. PDA_CLUSTER_MERGE=0 turns the
+  // cluster launch off for this handle (A/B runs, tests of the other path).
+  int max_clusters[17] = {};
   // TMA descriptors for the last (k_cache, v_cache, num_blocks) seen
   const void* tm_k = nullptr;
   const void* tm_v = nullptr;
@@ -233,6 +239,39 @@ struct pda_handle_s {
   alignas(64) CUtensorMap tmap_k;
   alignas(64) CUtensorMap tmap_v;
 };
+
+namespace {
+
+struct LaunchShape {
+  int splits, chunk_pages, ctas, cluster;
+  int64_t units;
+};
+
+// How a run of this handle is launched: the split plan, the work units, the
+// CTAs and, for the tensor-core kernel, whether the launch is one wave of
+// clusters (one per (sequence, kv head), the splits merging through
+// distributed shared memory) when every pair fits.
+LaunchShape launch_shape(const pda_handle_s* h, int batch, int max_blocks, int hint, int forced) {
+  const pda_config& c = h->cfg;
+  LaunchShape r{1, 1, 0, 0, 0};
+  plan_splits(c, h->kernel, h->num_sms, h->ctas_per_sm, batch, max_blocks, hint, forced,
+              &r.splits, &r.chunk_pages);
+  r.units = (int64_t)r.splits * c.num_kv_heads * batch;
+  if (h->kernel == pda::kPartialTensorCore) {
+    const int64_t max_ctas = (int64_t)h->num_sms * h->ctas_per_sm;
+    r.ctas = (int)(r.units < max_ctas ? r.units : max_ctas);
+    if (r.splits >= 2 && r.splits <= 16 &&
+        (int64_t)batch * c.num_kv_heads <= h->max_clusters[r.splits]) {
+      r.cluster = r.splits;
+      r.ctas = (int)r.units;
+    }
+  } else {
+    r.ctas = (int)(r.units < INT_MAX ? r.units : INT_MAX);
+  }
+  return r;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -280,6 +319,11 @@ int paged_decode_attn_create(const pda_config* cfg, pda_handle* out_handle) {
     delete h;
     return cuda_fail("cudaFuncSetAttribute", e);
   }
+  const char* cl_env = std::getenv("PDA_CLUSTER_MERGE");
+  if (h->kernel == pda::kPartialTensorCore && !(cl_env && std::strcmp(cl_env, "0") == 0))
+    for (int c = 2; c <= 16 && c <= cfg->max_splits; ++c)
+      h->max_clusters[c] = pda::partial_max_clusters(h->group, cfg->head_dim, cfg->block_size,
+                                                     cfg->dtype, kv8, c);
   // Plan with the residency the kernel is built for, so paged_decode_attn_plan
   // (no GPU) and run agree; fall back to the measured figure if it is lower.
   const int occ =
@@ -418,10 +462,10 @@ int paged_decode_attn_run_scaled(pda_handle h, const void* q, const void* k_cach
     h->tm_nb = num_blocks;
   }
 
-  int S = 1, chunk = 1;
-  plan_splits(c, h->kernel, h->num_sms, h->ctas_per_sm, batch, max_blocks, max_context_len_hint,
-              num_splits, &S, &chunk);
-  const int64_t units = (int64_t)S * c.num_kv_heads * batch;
+  const LaunchShape shape =
+      launch_shape(h, batch, max_blocks, max_context_len_hint, num_splits);
+  const int S = shape.splits, chunk = shape.chunk_pages;
+  const int64_t units = shape.units;
   if (units > INT_MAX) return fail(PDA_EINVAL, "splits * num_kv_heads * batch exceeds 2^31");
   alignas(64) CUtensorMap tmap_q;
   if (h->kernel == pda::kPartialTensorCore) {
@@ -453,6 +497,7 @@ int paged_decode_attn_run_scaled(pda_handle h, const void* q, const void* k_cach
   p.k_scale = k_scale;
   p.v_scale = v_scale;
   p.scale_per_head = scale_per_head;
+  p.cluster = shape.cluster;
   if (h->test_stall_runs > 0) {
     --h->test_stall_runs;
     p.stall_units = 1;
@@ -472,6 +517,26 @@ int paged_decode_attn_run(pda_handle h, const void* q, const void* k_cache, cons
                           void* stream) {
   return paged_decode_attn_run_ex(h, q, k_cache, v_cache, block_table, context_lens, batch,
                                   max_blocks, num_blocks, scale, out, stream, 0, 0, -1);
+}
+
+int paged_decode_attn_launch_shape(pda_handle h, int batch, int max_blocks,
+                                   int max_context_len_hint, int num_splits, int* splits,
+                                   int* chunk_pages, int* ctas, int* cluster) {
+  if (!h) return fail(PDA_EINVAL, "handle is NULL");
+  if (!splits || !chunk_pages || !ctas || !cluster) return fail(PDA_EINVAL, "output pointer is NULL");
+  const pda_config& c = h->cfg;
+  if (batch < 1 || batch > c.max_batch) return fail(PDA_EINVAL, "batch out of [1, max_batch]");
+  if (max_blocks < 1 || max_blocks > c.max_blocks_per_seq)
+    return fail(PDA_EINVAL, "max_blocks out of [1, max_blocks_per_seq]");
+  if (num_splits < 0 || num_splits > c.max_splits)
+    return fail(PDA_EINVAL, "num_splits out of [0, max_splits]");
+  if (max_context_len_hint < 0) return fail(PDA_EINVAL, "max_context_len_hint < 0");
+  const LaunchShape r = launch_shape(h, batch, max_blocks, max_context_len_hint, num_splits);
+  *splits = r.splits;
+  *chunk_pages = r.chunk_pages;
+  *ctas = r.ctas;
+  *cluster = r.cluster > 1 ? r.cluster : 1;
+  return PDA_OK;
 }
 
 int paged_decode_attn_merge(const float* partial_o, const float* partial_lse, int rows,

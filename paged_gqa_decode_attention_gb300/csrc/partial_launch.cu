@@ -23,7 +23,8 @@ PDA_DECLARE_CC(fp16, 256)
                                             const CUtensorMap*, const PartialParams&,          \
                                             cudaStream_t);                                     \
   cudaError_t prepare_partial_tc_##dt##_d##D(int, int);                                        \
-  int occupancy_partial_tc_##dt##_d##D(int, int);
+  int occupancy_partial_tc_##dt##_d##D(int, int);                                             \
+  int max_clusters_partial_tc_##dt##_d##D(int, int, int);
 PDA_DECLARE_TC(bf16, 64)
 PDA_DECLARE_TC(bf16, 128)
 PDA_DECLARE_TC(fp16, 64)
@@ -56,7 +57,7 @@ template <typename F>
 auto with_tc(int dtype, int head_dim, bool kv_fp8, F f) {
 #define PDA_TC_CASE(dt, D)                                                             \
   return f(launch_partial_tc_##dt##_d##D, prepare_partial_tc_##dt##_d##D,              \
-           occupancy_partial_tc_##dt##_d##D)
+           occupancy_partial_tc_##dt##_d##D, max_clusters_partial_tc_##dt##_d##D)
   if (kv_fp8) PDA_TC_CASE(kv8_bf16, 128);
   if (dtype == 1) {
     if (head_dim == 64) PDA_TC_CASE(fp16, 64);
@@ -83,7 +84,7 @@ bool partial_kernel_supported(int kernel, int group, int head_dim, bool kv_fp8) 
 cudaError_t partial_prepare(int kernel, int group, int head_dim, int block_size, int dtype,
                             bool kv_fp8) {
   if (kernel == kPartialTensorCore)
-    return with_tc(dtype, head_dim, kv_fp8, [&](auto, auto prepare, auto) {
+    return with_tc(dtype, head_dim, kv_fp8, [&](auto, auto prepare, auto, auto) {
       return prepare(group, block_size);
     });
   return with_cc(dtype, head_dim, [&](auto, auto prepare, auto) {
@@ -94,11 +95,19 @@ cudaError_t partial_prepare(int kernel, int group, int head_dim, int block_size,
 int partial_ctas_per_sm(int kernel, int group, int head_dim, int block_size, int dtype,
                         bool kv_fp8) {
   if (kernel == kPartialTensorCore)
-    return with_tc(dtype, head_dim, kv_fp8, [&](auto, auto, auto occupancy) {
+    return with_tc(dtype, head_dim, kv_fp8, [&](auto, auto, auto occupancy, auto) {
       return occupancy(group, block_size);
     });
   return with_cc(dtype, head_dim, [&](auto, auto, auto occupancy) {
     return occupancy(group, block_size);
+  });
+}
+
+int partial_max_clusters(int group, int head_dim, int block_size, int dtype, bool kv_fp8,
+                         int cluster) {
+  if (!tc::geometry_supported(group, head_dim, kv_fp8) || cluster < 2 || cluster > 16) return 0;
+  return with_tc(dtype, head_dim, kv_fp8, [&](auto, auto, auto, auto max_clusters) {
+    return max_clusters(group, block_size, cluster);
   });
 }
 
@@ -107,7 +116,7 @@ cudaError_t launch_partial(int kernel, int group, int head_dim, int block_size, 
                            const CUtensorMap* tq, const PartialParams& p, int batch,
                            cudaStream_t stream) {
   if (kernel == kPartialTensorCore)
-    return with_tc(dtype, head_dim, kv_fp8, [&](auto launch, auto, auto) {
+    return with_tc(dtype, head_dim, kv_fp8, [&](auto launch, auto, auto, auto) {
       return launch(group, block_size, tk, tv, tq, p, stream);
     });
   return with_cc(dtype, head_dim, [&](auto launch, auto, auto) {

@@ -18,4 +18,8 @@ int occupancy_partial_tc_bf16_d64(int G, int BS) {
   return tc::Dispatch<64, false, false>::occupancy(G, BS);
 }
 
+int max_clusters_partial_tc_bf16_d64(int G, int BS, int cluster) {
+  return tc::Dispatch<64, false, false>::max_clusters(G, BS, cluster);
+}
+
 }  // namespace pda

@@ -123,7 +123,8 @@ constexpr int kUnitRing = 4;               // slots of the shared unit queue
 constexpr int kUnitConsumers = 4;
 constexpr int kUnitInts = 12;              // a unit ring entry: index + decoded Unit
 // A finished unit's state, softmax -> epilogue, double-buffered:
-// acc[8][128], max[8], sum[8], unit index (floats; the index as int).
+// acc[8][128], max[8], sum[8], then the unit index and its sequence's split
+// count (as ints).
 constexpr int kEpiFloats = 8 * 128 + 8 + 8 + 4;
 constexpr float kP8Scale = 256.f;          // FP8 K/V: P is split at p * 256
 
@@ -146,7 +147,7 @@ struct Layout {
   static constexpr int kOffRed = kOffQs + 2 * 8 * 4;
   static constexpr int kOffLred = kOffRed + 2 * 2 * 4 * 8 * 4;
   static constexpr int kOffBar = kOffLred + 2 * 4 * 8 * 4;
-  static constexpr int kNumBars = 4 * kStages + 14 + 2 * kUnitRing + 4 + 2;
+  static constexpr int kNumBars = 4 * kStages + 14 + 2 * kUnitRing + 4 + 2 + 1;
   static constexpr int kOffTmem = kOffBar + kNumBars * 8;
   // [kUnitRing] unit index + decoded unit, so no reader repeats its global loads
   static constexpr int kOffURing = kOffTmem + 16;
@@ -275,6 +276,19 @@ __device__ __forceinline__ Unit load_unit(const PartialParams& p, int u) {
   return U;
 }
 
+// Units that no role has to process: neither pages nor output rows.
+__device__ __forceinline__ bool unit_has_work(const Unit& U) { return U.n_chunks > 0 || U.zero_fill; }
+
+// Block-table entries p0 + lane of unit u's sequence, with p0 the unit's first
+// page, requested before the unit's context length is known (the entries
+// past the sequence's pages are loaded but never used).
+__device__ __forceinline__ int unit_first_window(const PartialParams& p, int u, int lane) {
+  const int split = u % p.num_splits;
+  const int b = u / p.num_splits / p.Hkv;
+  const int idx = split * p.chunk_pages + lane;
+  return idx < p.max_blocks ? __ldg(p.block_table + (int64_t)b * p.max_blocks + idx) : 0;
+}
+
 // Walks a sequence of units with work, chunk by chunk: c counts chunks over
 // the whole walk (ring slots and buffer parities follow it), j counts units.
 // `next()` of the source yields unit indices in order, -1 at the end; units
@@ -359,6 +373,9 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
   auto ep_empty = [&](int s) { return bar0 + 8u * (4 * kStages + 16 + 2 * kUnitRing + s); };
   // FP8 K/V: the unit's fp8 Q terms and row scales are ready (buffer b)
   auto q8_full = [&](int b) { return bar0 + 8u * (4 * kStages + 18 + 2 * kUnitRing + b); };
+  // cluster launches: every other CTA of the cluster has its split's partial
+  // in its state slot (one arrival per other CTA)
+  const uint32_t cl_bar = bar0 + 8u * (4 * kStages + 20 + 2 * kUnitRing);
   volatile int* uring = reinterpret_cast<volatile int*>(base + kOffURing);
 
   const int warp = threadIdx.x >> 5;
@@ -366,11 +383,13 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
   bool failed = false;
   const uint64_t wlim = p.wait_ns ? (uint64_t)p.wait_ns : kWaitLimitNs;
 
-  // Work units are handed out dynamically: the K-producer warp takes unit
-  // indices from a global counter (p.sched[0]) and publishes every one that
-  // has output to write into the unit ring; the V producer, the MMA warp and
-  // softmax warp 0 read the ring in order. The CTA that runs out last resets
-  // the counters for the next call.
+  // Work units: CTA i starts with unit i (every role decodes it itself, so the
+  // first page loads wait for no counter round trip and no ring hand-off);
+  // after that the K-producer warp takes unit indices gridDim.x + k from a
+  // global counter (p.sched[0]) and publishes every one that has output to
+  // write into the unit ring; the V producer, the MMA warps and softmax warp 0
+  // read the ring in order. The CTA that runs out last resets the counters
+  // for the next call. (The grid never has more CTAs than units.)
   struct FetchSource {
     const PartialParams* p;
     volatile int* ring;
@@ -379,6 +398,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     bool* failed;
     uint64_t wlim;
     bool counted;
+    bool first;  // the next unit is this CTA's static first unit
     // This CTA takes no more units: count it done exactly once (also after a
     // timed-out wait), so the CTA that finishes last resets the counters and
     // the next call starts from zero.
@@ -400,14 +420,19 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
         done();
         return -1;
       }
+      if (first) {
+        first = false;
+        U = load_unit<BS>(*p, (int)blockIdx.x);
+        if (unit_has_work(U)) return (int)blockIdx.x;
+      }
       while (true) {
         int u = 0;
-        if (lane == 0) u = atomicAdd(p->sched, 1);
+        if (lane == 0) u = (int)gridDim.x + atomicAdd(p->sched, 1);
         u = __shfl_sync(kFull, u, 0);
         const int pub = u < p->num_units ? u : -1;
         if (pub >= 0) {
           U = load_unit<BS>(*p, pub);
-          if (U.n_chunks == 0 && !U.zero_fill) continue;  // nothing to do for this unit
+          if (!unit_has_work(U)) continue;  // nothing to do for this unit
         }
         const int slot = k % kUnitRing;
         bool ok = true;
@@ -432,12 +457,21 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     }
   };
   struct RingSource {
+    const PartialParams* p;
     volatile int* ring;
     uint32_t full0, empty0;
     int lane, k;
     bool* failed;
     uint64_t wlim;
+    bool first;  // the next unit is this CTA's static first unit
     __device__ __forceinline__ int next(Unit& U) {
+      if (first) {
+        first = false;
+        if (!p->stall_units && !*failed) {
+          U = load_unit<BS>(*p, (int)blockIdx.x);
+          if (unit_has_work(U)) return (int)blockIdx.x;
+        }
+      }
       const int slot = k % kUnitRing;
       const bool ok = !*failed && mbar_wait(full0 + 8u * slot, (k / kUnitRing) & 1, wlim);
       if (!__all_sync(kFull, ok)) {
@@ -452,7 +486,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     }
   };
   auto ring_source = [&]() {
-    return RingSource{uring, uring_full(0), uring_empty(0), lane, 0, &failed, wlim};
+    return RingSource{&p, uring, uring_full(0), uring_empty(0), lane, 0, &failed, wlim, true};
   };
 
   if (threadIdx.x == 0) {
@@ -481,6 +515,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       mbar_init(q_empty(b2), KV8 ? 1 + kGroups : 1);
       mbar_init(q8_full(b2), 1);
     }
+    if (p.cluster > 1) mbar_init(cl_bar, (uint32_t)(p.cluster - 1));
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -497,6 +532,9 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // every CTA of a cluster has initialised its barriers before any other CTA
+  // may arrive on them
+  if (p.cluster > 1) cluster_sync_all();
   // Everything above touches only this CTA's resources; from here on the
   // kernel reads the inputs and the shared counters, which the previous
   // grid in the stream may still be writing (programmatic dependent launch).
@@ -517,10 +555,14 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       prefetch_tensormap(map);
       if (r == 0) prefetch_tensormap(&tmap_q);
     }
-    FetchSource fetch{&p, uring, uring_full(0), uring_empty(0), lane, 0, &failed, wlim, false};
+    FetchSource fetch{&p, uring, uring_full(0), uring_empty(0), lane, 0, &failed, wlim, false,
+                      true};
     RingSource ring = ring_source();
     Cursor<BS, FetchSource> cur_k;
     Cursor<BS, RingSource> cur_v;
+    // the first window of the static first unit, requested together with its
+    // context length
+    const int first_win = p.stall_units ? 0 : unit_first_window(p, (int)blockIdx.x, lane);
     if (r == 0) cur_k.start(p, fetch); else cur_v.start(p, ring);
     // block-table entries in windows of 32 pages, the next window prefetched
     int win_base = 0, win_blk = 0, nxt_blk = 0;
@@ -528,11 +570,13 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       const int cu_i = r == 0 ? cur_k.i : cur_v.i;
       const int cu_c = r == 0 ? cur_k.c : cur_v.c;
       const int cu_j = r == 0 ? cur_k.j : cur_v.j;
+      const int cu_u = r == 0 ? cur_k.u : cur_v.u;
       const Unit& U = r == 0 ? cur_k.U : cur_v.U;
       const int32_t* table = p.block_table + (int64_t)U.b * p.max_blocks;
       if (cu_i == 0) {
         win_base = U.p0;
-        win_blk = (U.p0 + lane < U.p1) ? __ldg(table + U.p0 + lane) : 0;
+        if (cu_j == 0 && cu_u == (int)blockIdx.x) win_blk = first_win;
+        else win_blk = (U.p0 + lane < U.p1) ? __ldg(table + U.p0 + lane) : 0;
         nxt_blk = (U.p0 + 32 + lane < U.p1) ? __ldg(table + U.p0 + 32 + lane) : 0;
         if (r == 0) {
           // this unit's G query rows -> Q operand buffer j & 1
@@ -611,10 +655,12 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       prefetch_tensormap(map);
       if (fetcher) prefetch_tensormap(&tmap_q);
     }
-    FetchSource fetch{&p, uring, uring_full(0), uring_empty(0), lane, 0, &failed, wlim, false};
+    FetchSource fetch{&p, uring, uring_full(0), uring_empty(0), lane, 0, &failed, wlim, false,
+                      true};
     RingSource ring = ring_source();
     Cursor<BS, FetchSource> cur_k;
     Cursor<BS, RingSource> cur_v;
+    const int first_win = p.stall_units ? 0 : unit_first_window(p, (int)blockIdx.x, lane);
     if (fetcher) cur_k.start(p, fetch); else cur_v.start(p, ring);
     // block-table entries in windows of 32 pages, the next window prefetched
     int win_base = 0, win_blk = 0, nxt_blk = 0;
@@ -622,11 +668,13 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       const int cu_i = fetcher ? cur_k.i : cur_v.i;
       const int cu_c = fetcher ? cur_k.c : cur_v.c;
       const int cu_j = fetcher ? cur_k.j : cur_v.j;
+      const int cu_u = fetcher ? cur_k.u : cur_v.u;
       const Unit& U = fetcher ? cur_k.U : cur_v.U;
       const int32_t* table = p.block_table + (int64_t)U.b * p.max_blocks;
       if (cu_i == 0) {
         win_base = U.p0;
-        win_blk = (U.p0 + lane < U.p1) ? __ldg(table + U.p0 + lane) : 0;
+        if (cu_j == 0 && cu_u == (int)blockIdx.x) win_blk = first_win;
+        else win_blk = (U.p0 + lane < U.p1) ? __ldg(table + U.p0 + lane) : 0;
         nxt_blk = (U.p0 + 32 + lane < U.p1) ? __ldg(table + U.p0 + 32 + lane) : 0;
         if (fetcher) {
           // this unit's G query rows -> Q operand buffer j & 1
@@ -863,7 +911,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       // waits until the next unit's first P is written, so the unit boundary
       // does not wait for the last PV to complete.
       float m_pd[kGA], l_pd[kGA], acc_pd[kGA], alpha_pd[kGA];
-      int u_pd = -1;
+      int u_pd = -1, nsb_pd = 0;  // its index and its sequence's split count
       // a = a * al + O(c), this group's columns
       auto fold = [&](int c, float (&a)[kGA], const float (&al)[kGA]) {
         bool ok = !failed && mbar_wait(o_full(c & 1), (c >> 1) & 1, wlim);
@@ -903,7 +951,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       // Hands a finished unit's state (this group's columns) to the epilogue
       // group: the softmax denominators are the per-token partial sums added
       // over the group.
-      auto finish = [&](int uf, const float (&mf)[kGA], const float (&lf)[kGA],
+      auto finish = [&](int uf, int nsb, const float (&mf)[kGA], const float (&lf)[kGA],
                         const float (&af)[kGA]) {
 #pragma unroll
         for (int j = 0; j < kGA; ++j) {
@@ -933,7 +981,10 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
               st[8 * kHeadDim + 8 + g0 + j] = Ls[j];
             }
           }
-          if (grp == 0) reinterpret_cast<int*>(st)[8 * kHeadDim + 16] = uf;
+          if (grp == 0) {
+            reinterpret_cast<int*>(st)[8 * kHeadDim + 16] = uf;
+            reinterpret_cast<int*>(st)[8 * kHeadDim + 17] = nsb;
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(ep_full(es));
@@ -1052,7 +1103,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
           } else if (u_pd >= 0) {
             // the previous unit's last chunk
             fold(c - 1, acc_pd, alpha_pd);
-            finish(u_pd, m_pd, l_pd, acc_pd);
+            finish(u_pd, nsb_pd, m_pd, l_pd, acc_pd);
             u_pd = -1;
           }
 #pragma unroll
@@ -1066,11 +1117,12 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
           alpha_pd[j] = alpha_prev[j];
         }
         u_pd = u;
+        nsb_pd = U.n_splits_b;
         ++jq;
       }
       if (u_pd >= 0) {
         fold(c - 1, acc_pd, alpha_pd);
-        finish(u_pd, m_pd, l_pd, acc_pd);
+        finish(u_pd, nsb_pd, m_pd, l_pd, acc_pd);
       }
       // end of work: an empty state tells the epilogue group to stop
       {
@@ -1102,12 +1154,96 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       }
       float* st = reinterpret_cast<float*>(base + kOffEpi) + es * kEpiFloats;
       const int u = reinterpret_cast<volatile int*>(st)[8 * kHeadDim + 16];
-      if (u < 0) break;
-      const Unit U = load_unit<BS>(p, u);
+      if (u < 0) {
+        // a cluster CTA whose split had nothing to merge still counts toward
+        // the other CTAs' merge barriers
+        if (p.cluster > 1 && je == 0 && t == 0) {
+          const uint32_t me = cluster_ctarank();
+          for (int q = 0; q < p.cluster; ++q)
+            if (q != (int)me) mbar_arrive_remote(cluster_map(cl_bar, (uint32_t)q));
+        }
+        break;
+      }
+      // the unit from its index alone (no global load on this path): its
+      // split, kv head and sequence, and the sequence's split count
+      Unit U;
+      U.split = u % p.num_splits;
+      U.h = (u / p.num_splits) % p.Hkv;
+      U.b = u / p.num_splits / p.Hkv;
+      U.n_splits_b = reinterpret_cast<volatile int*>(st)[8 * kHeadDim + 17];
       const int hq0 = U.h * G;
       // V dequantisation scale (and the fp8 split factor of P)
       const float vsc = (p.v_scale ? __ldg(p.v_scale + (p.scale_per_head ? U.h : 0)) : 1.f) *
                         (KV8 ? 1.f / kP8Scale : 1.f);
+      if (p.cluster > 1 && U.n_splits_b > 1) {
+        // Cluster launch: this split's normalised partial and log-sum-exp stay
+        // in this CTA's state slot; once every other CTA of the cluster has
+        // signalled, each split with pages merges its share of the outputs,
+        // reading the other splits' slots through distributed shared memory.
+        if (t < D) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) st[g * kHeadDim + t] = st[g * kHeadDim + t] / st[8 * kHeadDim + 8 + g] * vsc;
+        }
+        if (t == 0) {
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+            st[8 * kHeadDim + g] = (st[8 * kHeadDim + g] + log2f(st[8 * kHeadDim + 8 + g])) * kLn2;
+        }
+        named_bar_sync(2, 128);  // this CTA's slot holds its split's o and lse
+        if (t == 0) {
+          fence_acq_rel_cluster();
+          for (int q = 0; q < p.cluster; ++q)
+            if (q != U.split) mbar_arrive_remote(cluster_map(cl_bar, (uint32_t)q));
+        }
+        const bool okm = mbar_wait_cluster(cl_bar, 0, wlim);
+        if (!__all_sync(kFull, okm)) failed = true;
+        if (!failed) {
+          // this split's share of the G x D outputs, each merged over the
+          // sequence's splits with all their loads in flight together
+          const int nsb = U.n_splits_b;
+          const int per = (G * D + nsb - 1) / nsb;
+          const int lo = U.split * per, hi = min(G * D, lo + per);
+          const uint32_t st_u32 = smem_u32(st);
+          for (int oi = lo + t; oi < hi; oi += 128) {
+            const int g = oi / D, d = oi - g * D;
+            // groups of 8 splits, a running maximum across the groups
+            float M = -INFINITY, wsum = 0.f, acc = 0.f;
+            for (int s0 = 0; s0 < nsb; s0 += 8) {
+              float l[8], v[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                if (s0 + k < nsb) {
+                  const uint32_t rb = cluster_map(st_u32, (uint32_t)(s0 + k));
+                  l[k] = ld_cluster_f32(rb + (uint32_t)(8 * kHeadDim + g) * 4u);
+                  v[k] = ld_cluster_f32(rb + (uint32_t)(g * kHeadDim + d) * 4u);
+                }
+              }
+              float Mn = M;
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                if (s0 + k < nsb) Mn = fmaxf(Mn, l[k]);
+              const float r = exp2f((M - Mn) * kLog2e);  // 0 on the first group
+              wsum *= r;
+              acc *= r;
+              M = Mn;
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                if (s0 + k < nsb) {
+                  const float w = exp2f((l[k] - M) * kLog2e);
+                  wsum += w;
+                  acc = fmaf(w, v[k], acc);
+                }
+              }
+            }
+            const int64_t row = (int64_t)U.b * p.Hq + hq0 + g;
+            if (p.out_f32) static_cast<float*>(p.out)[row * D + d] = acc / wsum;
+            else static_cast<TNat*>(p.out)[row * D + d] = to_out<TNat>(acc / wsum);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ep_empty(es));
+        continue;
+      }
       if (t < D) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -1127,8 +1263,11 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       named_bar_sync(2, 128);  // the state is read; the slot serves as merge scratch
       // the last split of this (sequence, kv head) merges all of them into `out`
       if (U.n_splits_b > 1) {
-        if (p.out_f32) finish_split<G, D, float>(p, U.b, U.h, U.n_splits_b, t, st, 2);
-        else finish_split<G, D, TNat>(p, U.b, U.h, U.n_splits_b, t, st, 2);
+        // merge loads in flight per thread: fewer with the 576-thread launch,
+        // whose register budget is smaller
+        constexpr int kMergeChunk = kDual ? 4 : 8;
+        if (p.out_f32) finish_split<G, D, float, kMergeChunk>(p, U.b, U.h, U.n_splits_b, t, st, 2);
+        else finish_split<G, D, TNat, kMergeChunk>(p, U.b, U.h, U.n_splits_b, t, st, 2);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(ep_empty(es));
@@ -1142,6 +1281,9 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // no CTA of a cluster leaves while another may still read its shared memory
+  // or arrive on its barriers
+  if (p.cluster > 1) cluster_sync_all();
 }
 
 template <int G, int D, int BS, bool FP16, bool KV8>
@@ -1157,19 +1299,60 @@ cudaError_t launch_one(const CUtensorMap* tk, const CUtensorMap* tv, const CUten
   cfg.blockDim = dim3(tc_threads(G, D, KV8));
   cfg.dynamicSmemBytes = Layout<KV8, D>::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n_attr = 0;
+  if (pdl_enabled()) {
+    attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+    ++n_attr;
+  }
+  if (p.cluster > 1) {
+    // one CTA per unit, clusters of the p.cluster splits of one (sequence, kv head)
+    if (p.num_units % p.cluster != 0) return cudaErrorInvalidValue;
+    cfg.gridDim = dim3((unsigned)p.num_units);
+    attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+    attr[n_attr].val.clusterDim.x = (unsigned)p.cluster;
+    attr[n_attr].val.clusterDim.y = 1;
+    attr[n_attr].val.clusterDim.z = 1;
+    ++n_attr;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  cfg.numAttrs = n_attr;
   return cudaLaunchKernelEx(&cfg, paged_partial_tc_kernel<G, D, BS, FP16, KV8>, *tk, *tv, *tq, p);
 }
 
 template <int G, int D, int BS, bool FP16, bool KV8>
+int max_clusters_one(int cluster) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cluster * 64u);
+  cfg.blockDim = dim3(tc_threads(G, D, KV8));
+  cfg.dynamicSmemBytes = Layout<KV8, D>::kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, paged_partial_tc_kernel<G, D, BS, FP16, KV8>, &cfg) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <int G, int D, int BS, bool FP16, bool KV8>
 cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(paged_partial_tc_kernel<G, D, BS, FP16, KV8>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)Layout<KV8, D>::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(paged_partial_tc_kernel<G, D, BS, FP16, KV8>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)Layout<KV8, D>::kSmemBytes);
+  // clusters of up to 16 CTAs (the splits of one sequence's kv head)
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(paged_partial_tc_kernel<G, D, BS, FP16, KV8>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
 }
 
 template <int G, int D, int BS, bool FP16, bool KV8>
@@ -1210,6 +1393,14 @@ struct Dispatch {
     return cudaErrorInvalidValue;
   }
   template <int G>
+  static int max_clusters_g(int BS, int cluster) {
+    if constexpr (geometry_supported(G, D, KV8)) {
+      return BS == 16 ? max_clusters_one<G, D, 16, FP16, KV8>(cluster)
+                      : max_clusters_one<G, D, 32, FP16, KV8>(cluster);
+    }
+    return 0;
+  }
+  template <int G>
   static int occupancy_g(int BS) {
     if constexpr (geometry_supported(G, D, KV8)) {
       return BS == 16 ? occupancy_one<G, D, 16, FP16, KV8>() : occupancy_one<G, D, 32, FP16, KV8>();
@@ -1241,6 +1432,19 @@ struct Dispatch {
       case 7: return prepare_g<7>(BS);
       case 8: return prepare_g<8>(BS);
       default: return cudaErrorInvalidValue;
+    }
+  }
+  static int max_clusters(int G, int BS, int cluster) {
+    switch (G) {
+      case 1: return max_clusters_g<1>(BS, cluster);
+      case 2: return max_clusters_g<2>(BS, cluster);
+      case 3: return max_clusters_g<3>(BS, cluster);
+      case 4: return max_clusters_g<4>(BS, cluster);
+      case 5: return max_clusters_g<5>(BS, cluster);
+      case 6: return max_clusters_g<6>(BS, cluster);
+      case 7: return max_clusters_g<7>(BS, cluster);
+      case 8: return max_clusters_g<8>(BS, cluster);
+      default: return 0;
     }
   }
   static int occupancy(int G, int BS) {

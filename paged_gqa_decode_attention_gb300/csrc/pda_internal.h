@@ -52,6 +52,11 @@ struct PartialParams {
   // default kWaitLimitNs) shortens every pipeline wait.
   int stall_units = 0;
   unsigned long long wait_ns = 0;
+  // Tensor-core kernel: > 1 when the launch is made of thread-block clusters
+  // of this many CTAs, one per split of a (sequence, kv head), every CTA one
+  // unit; the splits then merge through distributed shared memory instead
+  // of the workspace and the split tickets.
+  int cluster = 0;
 };
 
 struct MergeParams {
@@ -112,6 +117,10 @@ cudaError_t partial_prepare(int kernel, int group, int head_dim, int block_size,
                             bool kv_fp8);
 int partial_ctas_per_sm(int kernel, int group, int head_dim, int block_size, int dtype,
                         bool kv_fp8);
+// How many clusters of `cluster` CTAs of the tensor-core kernel can be
+// resident at once (0 if none, or if that cluster size is not allowed).
+int partial_max_clusters(int group, int head_dim, int block_size, int dtype, bool kv_fp8,
+                         int cluster);
 
 // tmap_q (a [B * Hq, D] view of q, boxes of 64 dims x G rows) is read by
 // the tensor-core kernel only; both kernels take the output type from

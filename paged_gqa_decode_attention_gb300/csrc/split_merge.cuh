@@ -33,16 +33,23 @@ __device__ __forceinline__ TOut merge_to_out(float x) {
 }
 
 // Called by 128 threads (tid 0..127) after each has written its part of this
-// split's partial (head dim D). `sw` is shared scratch of at least G * 64 + 1
-// floats, `bar_id` a named barrier over exactly these 128 threads.
-template <int G, int D, typename TOut>
+// split's partial (head dim D). `sw` is shared scratch of at least one word,
+// `bar_id` a named barrier over exactly these 128 threads.
+//
+// The merging CTA is on the step's critical path (it finishes last), so the
+// merge is one pass of loads with no further barrier: each thread owns
+// (head g, 4 consecutive dims) pairs and reads, per group of kChunk splits,
+// the splits' log-sum-exps and its four columns of their partials together
+// (all in flight at once), folding them with a running maximum:
+//   M = max_s lse_s,  out = sum_s e^(lse_s - M) o_s / sum_s e^(lse_s - M).
+template <int G, int D, typename TOut, int kChunk = 8>
 __device__ __forceinline__ void finish_split(const PartialParams& p, int b, int h, int n_splits_b,
                                              int tid, float* sw, int bar_id) {
   static_assert(D % 4 == 0, "float4 columns");
   constexpr int kCols = D / 4;
   __threadfence();
   named_bar_sync(bar_id, 128);
-  int* flag = reinterpret_cast<int*>(sw + G * 64);
+  int* flag = reinterpret_cast<int*>(sw);
   if (tid == 0) {
     const int prev = atomicAdd(p.counters + (int64_t)b * p.Hkv + h, 1);
     *flag = (prev == n_splits_b - 1);
@@ -52,58 +59,55 @@ __device__ __forceinline__ void finish_split(const PartialParams& p, int b, int 
   __threadfence();
   const int hq0 = h * G;
   const int64_t row0 = (int64_t)b * p.Hq + hq0;
-  for (int i = tid; i < G * n_splits_b; i += 128) {
-    const int g = i / n_splits_b, s = i - g * n_splits_b;
-    sw[g * 64 + s] = __ldcg(p.ws_lse + (row0 + g) * p.num_splits + s);
-  }
-  named_bar_sync(bar_id, 128);
-  if (tid < G) {
-    float* w = sw + tid * 64;
-    float M = -INFINITY;
-    for (int s = 0; s < n_splits_b; ++s) M = fmaxf(M, w[s]);
-    float sum = 0.f;
-    for (int s = 0; s < n_splits_b; ++s) {
-      const float e = (w[s] == -INFINITY) ? 0.f : exp2f((w[s] - M) * kLog2e);
-      w[s] = e;
-      sum += e;
-    }
-    const float inv = 1.f / sum;
-    for (int s = 0; s < n_splits_b; ++s) w[s] *= inv;
-  }
-  named_bar_sync(bar_id, 128);
-  // thread -> (head g, 4 consecutive dims): G * D / 4 such pairs over 128
-  // threads, float4 loads, 8 splits in flight per step
   TOut* out = static_cast<TOut*>(p.out);
   for (int pair = tid; pair < G * kCols; pair += 128) {
     const int g = pair / kCols, d4 = (pair - g * kCols) * 4;
+    const float* lrow = p.ws_lse + (row0 + g) * p.num_splits;
     const float4* o = reinterpret_cast<const float4*>(p.ws_o + ((row0 + g) * p.num_splits) * D + d4);
-    const float* w = sw + g * 64;
+    float M = -INFINITY, wsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int s = 0;
-    for (; s + 8 <= n_splits_b; s += 8) {
-      float4 v[8];
+    for (int s0 = 0; s0 < n_splits_b; s0 += kChunk) {
+      const int n = min(kChunk, n_splits_b - s0);
+      float l[kChunk];
+      float4 v[kChunk];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = __ldcg(o + (s + k) * kCols);
+      for (int k = 0; k < kChunk; ++k) {
+        if (k < n) {
+          l[k] = __ldcg(lrow + s0 + k);
+          v[k] = __ldcg(o + (s0 + k) * kCols);
+        }
+      }
+      float mc = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        acc.x = fmaf(w[s + k], v[k].x, acc.x);
-        acc.y = fmaf(w[s + k], v[k].y, acc.y);
-        acc.z = fmaf(w[s + k], v[k].z, acc.z);
-        acc.w = fmaf(w[s + k], v[k].w, acc.w);
+      for (int k = 0; k < kChunk; ++k)
+        if (k < n) mc = fmaxf(mc, l[k]);
+      const float Mn = fmaxf(M, mc);
+      if (Mn == -INFINITY) continue;  // every split so far is empty
+      const float r = (M == -INFINITY) ? 0.f : exp2f((M - Mn) * kLog2e);
+      wsum *= r;
+      acc.x *= r;
+      acc.y *= r;
+      acc.z *= r;
+      acc.w *= r;
+      M = Mn;
+#pragma unroll
+      for (int k = 0; k < kChunk; ++k) {
+        if (k < n) {
+          const float w = (l[k] == -INFINITY) ? 0.f : exp2f((l[k] - M) * kLog2e);
+          wsum += w;
+          acc.x = fmaf(w, v[k].x, acc.x);
+          acc.y = fmaf(w, v[k].y, acc.y);
+          acc.z = fmaf(w, v[k].z, acc.z);
+          acc.w = fmaf(w, v[k].w, acc.w);
+        }
       }
     }
-    for (; s < n_splits_b; ++s) {
-      const float4 v = __ldcg(o + s * kCols);
-      acc.x = fmaf(w[s], v.x, acc.x);
-      acc.y = fmaf(w[s], v.y, acc.y);
-      acc.z = fmaf(w[s], v.z, acc.z);
-      acc.w = fmaf(w[s], v.w, acc.w);
-    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     TOut* dst = out + (row0 + g) * D + d4;
-    dst[0] = merge_to_out<TOut>(acc.x);
-    dst[1] = merge_to_out<TOut>(acc.y);
-    dst[2] = merge_to_out<TOut>(acc.z);
-    dst[3] = merge_to_out<TOut>(acc.w);
+    dst[0] = merge_to_out<TOut>(acc.x * inv);
+    dst[1] = merge_to_out<TOut>(acc.y * inv);
+    dst[2] = merge_to_out<TOut>(acc.z * inv);
+    dst[3] = merge_to_out<TOut>(acc.w * inv);
   }
   if (tid == 0) p.counters[(int64_t)b * p.Hkv + h] = 0;  // ready for the next call
 }

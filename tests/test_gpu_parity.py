@@ -335,3 +335,33 @@ def test_timed_out_call_reports_and_next_call_is_exact(Hq, Hkv, D, monkeypatch):
     assert_close(run_gpu(attn, wl), ref, "heuristic splits after the error was read")
     assert attn.check_device_error() == (0, 0)
     attn.close()
+
+
+@pytest.mark.parametrize("cluster", ["1", "0"])
+@pytest.mark.parametrize("Hq,Hkv,D,bs", [(8, 1, 128, 16), (14, 2, 64, 32), (32, 8, 128, 16)])
+def test_split_merge_paths(cluster, Hq, Hkv, D, bs, monkeypatch):
+    """The splits of a (sequence, kv head) merge either inside one
+    thread-block cluster through distributed shared memory (split counts 2..16
+    when every (sequence, kv head) pair fits in one wave of clusters) or
+    through the workspace and the split tickets (PDA_CLUSTER_MERGE=0, and
+    whenever the pairs do not fit). Both are exact, including sequences
+    shorter than the split count (empty splits inside a cluster), in 16-bit
+    and fp32 output."""
+    monkeypatch.setenv("PDA_CLUSTER_MERGE", cluster)
+    lens = [1, bs + 1, 700, 3000, 4000, 129]
+    wl = workloads.custom(seed=Hq + D + bs, B=len(lens), Hq=Hq, Hkv=Hkv, D=D, block_size=bs,
+                          lens=lens, num_blocks=700)
+    attn = make_attn(wl)
+    shapes = {S: attn.launch_shape(wl.batch, wl.max_blocks, num_splits=S)
+              for S in (2, 3, 5, 8, 13, 16)}
+    attn.close()
+    # pairs of 2 CTAs always fit one wave at these batch sizes
+    assert shapes[2]["cluster"] == (2 if cluster == "1" else 1), shapes[2]
+    for S, sh in shapes.items():
+        assert sh["splits"] == S and sh["cluster"] in (1, S), sh
+    for splits in (2, 3, 5, 8, 13, 16):
+        check(wl, num_splits=splits)
+    err = check(wl, num_splits=16, out_dtype=torch.float32)
+    assert err < 1e-4, err
+    err = check(wl, num_splits=4, out_dtype=torch.float32)
+    assert err < 1e-4, err
