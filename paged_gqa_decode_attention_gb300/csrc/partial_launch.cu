@@ -30,6 +30,7 @@ PDA_DECLARE_TC(bf16, 128)
 PDA_DECLARE_TC(fp16, 64)
 PDA_DECLARE_TC(fp16, 128)
 PDA_DECLARE_TC(kv8_bf16, 128)
+PDA_DECLARE_TC(kv8_fp16, 128)
 #undef PDA_DECLARE_TC
 
 namespace {
@@ -52,13 +53,17 @@ auto with_cc(int dtype, int head_dim, F f) {
 #undef PDA_CC_CASE
 }
 
-// Same for the tensor-core kernel (head dims 64 and 128; FP8 K/V at 128).
+// Same for the tensor-core kernel (head dims 64 and 128; FP8 K/V at 128 with bf16 or
+// fp16 queries).
 template <typename F>
 auto with_tc(int dtype, int head_dim, bool kv_fp8, F f) {
 #define PDA_TC_CASE(dt, D)                                                             \
   return f(launch_partial_tc_##dt##_d##D, prepare_partial_tc_##dt##_d##D,              \
            occupancy_partial_tc_##dt##_d##D, max_clusters_partial_tc_##dt##_d##D)
-  if (kv_fp8) PDA_TC_CASE(kv8_bf16, 128);
+  if (kv_fp8) {
+    if (dtype == 1) PDA_TC_CASE(kv8_fp16, 128);
+    PDA_TC_CASE(kv8_bf16, 128);
+  }
   if (dtype == 1) {
     if (head_dim == 64) PDA_TC_CASE(fp16, 64);
     PDA_TC_CASE(fp16, 128);
@@ -72,7 +77,8 @@ auto with_tc(int dtype, int head_dim, bool kv_fp8, F f) {
 
 bool partial_supported(int group, int head_dim, int block_size, int dtype, bool kv_fp8) {
   const bool bs_ok = block_size == 16 || block_size == 32;
-  if (kv_fp8) return tc::geometry_supported(group, head_dim, true) && bs_ok && dtype == 0;
+  if (kv_fp8)
+    return tc::geometry_supported(group, head_dim, true) && bs_ok && (dtype == 0 || dtype == 1);
   return partial::geometry_supported(group, head_dim) && bs_ok && (dtype == 0 || dtype == 1);
 }
 

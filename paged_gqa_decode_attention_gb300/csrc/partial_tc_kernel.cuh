@@ -31,7 +31,8 @@
 // overlap. So the terms are stacked (half the PV instructions), and QK^T
 // and PV are issued by two different warps.
 //
-// Warp roles (512 threads; 576 with second producers):
+// Warp roles (512 threads; 576 with second producers; 32 more with a second
+// PV issuer):
 //   warps 0-3 and 11-14: softmax, two groups of four that split the G query
 //     heads' columns (group 0 the first ceil(G/2), group 1 the rest; G = 1
 //     uses one group). Thread t of a group reads TMEM lane t of S (token t of
@@ -55,7 +56,10 @@
 //   warp 6: allocates 256 TMEM columns (S and O, double-buffered), issues
 //     the QK^T MMAs and commits their completion to mbarriers; with FP8 K/V
 //     it also turns each unit's 16-bit q tile into the two fp8 q terms.
-//   warp 15: issues the PV MMAs and commits their completion. The terms of a
+//   warp 15: issues the PV MMAs and commits their completion. At 16-bit head
+//     dim 64 (G <= 4) it takes the even chunks and warp 18 the odd ones: an
+//     M = 64 PV needs as many MMAs per chunk as M = 128 for half the bytes
+//     (a second QK^T issuer as well measured no faster). The terms of a
 //     split operand (P_hi / P_lo; with FP8, q_hi / q_lo and the three P
 //     terms) are stacked along N, so each contraction step is one MMA.
 // S, O and P are double-buffered by chunk parity so the chunks overlap:
@@ -99,8 +103,16 @@ constexpr int kOpBytes = 2 * kOpHalf;      // Q, P_hi or P_lo operand
 __host__ __device__ constexpr bool dual_producers(int G, int D, bool kv8) {
   return (kv8 || D == 64) && G <= 4;
 }
+// A second PV-issuing warp (alternate chunks) for 16-bit head dim 64 at
+// G <= 4: its PV is an M = 64 MMA per 16 tokens, so one issuing thread (~185
+// cycles per MMA) needed ~1480 cycles per 128-token chunk that arrives in
+// ~800. (At G >= 5 a 17th warp would cut the register budget from 128 to 96
+// per thread, since one SM sub-partition would then hold five warps.)
+__host__ __device__ constexpr bool dual_pv(int G, int D, bool kv8) {
+  return D == 64 && !kv8 && G <= 4;
+}
 __host__ __device__ constexpr int tc_threads(int G, int D, bool kv8) {
-  return dual_producers(G, D, kv8) ? 576 : 512;
+  return 512 + (dual_producers(G, D, kv8) ? 64 : 0) + (dual_pv(G, D, kv8) ? 32 : 0);
 }
 constexpr int kWarpProducerK = 4;
 constexpr int kWarpProducerV = 5;
@@ -110,6 +122,10 @@ constexpr int kWarpSmxB0 = 11;             // warps 11-14: second softmax group
 constexpr int kWarpMmaPV = 15;             // issues PV
 constexpr int kWarpProducerK2 = 16;        // second K producer (odd chunks)
 constexpr int kWarpProducerV2 = 17;        // second V producer (odd chunks)
+// second PV issuer (odd chunks): the warp after the last producer
+__host__ __device__ constexpr int warp_pv2(int G, int D, bool kv8) {
+  return dual_producers(G, D, kv8) ? 18 : 16;
+}
 // TMEM columns: S and O, double-buffered. The terms of a split operand are
 // stacked along N so one MMA carries all of them (the tensor pipe's cost
 // is per instruction at these small N): S holds 16 columns (32 with FP8
@@ -323,7 +339,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
                             const __grid_constant__ CUtensorMap tmap_q, const PartialParams p) {
   static_assert(G >= 1 && G <= 8, "tensor-core path packs up to 8 query heads");
   static_assert(D == 64 || D == 128, "head dim 64 or 128");
-  static_assert(!KV8 || (D == 128 && !FP16), "FP8 K/V: head dim 128, bf16 queries");
+  static_assert(!KV8 || D == 128, "FP8 K/V: head dim 128");
   using L = Layout<KV8, D>;
   constexpr int kStages = L::kStages;
   constexpr int kSlotBytes = L::kSlotBytes;
@@ -345,6 +361,8 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
   constexpr int PPS = kT / BS;  // pages per stage
   constexpr int kGroups = G >= 2 ? 2 : 1;  // softmax warp groups (query-head columns split)
   constexpr bool kDual = dual_producers(G, D, KV8);
+  constexpr bool kDualPV = dual_pv(G, D, KV8);
+  constexpr int kWarpMmaPV2 = warp_pv2(G, D, KV8);
   constexpr int kGA = (G + 1) / 2 > 0 ? (G + 1) / 2 : 1;  // columns of group 0 (group 1: G - kGA)
   static_assert(kT % BS == 0 && PPS <= 32, "stage must hold whole pages");
   using TNat = std::conditional_t<FP16, __half, __nv_bfloat16>;
@@ -492,7 +510,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
   if (threadIdx.x == 0) {
     for (int s2 = 0; s2 < kUnitRing; ++s2) {
       mbar_init(uring_full(s2), 1);
-      mbar_init(uring_empty(s2), kUnitConsumers + (kDual ? 2 : 0));
+      mbar_init(uring_empty(s2), kUnitConsumers + (kDual ? 2 : 0) + (kDualPV ? 1 : 0));
     }
     for (int s2 = 0; s2 < 2; ++s2) {
       mbar_init(ep_full(s2), 4 * kGroups);
@@ -640,7 +658,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     }
     if (r == 0) fetch.done();  // counted already unless a wait timed out
   } else if (kDual && (warp == kWarpProducerK || warp == kWarpProducerV ||
-                        warp >= kWarpProducerK2)) {
+                        warp == kWarpProducerK2 || warp == kWarpProducerV2)) {
     // ------- producers: K ring (warps 4, 16), V ring (warps 5, 17) -------
     // With kDual each ring has two producer warps that take alternate
     // chunks: one thread issues a TMA box in ~80 cycles, so a single warp
@@ -648,7 +666,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     // Warp 4 also takes units from the counter and loads each unit's Q; the
     // others follow the unit ring.
     const int r = (warp == kWarpProducerV || warp == kWarpProducerV2) ? 1 : 0;
-    const int par = warp >= kWarpProducerK2 ? 1 : 0;  // this warp's chunks: c % 2 == par
+    const int par = (warp == kWarpProducerK2 || warp == kWarpProducerV2) ? 1 : 0;  // chunks c % 2 == par
     const bool fetcher = warp == kWarpProducerK;
     const CUtensorMap* map = r == 0 ? &tmap_k : &tmap_v;
     if (lane == 0) {
@@ -740,7 +758,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       if (fetcher) cur_k.advance(p, fetch); else cur_v.advance(p, ring);
     }
     if (fetcher) fetch.done();  // counted already unless a wait timed out
-  } else if (warp == kWarpMma || warp == kWarpMmaPV) {
+  } else if (warp == kWarpMma || warp == kWarpMmaPV || (kDualPV && warp == kWarpMmaPV2)) {
     // ------------------------------ MMA issue -----------------------------
     // kind::f16: type fields 1 = bf16, 0 = f16; kind::f8f6f4: 0 = E4M3
     constexpr uint32_t idesc_qk = idesc_f16(128, kSCols, !FP16 && !KV8, false, false);
@@ -770,8 +788,20 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
 #pragma unroll
           for (int g = 0; g < G; ++g) {
             const uint2 w = *reinterpret_cast<const uint2*>(qt + op_offset(g, d0));
-            const float x[4] = {__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
-                                __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u)};
+            float x[4];
+            if constexpr (FP16) {
+              const __half2 lo2 = *reinterpret_cast<const __half2*>(&w.x);
+              const __half2 hi2 = *reinterpret_cast<const __half2*>(&w.y);
+              x[0] = __low2float(lo2);
+              x[1] = __high2float(lo2);
+              x[2] = __low2float(hi2);
+              x[3] = __high2float(hi2);
+            } else {
+              x[0] = __uint_as_float(w.x << 16);
+              x[1] = __uint_as_float(w.x & 0xffff0000u);
+              x[2] = __uint_as_float(w.y << 16);
+              x[3] = __uint_as_float(w.y & 0xffff0000u);
+            }
             float mx = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
@@ -870,13 +900,17 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     };
     // Each issuing warp walks the same chunk sequence: warp 6 issues QK^T,
     // warp 15 PV. Their MMAs overlap in the tensor pipe.
+    // With two PV warps, warp 15 issues the even chunks' PV and the second
+    // one the odd chunks' (separate O buffers, V slots and P buffers).
     const bool is_qk = warp == kWarpMma;
+    const int pv_par = (kDualPV && warp == kWarpMmaPV2) ? 1 : 0;
     RingSource ring = ring_source();
     Cursor<BS, RingSource> cur;
     cur.start(p, ring);
     int last_c = -1;
     while (!failed && cur.valid()) {
-      if (is_qk) issue_qk(cur); else issue_pv(cur.c);
+      if (is_qk) issue_qk(cur);
+      else if (!kDualPV || (cur.c & 1) == pv_par) issue_pv(cur.c);
       last_c = cur.c;
       cur.advance(p, ring);
     }
@@ -1366,7 +1400,7 @@ int occupancy_one() {
 }
 
 // 16-bit K/V: G 3..8 (G 1 and 2 go to the CUDA-core kernel), D 64 or 128.
-// FP8 K/V: any G up to 8, D 128, bf16 queries.
+// FP8 K/V: any G up to 8, D 128, bf16 or fp16 queries.
 __host__ __device__ constexpr bool geometry_supported(int G, int D, bool kv8 = false) {
   return kv8 ? (G >= 1 && G <= 8 && D == 128) : (G >= 3 && G <= 8 && (D == 64 || D == 128));
 }

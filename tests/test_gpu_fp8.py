@@ -88,9 +88,25 @@ def test_scaled_16bit_caches(kernel, monkeypatch):
     check(wl, num_splits=7)
 
 
+@pytest.mark.parametrize("G,Hkv", [(4, 8), (7, 2), (8, 1), (1, 8)])
+@pytest.mark.parametrize("bs", [16, 32])
+def test_fp8_fp16_queries_exact(G, Hkv, bs):
+    """FP8 K/V with fp16 queries (and fp16 output): the q tile is split into
+    its two fp8 terms from fp16, per-kv-head scales, every split count."""
+    lens = [1, bs + 1, 700, 3000, 64, 129]
+    wl = workloads.to_fp8_kv(workloads.custom(seed=G * 13 + Hkv + bs, B=len(lens), Hq=G * Hkv,
+                                              Hkv=Hkv, D=128, block_size=bs, lens=lens,
+                                              dtype="fp16", num_blocks=700))
+    assert wl.q.dtype == torch.float16
+    for splits in (0, 1, 5, 64):
+        check(wl, num_splits=splits)
+    err = check(wl, out_dtype=torch.float32)
+    assert err < 2e-3, err
+
+
 def test_fp8_unsupported_geometries_rejected():
     from paged_gqa_decode_attention_gb300 import PagedDecodeAttention
-    for kw in (dict(head_dim=64), dict(dtype=torch.float16)):
+    for kw in (dict(head_dim=64), dict(head_dim=256)):
         args = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
                     dtype=torch.bfloat16)
         args.update(kw)
