@@ -52,8 +52,10 @@ TC_KERNEL_SOURCES = ("partial_tc_kernel.cuh", "ptx.cuh", "split_merge.cuh", "pda
 ROPE_KERNEL_SOURCES = ("rope_kv_write.cu", "ptx.cuh", "pda_internal.h")
 NCU_TRAFFIC = {
     # workload: (bytes per launch, kernel sources, their SHA-256 at capture)
-    "long_b4_l32768": (None, TC_KERNEL_SOURCES, None),
-    "rope_prefill_t32768": (768_166_400, ROPE_KERNEL_SOURCES, None),
+    "long_b4_l32768": (540_337_920, TC_KERNEL_SOURCES,
+                       "268786a97f39b1021dfaecb323afcd23013c94e74cdc241c29bdd723dccf4cfb"),
+    "rope_prefill_t32768": (768_392_448, ROPE_KERNEL_SOURCES,
+                            "df5a0b52b1f3f70e6d0d2f41abec52a82ddda21f0b621cf7a36b12f1b3c25efd"),
 }
 
 
