@@ -131,6 +131,9 @@ def make_workload(name: str, seed: int, device):
     if name == "geo_d64_b8_l32768":  # 32/8 heads, D 64 (B = 8: the same bytes)
         return W.custom(seed=seed, B=8, Hq=32, Hkv=8, D=64, block_size=16, lens=[32768] * 8,
                         device=device)
+    if name == "geo_fp8_d64_b16_l32768":  # FP8 cache, 32/8 heads, D 64 (the headline's bytes)
+        return W.to_fp8_kv(W.custom(seed=seed, B=16, Hq=32, Hkv=8, D=64, block_size=16,
+                                    lens=[32768] * 16, device=device))
     if name == "long_b8_l32768_fp8_g8":  # FP8 cache, 64/8 heads
         return W.to_fp8_kv(W.custom(seed=seed, B=8, Hq=64, Hkv=8, D=128, block_size=16,
                                     lens=[32768] * 8, device=device))

@@ -77,7 +77,7 @@ typedef enum {
 
 /* Fixed at create time. Supported geometries: G = Hq / Hkv from 1 to 8 at
  * head_dim 64 or 128, 1 to 4 at head_dim 256; with kv_fp8, any G up to 8 at
- * head_dim 128 and dtype PDA_BF16 or PDA_FP16. */
+ * head_dim 64 or 128 and dtype PDA_BF16 or PDA_FP16. */
 typedef struct {
   int num_q_heads;        /* Hq; a multiple of num_kv_heads */
   int num_kv_heads;       /* Hkv */

@@ -73,8 +73,8 @@ int check_config(const pda_config* c) {
     return fail(PDA_EUNSUPPORTED, "head_dim must be 64, 128 or 256");
   if (c->kv_fp8 && !pda::partial_supported(G, c->head_dim, c->block_size, c->dtype, true))
     return fail(PDA_EUNSUPPORTED,
-                "FP8 K/V caches need head_dim 128, group size 1..8, dtype PDA_BF16 or "
-                "PDA_FP16 and block_size 16 or 32");
+                "FP8 K/V caches need head_dim 64 or 128, group size 1..8, dtype PDA_BF16 "
+                "or PDA_FP16 and block_size 16 or 32");
   if (!pda::partial_supported(G, c->head_dim, c->block_size, c->dtype, c->kv_fp8 != 0))
     return fail(PDA_EUNSUPPORTED,
                 "unsupported geometry: group size must be 1..8 (1..4 at head_dim 256) and "
@@ -132,19 +132,21 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // A [num_blocks * block_size, Hkv * D] view of a cache, loaded as boxes of
 // 128 bytes (64 16-bit dims or 128 fp8 dims) x block_size rows with 128-byte
-// swizzle.
+// swizzle; FP8 at head dim 64: 64-byte boxes with 64-byte swizzle.
 int encode_cache_map(CUtensorMap* m, const void* base, int Hkv, int D, int bs,
                      int64_t num_blocks, bool fp8 = false) {
   auto fn = tensor_map_encoder();
   if (!fn) return fail(PDA_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const int esz = fp8 ? 1 : 2;
+  const int box_bytes = (fp8 && D == 64) ? 64 : 128;
   cuuint64_t dims[2] = {(cuuint64_t)Hkv * D, (cuuint64_t)num_blocks * bs};
   cuuint64_t strides[1] = {(cuuint64_t)Hkv * D * esz};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / esz), (cuuint32_t)bs};
+  cuuint32_t box[2] = {(cuuint32_t)(box_bytes / esz), (cuuint32_t)bs};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
-                  const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(PDA_ECUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));

@@ -29,7 +29,9 @@ PDA_DECLARE_TC(bf16, 64)
 PDA_DECLARE_TC(bf16, 128)
 PDA_DECLARE_TC(fp16, 64)
 PDA_DECLARE_TC(fp16, 128)
+PDA_DECLARE_TC(kv8_bf16, 64)
 PDA_DECLARE_TC(kv8_bf16, 128)
+PDA_DECLARE_TC(kv8_fp16, 64)
 PDA_DECLARE_TC(kv8_fp16, 128)
 #undef PDA_DECLARE_TC
 
@@ -53,7 +55,7 @@ auto with_cc(int dtype, int head_dim, F f) {
 #undef PDA_CC_CASE
 }
 
-// Same for the tensor-core kernel (head dims 64 and 128; FP8 K/V at 128 with bf16 or
+// Same for the tensor-core kernel (head dims 64 and 128, 16-bit or FP8 K/V, bf16 or
 // fp16 queries).
 template <typename F>
 auto with_tc(int dtype, int head_dim, bool kv_fp8, F f) {
@@ -61,7 +63,11 @@ auto with_tc(int dtype, int head_dim, bool kv_fp8, F f) {
   return f(launch_partial_tc_##dt##_d##D, prepare_partial_tc_##dt##_d##D,              \
            occupancy_partial_tc_##dt##_d##D, max_clusters_partial_tc_##dt##_d##D)
   if (kv_fp8) {
-    if (dtype == 1) PDA_TC_CASE(kv8_fp16, 128);
+    if (dtype == 1) {
+      if (head_dim == 64) PDA_TC_CASE(kv8_fp16, 64);
+      PDA_TC_CASE(kv8_fp16, 128);
+    }
+    if (head_dim == 64) PDA_TC_CASE(kv8_bf16, 64);
     PDA_TC_CASE(kv8_bf16, 128);
   }
   if (dtype == 1) {

@@ -109,7 +109,7 @@ __host__ __device__ constexpr bool dual_producers(int G, int D, bool kv8) {
 // ~800. (At G >= 5 a 17th warp would cut the register budget from 128 to 96
 // per thread, since one SM sub-partition would then hold five warps.)
 __host__ __device__ constexpr bool dual_pv(int G, int D, bool kv8) {
-  return D == 64 && !kv8 && G <= 4;
+  return D == 64 && G <= 4;
 }
 __host__ __device__ constexpr int tc_threads(int G, int D, bool kv8) {
   return 512 + (dual_producers(G, D, kv8) ? 64 : 0) + (dual_pv(G, D, kv8) ? 32 : 0);
@@ -147,12 +147,13 @@ constexpr float kP8Scale = 256.f;          // FP8 K/V: P is split at p * 256
 // Shared-memory layout. 16-bit K/V at D 128: 3-slot rings of 32 KiB slots
 // (two 64-dim halves of 128 tokens). 16-bit K/V at D 64: 6-slot rings of
 // 16 KiB slots (one 64-dim half), the same bytes in flight. FP8 K/V (KV8):
-// 5-slot rings of 16 KiB slots (one 128-byte row per token), two fp8 terms
-// of Q next to the 16-bit Q tile, three fp8 terms of P in the P buffers.
+// rings of 80 KiB in slots of one D-byte row per token (5 x 16 KiB at D 128,
+// 10 x 8 KiB at D 64 with 64-byte swizzled rows), two fp8 terms of Q next to
+// the 16-bit Q tile, three fp8 terms of P in the P buffers.
 template <bool KV8, int D = 128>
 struct Layout {
-  static constexpr int kStages = KV8 ? 5 : (D == 64 ? 6 : 3);
-  static constexpr int kSlotBytes = KV8 ? kT * 128 : (D / 64) * kHalf;
+  static constexpr int kStages = KV8 ? (D == 64 ? 10 : 5) : (D == 64 ? 6 : 3);
+  static constexpr int kSlotBytes = KV8 ? kT * D : (D / 64) * kHalf;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kStages * kSlotBytes;
   static constexpr int kOffQ = 2 * kStages * kSlotBytes;  // [2 buffers] Q tiles (TMA)
@@ -217,6 +218,25 @@ __device__ __forceinline__ uint32_t op32_offset(int n, int k) {
 // (one 128-byte row per n, 128-byte swizzle).
 __device__ __forceinline__ uint32_t op8_offset(int n, int k) {
   return (n >> 3) * 1024 + (n & 7) * 128 + ((((k >> 4) ^ (n & 7))) << 4) + (k & 15);
+}
+
+// Same for a K-major fp8 operand of 64-byte rows (64-byte swizzle: the 16-byte
+// chunk index XOR bits 1-2 of the row).
+__device__ __forceinline__ uint32_t op8_sw64_offset(int n, int k) {
+  return n * 64 + ((((k >> 4) ^ ((n >> 1) & 3))) << 4) + (k & 15);
+}
+
+// The fp8 q operand of head dim D: rows of D bytes.
+template <int D>
+__device__ __forceinline__ uint32_t op8q_offset(int n, int k) {
+  if constexpr (D == 64) return op8_sw64_offset(n, k); else return op8_offset(n, k);
+}
+
+// Shared-memory descriptor of a swizzled operand whose rows are `row` bytes
+// (128 or 64): 8-row groups `8 * row` bytes apart.
+template <int kRow>
+__device__ __forceinline__ uint64_t sdesc_rows(uint32_t saddr, uint32_t lbo) {
+  if constexpr (kRow == 64) return sdesc_sw64(saddr, lbo, 512); else return sdesc_sw128(saddr, lbo, 1024);
 }
 
 __device__ __forceinline__ uint8_t to_e4m3(float x) {
@@ -339,7 +359,9 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
                             const __grid_constant__ CUtensorMap tmap_q, const PartialParams p) {
   static_assert(G >= 1 && G <= 8, "tensor-core path packs up to 8 query heads");
   static_assert(D == 64 || D == 128, "head dim 64 or 128");
-  static_assert(!KV8 || D == 128, "FP8 K/V: head dim 128");
+  // bytes of one token row of one head in a K/V ring slot (FP8: D, 64-byte
+  // swizzled rows at D 64; 16-bit: 128, one 64-dim half)
+  constexpr int kKVRow = KV8 ? D : kRowBytes;
   using L = Layout<KV8, D>;
   constexpr int kStages = L::kStages;
   constexpr int kSlotBytes = L::kSlotBytes;
@@ -640,13 +662,13 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
         // 16-bit K/V: D / 64 boxes of 64 dims per page; FP8: one box of D bytes
         constexpr int kBoxes = KV8 ? 1 : NB;
         constexpr int kBoxElems = KV8 ? D : 64;
-        mbar_arrive_expect_tx(fb, (uint32_t)npg * BS * kBoxes * kRowBytes);
+        mbar_arrive_expect_tx(fb, (uint32_t)npg * BS * kBoxes * kKVRow);
         const uint32_t st = base_u32 + (r == 0 ? kOffK : kOffV) + slot * kSlotBytes;
 #pragma unroll
         for (int i = 0; i < PPS; ++i) {
           if (i < npg) {
             const int y = blk[i] * BS;
-            const uint32_t ro = (uint32_t)(i * BS * kRowBytes);
+            const uint32_t ro = (uint32_t)(i * BS * kKVRow);
 #pragma unroll
             for (int bx = 0; bx < kBoxes; ++bx)
               tma_load_2d(st + bx * kHalf + ro, map, U.h * D + bx * kBoxElems, y, fb);
@@ -740,13 +762,13 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
           // 16-bit K/V: D / 64 boxes of 64 dims per page; FP8: one box of D bytes
           constexpr int kBoxes = KV8 ? 1 : NB;
           constexpr int kBoxElems = KV8 ? D : 64;
-          mbar_arrive_expect_tx(fb, (uint32_t)npg * BS * kBoxes * kRowBytes);
+          mbar_arrive_expect_tx(fb, (uint32_t)npg * BS * kBoxes * kKVRow);
           const uint32_t st = base_u32 + (r == 0 ? kOffK : kOffV) + slot * kSlotBytes;
 #pragma unroll
           for (int i = 0; i < PPS; ++i) {
             if (i < npg) {
               const int y = blk[i] * BS;
-              const uint32_t ro = (uint32_t)(i * BS * kRowBytes);
+              const uint32_t ro = (uint32_t)(i * BS * kKVRow);
 #pragma unroll
               for (int bx = 0; bx < kBoxes; ++bx)
                 tma_load_2d(st + bx * kHalf + ro, map, U.h * D + bx * kBoxElems, y, fb);
@@ -784,7 +806,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
           const uint8_t* qt = base + kOffQ + qb * kOpBytes;
           uint8_t* q8 = base + kOffQ8 + qb * kOpBytes;
           float* qs = reinterpret_cast<float*>(base + kOffQs) + qb * 8;
-          const int d0 = 4 * lane;
+          const int d0 = 4 * lane;  // lanes past D read the tile's zero half
 #pragma unroll
           for (int g = 0; g < G; ++g) {
             const uint2 w = *reinterpret_cast<const uint2*>(qt + op_offset(g, d0));
@@ -817,8 +839,10 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
               hw |= (uint32_t)hb << (8 * i);
               lw |= (uint32_t)lb << (8 * i);
             }
-            *reinterpret_cast<uint32_t*>(q8 + op8_offset(g, d0)) = hw;
-            *reinterpret_cast<uint32_t*>(q8 + kOpHalf + op8_offset(g, d0)) = lw;
+            if (d0 < D) {
+              *reinterpret_cast<uint32_t*>(q8 + op8q_offset<D>(g, d0)) = hw;
+              *reinterpret_cast<uint32_t*>(q8 + op8q_offset<D>(kN + g, d0)) = lw;
+            }
             if (lane == 0) qs[g] = 1.f / sig;
           }
           fence_proxy_async_smem();
@@ -839,8 +863,8 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
           const uint32_t q8 = base_u32 + kOffQ8 + qb * kOpBytes;
 #pragma unroll
           for (int k = 0; k < D / 32; ++k) {
-            const uint64_t a = sdesc_sw128(kb + k * 32, 16, 1024);
-            const uint64_t bq = sdesc_sw128(q8 + k * 32, 16, 1024);
+            const uint64_t a = sdesc_rows<kKVRow>(kb + k * 32, 16);
+            const uint64_t bq = sdesc_rows<kKVRow>(q8 + k * 32, 16);
             mma_f8_ss(tS(c & 1), a, bq, idesc_qk, k > 0 ? 1u : 0u);
           }
         } else {
@@ -877,7 +901,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
           const uint32_t p8 = base_u32 + kOffP + (c & 1) * 3 * kOpHalf;
 #pragma unroll
           for (int k = 0; k < kT / 32; ++k) {
-            const uint64_t a = sdesc_sw128(vb + k * 32 * 128, kSlotBytes, 1024);
+            const uint64_t a = sdesc_rows<kKVRow>(vb + k * 32 * kKVRow, kSlotBytes);
             mma_f8_ss(tO(c & 1), a, sdesc_sw128(p8 + k * 32, 16, 1024), idesc_pv,
                       k > 0 ? 1u : 0u);
           }
@@ -1121,11 +1145,11 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
             ok = !failed && mbar_wait(full_bar(1, slot), (c / kStages) & 1, wlim);
             if (!__all_sync(kFull, ok)) failed = true;
             if (t >= n_valid) {
-              uint8_t* vrow = base + kOffV + slot * kSlotBytes + t * kRowBytes;
+              uint8_t* vrow = base + kOffV + slot * kSlotBytes + t * kKVRow;
 #pragma unroll
               for (int hh = 0; hh < (KV8 ? 1 : NB); ++hh)
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
+                for (int q = 0; q < kKVRow / 16; ++q)
                   *reinterpret_cast<uint4*>(vrow + hh * kHalf + q * 16) = make_uint4(0, 0, 0, 0);
             }
           }
@@ -1400,9 +1424,10 @@ int occupancy_one() {
 }
 
 // 16-bit K/V: G 3..8 (G 1 and 2 go to the CUDA-core kernel), D 64 or 128.
-// FP8 K/V: any G up to 8, D 128, bf16 or fp16 queries.
+// FP8 K/V: any G up to 8, D 64 or 128, bf16 or fp16 queries.
 __host__ __device__ constexpr bool geometry_supported(int G, int D, bool kv8 = false) {
-  return kv8 ? (G >= 1 && G <= 8 && D == 128) : (G >= 3 && G <= 8 && (D == 64 || D == 128));
+  return kv8 ? (G >= 1 && G <= 8 && (D == 64 || D == 128))
+             : (G >= 3 && G <= 8 && (D == 64 || D == 128));
 }
 
 // Dispatch over (G, block size) for one head dim, input dtype and K/V type;

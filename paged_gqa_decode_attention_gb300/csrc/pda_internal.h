@@ -110,7 +110,7 @@ constexpr int partial_ctas_per_sm_hint(int kernel, int group, int head_dim) {
 // SM, as does the CUDA-core kernel. PDA_PLAN_SLOTS overrides (experiments).
 int planning_slots(int kernel, bool kv_fp8, int num_sms, int ctas_per_sm);
 
-// kv_fp8: K/V caches hold FP8 E4M3 (tensor-core kernel, D 128, bf16 or fp16 q).
+// kv_fp8: K/V caches hold FP8 E4M3 (tensor-core kernel, D 64 or 128, bf16 or fp16 q).
 bool partial_supported(int group, int head_dim, int block_size, int dtype, bool kv_fp8);
 bool partial_kernel_supported(int kernel, int group, int head_dim, bool kv_fp8);
 cudaError_t partial_prepare(int kernel, int group, int head_dim, int block_size, int dtype,

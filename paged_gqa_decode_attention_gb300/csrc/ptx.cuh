@@ -270,6 +270,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Same with 64-byte swizzle (layout type 4): 64-byte rows in 8-row atoms of
+// 512 bytes.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;
+  return d;
+}
+
 // Instruction descriptor for kind::f16: fp32 accumulator, A/B both bf16 or
 // both fp16, A/B major-ness (0 = K-major, 1 = MN-major), N >> 3 at bits 17-22,
 // M >> 4 at bits 24-28.

@@ -202,8 +202,8 @@ void abi_checks() {
   expect(paged_decode_attn_create(&bad, &h) == PDA_EUNSUPPORTED, "create head_dim 96");
   bad = c;
   bad.kv_fp8 = 1;
-  bad.head_dim = 64;
-  expect(paged_decode_attn_create(&bad, &h) == PDA_EUNSUPPORTED, "create fp8 head_dim 64");
+  bad.head_dim = 256;
+  expect(paged_decode_attn_create(&bad, &h) == PDA_EUNSUPPORTED, "create fp8 head_dim 256");
   expect(std::strlen(paged_decode_attn_last_error()) > 0, "last_error set");
   expect(paged_decode_attn_create(nullptr, &h) != PDA_OK, "create null config");
   paged_decode_attn_destroy(nullptr);

@@ -104,9 +104,30 @@ def test_fp8_fp16_queries_exact(G, Hkv, bs):
     assert err < 2e-3, err
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (14, 2), (8, 8), (16, 2), (6, 2)])
+@pytest.mark.parametrize("bs", [16, 32])
+def test_fp8_head_dim_64_exact(Hq, Hkv, bs):
+    """FP8 K/V at head dim 64 (64-byte swizzled rows, M = 64 PV): the
+    Qwen2.5-0.5B layout (14/2 heads) and other group sizes, both block sizes,
+    every split count, bf16 and fp16 queries, fp32 output."""
+    lens = [1, bs + 1, 700, 3000, 64, 129]
+    wl = workloads.to_fp8_kv(workloads.custom(seed=Hq * 5 + Hkv + bs, B=len(lens), Hq=Hq,
+                                              Hkv=Hkv, D=64, block_size=bs, lens=lens,
+                                              num_blocks=700))
+    for splits in (0, 1, 5, 64):
+        check(wl, num_splits=splits)
+    err = check(wl, out_dtype=torch.float32)
+    assert err < 2e-3, err
+    wl16 = workloads.to_fp8_kv(workloads.custom(seed=Hq + bs, B=3, Hq=Hq, Hkv=Hkv, D=64,
+                                                block_size=bs, lens=[500, 64, 2000],
+                                                dtype="fp16"))
+    check(wl16)
+    check(wl16, num_splits=7)
+
+
 def test_fp8_unsupported_geometries_rejected():
     from paged_gqa_decode_attention_gb300 import PagedDecodeAttention
-    for kw in (dict(head_dim=64), dict(head_dim=256)):
+    for kw in (dict(head_dim=256), dict(num_q_heads=8 * 9)):
         args = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
                     dtype=torch.bfloat16)
         args.update(kw)
