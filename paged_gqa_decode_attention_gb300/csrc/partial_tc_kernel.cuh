@@ -1108,16 +1108,23 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
           named_bar_sync(bar, 128);
           // every softmax thread has read the row scales of this unit's Q buffer
           if (KV8 && i == 0 && t == 0) mbar_arrive(q_empty(jq & 1));
-          float alpha[kGA];
+          float alpha[kGA], prs[kGA];
           uint8_t* pb = base + kOffP + (c & 1) * (KV8 ? 3 * kOpHalf : 2 * kOpBytes);
+          // Every column's maxima are read before any P store: the byte and
+          // 16-bit P stores may alias the float buffer as far as the compiler
+          // knows, so interleaved they would serialise the columns.
 #pragma unroll
           for (int j = 0; j < kGA; ++j) {
             const float mx = fmaxf(fmaxf(rb[j], rb[8 + j]), fmaxf(rb[16 + j], rb[24 + j]));
             const float mn = fmaxf(m_run[j], mx);  // finite: every chunk holds a valid token
             alpha[j] = exp2f(m_run[j] - mn);
             m_run[j] = mn;
-            const float pr = exp2f(s[j] - mn);
-            l_th[j] = l_th[j] * alpha[j] + pr;
+            prs[j] = exp2f(s[j] - mn);
+            l_th[j] = l_th[j] * alpha[j] + prs[j];
+          }
+#pragma unroll
+          for (int j = 0; j < kGA; ++j) {
+            const float pr = prs[j];
             if (j < ng) {  // rows of padding heads stay zero
               const int g = g0 + j;
               if constexpr (KV8) {
