@@ -654,25 +654,21 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
         win_blk = nxt_blk;
         nxt_blk = (win_base + 32 + lane < U.p1) ? __ldg(table + win_base + 32 + lane) : 0;
       }
-      int blk[PPS];
-#pragma unroll
-      for (int i = 0; i < PPS; ++i) blk[i] = __shfl_sync(kFull, win_blk, (pg0 + i - win_base) & 31);
-      if (lane == 0) {
+      {
         const uint32_t fb = full_bar(r, slot);
         // 16-bit K/V: D / 64 boxes of 64 dims per page; FP8: one box of D bytes
         constexpr int kBoxes = KV8 ? 1 : NB;
         constexpr int kBoxElems = KV8 ? D : 64;
-        mbar_arrive_expect_tx(fb, (uint32_t)npg * BS * kBoxes * kKVRow);
-        const uint32_t st = base_u32 + (r == 0 ? kOffK : kOffV) + slot * kSlotBytes;
+        if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)npg * BS * kBoxes * kKVRow);
+        __syncwarp();
+        // lane i issues page i's boxes
+        const int bl = __shfl_sync(kFull, win_blk, (pg0 + lane - win_base) & 31);
+        if (lane < npg) {
+          const uint32_t st = base_u32 + (r == 0 ? kOffK : kOffV) + slot * kSlotBytes;
+          const uint32_t ro = (uint32_t)(lane * BS * kKVRow);
 #pragma unroll
-        for (int i = 0; i < PPS; ++i) {
-          if (i < npg) {
-            const int y = blk[i] * BS;
-            const uint32_t ro = (uint32_t)(i * BS * kKVRow);
-#pragma unroll
-            for (int bx = 0; bx < kBoxes; ++bx)
-              tma_load_2d(st + bx * kHalf + ro, map, U.h * D + bx * kBoxElems, y, fb);
-          }
+          for (int bx = 0; bx < kBoxes; ++bx)
+            tma_load_2d(st + bx * kHalf + ro, map, U.h * D + bx * kBoxElems, bl * BS, fb);
         }
       }
       __syncwarp();
@@ -754,25 +750,21 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       }
       if (mine) {
         const int slot = c % kStages;
-        int blk[PPS];
-#pragma unroll
-        for (int i = 0; i < PPS; ++i) blk[i] = __shfl_sync(kFull, win_blk, (pg0 + i - win_base) & 31);
-        if (lane == 0) {
+        {
           const uint32_t fb = full_bar(r, slot);
           // 16-bit K/V: D / 64 boxes of 64 dims per page; FP8: one box of D bytes
           constexpr int kBoxes = KV8 ? 1 : NB;
           constexpr int kBoxElems = KV8 ? D : 64;
-          mbar_arrive_expect_tx(fb, (uint32_t)npg * BS * kBoxes * kKVRow);
-          const uint32_t st = base_u32 + (r == 0 ? kOffK : kOffV) + slot * kSlotBytes;
+          if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)npg * BS * kBoxes * kKVRow);
+          __syncwarp();
+          // lane i issues page i's boxes
+          const int bl = __shfl_sync(kFull, win_blk, (pg0 + lane - win_base) & 31);
+          if (lane < npg) {
+            const uint32_t st = base_u32 + (r == 0 ? kOffK : kOffV) + slot * kSlotBytes;
+            const uint32_t ro = (uint32_t)(lane * BS * kKVRow);
 #pragma unroll
-          for (int i = 0; i < PPS; ++i) {
-            if (i < npg) {
-              const int y = blk[i] * BS;
-              const uint32_t ro = (uint32_t)(i * BS * kKVRow);
-#pragma unroll
-              for (int bx = 0; bx < kBoxes; ++bx)
-                tma_load_2d(st + bx * kHalf + ro, map, U.h * D + bx * kBoxElems, y, fb);
-            }
+            for (int bx = 0; bx < kBoxes; ++bx)
+              tma_load_2d(st + bx * kHalf + ro, map, U.h * D + bx * kBoxElems, bl * BS, fb);
           }
         }
         __syncwarp();
@@ -944,6 +936,15 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     for (int c = last_c - kStages + 1 > 0 ? last_c - kStages + 1 : 0; c <= last_c && !failed; ++c) {
       const bool ok = mbar_wait(empty_bar(r, c % kStages), (c / kStages) & 1, wlim);
       if (!__all_sync(kFull, ok)) failed = true;
+    }
+    // The QK^T warp also committed the release of the last two units' Q
+    // buffers (unit j: buffer j & 1, phase (j >> 1) & 1), which no producer
+    // waits for; wait for those arrivals too.
+    if (is_qk) {
+      for (int j = cur.j - 2 > 0 ? cur.j - 2 : 0; j < cur.j && !failed; ++j) {
+        const bool ok = mbar_wait(q_empty(j & 1), (j >> 1) & 1, wlim);
+        if (!__all_sync(kFull, ok)) failed = true;
+      }
     }
   } else if (warp < 4 || (warp >= kWarpSmxB0 && warp < kWarpSmxB0 + 4)) {
     // ------------------------------ softmax -------------------------------
