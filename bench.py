@@ -134,6 +134,12 @@ def make_workload(name: str, seed: int, device):
     if name == "geo_fp8_d64_b16_l32768":  # FP8 cache, 32/8 heads, D 64 (the headline's bytes)
         return W.to_fp8_kv(W.custom(seed=seed, B=16, Hq=32, Hkv=8, D=64, block_size=16,
                                     lens=[32768] * 16, device=device))
+    if name == "long_b4_l32768_g16":  # 128/8 heads (G = 16: all 16 MMA columns), the headline's bytes
+        return W.custom(seed=seed, B=4, Hq=128, Hkv=8, D=128, block_size=16, lens=[32768] * 4,
+                        device=device)
+    if name == "long_b8_l32768_fp8_g16":  # FP8 cache, 128/8 heads
+        return W.to_fp8_kv(W.custom(seed=seed, B=8, Hq=128, Hkv=8, D=128, block_size=16,
+                                    lens=[32768] * 8, device=device))
     if name == "long_b8_l32768_fp8_g8":  # FP8 cache, 64/8 heads
         return W.to_fp8_kv(W.custom(seed=seed, B=8, Hq=64, Hkv=8, D=128, block_size=16,
                                     lens=[32768] * 8, device=device))

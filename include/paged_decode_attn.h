@@ -75,9 +75,10 @@ typedef enum {
   PDA_F32 = 2 /* output only: fp32 out for accuracy checks */
 } pda_dtype;
 
-/* Fixed at create time. Supported geometries: G = Hq / Hkv from 1 to 8 at
- * head_dim 64 or 128, 1 to 4 at head_dim 256; with kv_fp8, any G up to 8 at
- * head_dim 64 or 128 and dtype PDA_BF16 or PDA_FP16. */
+/* Fixed at create time. Supported geometries: G = Hq / Hkv from 1 to 16 at
+ * head_dim 64 or 128 (G 9..16 on the tensor-core kernel only), 1 to 4 at
+ * head_dim 256; with kv_fp8, any G up to 16 at head_dim 64 or 128 and dtype
+ * PDA_BF16 or PDA_FP16. */
 typedef struct {
   int num_q_heads;        /* Hq; a multiple of num_kv_heads */
   int num_kv_heads;       /* Hkv */
@@ -170,7 +171,7 @@ int paged_decode_attn_run_scaled(pda_handle handle, const void* q, const void* k
  * *num_splits receives S (1 .. cfg->max_splits) and *chunk_pages the pages
  * each split covers; sequence b then uses min(S, ceil(ceil(L_b / block_size)
  * / chunk_pages)) splits. Waves of work units are counted over 27/32 of the
- * SMs for the 16-bit tensor-core kernel (G 3..8 at head_dim 64/128) and over
+ * SMs for the 16-bit tensor-core kernel (G 3..16 at head_dim 64/128) and over
  * every SM (times CTAs per SM) otherwise. */
 int paged_decode_attn_plan(const pda_config* cfg, int num_sms, int batch, int max_blocks,
                            int max_context_len_hint, int* num_splits, int* chunk_pages);

@@ -1,6 +1,6 @@
 // Split-K partial kernel on the 5th-generation tensor cores (tcgen05, TMEM
-// accumulators) for GQA groups of G = 3..8 query heads per kv head and head
-// dims D of 128 or 64.
+// accumulators) for GQA groups of G = 3..16 query heads per kv head (1..16
+// with FP8 K/V) and head dims D of 128 or 64.
 //
 // Same method and work units as the CUDA-core kernel (partial_kernel.cuh):
 // a unit is one (split, kv head, sequence), split-K with a normalised partial
@@ -138,10 +138,14 @@ constexpr int kUnitRing = 4;               // slots of the shared unit queue
 // second producers when a ring has two)
 constexpr int kUnitConsumers = 4;
 constexpr int kUnitInts = 12;              // a unit ring entry: index + decoded Unit
-// A finished unit's state, softmax -> epilogue, double-buffered:
-// acc[8][128], max[8], sum[8], then the unit index and its sequence's split
-// count (as ints).
-constexpr int kEpiFloats = 8 * 128 + 8 + 8 + 4;
+// A finished unit's state, softmax -> epilogue: acc[H][128], max[H], sum[H],
+// then the unit index and its sequence's split count (as ints), for H = 8
+// query heads (16 for G 9..16). Two slots, so a unit's state can wait while
+// the previous one is written out; one for G 9..16 with 16-bit K/V, whose
+// rings leave no room for two.
+__host__ __device__ constexpr int epi_heads(int G) { return G > 8 ? 16 : 8; }
+__host__ __device__ constexpr int epi_floats(int G) { return epi_heads(G) * 128 + 2 * epi_heads(G) + 4; }
+__host__ __device__ constexpr int epi_slots(int G, bool kv8) { return G > 8 && !kv8 ? 1 : 2; }
 constexpr float kP8Scale = 256.f;          // FP8 K/V: P is split at p * 256
 
 // Shared-memory layout. 16-bit K/V at D 128: 3-slot rings of 32 KiB slots
@@ -150,7 +154,7 @@ constexpr float kP8Scale = 256.f;          // FP8 K/V: P is split at p * 256
 // rings of 80 KiB in slots of one D-byte row per token (5 x 16 KiB at D 128,
 // 10 x 8 KiB at D 64 with 64-byte swizzled rows), two fp8 terms of Q next to
 // the 16-bit Q tile, three fp8 terms of P in the P buffers.
-template <bool KV8, int D = 128>
+template <bool KV8, int D = 128, int G = 8>
 struct Layout {
   static constexpr int kStages = KV8 ? (D == 64 ? 10 : 5) : (D == 64 ? 6 : 3);
   static constexpr int kSlotBytes = KV8 ? kT * D : (D / 64) * kHalf;
@@ -159,9 +163,10 @@ struct Layout {
   static constexpr int kOffQ = 2 * kStages * kSlotBytes;  // [2 buffers] Q tiles (TMA)
   static constexpr int kOffQ8 = kOffQ + 2 * kOpBytes;     // [2 buffers] fp8 Q terms (KV8)
   static constexpr int kOffP = kOffQ8 + (KV8 ? 2 * kOpBytes : 0);  // [2 buffers] P operands
-  static constexpr int kOffQs = kOffP + 4 * kOpBytes;     // [2 buffers][8] 1/sigma per row (KV8)
+  // [2 buffers][epi_heads(G)] 1/sigma per row (KV8)
+  static constexpr int kOffQs = kOffP + 4 * kOpBytes;
   // per softmax group: 2 x [4 warps][8] floats (chunk maxima), [4 warps][8] (final sums)
-  static constexpr int kOffRed = kOffQs + 2 * 8 * 4;
+  static constexpr int kOffRed = kOffQs + 2 * epi_heads(G) * 4;
   static constexpr int kOffLred = kOffRed + 2 * 2 * 4 * 8 * 4;
   static constexpr int kOffBar = kOffLred + 2 * 4 * 8 * 4;
   static constexpr int kNumBars = 4 * kStages + 14 + 2 * kUnitRing + 4 + 2 + 1;
@@ -171,7 +176,7 @@ struct Layout {
   static constexpr int kOffUBcast = kOffURing + kUnitRing * kUnitInts * 4;  // same, softmax warp 0 -> rest
   static constexpr int kOffEpiFlag = kOffUBcast + kUnitInts * 4;  // epilogue group's wait outcome
   static constexpr int kOffEpi = (kOffEpiFlag + 4 + 15) & ~15;
-  static constexpr size_t kSmemBytes = 1024 + kOffEpi + 2 * kEpiFloats * 4;
+  static constexpr size_t kSmemBytes = 1024 + kOffEpi + epi_slots(G, KV8) * epi_floats(G) * 4;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -357,12 +362,12 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     paged_partial_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v,
                             const __grid_constant__ CUtensorMap tmap_q, const PartialParams p) {
-  static_assert(G >= 1 && G <= 8, "tensor-core path packs up to 8 query heads");
+  static_assert(G >= 1 && G <= 16, "tensor-core path packs up to 16 query heads (MMA N = 16)");
   static_assert(D == 64 || D == 128, "head dim 64 or 128");
   // bytes of one token row of one head in a K/V ring slot (FP8: D, 64-byte
   // swizzled rows at D 64; 16-bit: 128, one 64-dim half)
   constexpr int kKVRow = KV8 ? D : kRowBytes;
-  using L = Layout<KV8, D>;
+  using L = Layout<KV8, D, G>;
   constexpr int kStages = L::kStages;
   constexpr int kSlotBytes = L::kSlotBytes;
   constexpr int kOffK = L::kOffK;
@@ -386,6 +391,12 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
   constexpr bool kDualPV = dual_pv(G, D, KV8);
   constexpr int kWarpMmaPV2 = warp_pv2(G, D, KV8);
   constexpr int kGA = (G + 1) / 2 > 0 ? (G + 1) / 2 : 1;  // columns of group 0 (group 1: G - kGA)
+  constexpr int kLd = kGA > 4 ? 8 : 4;      // TMEM columns a softmax thread loads per operand
+  constexpr int kGE = epi_heads(G);         // heads of a state slot
+  constexpr int kEpiF = epi_floats(G);      // floats of a state slot
+  constexpr int kEpiSlots = epi_slots(G, KV8);
+  // state slot offsets: per-head maxima, per-head sums, unit index, split count
+  constexpr int kStMax = kGE * kHeadDim, kStSum = kStMax + kGE, kStU = kStSum + kGE;
   static_assert(kT % BS == 0 && PPS <= 32, "stage must hold whole pages");
   using TNat = std::conditional_t<FP16, __half, __nv_bfloat16>;
   using H = Half16<FP16>;
@@ -797,7 +808,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
           // a unit's Q.
           const uint8_t* qt = base + kOffQ + qb * kOpBytes;
           uint8_t* q8 = base + kOffQ8 + qb * kOpBytes;
-          float* qs = reinterpret_cast<float*>(base + kOffQs) + qb * 8;
+          float* qs = reinterpret_cast<float*>(base + kOffQs) + qb * kGE;
           const int d0 = 4 * lane;  // lanes past D read the tile's zero half
 #pragma unroll
           for (int g = 0; g < G; ++g) {
@@ -971,19 +982,23 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       // does not wait for the last PV to complete.
       float m_pd[kGA], l_pd[kGA], acc_pd[kGA], alpha_pd[kGA];
       int u_pd = -1, nsb_pd = 0;  // its index and its sequence's split count
+      // kLd consecutive TMEM columns of this thread's lane
+      auto tld = [&](uint32_t taddr, float (&v)[kLd]) {
+        if constexpr (kLd == 8) tmem_ld_x8(taddr, v); else tmem_ld_x4(taddr, v);
+      };
       // a = a * al + O(c), this group's columns
       auto fold = [&](int c, float (&a)[kGA], const float (&al)[kGA]) {
         bool ok = !failed && mbar_wait(o_full(c & 1), (c >> 1) & 1, wlim);
         if (!__all_sync(kFull, ok)) failed = true;
         tc_fence_after();
         // the stacked term columns of each head: g, 16 + g (, 32 + g)
-        float o[4], o2[4], o3[4];
-        tmem_ld_x4(tO(c & 1) + lane_base + (uint32_t)g0, o);
-        tmem_ld_x4(tO(c & 1) + lane_base + (uint32_t)(kN + g0), o2);
-        if constexpr (KV8) tmem_ld_x4(tO(c & 1) + lane_base + (uint32_t)(2 * kN + g0), o3);
+        float o[kLd], o2[kLd], o3[kLd];
+        tld(tO(c & 1) + lane_base + (uint32_t)g0, o);
+        tld(tO(c & 1) + lane_base + (uint32_t)(kN + g0), o2);
+        if constexpr (KV8) tld(tO(c & 1) + lane_base + (uint32_t)(2 * kN + g0), o3);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o[j] += KV8 ? o2[j] + o3[j] : o2[j];
+        for (int j = 0; j < kLd; ++j) o[j] += KV8 ? o2[j] + o3[j] : o2[j];
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(o_free(c & 1));
@@ -1024,11 +1039,12 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
 #pragma unroll
         for (int j = 0; j < kGA; ++j) Ls[j] = lred[j] + lred[8 + j] + lred[16 + j] + lred[24 + j];
         named_bar_sync(bar, 128);  // lred is rewritten by the next unit
-        const int es = je & 1;
+        const int es = je % kEpiSlots;
         bool ok2 = !failed;
-        if (ok2 && je >= 2) ok2 = mbar_wait(ep_empty(es), ((je - 2) >> 1) & 1, wlim);
+        if (ok2 && je >= kEpiSlots)
+          ok2 = mbar_wait(ep_empty(es), ((je - kEpiSlots) / kEpiSlots) & 1, wlim);
         if (!__all_sync(kFull, ok2)) failed = true;
-        float* st = reinterpret_cast<float*>(base + kOffEpi) + es * kEpiFloats;
+        float* st = reinterpret_cast<float*>(base + kOffEpi) + es * kEpiF;
 #pragma unroll
         for (int j = 0; j < kGA; ++j)
           if (j < ng && od_ok) st[(g0 + j) * kHeadDim + od] = af[j];
@@ -1036,13 +1052,13 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
 #pragma unroll
           for (int j = 0; j < kGA; ++j) {
             if (j < ng) {
-              st[8 * kHeadDim + g0 + j] = mf[j];
-              st[8 * kHeadDim + 8 + g0 + j] = Ls[j];
+              st[kStMax + g0 + j] = mf[j];
+              st[kStSum + g0 + j] = Ls[j];
             }
           }
           if (grp == 0) {
-            reinterpret_cast<int*>(st)[8 * kHeadDim + 16] = uf;
-            reinterpret_cast<int*>(st)[8 * kHeadDim + 17] = nsb;
+            reinterpret_cast<int*>(st)[kStU] = uf;
+            reinterpret_cast<int*>(st)[kStU + 1] = nsb;
           }
         }
         __syncwarp();
@@ -1072,7 +1088,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
         if constexpr (KV8) {
           const bool okq = !failed && mbar_wait(q8_full(jq & 1), (jq >> 1) & 1, wlim);
           if (!__all_sync(kFull, okq)) failed = true;
-          const float* qs = reinterpret_cast<const float*>(base + kOffQs) + (jq & 1) * 8;
+          const float* qs = reinterpret_cast<const float*>(base + kOffQs) + (jq & 1) * kGE;
 #pragma unroll
           for (int j = 0; j < kGA; ++j) qsc[j] = j < ng ? p.qscale * ksc * qs[g0 + j] : 0.f;
         } else {
@@ -1085,13 +1101,13 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
           bool ok = !failed && mbar_wait(s_full(c & 1), (c >> 1) & 1, wlim);
           if (!__all_sync(kFull, ok)) failed = true;
           tc_fence_after();
-          float s[4], s2[4];
-          tmem_ld_x4(tS(c & 1) + lane_base + (uint32_t)g0, s);
-          if constexpr (KV8) tmem_ld_x4(tS(c & 1) + lane_base + (uint32_t)(kN + g0), s2);
+          float s[kLd], s2[kLd];
+          tld(tS(c & 1) + lane_base + (uint32_t)g0, s);
+          if constexpr (KV8) tld(tS(c & 1) + lane_base + (uint32_t)(kN + g0), s2);
           tmem_ld_wait();
           if constexpr (KV8) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) s[j] += s2[j];
+            for (int j = 0; j < kLd; ++j) s[j] += s2[j];
           }
           tc_fence_before();
           __syncwarp();
@@ -1192,12 +1208,13 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       }
       // end of work: an empty state tells the epilogue group to stop
       {
-        const int es = je & 1;
+        const int es = je % kEpiSlots;
         bool ok2 = !failed;
-        if (ok2 && je >= 2) ok2 = mbar_wait(ep_empty(es), ((je - 2) >> 1) & 1, wlim);
+        if (ok2 && je >= kEpiSlots)
+          ok2 = mbar_wait(ep_empty(es), ((je - kEpiSlots) / kEpiSlots) & 1, wlim);
         if (!__all_sync(kFull, ok2)) failed = true;
-        float* st = reinterpret_cast<float*>(base + kOffEpi) + es * kEpiFloats;
-        if (grp == 0 && t == 0) reinterpret_cast<int*>(st)[8 * kHeadDim + 16] = -1;
+        float* st = reinterpret_cast<float*>(base + kOffEpi) + es * kEpiF;
+        if (grp == 0 && t == 0) reinterpret_cast<int*>(st)[kStU] = -1;
         __syncwarp();
         if (lane == 0) mbar_arrive(ep_full(es));
       }
@@ -1207,8 +1224,8 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     const int t = threadIdx.x - kWarpEpi0 * 32;  // output dim
     volatile int* flag = reinterpret_cast<volatile int*>(base + kOffEpiFlag);
     for (int je = 0;; ++je) {
-      const int es = je & 1;
-      const bool ok = !failed && mbar_wait(ep_full(es), (je >> 1) & 1, wlim);
+      const int es = je % kEpiSlots;
+      const bool ok = !failed && mbar_wait(ep_full(es), (je / kEpiSlots) & 1, wlim);
       // the four warps agree on the outcome before acting on it
       if (t == 0) *flag = 0;
       named_bar_sync(2, 128);
@@ -1218,8 +1235,8 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
         failed = true;
         break;
       }
-      float* st = reinterpret_cast<float*>(base + kOffEpi) + es * kEpiFloats;
-      const int u = reinterpret_cast<volatile int*>(st)[8 * kHeadDim + 16];
+      float* st = reinterpret_cast<float*>(base + kOffEpi) + es * kEpiF;
+      const int u = reinterpret_cast<volatile int*>(st)[kStU];
       if (u < 0) {
         // a cluster CTA whose split had nothing to merge still counts toward
         // the other CTAs' merge barriers
@@ -1236,7 +1253,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       U.split = u % p.num_splits;
       U.h = (u / p.num_splits) % p.Hkv;
       U.b = u / p.num_splits / p.Hkv;
-      U.n_splits_b = reinterpret_cast<volatile int*>(st)[8 * kHeadDim + 17];
+      U.n_splits_b = reinterpret_cast<volatile int*>(st)[kStU + 1];
       const int hq0 = U.h * G;
       // V dequantisation scale (and the fp8 split factor of P)
       const float vsc = (p.v_scale ? __ldg(p.v_scale + (p.scale_per_head ? U.h : 0)) : 1.f) *
@@ -1248,12 +1265,12 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
         // reading the other splits' slots through distributed shared memory.
         if (t < D) {
 #pragma unroll
-          for (int g = 0; g < G; ++g) st[g * kHeadDim + t] = st[g * kHeadDim + t] / st[8 * kHeadDim + 8 + g] * vsc;
+          for (int g = 0; g < G; ++g) st[g * kHeadDim + t] = st[g * kHeadDim + t] / st[kStSum + g] * vsc;
         }
         if (t == 0) {
 #pragma unroll
           for (int g = 0; g < G; ++g)
-            st[8 * kHeadDim + g] = (st[8 * kHeadDim + g] + log2f(st[8 * kHeadDim + 8 + g])) * kLn2;
+            st[kStMax + g] = (st[kStMax + g] + log2f(st[kStSum + g])) * kLn2;
         }
         named_bar_sync(2, 128);  // this CTA's slot holds its split's o and lse
         if (t == 0) {
@@ -1280,7 +1297,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
               for (int k = 0; k < 8; ++k) {
                 if (s0 + k < nsb) {
                   const uint32_t rb = cluster_map(st_u32, (uint32_t)(s0 + k));
-                  l[k] = ld_cluster_f32(rb + (uint32_t)(8 * kHeadDim + g) * 4u);
+                  l[k] = ld_cluster_f32(rb + (uint32_t)(kStMax + g) * 4u);
                   v[k] = ld_cluster_f32(rb + (uint32_t)(g * kHeadDim + d) * 4u);
                 }
               }
@@ -1313,7 +1330,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       if (t < D) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float Ls = st[8 * kHeadDim + 8 + g];
+          const float Ls = st[kStSum + g];
           const float o = st[g * kHeadDim + t] / Ls * vsc;
           const int64_t row = (int64_t)U.b * p.Hq + hq0 + g;
           if (U.n_splits_b == 1) {
@@ -1322,7 +1339,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
           } else {
             const int64_t r = row * p.num_splits + U.split;
             p.ws_o[r * D + t] = o;
-            if (t == 0) p.ws_lse[r] = (st[8 * kHeadDim + g] + log2f(Ls)) * kLn2;
+            if (t == 0) p.ws_lse[r] = (st[kStMax + g] + log2f(Ls)) * kLn2;
           }
         }
       }
@@ -1363,7 +1380,7 @@ cudaError_t launch_one(const CUtensorMap* tk, const CUtensorMap* tv, const CUten
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ctas);
   cfg.blockDim = dim3(tc_threads(G, D, KV8));
-  cfg.dynamicSmemBytes = Layout<KV8, D>::kSmemBytes;
+  cfg.dynamicSmemBytes = Layout<KV8, D, G>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   unsigned n_attr = 0;
@@ -1392,7 +1409,7 @@ int max_clusters_one(int cluster) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)cluster * 64u);
   cfg.blockDim = dim3(tc_threads(G, D, KV8));
-  cfg.dynamicSmemBytes = Layout<KV8, D>::kSmemBytes;
+  cfg.dynamicSmemBytes = Layout<KV8, D, G>::kSmemBytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cluster;
@@ -1413,7 +1430,7 @@ template <int G, int D, int BS, bool FP16, bool KV8>
 cudaError_t prepare_one() {
   cudaError_t e = cudaFuncSetAttribute(paged_partial_tc_kernel<G, D, BS, FP16, KV8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)Layout<KV8, D>::kSmemBytes);
+                                       (int)Layout<KV8, D, G>::kSmemBytes);
   // clusters of up to 16 CTAs (the splits of one sequence's kv head)
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(paged_partial_tc_kernel<G, D, BS, FP16, KV8>,
@@ -1426,26 +1443,29 @@ int occupancy_one() {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
           &n, paged_partial_tc_kernel<G, D, BS, FP16, KV8>, tc_threads(G, D, KV8),
-          Layout<KV8, D>::kSmemBytes) != cudaSuccess)
+          Layout<KV8, D, G>::kSmemBytes) != cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }
 
-// 16-bit K/V: G 3..8 (G 1 and 2 go to the CUDA-core kernel), D 64 or 128.
-// FP8 K/V: any G up to 8, D 64 or 128, bf16 or fp16 queries.
+// 16-bit K/V: G 3..16 (G 1 and 2 go to the CUDA-core kernel), D 64 or 128.
+// FP8 K/V: any G up to 16, D 64 or 128, bf16 or fp16 queries.
 __host__ __device__ constexpr bool geometry_supported(int G, int D, bool kv8 = false) {
-  return kv8 ? (G >= 1 && G <= 8 && (D == 64 || D == 128))
-             : (G >= 3 && G <= 8 && (D == 64 || D == 128));
+  return kv8 ? (G >= 1 && G <= 16 && (D == 64 || D == 128))
+             : (G >= 3 && G <= 16 && (D == 64 || D == 128));
 }
 
 // Dispatch over (G, block size) for one head dim, input dtype and K/V type;
-// each combination is instantiated in its own translation unit.
-template <int D, bool FP16, bool KV8>
+// each (head dim, dtype, K/V type) and G range GLo..GHi is instantiated in its
+// own translation unit (G 1..8 and G 9..16 compile in parallel).
+template <int D, bool FP16, bool KV8, int GLo = 1, int GHi = 8>
 struct Dispatch {
+  template <int G>
+  static constexpr bool kBuilt = G >= GLo && G <= GHi && geometry_supported(G, D, KV8);
   template <int G>
   static cudaError_t launch_g(int BS, const CUtensorMap* tk, const CUtensorMap* tv,
                               const CUtensorMap* tq, const PartialParams& p, cudaStream_t s) {
-    if constexpr (geometry_supported(G, D, KV8)) {
+    if constexpr (kBuilt<G>) {
       if (BS == 16) return launch_one<G, D, 16, FP16, KV8>(tk, tv, tq, p, s);
       if (BS == 32) return launch_one<G, D, 32, FP16, KV8>(tk, tv, tq, p, s);
     }
@@ -1453,7 +1473,7 @@ struct Dispatch {
   }
   template <int G>
   static cudaError_t prepare_g(int BS) {
-    if constexpr (geometry_supported(G, D, KV8)) {
+    if constexpr (kBuilt<G>) {
       if (BS == 16) return prepare_one<G, D, 16, FP16, KV8>();
       if (BS == 32) return prepare_one<G, D, 32, FP16, KV8>();
     }
@@ -1461,7 +1481,7 @@ struct Dispatch {
   }
   template <int G>
   static int max_clusters_g(int BS, int cluster) {
-    if constexpr (geometry_supported(G, D, KV8)) {
+    if constexpr (kBuilt<G>) {
       return BS == 16 ? max_clusters_one<G, D, 16, FP16, KV8>(cluster)
                       : max_clusters_one<G, D, 32, FP16, KV8>(cluster);
     }
@@ -1469,7 +1489,7 @@ struct Dispatch {
   }
   template <int G>
   static int occupancy_g(int BS) {
-    if constexpr (geometry_supported(G, D, KV8)) {
+    if constexpr (kBuilt<G>) {
       return BS == 16 ? occupancy_one<G, D, 16, FP16, KV8>() : occupancy_one<G, D, 32, FP16, KV8>();
     }
     return 1;
@@ -1485,6 +1505,14 @@ struct Dispatch {
       case 6: return launch_g<6>(BS, tk, tv, tq, p, s);
       case 7: return launch_g<7>(BS, tk, tv, tq, p, s);
       case 8: return launch_g<8>(BS, tk, tv, tq, p, s);
+      case 9: return launch_g<9>(BS, tk, tv, tq, p, s);
+      case 10: return launch_g<10>(BS, tk, tv, tq, p, s);
+      case 11: return launch_g<11>(BS, tk, tv, tq, p, s);
+      case 12: return launch_g<12>(BS, tk, tv, tq, p, s);
+      case 13: return launch_g<13>(BS, tk, tv, tq, p, s);
+      case 14: return launch_g<14>(BS, tk, tv, tq, p, s);
+      case 15: return launch_g<15>(BS, tk, tv, tq, p, s);
+      case 16: return launch_g<16>(BS, tk, tv, tq, p, s);
       default: return cudaErrorInvalidValue;
     }
   }
@@ -1498,6 +1526,14 @@ struct Dispatch {
       case 6: return prepare_g<6>(BS);
       case 7: return prepare_g<7>(BS);
       case 8: return prepare_g<8>(BS);
+      case 9: return prepare_g<9>(BS);
+      case 10: return prepare_g<10>(BS);
+      case 11: return prepare_g<11>(BS);
+      case 12: return prepare_g<12>(BS);
+      case 13: return prepare_g<13>(BS);
+      case 14: return prepare_g<14>(BS);
+      case 15: return prepare_g<15>(BS);
+      case 16: return prepare_g<16>(BS);
       default: return cudaErrorInvalidValue;
     }
   }
@@ -1511,6 +1547,14 @@ struct Dispatch {
       case 6: return max_clusters_g<6>(BS, cluster);
       case 7: return max_clusters_g<7>(BS, cluster);
       case 8: return max_clusters_g<8>(BS, cluster);
+      case 9: return max_clusters_g<9>(BS, cluster);
+      case 10: return max_clusters_g<10>(BS, cluster);
+      case 11: return max_clusters_g<11>(BS, cluster);
+      case 12: return max_clusters_g<12>(BS, cluster);
+      case 13: return max_clusters_g<13>(BS, cluster);
+      case 14: return max_clusters_g<14>(BS, cluster);
+      case 15: return max_clusters_g<15>(BS, cluster);
+      case 16: return max_clusters_g<16>(BS, cluster);
       default: return 0;
     }
   }
@@ -1524,6 +1568,14 @@ struct Dispatch {
       case 6: return occupancy_g<6>(BS);
       case 7: return occupancy_g<7>(BS);
       case 8: return occupancy_g<8>(BS);
+      case 9: return occupancy_g<9>(BS);
+      case 10: return occupancy_g<10>(BS);
+      case 11: return occupancy_g<11>(BS);
+      case 12: return occupancy_g<12>(BS);
+      case 13: return occupancy_g<13>(BS);
+      case 14: return occupancy_g<14>(BS);
+      case 15: return occupancy_g<15>(BS);
+      case 16: return occupancy_g<16>(BS);
       default: return 1;
     }
   }

@@ -78,7 +78,7 @@ enum PartialKernel : int {
   kPartialCudaCore = 0,    // QK/PV on the FMA pipe (partial_kernel.cuh): G 1..8 at D 64 and
                            // 128, G 1..4 at D 256
   kPartialTensorCore = 1,  // QK/PV with tcgen05 MMAs into TMEM (partial_tc_kernel.cuh):
-                           // G 3..8, D 64 and 128
+                           // G 3..16, D 64 and 128 (FP8 K/V: G 1..16)
 };
 
 // The kernel a geometry uses unless overridden (PDA_PARTIAL_KERNEL): the
@@ -87,7 +87,7 @@ enum PartialKernel : int {
 // L=32768 at G=4: 0.0974 vs 0.1000 ms; the 128-sequence serving mix at G=8:
 // 0.114 vs 0.255 ms); otherwise the CUDA-core kernel is used.
 constexpr int default_partial_kernel(int group, int head_dim, bool kv_fp8 = false) {
-  return (kv_fp8 || (group >= 3 && group <= 8 && (head_dim == 64 || head_dim == 128)))
+  return (kv_fp8 || (group >= 3 && group <= 16 && (head_dim == 64 || head_dim == 128)))
              ? kPartialTensorCore
              : kPartialCudaCore;
 }

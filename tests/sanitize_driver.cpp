@@ -201,6 +201,9 @@ void abi_checks() {
   bad.head_dim = 96;
   expect(paged_decode_attn_create(&bad, &h) == PDA_EUNSUPPORTED, "create head_dim 96");
   bad = c;
+  bad.num_q_heads = 17 * bad.num_kv_heads;
+  expect(paged_decode_attn_create(&bad, &h) == PDA_EUNSUPPORTED, "create group size 17");
+  bad = c;
   bad.kv_fp8 = 1;
   bad.head_dim = 256;
   expect(paged_decode_attn_create(&bad, &h) == PDA_EUNSUPPORTED, "create fp8 head_dim 256");

@@ -49,7 +49,7 @@ def test_library_needs_no_driver_to_load(lib):
 @pytest.mark.parametrize("field,value,status", [
     ("num_q_heads", 0, pda.PDA_EINVAL),
     ("num_q_heads", 30, pda.PDA_EINVAL),        # not a multiple of Hkv = 8
-    ("num_q_heads", 8 * 9, pda.PDA_EUNSUPPORTED),  # group size 9
+    ("num_q_heads", 8 * 17, pda.PDA_EUNSUPPORTED),  # group size 17
     ("head_dim", 96, pda.PDA_EUNSUPPORTED),
     ("head_dim", 0, pda.PDA_EINVAL),
     ("block_size", 8, pda.PDA_EUNSUPPORTED),
@@ -72,9 +72,11 @@ def test_create_rejects_bad_config_before_cuda(lib, field, value, status):
 @pytest.mark.parametrize("Hq,Hkv,D,ok", [(14, 2, 64, True), (28, 4, 128, True), (40, 8, 128, True),
                                          (24, 8, 128, True), (8, 1, 256, False), (16, 8, 256, True),
                                          (32, 8, 256, True), (12, 2, 256, False), (8, 8, 64, True),
-                                         (4, 1, 64, True)])
+                                         (4, 1, 64, True), (128, 8, 128, True), (72, 8, 64, True),
+                                         (16, 1, 128, True), (136, 8, 128, False),
+                                         (17, 1, 64, False), (40, 8, 256, False)])
 def test_create_geometries_before_cuda(lib, Hq, Hkv, D, ok):
-    """Group sizes 1..8 at head dims 64 and 128, 1..4 at 256: accepted by the
+    """Group sizes 1..16 at head dims 64 and 128, 1..4 at 256: accepted by the
     config checks (creation then needs a GPU), others are unsupported."""
     cfg = pda.make_config(Hq, Hkv, D, 16)
     h = ctypes.c_void_p()

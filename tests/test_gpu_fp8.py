@@ -125,9 +125,29 @@ def test_fp8_head_dim_64_exact(Hq, Hkv, bs):
     check(wl16, num_splits=7)
 
 
+@pytest.mark.parametrize("Hq,Hkv,D", [(128, 8, 128), (64, 4, 64), (9, 1, 128), (28, 2, 64)])
+@pytest.mark.parametrize("bs", [16, 32])
+def test_fp8_large_groups_exact(Hq, Hkv, D, bs):
+    """FP8 K/V with group sizes 9..16 (up to all 16 MMA columns), bf16 and fp16
+    queries, every split count, fp32 output."""
+    lens = [1, bs + 1, 700, 3000, 64, 129]
+    wl = workloads.to_fp8_kv(workloads.custom(seed=Hq * 11 + Hkv + D + bs, B=len(lens), Hq=Hq,
+                                              Hkv=Hkv, D=D, block_size=bs, lens=lens,
+                                              num_blocks=700))
+    for splits in (0, 1, 5, 64):
+        check(wl, num_splits=splits)
+    err = check(wl, out_dtype=torch.float32)
+    assert err < 2e-3, err
+    wl16 = workloads.to_fp8_kv(workloads.custom(seed=Hq + bs + 1, B=3, Hq=Hq, Hkv=Hkv, D=D,
+                                                block_size=bs, lens=[500, 64, 2000],
+                                                dtype="fp16"))
+    check(wl16)
+    check(wl16, num_splits=7)
+
+
 def test_fp8_unsupported_geometries_rejected():
     from paged_gqa_decode_attention_gb300 import PagedDecodeAttention
-    for kw in (dict(head_dim=256), dict(num_q_heads=8 * 9)):
+    for kw in (dict(head_dim=256), dict(num_q_heads=8 * 17)):
         args = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
                     dtype=torch.bfloat16)
         args.update(kw)

@@ -276,6 +276,35 @@ def test_geometries_exact(Hq, Hkv, D, bs):
         check(wl, num_splits=splits)
 
 
+# Group sizes 9..16 (tensor-core kernel only: the group fills up to all 16
+# MMA columns): 128/8 and 64/4 heads (G 16), 96/8 (G 12), 28/2 at D 64
+# (G 14), 72/8 (G 9), MQA with 11 query heads, 60/4 (G 15).
+LARGE_GROUPS = [(128, 8, 128), (64, 4, 64), (96, 8, 128), (28, 2, 64), (72, 8, 128), (11, 1, 128),
+                (60, 4, 64), (40, 4, 128)]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", LARGE_GROUPS)
+@pytest.mark.parametrize("bs", [16, 32])
+def test_large_groups_exact(Hq, Hkv, D, bs):
+    lens = [1, bs + 1, 700, 3000, 64, 129]
+    wl = workloads.custom(seed=Hq * 3 + Hkv + D + bs, B=len(lens), Hq=Hq, Hkv=Hkv, D=D,
+                          block_size=bs, lens=lens, num_blocks=600)
+    for splits in (0, 1, 5, 64):
+        check(wl, num_splits=splits)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(128, 8, 128), (28, 2, 64), (72, 8, 128)])
+def test_large_groups_fp16_and_fp32_out(Hq, Hkv, D):
+    lens = [900, 17, 2048, 300]
+    wl = workloads.custom(seed=D + Hq + 5, B=4, Hq=Hq, Hkv=Hkv, D=D, block_size=16, lens=lens,
+                          dtype="fp16", num_blocks=300)
+    check(wl)
+    check(wl, num_splits=3)
+    wl = workloads.custom(seed=D + Hq + 6, B=4, Hq=Hq, Hkv=Hkv, D=D, block_size=32, lens=lens)
+    err = check(wl, out_dtype=torch.float32)
+    assert err < 1e-4, err
+
+
 @pytest.mark.parametrize("Hq,Hkv,D", [(14, 2, 64), (16, 8, 256), (28, 4, 128)])
 def test_geometries_fp16_and_fp32_out(Hq, Hkv, D):
     lens = [900, 17, 2048, 300]
@@ -338,7 +367,8 @@ def test_timed_out_call_reports_and_next_call_is_exact(Hq, Hkv, D, monkeypatch):
 
 
 @pytest.mark.parametrize("cluster", ["1", "0"])
-@pytest.mark.parametrize("Hq,Hkv,D,bs", [(8, 1, 128, 16), (14, 2, 64, 32), (32, 8, 128, 16)])
+@pytest.mark.parametrize("Hq,Hkv,D,bs", [(8, 1, 128, 16), (14, 2, 64, 32), (32, 8, 128, 16),
+                                         (128, 8, 128, 16)])
 def test_split_merge_paths(cluster, Hq, Hkv, D, bs, monkeypatch):
     """The splits of a (sequence, kv head) merge either inside one
     thread-block cluster through distributed shared memory (split counts 2..16
