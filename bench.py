@@ -52,8 +52,8 @@ TC_KERNEL_SOURCES = ("partial_tc_kernel.cuh", "ptx.cuh", "split_merge.cuh", "pda
 ROPE_KERNEL_SOURCES = ("rope_kv_write.cu", "ptx.cuh", "pda_internal.h")
 NCU_TRAFFIC = {
     # workload: (bytes per launch, kernel sources, their SHA-256 at capture)
-    "long_b4_l32768": (540_337_920, TC_KERNEL_SOURCES,
-                       "268786a97f39b1021dfaecb323afcd23013c94e74cdc241c29bdd723dccf4cfb"),
+    "long_b4_l32768": (540_902_656, TC_KERNEL_SOURCES,
+                       "8f89a16174eb09d5c93d5cb7837516b780df005d123e0c45d0ae98a2358292db"),
     "rope_prefill_t32768": (768_392_448, ROPE_KERNEL_SOURCES,
                             "df5a0b52b1f3f70e6d0d2f41abec52a82ddda21f0b621cf7a36b12f1b3c25efd"),
 }
