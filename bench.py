@@ -54,8 +54,8 @@ NCU_TRAFFIC = {
     # workload: (bytes per launch, kernel sources, their SHA-256 at capture)
     "long_b4_l32768": (540_902_656, TC_KERNEL_SOURCES,
                        "8f89a16174eb09d5c93d5cb7837516b780df005d123e0c45d0ae98a2358292db"),
-    "rope_prefill_t32768": (768_392_448, ROPE_KERNEL_SOURCES,
-                            "df5a0b52b1f3f70e6d0d2f41abec52a82ddda21f0b621cf7a36b12f1b3c25efd"),
+    "rope_prefill_t32768": (768_234_496, ROPE_KERNEL_SOURCES,
+                            "fa980a506c38f4a633447bab730832813569500c8a40c5ee3795b4ff6925ceb9"),
 }
 
 
