@@ -221,6 +221,11 @@ struct pda_handle_s {
   int kernel = 0;  // pda::PartialKernel
   int num_sms = 1;
   int ctas_per_sm = 1;
+  // Calls of short contexts run on the CUDA-core kernel where the tensor-core
+  // kernel is the default (pda::call_partial_kernel); off when
+  // PDA_PARTIAL_KERNEL pins the kernel.
+  bool small_cc = false;
+  int cc_ctas_per_sm = 1;
   void* ws = nullptr;
   float* ws_o = nullptr;
   float* ws_lse = nullptr;
@@ -247,7 +252,15 @@ namespace {
 struct LaunchShape {
   int splits, chunk_pages, ctas, cluster;
   int64_t units;
+  int kernel, ctas_per_sm;  // the kernel this call runs and its CTAs per SM
 };
+
+// The longest context a call can have: its table width in tokens, or the
+// hint when that is smaller.
+int64_t call_max_len(const pda_config& c, int max_blocks, int hint) {
+  const int64_t len = (int64_t)max_blocks * c.block_size;
+  return hint > 0 && hint < len ? hint : len;
+}
 
 // How a run of this handle is launched: the split plan, the work units, the
 // CTAs and, for the tensor-core kernel, whether the launch is one wave of
@@ -255,12 +268,18 @@ struct LaunchShape {
 // distributed shared memory) when every pair fits.
 LaunchShape launch_shape(const pda_handle_s* h, int batch, int max_blocks, int hint, int forced) {
   const pda_config& c = h->cfg;
-  LaunchShape r{1, 1, 0, 0, 0};
-  plan_splits(c, h->kernel, h->num_sms, h->ctas_per_sm, batch, max_blocks, hint, forced,
+  LaunchShape r{1, 1, 0, 0, 0, h->kernel, h->ctas_per_sm};
+  if (h->small_cc &&
+      pda::call_partial_kernel(h->group, c.head_dim, false, call_max_len(c, max_blocks, hint),
+                               batch, c.num_kv_heads) == pda::kPartialCudaCore) {
+    r.kernel = pda::kPartialCudaCore;
+    r.ctas_per_sm = h->cc_ctas_per_sm;
+  }
+  plan_splits(c, r.kernel, h->num_sms, r.ctas_per_sm, batch, max_blocks, hint, forced,
               &r.splits, &r.chunk_pages);
   r.units = (int64_t)r.splits * c.num_kv_heads * batch;
-  if (h->kernel == pda::kPartialTensorCore) {
-    const int64_t max_ctas = (int64_t)h->num_sms * h->ctas_per_sm;
+  if (r.kernel == pda::kPartialTensorCore) {
+    const int64_t max_ctas = (int64_t)h->num_sms * r.ctas_per_sm;
     r.ctas = (int)(r.units < max_ctas ? r.units : max_ctas);
     if (r.splits >= 2 && r.splits <= 16 &&
         (int64_t)batch * c.num_kv_heads <= h->max_clusters[r.splits]) {
@@ -302,7 +321,12 @@ int paged_decode_attn_create(const pda_config* cfg, pda_handle* out_handle) {
   // handle (A/B measurements and tests).
   const bool kv8 = cfg->kv_fp8 != 0;
   h->kernel = pda::default_partial_kernel(h->group, cfg->head_dim, kv8);
-  if (const char* env = std::getenv("PDA_PARTIAL_KERNEL")) {
+  const char* kernel_env = std::getenv("PDA_PARTIAL_KERNEL");
+  h->small_cc = !kernel_env &&
+                pda::call_partial_kernel(h->group, cfg->head_dim, kv8, 1, 1, 1) ==
+                    pda::kPartialCudaCore &&
+                h->kernel == pda::kPartialTensorCore;
+  if (const char* env = kernel_env) {
     if (std::strcmp(env, "cuda_core") == 0 &&
         pda::partial_kernel_supported(pda::kPartialCudaCore, h->group, cfg->head_dim, kv8))
       h->kernel = pda::kPartialCudaCore;
@@ -333,6 +357,19 @@ int paged_decode_attn_create(const pda_config* cfg, pda_handle* out_handle) {
                                kv8);
   const int hint = pda::partial_ctas_per_sm_hint(h->kernel, h->group, cfg->head_dim);
   h->ctas_per_sm = occ < hint ? occ : hint;
+  if (h->small_cc) {
+    e = pda::partial_prepare(pda::kPartialCudaCore, h->group, cfg->head_dim, cfg->block_size,
+                             cfg->dtype, false);
+    if (e != cudaSuccess) {
+      delete h;
+      return cuda_fail("cudaFuncSetAttribute", e);
+    }
+    const int occ_cc = pda::partial_ctas_per_sm(pda::kPartialCudaCore, h->group, cfg->head_dim,
+                                                cfg->block_size, cfg->dtype, false);
+    const int hint_cc =
+        pda::partial_ctas_per_sm_hint(pda::kPartialCudaCore, h->group, cfg->head_dim);
+    h->cc_ctas_per_sm = occ_cc < hint_cc ? occ_cc : hint_cc;
+  }
   const size_t rows = (size_t)cfg->max_batch * cfg->num_q_heads * cfg->max_splits;
   const size_t o_bytes = rows * cfg->head_dim * sizeof(float);
   const size_t lse_bytes = ((rows * sizeof(float)) + 255) & ~size_t(255);
@@ -380,7 +417,9 @@ int paged_decode_attn_plan(const pda_config* cfg, int num_sms, int batch, int ma
     return fail(PDA_EINVAL, "max_blocks out of range");
   if (max_context_len_hint < 0) return fail(PDA_EINVAL, "max_context_len_hint < 0");
   const int G = cfg->num_q_heads / cfg->num_kv_heads;
-  const int kernel = pda::default_partial_kernel(G, cfg->head_dim, cfg->kv_fp8 != 0);
+  const int kernel = pda::call_partial_kernel(G, cfg->head_dim, cfg->kv_fp8 != 0,
+                                              call_max_len(*cfg, max_blocks, max_context_len_hint),
+                                              batch, cfg->num_kv_heads);
   plan_splits(*cfg, kernel, num_sms, pda::partial_ctas_per_sm_hint(kernel, G, cfg->head_dim),
               batch, max_blocks, max_context_len_hint, 0, num_splits, chunk_pages);
   return PDA_OK;
@@ -470,7 +509,7 @@ int paged_decode_attn_run_scaled(pda_handle h, const void* q, const void* k_cach
   const int64_t units = shape.units;
   if (units > INT_MAX) return fail(PDA_EINVAL, "splits * num_kv_heads * batch exceeds 2^31");
   alignas(64) CUtensorMap tmap_q;
-  if (h->kernel == pda::kPartialTensorCore) {
+  if (shape.kernel == pda::kPartialTensorCore) {
     int st = encode_q_map(&tmap_q, q, (int64_t)batch * c.num_q_heads, c.head_dim, h->group);
     if (st != PDA_OK) return st;
   } else {
@@ -494,19 +533,19 @@ int paged_decode_attn_run_scaled(pda_handle h, const void* q, const void* k_cach
   p.num_splits = S;
   p.qscale = scale * pda::kLog2e;
   p.num_units = (int)units;
-  p.max_ctas = h->num_sms * h->ctas_per_sm;
+  p.max_ctas = h->num_sms * shape.ctas_per_sm;
   p.out_f32 = out_dtype == PDA_F32;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
   p.scale_per_head = scale_per_head;
   p.cluster = shape.cluster;
-  if (h->test_stall_runs > 0) {
+  if (h->test_stall_runs > 0 && shape.kernel == pda::kPartialTensorCore) {
     --h->test_stall_runs;
     p.stall_units = 1;
     p.wait_ns = 1000ull * 1000ull;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = pda::launch_partial(h->kernel, h->group, c.head_dim, c.block_size, c.dtype,
+  cudaError_t e = pda::launch_partial(shape.kernel, h->group, c.head_dim, c.block_size, c.dtype,
                                       c.kv_fp8 != 0, &h->tmap_k, &h->tmap_v, &tmap_q, p, batch,
                                       s);
   if (e != cudaSuccess) return cuda_fail("partial kernel launch", e);

@@ -40,6 +40,27 @@ def test_short_batch(seed, bs, dtype):
     check(workloads.short_batch(seed=seed, block_size=bs, dtype=dtype))
 
 
+def test_short_and_long_calls_alternate_on_one_handle():
+    """Calls whose longest context is at most 256 tokens run on the CUDA-core
+    kernel, longer ones on the tensor cores, chosen per call; both use the
+    handle's split tickets and the persistent kernel's counters, so calls of
+    the two kinds alternate on one handle, each compared with the oracle."""
+    short = workloads.custom(seed=31, B=6, Hq=32, Hkv=8, D=128, block_size=16,
+                             lens=[1, 17, 64, 200, 256, 129], num_blocks=300)
+    long_ = workloads.custom(seed=32, B=6, Hq=32, Hkv=8, D=128, block_size=16,
+                             lens=[3000, 5, 700, 257, 1, 2048], num_blocks=600)
+    assert short.max_blocks * short.block_size <= 256 < long_.max_blocks * long_.block_size
+    refs = [oracle_ref(short), oracle_ref(long_)]
+    wls = [short.to(DEV), long_.to(DEV)]
+    attn = make_attn(wls[1])
+    for _ in range(2):
+        for wl, ref in zip(wls, refs):
+            for splits in (0, 3):
+                assert_close(run_gpu(attn, wl, num_splits=splits), ref, f"{wl.name} S={splits}")
+    assert attn.check_device_error() == (0, 0)
+    attn.close()
+
+
 @pytest.mark.parametrize("seed", [0, 1, 2])
 def test_mid_ragged_peaky(seed):
     check(workloads.mid_ragged(seed=seed))
