@@ -82,6 +82,32 @@ int check_config(const pda_config* c) {
   return PDA_OK;
 }
 
+// A small call of short contexts runs on the CUDA-core kernel even where the
+// tensor-core kernel is the default (16-bit K/V, a geometry both support):
+// with one or two 128-token chunks per unit and few units the step is all
+// fixed cost, and the CUDA-core kernel's (no TMEM, no persistent scheduling,
+// 160-thread CTAs, two per SM) is the smaller. Measured on GB300 at 32/8
+// heads, back to back / cold: 32 sequences of 16-64 tokens 4.6 / 10.2 us
+// against 9.5 / 16.7; 32 x 256 tokens (34 MB) 9.3 / 16.4 against 10.3 / 20.5;
+// but 128 x 256 tokens (134 MB) 38.9 / 43.0 against 28.7 / 35.2, so the
+// call's KV bytes (at most) are bounded too.
+constexpr int kSmallContextTokens = 256;
+constexpr int64_t kSmallStepKvBytes = int64_t(64) << 20;
+
+// The kernel one call runs: the default for the geometry, or the CUDA-core
+// kernel for a small call of short contexts (max_len: the call's longest
+// context, its table width times the block size or the hint when smaller;
+// batch x Hkv x max_len x D x 4 bytes bounds its 16-bit K/V bytes).
+constexpr int call_partial_kernel(int group, int head_dim, bool kv_fp8, int64_t max_len,
+                                  int64_t batch, int num_kv_heads) {
+  return (pda::default_partial_kernel(group, head_dim, kv_fp8) == pda::kPartialTensorCore &&
+          !kv_fp8 && group <= 8 && (head_dim == 64 || head_dim == 128) &&
+          max_len <= kSmallContextTokens &&
+          batch * num_kv_heads * max_len * head_dim * 4 <= kSmallStepKvBytes)
+             ? pda::kPartialCudaCore
+             : pda::default_partial_kernel(group, head_dim, kv_fp8);
+}
+
 void plan_splits(const pda_config& c, int kernel, int num_sms, int ctas_per_sm, int batch,
                  int max_blocks, int hint, int forced, int* S_out, int* chunk_out) {
   const int overhead = kernel == pda::kPartialTensorCore ? kOverheadTokensTensorCore
@@ -222,7 +248,7 @@ struct pda_handle_s {
   int num_sms = 1;
   int ctas_per_sm = 1;
   // Calls of short contexts run on the CUDA-core kernel where the tensor-core
-  // kernel is the default (pda::call_partial_kernel); off when
+  // kernel is the default (call_partial_kernel); off when
   // PDA_PARTIAL_KERNEL pins the kernel.
   bool small_cc = false;
   int cc_ctas_per_sm = 1;
@@ -270,7 +296,7 @@ LaunchShape launch_shape(const pda_handle_s* h, int batch, int max_blocks, int h
   const pda_config& c = h->cfg;
   LaunchShape r{1, 1, 0, 0, 0, h->kernel, h->ctas_per_sm};
   if (h->small_cc &&
-      pda::call_partial_kernel(h->group, c.head_dim, false, call_max_len(c, max_blocks, hint),
+      call_partial_kernel(h->group, c.head_dim, false, call_max_len(c, max_blocks, hint),
                                batch, c.num_kv_heads) == pda::kPartialCudaCore) {
     r.kernel = pda::kPartialCudaCore;
     r.ctas_per_sm = h->cc_ctas_per_sm;
@@ -323,7 +349,7 @@ int paged_decode_attn_create(const pda_config* cfg, pda_handle* out_handle) {
   h->kernel = pda::default_partial_kernel(h->group, cfg->head_dim, kv8);
   const char* kernel_env = std::getenv("PDA_PARTIAL_KERNEL");
   h->small_cc = !kernel_env &&
-                pda::call_partial_kernel(h->group, cfg->head_dim, kv8, 1, 1, 1) ==
+                call_partial_kernel(h->group, cfg->head_dim, kv8, 1, 1, 1) ==
                     pda::kPartialCudaCore &&
                 h->kernel == pda::kPartialTensorCore;
   if (const char* env = kernel_env) {
@@ -417,7 +443,7 @@ int paged_decode_attn_plan(const pda_config* cfg, int num_sms, int batch, int ma
     return fail(PDA_EINVAL, "max_blocks out of range");
   if (max_context_len_hint < 0) return fail(PDA_EINVAL, "max_context_len_hint < 0");
   const int G = cfg->num_q_heads / cfg->num_kv_heads;
-  const int kernel = pda::call_partial_kernel(G, cfg->head_dim, cfg->kv_fp8 != 0,
+  const int kernel = call_partial_kernel(G, cfg->head_dim, cfg->kv_fp8 != 0,
                                               call_max_len(*cfg, max_blocks, max_context_len_hint),
                                               batch, cfg->num_kv_heads);
   plan_splits(*cfg, kernel, num_sms, pda::partial_ctas_per_sm_hint(kernel, G, cfg->head_dim),

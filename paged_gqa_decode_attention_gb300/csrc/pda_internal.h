@@ -92,31 +92,6 @@ constexpr int default_partial_kernel(int group, int head_dim, bool kv_fp8 = fals
              : kPartialCudaCore;
 }
 
-// A small call of short contexts runs on the CUDA-core kernel even where the
-// tensor-core kernel is the default (16-bit K/V, a geometry both support):
-// with one or two 128-token chunks per unit and few units the step is all
-// fixed cost, and the CUDA-core kernel's (no TMEM, no persistent scheduling,
-// 160-thread CTAs, two per SM) is the smaller. Measured on GB300 at 32/8
-// heads, back to back / cold: 32 sequences of 16-64 tokens 4.6 / 10.2 us
-// against 9.5 / 16.7; 32 x 256 tokens (34 MB) 9.3 / 16.4 against 10.3 / 20.5;
-// but 128 x 256 tokens (134 MB) 38.9 / 43.0 against 28.7 / 35.2, so the
-// call's KV bytes (at most) are bounded too.
-constexpr int kSmallContextTokens = 256;
-constexpr int64_t kSmallStepKvBytes = int64_t(64) << 20;
-
-// The kernel one call runs: the default for the geometry, or the CUDA-core
-// kernel for a small call of short contexts (max_len: the call's longest
-// context, its table width times the block size or the hint when smaller;
-// batch x Hkv x max_len x D x 4 bytes bounds its 16-bit K/V bytes).
-constexpr int call_partial_kernel(int group, int head_dim, bool kv_fp8, int64_t max_len,
-                                  int64_t batch, int num_kv_heads) {
-  return (default_partial_kernel(group, head_dim, kv_fp8) == kPartialTensorCore && !kv_fp8 &&
-          group <= 8 && (head_dim == 64 || head_dim == 128) && max_len <= kSmallContextTokens &&
-          batch * num_kv_heads * max_len * head_dim * 4 <= kSmallStepKvBytes)
-             ? kPartialCudaCore
-             : default_partial_kernel(group, head_dim, kv_fp8);
-}
-
 // CTAs per SM each kernel is built for (its launch bounds and shared memory);
 // the planner's figure when no GPU is queried.
 constexpr int partial_ctas_per_sm_hint(int kernel, int group, int head_dim) {
