@@ -173,10 +173,11 @@ int paged_decode_attn_run_scaled(pda_handle handle, const void* q, const void* k
  * / chunk_pages)) splits. Waves of work units are counted over 27/32 of the
  * SMs for the 16-bit tensor-core kernel (G 3..16 at head_dim 64/128) and over
  * every SM (times CTAs per SM) otherwise. The kernel is chosen per call: a
- * call of 16-bit K/V at G <= 8 whose longest context (max_blocks * block_size,
- * or the hint when smaller) is at most 256 tokens and whose K/V bytes are at
- * most 64 MiB (batch * Hkv * that length * head_dim * 4) runs on the CUDA-core
- * kernel, where the tensor-core kernel's fixed cost would dominate. */
+ * call of 16-bit K/V at G <= 8 whose longest context L (max_blocks *
+ * block_size, or the hint when smaller) and K/V bytes (at most batch * Hkv *
+ * L * head_dim * 4) are small (L <= 256 and <= 48 MiB, or L <= 1024 and
+ * <= 20 MiB) runs on the CUDA-core kernel, where the tensor-core kernel's
+ * fixed cost would dominate. */
 int paged_decode_attn_plan(const pda_config* cfg, int num_sms, int batch, int max_blocks,
                            int max_context_len_hint, int* num_splits, int* chunk_pages);
 

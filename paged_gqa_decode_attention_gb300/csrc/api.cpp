@@ -82,28 +82,34 @@ int check_config(const pda_config* c) {
   return PDA_OK;
 }
 
-// A small call of short contexts runs on the CUDA-core kernel even where the
-// tensor-core kernel is the default (16-bit K/V, a geometry both support):
-// with one or two 128-token chunks per unit and few units the step is all
-// fixed cost, and the CUDA-core kernel's (no TMEM, no persistent scheduling,
-// 160-thread CTAs, two per SM) is the smaller. Measured on GB300 at 32/8
-// heads, back to back / cold: 32 sequences of 16-64 tokens 4.6 / 10.2 us
-// against 9.5 / 16.7; 32 x 256 tokens (34 MB) 9.3 / 16.4 against 10.3 / 20.5;
-// but 128 x 256 tokens (134 MB) 38.9 / 43.0 against 28.7 / 35.2, so the
-// call's KV bytes (at most) are bounded too.
-constexpr int kSmallContextTokens = 256;
-constexpr int64_t kSmallStepKvBytes = int64_t(64) << 20;
+// A small call runs on the CUDA-core kernel even where the tensor-core kernel
+// is the default (16-bit K/V, a geometry both support): with few short units
+// the step is mostly fixed cost, and the CUDA-core kernel's (no TMEM, no
+// persistent scheduling, 160-thread CTAs, two per SM) is the smaller.
+// Measured on GB300 at 32/8 heads, back to back / cold, CUDA-core against
+// tensor-core: 32 sequences of 16-64 tokens 4.6 / 10.2 us against 9.5 / 16.7;
+// 32 x 256 tokens (34 MB) 9.3 / 16.4 against 10.3 / 20.5; 8 x 512 (17 MB)
+// 8.8 / 14.8 against 9.8 / 21.1; 2 x 1024 8.2 / 14.3 against 9.6 / 18.4. The
+// tensor cores win back to back from 34 MB at 1024-2048 tokens (8 x 1024:
+// 11.8 against 11.2) and at 67 MB of 256-token contexts (64 x 256: 18.0
+// against 16.6). So: contexts up to 256 tokens and 48 MiB of K/V, or up to
+// 1024 tokens and 20 MiB (the call's bytes bounded from its table width).
+constexpr int kShortContextTokens = 256;
+constexpr int64_t kShortStepKvBytes = int64_t(48) << 20;
+constexpr int kMidContextTokens = 1024;
+constexpr int64_t kMidStepKvBytes = int64_t(20) << 20;
 
 // The kernel one call runs: the default for the geometry, or the CUDA-core
-// kernel for a small call of short contexts (max_len: the call's longest
-// context, its table width times the block size or the hint when smaller;
-// batch x Hkv x max_len x D x 4 bytes bounds its 16-bit K/V bytes).
+// kernel for a small call (max_len: the call's longest context, its table
+// width times the block size or the hint when smaller; batch x Hkv x max_len
+// x D x 4 bytes bounds its 16-bit K/V bytes).
 constexpr int call_partial_kernel(int group, int head_dim, bool kv_fp8, int64_t max_len,
                                   int64_t batch, int num_kv_heads) {
+  const int64_t bytes = batch * num_kv_heads * max_len * head_dim * 4;
   return (pda::default_partial_kernel(group, head_dim, kv_fp8) == pda::kPartialTensorCore &&
           !kv_fp8 && group <= 8 && (head_dim == 64 || head_dim == 128) &&
-          max_len <= kSmallContextTokens &&
-          batch * num_kv_heads * max_len * head_dim * 4 <= kSmallStepKvBytes)
+          ((max_len <= kShortContextTokens && bytes <= kShortStepKvBytes) ||
+           (max_len <= kMidContextTokens && bytes <= kMidStepKvBytes)))
              ? pda::kPartialCudaCore
              : pda::default_partial_kernel(group, head_dim, kv_fp8);
 }

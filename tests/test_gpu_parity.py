@@ -41,10 +41,11 @@ def test_short_batch(seed, bs, dtype):
 
 
 def test_short_and_long_calls_alternate_on_one_handle():
-    """Calls whose longest context is at most 256 tokens run on the CUDA-core
-    kernel, longer ones on the tensor cores, chosen per call; both use the
-    handle's split tickets and the persistent kernel's counters, so calls of
-    the two kinds alternate on one handle, each compared with the oracle."""
+    """Small calls (here: contexts up to 256 tokens, 6 MB of K/V) run on the
+    CUDA-core kernel, larger ones on the tensor cores, chosen per call; both
+    use the handle's split tickets and the persistent kernel's counters, so
+    calls of the two kinds alternate on one handle, each compared with the
+    oracle."""
     short = workloads.custom(seed=31, B=6, Hq=32, Hkv=8, D=128, block_size=16,
                              lens=[1, 17, 64, 200, 256, 129], num_blocks=300)
     long_ = workloads.custom(seed=32, B=6, Hq=32, Hkv=8, D=128, block_size=16,
