@@ -76,6 +76,27 @@ def test_fp8_full_size_long_context_every_split_count():
     torch.cuda.empty_cache()
 
 
+def test_fp8_full_size_group_16():
+    """FP8 K/V at 128/8 heads (G = 16) and the headline's bytes (B=8,
+    L=32768): every row against the oracle at three split counts and in fp32
+    output."""
+    wl = workloads.to_fp8_kv(workloads.custom(seed=8, B=8, Hq=128, Hkv=8, D=128, block_size=16,
+                                              lens=[32768] * 8, device=DEV))
+    ks = wl.meta["k_scale"].double().cpu().numpy()
+    vs = wl.meta["v_scale"].double().cpu().numpy()
+    q, k, v, bt, cl = workloads.compact_for_rows(wl, range(wl.batch))
+    ref = oracle.paged_decode_kv(q, k, v, bt, cl, oracle.BF16, oracle.FP8_E4M3, wl.scale, ks, vs)
+    del q, k, v
+    attn = make_attn(wl)
+    for splits in (0, 7, 64):
+        assert_close(run_gpu(attn, wl, num_splits=splits), ref, f"fp8 g16 splits={splits}")
+    err = assert_close(run_gpu(attn, wl, out_dtype=torch.float32), ref, "fp8 g16 fp32 out")
+    assert err < 2e-3, err
+    attn.close()
+    del wl
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("kernel", ["cuda_core", "tensor_core"])
 def test_scaled_16bit_caches(kernel, monkeypatch):
     """Dequantisation scales on bf16 caches (both kernels)."""

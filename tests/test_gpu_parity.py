@@ -133,6 +133,24 @@ def test_full_size_long_context_every_split_count(long_pool, batch, context):
     attn.close()
 
 
+def test_full_size_group_16_every_split_count():
+    """128/8 heads (G = 16: all 16 MMA columns) at the headline's bytes (B=4,
+    L=32768): every row against the oracle at the heuristic's split count and
+    across the sweep, and in fp32 output."""
+    wl = workloads.custom(seed=7, B=4, Hq=128, Hkv=8, D=128, block_size=16, lens=[32768] * 4,
+                          device=DEV)
+    ref = oracle.paged_decode(*workloads.compact_for_rows(wl, range(wl.batch)), oracle.BF16,
+                              wl.scale)
+    attn = make_attn(wl)
+    for splits in (0, 1, 4, 16, 64):
+        assert_close(run_gpu(attn, wl, num_splits=splits), ref, f"{wl.name} splits={splits}")
+    err = assert_close(run_gpu(attn, wl, out_dtype=torch.float32), ref, f"{wl.name} fp32 out")
+    assert err < 1e-4, err
+    attn.close()
+    del wl
+    torch.cuda.empty_cache()
+
+
 def test_fp32_output_mode_every_config():
     """The kernel's own accuracy (fp32 out) on the tiny, short-batch (both
     dtypes, both block sizes), mid-ragged and serving-mix configs: within the
