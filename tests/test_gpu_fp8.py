@@ -97,6 +97,29 @@ def test_fp8_full_size_group_16():
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,L", [(16, 32, 8, 32768), (128, 14, 2, 8192)])
+def test_fp8_full_size_head_dim_64(B, Hq, Hkv, L):
+    """FP8 K/V at head dim 64 at full size: the bench's 32/8-head step (B=16,
+    L=32768, the headline's bytes) and the Qwen2.5-0.5B geometry (14/2 heads,
+    B=128, L=8192): every row against the oracle at the heuristic's split count
+    and one other, and in fp32 output."""
+    wl = workloads.to_fp8_kv(workloads.custom(seed=Hq + B, B=B, Hq=Hq, Hkv=Hkv, D=64,
+                                              block_size=16, lens=[L] * B, device=DEV))
+    ks = wl.meta["k_scale"].double().cpu().numpy()
+    vs = wl.meta["v_scale"].double().cpu().numpy()
+    q, k, v, bt, cl = workloads.compact_for_rows(wl, range(wl.batch))
+    ref = oracle.paged_decode_kv(q, k, v, bt, cl, oracle.BF16, oracle.FP8_E4M3, wl.scale, ks, vs)
+    del q, k, v
+    attn = make_attn(wl)
+    for splits in (0, 5):
+        assert_close(run_gpu(attn, wl, num_splits=splits), ref, f"fp8 d64 splits={splits}")
+    err = assert_close(run_gpu(attn, wl, out_dtype=torch.float32), ref, "fp8 d64 fp32 out")
+    assert err < 2e-3, err
+    attn.close()
+    del wl
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("kernel", ["cuda_core", "tensor_core"])
 def test_scaled_16bit_caches(kernel, monkeypatch):
     """Dequantisation scales on bf16 caches (both kernels)."""

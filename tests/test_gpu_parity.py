@@ -151,6 +151,27 @@ def test_full_size_group_16_every_split_count():
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,D,L", [(8, 32, 8, 64, 32768), (64, 14, 2, 64, 8192),
+                                          (16, 28, 4, 128, 8192), (64, 8, 1, 128, 8192)])
+def test_full_size_other_geometries(B, Hq, Hkv, D, L):
+    """The other geometries' bench workloads at full size: 32/8 heads at D 64
+    (two producer and two PV warps), Qwen2.5-0.5B (14/2, D 64) and
+    Qwen2.5-7B (28/4) attention, MQA (8/1); every row against the oracle at
+    the heuristic's split count and one other, and in fp32 output."""
+    wl = workloads.custom(seed=Hq + D, B=B, Hq=Hq, Hkv=Hkv, D=D, block_size=16, lens=[L] * B,
+                          device=DEV)
+    ref = oracle.paged_decode(*workloads.compact_for_rows(wl, range(wl.batch)), oracle.BF16,
+                              wl.scale)
+    attn = make_attn(wl)
+    for splits in (0, 5):
+        assert_close(run_gpu(attn, wl, num_splits=splits), ref, f"{wl.name} splits={splits}")
+    err = assert_close(run_gpu(attn, wl, out_dtype=torch.float32), ref, f"{wl.name} fp32 out")
+    assert err < 1e-4, err
+    attn.close()
+    del wl
+    torch.cuda.empty_cache()
+
+
 def test_fp32_output_mode_every_config():
     """The kernel's own accuracy (fp32 out) on the tiny, short-batch (both
     dtypes, both block sizes), mid-ragged and serving-mix configs: within the
