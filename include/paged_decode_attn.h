@@ -83,7 +83,7 @@ typedef struct {
   int num_q_heads;        /* Hq; a multiple of num_kv_heads */
   int num_kv_heads;       /* Hkv */
   int head_dim;           /* D; 64, 128 or 256 */
-  int block_size;         /* tokens per page; 16 or 32 */
+  int block_size;         /* tokens per page; 16 or 32, or 64 at G <= 8 */
   int dtype;              /* pda_dtype of q and out (and of the caches unless kv_fp8):
                              PDA_BF16 or PDA_FP16 */
   int max_batch;          /* largest batch a run may pass (1 .. 65535) */

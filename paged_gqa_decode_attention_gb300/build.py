@@ -68,7 +68,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     nvcc = nvcc_path()
     os.makedirs(BUILD_DIR, exist_ok=True)
     srcs = sources()
-    with ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
+    with ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1, len(srcs)))) as ex:
         objs = list(ex.map(lambda s: _compile(nvcc, s, verbose_ptxas), srcs))
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]

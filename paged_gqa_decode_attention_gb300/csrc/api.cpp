@@ -74,11 +74,11 @@ int check_config(const pda_config* c) {
   if (c->kv_fp8 && !pda::partial_supported(G, c->head_dim, c->block_size, c->dtype, true))
     return fail(PDA_EUNSUPPORTED,
                 "FP8 K/V caches need head_dim 64 or 128, group size 1..16, dtype PDA_BF16 "
-                "or PDA_FP16 and block_size 16 or 32");
+                "or PDA_FP16 and block_size 16 or 32 (or 64 at group size <= 8)");
   if (!pda::partial_supported(G, c->head_dim, c->block_size, c->dtype, c->kv_fp8 != 0))
     return fail(PDA_EUNSUPPORTED,
                 "unsupported geometry: group size must be 1..16 (1..4 at head_dim 256) and "
-                "block_size 16 or 32");
+                "block_size 16 or 32 (or 64 at group size <= 8)");
   return PDA_OK;
 }
 

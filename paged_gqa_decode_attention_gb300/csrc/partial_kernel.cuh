@@ -480,6 +480,7 @@ struct Dispatch {
     if constexpr (geometry_supported(G, D)) {
       if (BS == 16) return launch_one<G, D, 16, FP16>(tk, tv, p, batch, s);
       if (BS == 32) return launch_one<G, D, 32, FP16>(tk, tv, p, batch, s);
+      if (BS == 64) return launch_one<G, D, 64, FP16>(tk, tv, p, batch, s);
     }
     return cudaErrorInvalidValue;
   }
@@ -488,13 +489,16 @@ struct Dispatch {
     if constexpr (geometry_supported(G, D)) {
       if (BS == 16) return prepare_one<G, D, 16, FP16>();
       if (BS == 32) return prepare_one<G, D, 32, FP16>();
+      if (BS == 64) return prepare_one<G, D, 64, FP16>();
     }
     return cudaErrorInvalidValue;
   }
   template <int G>
   static int occupancy_g(int BS) {
     if constexpr (geometry_supported(G, D)) {
-      return BS == 16 ? occupancy_one<G, D, 16, FP16>() : occupancy_one<G, D, 32, FP16>();
+      return BS == 16   ? occupancy_one<G, D, 16, FP16>()
+             : BS == 32 ? occupancy_one<G, D, 32, FP16>()
+                        : occupancy_one<G, D, 64, FP16>();
     }
     return 1;
   }

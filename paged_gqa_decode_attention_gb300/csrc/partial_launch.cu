@@ -107,7 +107,7 @@ auto with_tc(int dtype, int head_dim, bool kv_fp8, int group, F f) {
 }  // namespace
 
 bool partial_supported(int group, int head_dim, int block_size, int dtype, bool kv_fp8) {
-  const bool bs_ok = block_size == 16 || block_size == 32;
+  const bool bs_ok = block_size == 16 || block_size == 32 || (block_size == 64 && group <= 8);
   if (kv_fp8)
     return tc::geometry_supported(group, head_dim, true) && bs_ok && (dtype == 0 || dtype == 1);
   return (partial::geometry_supported(group, head_dim) ||

@@ -1455,7 +1455,8 @@ __host__ __device__ constexpr bool geometry_supported(int G, int D, bool kv8 = f
              : (G >= 3 && G <= 16 && (D == 64 || D == 128));
 }
 
-// Dispatch over (G, block size) for one head dim, input dtype and K/V type;
+// Dispatch over (G, block size 16 or 32, and 64 for G <= 8) for one head dim,
+// input dtype and K/V type;
 // each (head dim, dtype, K/V type) and G range GLo..GHi is instantiated in its
 // own translation unit (G 1..8 and G 9..16 compile in parallel).
 template <int D, bool FP16, bool KV8, int GLo = 1, int GHi = 8>
@@ -1468,6 +1469,8 @@ struct Dispatch {
     if constexpr (kBuilt<G>) {
       if (BS == 16) return launch_one<G, D, 16, FP16, KV8>(tk, tv, tq, p, s);
       if (BS == 32) return launch_one<G, D, 32, FP16, KV8>(tk, tv, tq, p, s);
+      if constexpr (G <= 8)
+        if (BS == 64) return launch_one<G, D, 64, FP16, KV8>(tk, tv, tq, p, s);
     }
     return cudaErrorInvalidValue;
   }
@@ -1476,21 +1479,28 @@ struct Dispatch {
     if constexpr (kBuilt<G>) {
       if (BS == 16) return prepare_one<G, D, 16, FP16, KV8>();
       if (BS == 32) return prepare_one<G, D, 32, FP16, KV8>();
+      if constexpr (G <= 8)
+        if (BS == 64) return prepare_one<G, D, 64, FP16, KV8>();
     }
     return cudaErrorInvalidValue;
   }
   template <int G>
   static int max_clusters_g(int BS, int cluster) {
     if constexpr (kBuilt<G>) {
-      return BS == 16 ? max_clusters_one<G, D, 16, FP16, KV8>(cluster)
-                      : max_clusters_one<G, D, 32, FP16, KV8>(cluster);
+      if (BS == 16) return max_clusters_one<G, D, 16, FP16, KV8>(cluster);
+      if (BS == 32) return max_clusters_one<G, D, 32, FP16, KV8>(cluster);
+      if constexpr (G <= 8)
+        if (BS == 64) return max_clusters_one<G, D, 64, FP16, KV8>(cluster);
     }
     return 0;
   }
   template <int G>
   static int occupancy_g(int BS) {
     if constexpr (kBuilt<G>) {
-      return BS == 16 ? occupancy_one<G, D, 16, FP16, KV8>() : occupancy_one<G, D, 32, FP16, KV8>();
+      if (BS == 16) return occupancy_one<G, D, 16, FP16, KV8>();
+      if (BS == 32) return occupancy_one<G, D, 32, FP16, KV8>();
+      if constexpr (G <= 8)
+        if (BS == 64) return occupancy_one<G, D, 64, FP16, KV8>();
     }
     return 1;
   }

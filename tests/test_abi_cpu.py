@@ -89,6 +89,22 @@ def test_create_geometries_before_cuda(lib, Hq, Hkv, D, ok):
         assert st == pda.PDA_EUNSUPPORTED
 
 
+@pytest.mark.parametrize("Hq,Hkv,D,bs,ok", [(32, 8, 128, 64, True), (14, 2, 64, 64, True),
+                                            (16, 8, 256, 64, True), (128, 8, 128, 64, False),
+                                            (32, 8, 128, 128, False), (32, 8, 128, 8, False)])
+def test_create_block_sizes_before_cuda(lib, Hq, Hkv, D, bs, ok):
+    """Block sizes 16 and 32 everywhere, 64 at group sizes up to 8."""
+    cfg = pda.make_config(Hq, Hkv, D, bs)
+    h = ctypes.c_void_p()
+    st = lib.paged_decode_attn_create(ctypes.byref(cfg), ctypes.byref(h))
+    if ok:
+        assert st != pda.PDA_EUNSUPPORTED and st != pda.PDA_EINVAL, lib.paged_decode_attn_last_error()
+        if st == pda.PDA_OK:
+            lib.paged_decode_attn_destroy(h)
+    else:
+        assert st == pda.PDA_EUNSUPPORTED
+
+
 def test_null_arguments(lib):
     h = ctypes.c_void_p()
     assert lib.paged_decode_attn_create(None, ctypes.byref(h)) == pda.PDA_EINVAL

@@ -189,6 +189,21 @@ def test_fp8_large_groups_exact(Hq, Hkv, D, bs):
     check(wl16, num_splits=7)
 
 
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (14, 2, 64), (64, 8, 128)])
+def test_fp8_block_size_64(Hq, Hkv, D):
+    """FP8 K/V in 64-token pages: every split count, fp16 queries, fp32 output."""
+    lens = [1, 63, 64, 65, 700, 3000, 129]
+    wl = workloads.to_fp8_kv(workloads.custom(seed=Hq * 3 + D, B=len(lens), Hq=Hq, Hkv=Hkv,
+                                              D=D, block_size=64, lens=lens, num_blocks=200))
+    for splits in (0, 1, 5, 64):
+        check(wl, num_splits=splits)
+    err = check(wl, out_dtype=torch.float32)
+    assert err < 2e-3, err
+    check(workloads.to_fp8_kv(workloads.custom(seed=Hq + 5, B=3, Hq=Hq, Hkv=Hkv, D=D,
+                                               block_size=64, lens=[500, 64, 2000],
+                                               dtype="fp16")))
+
+
 def test_fp8_unsupported_geometries_rejected():
     from paged_gqa_decode_attention_gb300 import PagedDecodeAttention
     for kw in (dict(head_dim=256), dict(num_q_heads=8 * 17)):

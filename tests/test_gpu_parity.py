@@ -366,6 +366,29 @@ def test_large_groups_fp16_and_fp32_out(Hq, Hkv, D):
     assert err < 1e-4, err
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (14, 2, 64), (8, 1, 128), (64, 8, 128),
+                                      (16, 8, 128), (16, 8, 256)])
+def test_block_size_64(kernel, Hq, Hkv, D, monkeypatch):
+    """64-token pages (two per tensor-core chunk, one per CUDA-core stage) on
+    both kernels where each supports the geometry: ragged and partial last
+    pages, every split count, fp16 inputs and fp32 output."""
+    G = Hq // Hkv
+    if kernel == "tensor_core" and (G < 3 or D == 256):
+        pytest.skip("tensor-core kernel: G 3..16 at head dim 64 or 128")
+    monkeypatch.setenv("PDA_PARTIAL_KERNEL", kernel)
+    lens = [1, 63, 64, 65, 700, 3000, 129]
+    wl = workloads.custom(seed=Hq + D + 64, B=len(lens), Hq=Hq, Hkv=Hkv, D=D, block_size=64,
+                          lens=lens, num_blocks=200)
+    for splits in (0, 1, 5, 64):
+        check(wl, num_splits=splits)
+    check(workloads.custom(seed=Hq + D + 65, B=3, Hq=Hq, Hkv=Hkv, D=D, block_size=64,
+                           lens=[500, 64, 2000], dtype="fp16"))
+    err = check(workloads.custom(seed=Hq + D + 66, B=3, Hq=Hq, Hkv=Hkv, D=D, block_size=64,
+                                 lens=[500, 64, 2000]), out_dtype=torch.float32)
+    assert err < 1e-4, err
+
+
 @pytest.mark.parametrize("Hq,Hkv,D", [(14, 2, 64), (16, 8, 256), (28, 4, 128)])
 def test_geometries_fp16_and_fp32_out(Hq, Hkv, D):
     lens = [900, 17, 2048, 300]
