@@ -52,8 +52,8 @@ TC_KERNEL_SOURCES = ("partial_tc_kernel.cuh", "ptx.cuh", "split_merge.cuh", "pda
 ROPE_KERNEL_SOURCES = ("rope_kv_write.cu", "ptx.cuh", "pda_internal.h")
 NCU_TRAFFIC = {
     # workload: (bytes per launch, kernel sources, their SHA-256 at capture)
-    "long_b4_l32768": (540_652_544, TC_KERNEL_SOURCES,
-                       "6401ee8def5bbac42d5d092edfa4721e34bcb4e36c136ab5138f8a29f268f2be"),
+    "long_b4_l32768": (540_981_760, TC_KERNEL_SOURCES,
+                       "9d54b0a72658dbd1b0ed990de896a3e78228f88ebff1598f7b029366fd744473"),
     "rope_prefill_t32768": (768_234_496, ROPE_KERNEL_SOURCES,
                             "fa980a506c38f4a633447bab730832813569500c8a40c5ee3795b4ff6925ceb9"),
 }

@@ -56,19 +56,22 @@
 //   warp 6: allocates 256 TMEM columns (S and O, double-buffered), issues
 //     the QK^T MMAs and commits their completion to mbarriers; with FP8 K/V
 //     it also turns each unit's 16-bit q tile into the two fp8 q terms.
-//   warp 15: issues the PV MMAs and commits their completion. At 16-bit head
-//     dim 64 (G <= 4) it takes the even chunks and warp 18 the odd ones: an
-//     M = 64 PV needs as many MMAs per chunk as M = 128 for half the bytes
-//     (a second QK^T issuer as well measured no faster). The terms of a
-//     split operand (P_hi / P_lo; with FP8, q_hi / q_lo and the three P
-//     terms) are stacked along N, so each contraction step is one MMA.
+//   warp 15: issues the PV MMAs and commits their completion. At head dim 64
+//     (G <= 4, and G 5..8 with 16-bit K/V) it takes the even chunks and a
+//     second PV warp the odd ones (warp 18 or 16 at G <= 4; at G 5..8 the
+//     epilogue group's warp 10): an M = 64 PV needs as many MMAs per chunk
+//     as M = 128 for half the bytes (a second QK^T issuer as well measured
+//     no faster). The terms of a split operand (P_hi / P_lo; with FP8, q_hi /
+//     q_lo and the three P terms) are stacked along N, so each contraction
+//     step is one MMA.
 // S, O and P are double-buffered by chunk parity so the chunks overlap:
 // QK^T of chunk c+1 is issued as soon as its K tile lands (while the
 // softmax warps work on chunk c), PV of chunk c once its P is written; the
 // softmax warps fold O of chunk c-1 into the running output after writing P
 // of chunk c.
-//   warps 7-10: epilogue. A finished unit's state (accumulators, max, sum)
-//     comes through a double-buffered shared-memory slot; this group
+//   warps 7-10 (7-9 when warp 10 issues PV): epilogue. A finished unit's
+//     state (accumulators, max, sum) comes through a double-buffered
+//     shared-memory slot; this group
 //     normalises it, stores the output or the split partial, and runs the
 //     split ticket and merge, while the softmax warps go on with the next
 //     unit (the unit boundary does not stall the pipeline).
@@ -103,28 +106,35 @@ constexpr int kOpBytes = 2 * kOpHalf;      // Q, P_hi or P_lo operand
 __host__ __device__ constexpr bool dual_producers(int G, int D, bool kv8) {
   return (kv8 || D == 64) && G <= 4;
 }
-// A second PV-issuing warp (alternate chunks) for 16-bit head dim 64 at
-// G <= 4: its PV is an M = 64 MMA per 16 tokens, so one issuing thread (~185
-// cycles per MMA) needed ~1480 cycles per 128-token chunk that arrives in
-// ~800. (At G >= 5 a 17th warp would cut the register budget from 128 to 96
-// per thread, since one SM sub-partition would then hold five warps.)
+// A second PV-issuing warp (alternate chunks) at head dim 64: its PV is an
+// M = 64 MMA per 16 tokens, so one issuing thread (~185 cycles per MMA)
+// needed ~1480 cycles per 128-token chunk that arrives in ~800. At G <= 4 it
+// is an extra warp. At G 5..8 (16-bit K/V) a 17th warp would cut every
+// thread's registers from 128 to 96 (one SM sub-partition would hold five
+// warps), so it is the epilogue group's last warp (10); the epilogue then
+// runs on three warps (its per-dim work needs 64 threads at D 64).
 __host__ __device__ constexpr bool dual_pv(int G, int D, bool kv8) {
-  return D == 64 && G <= 4;
+  return D == 64 && (G <= 4 || (!kv8 && G <= 8));
+}
+__host__ __device__ constexpr bool pv2_from_epilogue(int G, int D, bool kv8) {
+  return dual_pv(G, D, kv8) && G >= 5;
 }
 __host__ __device__ constexpr int tc_threads(int G, int D, bool kv8) {
-  return 512 + (dual_producers(G, D, kv8) ? 64 : 0) + (dual_pv(G, D, kv8) ? 32 : 0);
+  return 512 + (dual_producers(G, D, kv8) ? 64 : 0) +
+         (dual_pv(G, D, kv8) && !pv2_from_epilogue(G, D, kv8) ? 32 : 0);
 }
 constexpr int kWarpProducerK = 4;
 constexpr int kWarpProducerV = 5;
 constexpr int kWarpMma = 6;                // issues QK^T (and owns the TMEM allocation)
-constexpr int kWarpEpi0 = 7;               // warps 7-10: epilogue group
+constexpr int kWarpEpi0 = 7;               // warps 7-10 (or 7-9): epilogue group
 constexpr int kWarpSmxB0 = 11;             // warps 11-14: second softmax group
 constexpr int kWarpMmaPV = 15;             // issues PV
 constexpr int kWarpProducerK2 = 16;        // second K producer (odd chunks)
 constexpr int kWarpProducerV2 = 17;        // second V producer (odd chunks)
-// second PV issuer (odd chunks): the warp after the last producer
+// second PV issuer (odd chunks): the warp after the last producer, or at
+// G 5..8 the epilogue group's last warp
 __host__ __device__ constexpr int warp_pv2(int G, int D, bool kv8) {
-  return dual_producers(G, D, kv8) ? 18 : 16;
+  return pv2_from_epilogue(G, D, kv8) ? 10 : (dual_producers(G, D, kv8) ? 18 : 16);
 }
 // TMEM columns: S and O, double-buffered. The terms of a split operand are
 // stacked along N so one MMA carries all of them (the tensor pipe's cost
@@ -390,6 +400,8 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
   constexpr bool kDual = dual_producers(G, D, KV8);
   constexpr bool kDualPV = dual_pv(G, D, KV8);
   constexpr int kWarpMmaPV2 = warp_pv2(G, D, KV8);
+  constexpr int kEpiWarps = pv2_from_epilogue(G, D, KV8) ? 3 : 4;  // epilogue group
+  constexpr int kEpiThreads = 32 * kEpiWarps;
   constexpr int kGA = (G + 1) / 2 > 0 ? (G + 1) / 2 : 1;  // columns of group 0 (group 1: G - kGA)
   constexpr int kLd = kGA > 4 ? 8 : 4;      // TMEM columns a softmax thread loads per operand
   constexpr int kGE = epi_heads(G);         // heads of a state slot
@@ -547,7 +559,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
     }
     for (int s2 = 0; s2 < 2; ++s2) {
       mbar_init(ep_full(s2), 4 * kGroups);
-      mbar_init(ep_empty(s2), 4);
+      mbar_init(ep_empty(s2), kEpiWarps);
     }
     for (int r = 0; r < 2; ++r)
       for (int s = 0; s < kStages; ++s) {
@@ -1228,9 +1240,9 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
       const bool ok = !failed && mbar_wait(ep_full(es), (je / kEpiSlots) & 1, wlim);
       // the four warps agree on the outcome before acting on it
       if (t == 0) *flag = 0;
-      named_bar_sync(2, 128);
+      named_bar_sync(2, kEpiThreads);
       if (!ok && lane == 0) *flag = 1;
-      named_bar_sync(2, 128);
+      named_bar_sync(2, kEpiThreads);
       if (*flag) {
         failed = true;
         break;
@@ -1272,7 +1284,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
           for (int g = 0; g < G; ++g)
             st[kStMax + g] = (st[kStMax + g] + log2f(st[kStSum + g])) * kLn2;
         }
-        named_bar_sync(2, 128);  // this CTA's slot holds its split's o and lse
+        named_bar_sync(2, kEpiThreads);  // this CTA's slot holds its split's o and lse
         if (t == 0) {
           fence_acq_rel_cluster();
           for (int q = 0; q < p.cluster; ++q)
@@ -1287,7 +1299,7 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
           const int per = (G * D + nsb - 1) / nsb;
           const int lo = U.split * per, hi = min(G * D, lo + per);
           const uint32_t st_u32 = smem_u32(st);
-          for (int oi = lo + t; oi < hi; oi += 128) {
+          for (int oi = lo + t; oi < hi; oi += kEpiThreads) {
             const int g = oi / D, d = oi - g * D;
             // groups of 8 splits, a running maximum across the groups
             float M = -INFINITY, wsum = 0.f, acc = 0.f;
@@ -1343,14 +1355,14 @@ __global__ void __launch_bounds__(tc_threads(G, D, KV8), 1)
           }
         }
       }
-      named_bar_sync(2, 128);  // the state is read; the slot serves as merge scratch
+      named_bar_sync(2, kEpiThreads);  // the state is read; the slot serves as merge scratch
       // the last split of this (sequence, kv head) merges all of them into `out`
       if (U.n_splits_b > 1) {
         // merge loads in flight per thread: fewer with the 576-thread launch,
         // whose register budget is smaller
         constexpr int kMergeChunk = kDual ? 4 : 8;
-        if (p.out_f32) finish_split<G, D, float, kMergeChunk>(p, U.b, U.h, U.n_splits_b, t, st, 2);
-        else finish_split<G, D, TNat, kMergeChunk>(p, U.b, U.h, U.n_splits_b, t, st, 2);
+        if (p.out_f32) finish_split<G, D, float, kMergeChunk, kEpiThreads>(p, U.b, U.h, U.n_splits_b, t, st, 2);
+        else finish_split<G, D, TNat, kMergeChunk, kEpiThreads>(p, U.b, U.h, U.n_splits_b, t, st, 2);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(ep_empty(es));

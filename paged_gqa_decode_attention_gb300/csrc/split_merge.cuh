@@ -32,9 +32,9 @@ __device__ __forceinline__ TOut merge_to_out(float x) {
   }
 }
 
-// Called by 128 threads (tid 0..127) after each has written its part of this
-// split's partial (head dim D). `sw` is shared scratch of at least one word,
-// `bar_id` a named barrier over exactly these 128 threads.
+// Called by kThreads threads (tid 0..kThreads-1) after each has written its
+// part of this split's partial (head dim D). `sw` is shared scratch of at
+// least one word, `bar_id` a named barrier over exactly these threads.
 //
 // The merging CTA is on the step's critical path (it finishes last), so the
 // merge is one pass of loads with no further barrier: each thread owns
@@ -42,25 +42,25 @@ __device__ __forceinline__ TOut merge_to_out(float x) {
 // the splits' log-sum-exps and its four columns of their partials together
 // (all in flight at once), folding them with a running maximum:
 //   M = max_s lse_s,  out = sum_s e^(lse_s - M) o_s / sum_s e^(lse_s - M).
-template <int G, int D, typename TOut, int kChunk = 8>
+template <int G, int D, typename TOut, int kChunk = 8, int kThreads = 128>
 __device__ __forceinline__ void finish_split(const PartialParams& p, int b, int h, int n_splits_b,
                                              int tid, float* sw, int bar_id) {
   static_assert(D % 4 == 0, "float4 columns");
   constexpr int kCols = D / 4;
   __threadfence();
-  named_bar_sync(bar_id, 128);
+  named_bar_sync(bar_id, kThreads);
   int* flag = reinterpret_cast<int*>(sw);
   if (tid == 0) {
     const int prev = atomicAdd(p.counters + (int64_t)b * p.Hkv + h, 1);
     *flag = (prev == n_splits_b - 1);
   }
-  named_bar_sync(bar_id, 128);
+  named_bar_sync(bar_id, kThreads);
   if (!*flag) return;
   __threadfence();
   const int hq0 = h * G;
   const int64_t row0 = (int64_t)b * p.Hq + hq0;
   TOut* out = static_cast<TOut*>(p.out);
-  for (int pair = tid; pair < G * kCols; pair += 128) {
+  for (int pair = tid; pair < G * kCols; pair += kThreads) {
     const int g = pair / kCols, d4 = (pair - g * kCols) * 4;
     const float* lrow = p.ws_lse + (row0 + g) * p.num_splits;
     const float4* o = reinterpret_cast<const float4*>(p.ws_o + ((row0 + g) * p.num_splits) * D + d4);
